@@ -1,0 +1,213 @@
+// qmm_api.cu -- the C ABI (include/qmm.h): argument checks, per-device state
+// (error word, SM count), launches.  No entry point allocates device memory.
+#include "../../include/qmm.h"
+#include "qmm_internal.h"
+
+#include <atomic>
+#include <mutex>
+
+namespace qmm {
+
+// Device error word: written by kernels that give up a bounded wait, read
+// and cleared by qmm_get_device_error().  One per GPU (module-scope device
+// variable; no allocation).
+__device__ uint32_t g_device_error = 0;
+
+namespace {
+
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+
+std::atomic<uint64_t> g_timeout_ns{kDefaultTimeoutNs};
+
+struct DeviceState {
+    std::once_flag once;
+    cudaError_t init_err = cudaSuccess;
+    uint32_t *err_word = nullptr;
+    int sms = 0;
+};
+DeviceState g_dev[kMaxDevices];
+
+// Per-device set-up, once, with that device current.
+DeviceState *device_state(cudaError_t *err) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        *err = e != cudaSuccess ? e : cudaErrorInvalidDevice;
+        return nullptr;
+    }
+    DeviceState &st = g_dev[dev];
+    std::call_once(st.once, [&st, dev]() {
+        void *p = nullptr;
+        st.init_err = cudaGetSymbolAddress(&p, g_device_error);
+        if (st.init_err == cudaSuccess) {
+            st.err_word = static_cast<uint32_t *>(p);
+            st.init_err = cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev);
+        }
+    });
+    *err = st.init_err;
+    return st.init_err == cudaSuccess ? &st : nullptr;
+}
+
+bool make_ctx(LaunchCtx *ctx) {
+    cudaError_t e;
+    DeviceState *st = device_state(&e);
+    if (!st) return false;
+    ctx->err = st->err_word;
+    ctx->timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+    return true;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+qmm_status from_cuda(cudaError_t e) { return e == cudaSuccess ? QMM_OK : QMM_ERR_CUDA; }
+
+qmm_status check_wk(const void *w, int64_t n, int64_t k) {
+    if (!w) return QMM_ERR_NULL;
+    if (n < 1 || k < kQK || k % kQK != 0) return QMM_ERR_SHAPE;
+    // byte offsets of the largest index must fit comfortably in 64 bits
+    if (n > (int64_t(1) << 40) || k > (int64_t(1) << 31)) return QMM_ERR_SHAPE;
+    return QMM_OK;
+}
+
+// [a, a+an) and [b, b+bn) overlap
+bool overlaps(const void *a, size_t an, const void *b, size_t bn) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + bn && y < x + an;
+}
+
+qmm_status dequant(Fmt fmt, const void *w, float *out, int64_t n, int64_t k,
+                   qmm_stream_t stream) {
+    qmm_status s = check_wk(w, n, k);
+    if (s != QMM_OK) return s;
+    if (!out) return QMM_ERR_NULL;
+    if (!aligned(out, 4)) return QMM_ERR_ALIGN;
+    LaunchCtx ctx;
+    if (!make_ctx(&ctx)) return QMM_ERR_CUDA;
+    return from_cuda(launch_dequant(fmt, static_cast<const uint8_t *>(w), out, n, k,
+                                    reinterpret_cast<cudaStream_t>(stream), ctx));
+}
+
+qmm_status gemv(Fmt fmt, const void *w, const float *x, float *y, int m, int64_t n, int64_t k,
+                qmm_stream_t stream) {
+    qmm_status s = check_wk(w, n, k);
+    if (s != QMM_OK) return s;
+    if (!x || !y) return QMM_ERR_NULL;
+    if (m < 1 || m > QMM_GEMV_MAX_M) return QMM_ERR_SHAPE;
+    if (!aligned(x, 4) || !aligned(y, 4)) return QMM_ERR_ALIGN;
+    const size_t wbytes = static_cast<size_t>(n) * (k / kQK) * block_bytes(fmt);
+    const size_t ybytes = sizeof(float) * static_cast<size_t>(m) * n;
+    if (overlaps(y, ybytes, w, wbytes) || overlaps(y, ybytes, x, sizeof(float) * m * k))
+        return QMM_ERR_UNSUPPORTED;
+    LaunchCtx ctx;
+    if (!make_ctx(&ctx)) return QMM_ERR_CUDA;
+    return from_cuda(launch_gemv(fmt, static_cast<const uint8_t *>(w), x, y, m, n, k,
+                                 reinterpret_cast<cudaStream_t>(stream), ctx));
+}
+
+}  // namespace
+
+int current_device() {
+    int dev = 0;
+    return cudaGetDevice(&dev) == cudaSuccess ? dev : 0;
+}
+
+int device_sm_count() {
+    cudaError_t e;
+    DeviceState *st = device_state(&e);
+    return st ? st->sms : 1;
+}
+
+// ---- self-test: a wait that nothing completes ---------------------------------
+__global__ void selftest_wait_kernel(LaunchCtx ctx) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) mbar_init(&bar, 1);
+    fence_mbar_init();
+    __syncthreads();
+    if (threadIdx.x == 0) mbar_wait(&bar, 0, ctx);  // never completes: bounded by ctx.timeout_ns
+    __syncthreads();
+}
+
+cudaError_t launch_selftest_wait(cudaStream_t stream, const LaunchCtx &ctx) {
+    return launch_kernel(selftest_wait_kernel, dim3(1), dim3(32), 0, stream, 1, ctx);
+}
+
+}  // namespace qmm
+
+using namespace qmm;
+
+extern "C" {
+
+qmm_status qmm_dequant_q4_0(const void *w, float *out, int64_t n, int64_t k,
+                            qmm_stream_t stream) {
+    return dequant(Fmt::Q4_0, w, out, n, k, stream);
+}
+
+qmm_status qmm_dequant_q8_0(const void *w, float *out, int64_t n, int64_t k,
+                            qmm_stream_t stream) {
+    return dequant(Fmt::Q8_0, w, out, n, k, stream);
+}
+
+qmm_status qmm_gemv_q4_0(const void *w, const float *x, float *y, int m, int64_t n, int64_t k,
+                         qmm_stream_t stream) {
+    return gemv(Fmt::Q4_0, w, x, y, m, n, k, stream);
+}
+
+qmm_status qmm_gemv_q8_0(const void *w, const float *x, float *y, int m, int64_t n, int64_t k,
+                         qmm_stream_t stream) {
+    return gemv(Fmt::Q8_0, w, x, y, m, n, k, stream);
+}
+
+qmm_status qmm_gemm_q4_0(const void *w, const uint16_t *x_bf16, float *y, int64_t m, int64_t n,
+                         int64_t k, qmm_stream_t stream) {
+    qmm_status s = check_wk(w, n, k);
+    if (s != QMM_OK) return s;
+    if (!x_bf16 || !y) return QMM_ERR_NULL;
+    if (m < 1 || m > (int64_t(1) << 31)) return QMM_ERR_SHAPE;
+    if (k % 256 != 0 || n % 4 != 0) return QMM_ERR_UNSUPPORTED;
+    if (!aligned(w, 16) || !aligned(x_bf16, 16) || !aligned(y, 16)) return QMM_ERR_ALIGN;
+    LaunchCtx ctx;
+    if (!make_ctx(&ctx)) return QMM_ERR_CUDA;
+    return from_cuda(launch_gemm_q4_0(static_cast<const uint8_t *>(w), x_bf16, y, m, n, k,
+                                      reinterpret_cast<cudaStream_t>(stream), ctx));
+}
+
+const char *qmm_status_string(qmm_status status) {
+    switch (status) {
+        case QMM_OK: return "ok";
+        case QMM_ERR_NULL: return "null pointer argument";
+        case QMM_ERR_SHAPE: return "invalid shape (k % 32 != 0, a size < 1, or m out of range)";
+        case QMM_ERR_ALIGN: return "pointer alignment not supported by this call";
+        case QMM_ERR_UNSUPPORTED: return "valid arguments not supported by this build";
+        case QMM_ERR_CUDA: return "CUDA runtime error";
+        case QMM_ERR_TIMEOUT: return "a device-side wait timed out";
+    }
+    return "unknown status";
+}
+
+int qmm_version(void) { return 100; }
+
+qmm_status qmm_get_device_error(qmm_stream_t stream) {
+    cudaError_t e;
+    if (!device_state(&e)) return QMM_ERR_CUDA;
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return QMM_ERR_CUDA;
+    uint32_t word = 0;
+    const uint32_t zero = 0;
+    if (cudaMemcpyFromSymbol(&word, g_device_error, sizeof word) != cudaSuccess) return QMM_ERR_CUDA;
+    if (word != 0 && cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero) != cudaSuccess)
+        return QMM_ERR_CUDA;
+    return word == 0 ? QMM_OK : static_cast<qmm_status>(word);
+}
+
+void qmm_set_wait_timeout_ns(uint64_t ns) {
+    g_timeout_ns.store(ns == 0 ? kDefaultTimeoutNs : ns, std::memory_order_relaxed);
+}
+
+qmm_status qmm_selftest_wait_timeout(uint64_t timeout_ns, qmm_stream_t stream) {
+    LaunchCtx ctx;
+    if (!make_ctx(&ctx)) return QMM_ERR_CUDA;
+    ctx.timeout_ns = timeout_ns;
+    return from_cuda(launch_selftest_wait(reinterpret_cast<cudaStream_t>(stream), ctx));
+}
+
+}  // extern "C"

@@ -1,0 +1,563 @@
+// qmm_gemm.cu -- prefill GEMM Y[m][n] = sum_k X[m][k] * w[n][k] with bf16
+// activations X and GGUF Q4_0 weights W, on the 5th-generation tensor cores
+// (tcgen05, sm_103a).
+//
+// Prefill is the TTFT side of the Gemma4 rows in "Add generated quant-kernel
+// JIT and accelerate Gemma4, BGE-M3, and GLiNER2" ("Benchmarks": Gemma4 E2B
+// TTFT on M4 and L4); the products are the same Q4_0 dispatches as decode
+// ("Validation"), with M = prompt tokens.
+//
+// Per weight: w = (nibble - 8) * d is formed exactly in fp32 and rounded once
+// to bf16 (round to nearest even); products are summed in fp32 in tensor
+// memory.
+//
+// Structure (one persistent CTA per SM, 448 threads, warp-specialised):
+//   warp 0      producer: TMA loads of X tiles (128 x 64 bf16, 128-byte
+//               swizzle) and of raw Q4_0 tiles (256 rows x 144 bytes = 8
+//               blocks per row, no swizzle), each tracked by an mbarrier with
+//               a byte count.
+//   warps 2-9   dequantisers: thread t owns W row t of the tile; it reads its
+//               row's 144 raw bytes (conflict-free 16-byte loads), then for
+//               each of the four 64-wide K stages writes 64 bf16 weights into
+//               the B tile in the canonical K-major 128-byte-swizzled layout
+//               (16-byte chunk c of row r at chunk c ^ (r & 7)).
+//   warp 1      MMA issuer: one thread issues tcgen05.mma (M=128, N=256,
+//               K=16, kind::f16, bf16 x bf16 -> fp32) from the two shared-
+//               memory descriptors into one of two TMEM accumulators, and
+//               tcgen05.commit releases stages and hands accumulators over.
+//   warps 10-13 epilogue: tcgen05.ld of the 128 x 256 fp32 accumulator (warp
+//               w reads TMEM lanes 32*(w%4)..+31) and stores to Y; the second
+//               accumulator lets the next tile's MMAs run meanwhile.
+// Every wait is bounded (GPU global timer).  On a timeout the CTA records the
+// error, sets a shared abort flag that makes every other wait give up at
+// once, lets its own TMA copies and MMAs finish (bounded waits), frees TMEM
+// and exits.
+#include "qmm_internal.h"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+namespace qmm {
+namespace {
+
+constexpr int BM = 128;              // tokens per tile (MMA M)
+constexpr int BN = 256;              // weight rows per tile (MMA N)
+constexpr int BK = 64;               // K per operand stage (one 128-byte swizzle row)
+constexpr int UMMA_K = 16;           // K per tcgen05.mma (kind::f16)
+constexpr int RAW_K = 256;           // K per raw stage (8 Q4_0 blocks)
+constexpr int RAW_ROW_BYTES = 144;   // 8 blocks x 18 bytes
+constexpr int OP_STAGES = 3;
+constexpr int RAW_STAGES = 2;
+constexpr int X_STAGE_BYTES = BM * BK * 2;           // 16 KB
+constexpr int W_STAGE_BYTES = BN * BK * 2;           // 32 KB
+constexpr int RAW_STAGE_BYTES = BN * RAW_ROW_BYTES;  // 36 KB
+constexpr int NUM_ACC = 2;
+constexpr uint32_t TMEM_COLS = NUM_ACC * BN;         // 512 fp32 columns
+
+constexpr int WARP_PRODUCER = 0;
+constexpr int WARP_MMA = 1;
+constexpr int WARP_DEQ0 = 2;
+constexpr int NUM_DEQ_WARPS = BN / 32;               // 8
+constexpr int WARP_EPI0 = WARP_DEQ0 + NUM_DEQ_WARPS;  // 10
+constexpr int NUM_EPI_WARPS = 4;
+constexpr int NUM_THREADS = (WARP_EPI0 + NUM_EPI_WARPS) * 32;  // 448
+
+static_assert(BN == NUM_DEQ_WARPS * 32, "one dequantiser thread per W row");
+static_assert(RAW_K % BK == 0, "raw stage covers whole operand stages");
+
+struct SmemLayout {
+    static constexpr int x = 0;
+    static constexpr int w = x + OP_STAGES * X_STAGE_BYTES;
+    static constexpr int raw = w + OP_STAGES * W_STAGE_BYTES;
+    static constexpr int bars = raw + RAW_STAGES * RAW_STAGE_BYTES;
+    // barriers: x_full, w_ready, op_empty [OP_STAGES]; raw_full, raw_empty
+    // [RAW_STAGES]; acc_full, acc_empty [NUM_ACC]; final
+    static constexpr int nbars = 3 * OP_STAGES + 2 * RAW_STAGES + 2 * NUM_ACC + 1;
+    static constexpr int tmem_slot = bars + nbars * 8;
+    static constexpr int abort_flag = tmem_slot + 4;
+    static constexpr int total = abort_flag + 4;
+};
+constexpr size_t kSmemBytes = SmemLayout::total + 1024;  // + alignment slack
+
+struct GemmParams {
+    float *y;
+    int m, n, k;
+    int num_m_blocks;
+    int num_tiles;
+    LaunchCtx ctx;
+};
+
+// ---- PTX wrappers --------------------------------------------------------------
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, "
+        "{%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows
+// 128 bytes apart, 8-row groups 1024 bytes apart (SBO); LBO unused.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    uint64_t d = static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(1) << 16;             // LBO (ignored for swizzled K-major)
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;     // SBO
+    d |= static_cast<uint64_t>(1) << 46;             // descriptor version
+    d |= static_cast<uint64_t>(2) << 61;             // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
+                            (static_cast<uint32_t>(BN >> 3) << 17) |
+                            (static_cast<uint32_t>(BM >> 4) << 24);
+
+__device__ __forceinline__ bool abort_set(const int *flag) {
+    return *reinterpret_cast<const volatile int *>(flag) != 0;
+}
+
+// Bounded wait that also gives up as soon as another role has aborted.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, int *flag,
+                                              const LaunchCtx &ctx) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 0; it < (1u << 30); ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 15u) == 15u) {
+            if (abort_set(flag)) return false;
+            if (global_timer_ns() - t0 > ctx.timeout_ns) break;
+        }
+    }
+    *reinterpret_cast<volatile int *>(flag) = 1;
+    record_error(ctx, kDevErrTimeout);
+    return false;
+}
+
+// Warp-wide form: every lane polls, and the warp agrees on the outcome so
+// that the following __syncwarp / .sync.aligned instructions stay uniform.
+__device__ __forceinline__ bool warp_wait_or_abort(uint32_t bar, uint32_t parity, int *flag,
+                                                   const LaunchCtx &ctx) {
+    const bool ok = wait_or_abort(bar, parity, flag, ctx);
+    return __all_sync(0xFFFFFFFFu, ok);
+}
+
+// Bounded wait that ignores the abort flag (used to drain our own copies).
+__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, const LaunchCtx &ctx) {
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 0; it < (1u << 30); ++it) {
+        if (mbar_try_wait(bar, parity)) return;
+        if ((it & 15u) == 15u && global_timer_ns() - t0 > ctx.timeout_ns) break;
+    }
+    record_error(ctx, kDevErrTimeout);
+}
+
+__device__ __forceinline__ void mbar_init_addr(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_addr(uint32_t bar) {
+    asm volatile("{ .reg .b64 st; mbarrier.arrive.shared::cta.b64 st, [%0]; }" ::"r"(bar)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx_addr(uint32_t bar, uint32_t bytes) {
+    asm volatile("{ .reg .b64 st; mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1; }" ::"r"(
+                     bar),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ float mag(uint32_t v, uint32_t mask) {
+    return __uint_as_float((v & mask) | 0x4B000000u);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// bf16 pair (k, k+1) from two 2^23-magic nibble floats: exact (nibble-8)*2^s
+// by one packed add, exact (nibble-8)*d by one packed multiply with d*2^-s,
+// one rounding to bf16.
+__device__ __forceinline__ uint32_t w_pair(float ma, float mb, float2 c, float2 ds) {
+    const float2 f = __fadd2_rn(make_float2(ma, mb), c);
+    const float2 w = __fmul2_rn(f, ds);
+    return pack_bf16x2(w.x, w.y);
+}
+
+// Dequantise Q4_0 block `b` (0..7) of a 144-byte row chunk held in wd[36]
+// into 32 bf16 values = four 16-byte chunks q[0..3] (K order).
+__device__ __forceinline__ void dequant_block_bf16(const uint32_t (&wd)[36], int b,
+                                                   uint4 (&out)[4]) {
+    const int base = (18 * b) >> 2;
+    uint32_t dbits, q[4];
+    if ((b & 1) == 0) {
+        dbits = wd[base] & 0xFFFFu;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) q[i] = __byte_perm(wd[base + i], wd[base + i + 1], 0x5432);
+    } else {
+        dbits = wd[base] >> 16;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) q[i] = wd[base + 1 + i];
+    }
+    const float d = half_bits_to_float(dbits);
+    const float d4 = d * 0.0625f, d8 = d * 0.00390625f, d12 = d * 0.000244140625f,
+                d16 = d * 1.52587890625e-05f;
+    const float2 c08 = make_float2(-8388616.0f, -8390656.0f);  // s = 0, 8
+    const float2 c168 = make_float2(-8912896.0f, -8390656.0f); // s = 16, 8
+    const float2 c412 = make_float2(-8388736.0f, -8421376.0f); // s = 4, 12
+    const float2 d08 = make_float2(d, d8), d168 = make_float2(d16, d8), d412 = make_float2(d4, d12);
+    uint32_t lo[8], hi[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t v = q[i], u = v >> 16;
+        // low nibbles: weights 4i .. 4i+3
+        lo[2 * i + 0] = w_pair(mag(v, 0x0000000Fu), mag(v, 0x00000F00u), c08, d08);
+        lo[2 * i + 1] = w_pair(mag(v, 0x000F0000u), mag(u, 0x00000F00u), c168, d168);
+        // high nibbles: weights 16+4i .. 19+4i
+        hi[2 * i + 0] = w_pair(mag(v, 0x000000F0u), mag(v, 0x0000F000u), c412, d412);
+        hi[2 * i + 1] = w_pair(mag(u, 0x000000F0u), mag(u, 0x0000F000u), c412, d412);
+    }
+    out[0] = make_uint4(lo[0], lo[1], lo[2], lo[3]);  // k 0..7
+    out[1] = make_uint4(lo[4], lo[5], lo[6], lo[7]);  // k 8..15
+    out[2] = make_uint4(hi[0], hi[1], hi[2], hi[3]);  // k 16..23
+    out[3] = make_uint4(hi[4], hi[5], hi[6], hi[7]);  // k 24..31
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
+    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_q4_0_kernel(const __grid_constant__ CUtensorMap tmap_x,
+                     const __grid_constant__ CUtensorMap tmap_w, GemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_base = smem_addr(smem_raw);
+    const uint32_t sbase = (raw_base + 1023u) & ~1023u;  // 1024-byte aligned (swizzle atoms)
+    uint8_t *sgen = smem_raw + (sbase - raw_base);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const LaunchCtx ctx = p.ctx;
+
+    auto bar = [&](int i) -> uint32_t { return sbase + SmemLayout::bars + 8u * i; };
+    auto x_full = [&](int s) { return bar(s); };
+    auto w_ready = [&](int s) { return bar(OP_STAGES + s); };
+    auto op_empty = [&](int s) { return bar(2 * OP_STAGES + s); };
+    auto raw_full = [&](int r) { return bar(3 * OP_STAGES + r); };
+    auto raw_empty = [&](int r) { return bar(3 * OP_STAGES + RAW_STAGES + r); };
+    auto acc_full = [&](int a) { return bar(3 * OP_STAGES + 2 * RAW_STAGES + a); };
+    auto acc_empty = [&](int a) { return bar(3 * OP_STAGES + 2 * RAW_STAGES + NUM_ACC + a); };
+    const uint32_t final_bar = bar(SmemLayout::nbars - 1);
+    int *abort_flag = reinterpret_cast<int *>(sgen + SmemLayout::abort_flag);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sgen + SmemLayout::tmem_slot);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < OP_STAGES; ++s) {
+            mbar_init_addr(x_full(s), 1);
+            mbar_init_addr(w_ready(s), NUM_DEQ_WARPS);
+            mbar_init_addr(op_empty(s), 1);
+        }
+        for (int r = 0; r < RAW_STAGES; ++r) {
+            mbar_init_addr(raw_full(r), 1);
+            mbar_init_addr(raw_empty(r), NUM_DEQ_WARPS);
+        }
+        for (int a = 0; a < NUM_ACC; ++a) {
+            mbar_init_addr(acc_full(a), 1);
+            mbar_init_addr(acc_empty(a), NUM_EPI_WARPS);
+        }
+        mbar_init_addr(final_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == WARP_MMA) tmem_alloc(sbase + SmemLayout::tmem_slot, TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
+
+    pdl_wait();
+
+    const int KB = p.k / BK;             // operand stages per tile
+    const int KR = p.k / RAW_K;          // raw stages per tile
+
+    if (warp == WARP_PRODUCER) {
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_x)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_w)) : "memory");
+            uint32_t it = 0, rit = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+                const int mb = t % p.num_m_blocks, nb = t / p.num_m_blocks;
+                for (int kb = 0; ok && kb < KB; ++kb) {
+                    if (kb % (RAW_K / BK) == 0) {
+                        const int r = rit % RAW_STAGES;
+                        const uint32_t ph = (rit / RAW_STAGES) & 1u;
+                        if (!wait_or_abort(raw_empty(r), ph ^ 1u, abort_flag, ctx)) { ok = false; break; }
+                        mbar_expect_tx_addr(raw_full(r), RAW_STAGE_BYTES);
+                        tma_load_2d(sbase + SmemLayout::raw + r * RAW_STAGE_BYTES, &tmap_w,
+                                    (kb / (RAW_K / BK)) * RAW_ROW_BYTES, nb * BN, raw_full(r));
+                        ++rit;
+                    }
+                    const int s = it % OP_STAGES;
+                    const uint32_t ph = (it / OP_STAGES) & 1u;
+                    if (!wait_or_abort(op_empty(s), ph ^ 1u, abort_flag, ctx)) { ok = false; break; }
+                    mbar_expect_tx_addr(x_full(s), X_STAGE_BYTES);
+                    tma_load_2d(sbase + SmemLayout::x + s * X_STAGE_BYTES, &tmap_x, kb * BK,
+                                mb * BM, x_full(s));
+                    ++it;
+                }
+            }
+            // let our own copies land before the CTA may exit
+            for (int s = 0; s < OP_STAGES; ++s) {
+                if (it > static_cast<uint32_t>(s)) {
+                    const uint32_t last = it - 1 - ((it - 1 - s) % OP_STAGES);
+                    wait_drain(x_full(s), (last / OP_STAGES) & 1u, ctx);
+                }
+            }
+            for (int r = 0; r < RAW_STAGES; ++r) {
+                if (rit > static_cast<uint32_t>(r)) {
+                    const uint32_t last = rit - 1 - ((rit - 1 - r) % RAW_STAGES);
+                    wait_drain(raw_full(r), (last / RAW_STAGES) & 1u, ctx);
+                }
+            }
+        }
+    } else if (warp == WARP_MMA) {
+        if (lane == 0) {
+            uint32_t it = 0, ait = 0;
+            bool ok = true, issued = false;
+            for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+                const int a = ait % NUM_ACC;
+                const uint32_t aph = (ait / NUM_ACC) & 1u;
+                if (!wait_or_abort(acc_empty(a), aph ^ 1u, abort_flag, ctx)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + a * BN;
+                for (int kb = 0; kb < KB; ++kb) {
+                    const int s = it % OP_STAGES;
+                    const uint32_t ph = (it / OP_STAGES) & 1u;
+                    if (!wait_or_abort(x_full(s), ph, abort_flag, ctx) ||
+                        !wait_or_abort(w_ready(s), ph, abort_flag, ctx)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint64_t adesc = sw128_desc(sbase + SmemLayout::x + s * X_STAGE_BYTES);
+                    const uint64_t bdesc = sw128_desc(sbase + SmemLayout::w + s * W_STAGE_BYTES);
+#pragma unroll
+                    for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                        // advance 16 bf16 = 32 bytes along K inside the swizzle row
+                        umma_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, kIdesc,
+                                  (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    issued = true;
+                    umma_commit(op_empty(s));
+                    ++it;
+                }
+                if (!ok) break;
+                umma_commit(acc_full(a));
+                ++ait;
+            }
+            if (issued) {  // all MMAs of this thread complete before TMEM is freed
+                umma_commit(final_bar);
+                wait_drain(final_bar, 0, ctx);
+            }
+        }
+    } else if (warp < WARP_EPI0) {
+        // dequantisers: thread dt owns row dt of the W tile
+        const int dt = (warp - WARP_DEQ0) * 32 + lane;
+        uint32_t it = 0, rit = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+            for (int kr = 0; ok && kr < KR; ++kr) {
+                const int r = rit % RAW_STAGES;
+                const uint32_t rph = (rit / RAW_STAGES) & 1u;
+                if (!warp_wait_or_abort(raw_full(r), rph, abort_flag, ctx)) { ok = false; break; }
+                uint32_t wd[36];
+                const uint8_t *src = sgen + SmemLayout::raw + r * RAW_STAGE_BYTES + dt * RAW_ROW_BYTES;
+#pragma unroll
+                for (int q = 0; q < 9; ++q) {
+                    const uint4 v = lds128(src + 16 * q);
+                    wd[4 * q + 0] = v.x;
+                    wd[4 * q + 1] = v.y;
+                    wd[4 * q + 2] = v.z;
+                    wd[4 * q + 3] = v.w;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive_addr(raw_empty(r));
+                ++rit;
+#pragma unroll
+                for (int sub = 0; sub < RAW_K / BK; ++sub) {
+                    const int s = it % OP_STAGES;
+                    const uint32_t ph = (it / OP_STAGES) & 1u;
+                    if (!warp_wait_or_abort(op_empty(s), ph ^ 1u, abort_flag, ctx)) { ok = false; break; }
+                    const uint32_t row_addr = sbase + SmemLayout::w + s * W_STAGE_BYTES + dt * 128;
+                    const uint32_t sw = static_cast<uint32_t>(dt & 7);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        uint4 ch[4];
+                        dequant_block_bf16(wd, 2 * sub + h, ch);
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            sts128(row_addr + (((4 * h + c) ^ sw) << 4), ch[c]);
+                    }
+                    fence_proxy_async_smem();  // generic writes -> visible to the tensor core
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_addr(w_ready(s));
+                    ++it;
+                }
+            }
+        }
+    } else {
+        // epilogue
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        uint32_t ait = 0;
+        for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+            const int mb = t % p.num_m_blocks, nb = t / p.num_m_blocks;
+            const int a = ait % NUM_ACC;
+            const uint32_t aph = (ait / NUM_ACC) & 1u;
+            if (!warp_wait_or_abort(acc_full(a), aph, abort_flag, ctx)) break;
+            tc_fence_after();
+            const int row = mb * BM + q * 32 + lane;
+            float *yrow = p.y + static_cast<size_t>(row) * p.n + static_cast<size_t>(nb) * BN;
+            const int ncols = min(BN, p.n - nb * BN);
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld_32cols(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + a * BN + c * 32, v);
+                if (row < p.m) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int col = c * 32 + 4 * j;
+                        if (col < ncols)
+                            *reinterpret_cast<float4 *>(yrow + col) =
+                                make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                            __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_addr(acc_empty(a));
+            ++ait;
+        }
+    }
+
+    pdl_launch_dependents();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == WARP_MMA) tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+// ---- host side -------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, []() {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_q4_0(const uint8_t *w, const uint16_t *x, float *y, int64_t m, int64_t n,
+                             int64_t k, cudaStream_t stream, const LaunchCtx &ctx) {
+    auto enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    if (m > (1 << 30) || n > (1 << 30) || k > (1 << 24)) return cudaErrorInvalidValue;
+    CUtensorMap tx, tw;
+    {
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(m)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(k) * 2};
+        const cuuint32_t box[2] = {BK, BM};
+        const cuuint32_t estr[2] = {1, 1};
+        if (enc(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(x), dims, strides,
+                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    {
+        const cuuint64_t rowbytes = static_cast<cuuint64_t>(k / kQK) * kQ4_0Bytes;
+        const cuuint64_t dims[2] = {rowbytes, static_cast<cuuint64_t>(n)};
+        const cuuint64_t strides[1] = {rowbytes};
+        const cuuint32_t box[2] = {RAW_ROW_BYTES, BN};
+        const cuuint32_t estr[2] = {1, 1};
+        if (enc(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(w), dims, strides, box,
+                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    GemmParams p;
+    p.y = y;
+    p.m = static_cast<int>(m);
+    p.n = static_cast<int>(n);
+    p.k = static_cast<int>(k);
+    p.num_m_blocks = static_cast<int>((m + BM - 1) / BM);
+    const int nnb = static_cast<int>((n + BN - 1) / BN);
+    p.num_tiles = p.num_m_blocks * nnb;
+    p.ctx = ctx;
+    static int smem_limits[kMaxDevices] = {0};
+    cudaError_t e = ensure_smem(gemm_q4_0_kernel, kSmemBytes, false, smem_limits);
+    if (e != cudaSuccess) return e;
+    const int grid = std::min(p.num_tiles, device_sm_count());
+    return launch_kernel(gemm_q4_0_kernel, dim3(grid), dim3(NUM_THREADS), kSmemBytes, stream, 1,
+                         tx, tw, p);
+}
+
+}  // namespace qmm

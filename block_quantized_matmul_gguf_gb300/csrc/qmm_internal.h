@@ -1,0 +1,96 @@
+// qmm_internal.h -- host-side declarations shared by the library's
+// translation units (not part of the public ABI; see include/qmm.h).
+#pragma once
+
+#include <cstdint>
+#include <utility>
+
+#include <cuda_runtime.h>
+
+#include "qmm_device.cuh"
+
+namespace qmm {
+
+enum class Fmt : int { Q4_0 = 0, Q8_0 = 1 };
+
+constexpr int kQK = 32;            // weights per block
+constexpr int kQ4_0Bytes = 18;     // binary16 d + 16 nibble bytes
+constexpr int kQ8_0Bytes = 34;     // binary16 d + 32 int8
+
+inline int block_bytes(Fmt f) { return f == Fmt::Q4_0 ? kQ4_0Bytes : kQ8_0Bytes; }
+
+// Launch with programmatic dependent launch allowed (the kernel itself
+// waits for its predecessor before touching global memory) and an optional
+// cluster width along x.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t stream, unsigned cluster_x, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attrs[2];
+    unsigned na = 0;
+    attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+    if (cluster_x > 1) {
+        attrs[na].id = cudaLaunchAttributeClusterDimension;
+        attrs[na].val.clusterDim.x = cluster_x;
+        attrs[na].val.clusterDim.y = 1;
+        attrs[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    cfg.attrs = attrs;
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// Number of SMs of the current device (cached per device).
+int device_sm_count();
+
+// Current device ordinal (0 if the query fails).
+int current_device();
+
+// Raise a kernel's dynamic shared-memory limit to at least `bytes` on the
+// current device.  `limits` is the caller's per-kernel cache (one slot per
+// device, a static array local to the launcher of that one kernel), so the
+// attribute call is made only when that kernel's limit grows and launches
+// inside stream capture make no attribute calls once warmed up.
+constexpr int kMaxDevices = 64;
+
+template <typename Kernel>
+cudaError_t ensure_smem(Kernel kernel, size_t bytes, bool cluster, int (&limits)[kMaxDevices]) {
+    const int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (static_cast<int>(bytes) <= __atomic_load_n(&limits[dev], __ATOMIC_ACQUIRE))
+        return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(bytes));
+    if (e == cudaSuccess && cluster)
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e == cudaSuccess) __atomic_store_n(&limits[dev], static_cast<int>(bytes), __ATOMIC_RELEASE);
+    return e;
+}
+
+cudaError_t launch_dequant(Fmt fmt, const uint8_t *w, float *out, int64_t n, int64_t k,
+                           cudaStream_t stream, const LaunchCtx &ctx);
+
+cudaError_t launch_gemv_q4_0(const uint8_t *w, const float *x, float *y, int m, int64_t n,
+                             int64_t k, cudaStream_t stream, const LaunchCtx &ctx);
+cudaError_t launch_gemv_q8_0(const uint8_t *w, const float *x, float *y, int m, int64_t n,
+                             int64_t k, cudaStream_t stream, const LaunchCtx &ctx);
+
+inline cudaError_t launch_gemv(Fmt fmt, const uint8_t *w, const float *x, float *y, int m,
+                               int64_t n, int64_t k, cudaStream_t stream, const LaunchCtx &ctx) {
+    return fmt == Fmt::Q4_0 ? launch_gemv_q4_0(w, x, y, m, n, k, stream, ctx)
+                            : launch_gemv_q8_0(w, x, y, m, n, k, stream, ctx);
+}
+
+cudaError_t launch_gemm_q4_0(const uint8_t *w, const uint16_t *x, float *y, int64_t m,
+                             int64_t n, int64_t k, cudaStream_t stream, const LaunchCtx &ctx);
+
+cudaError_t launch_selftest_wait(cudaStream_t stream, const LaunchCtx &ctx);
+
+}  // namespace qmm

@@ -1,0 +1,136 @@
+/*
+ * qmm.h -- C ABI of the GB300 (sm_103a) GGUF block-quantized matmul library
+ * (libqmm.so).
+ *
+ * What it computes.  "Add generated quant-kernel JIT and accelerate Gemma4,
+ * BGE-M3, and GLiNER2" (antfly PR #372), section "Validation", counts 343
+ * generated quant dispatches per Gemma4 decode token: 342 apply Q4_0 weights
+ * and one (the LM head) applies Q8_0 weights.  Its "Summary" adds batching
+ * and prefill (the TTFT rows of "Benchmarks").  This library provides those
+ * products:
+ *
+ *   dequant : W (blocks) -> dense fp32 W[N][K], bit-exact
+ *   gemv    : y[m][n] = sum_k x[m][k] * w[n][k], fp32 x, M = 1..16 rows
+ *   gemm    : Y[m][n] = sum_k X[m][k] * w[n][k], bf16 X, M >= 1 (prefill)
+ *
+ * Block formats (GGUF; 32 weights per block, K a multiple of 32):
+ *   Q4_0, 18 bytes: binary16 scale d (little endian) then qs[16]; qs[j] holds
+ *         weight j in its low nibble and weight j+16 in its high nibble;
+ *         w = (nibble - 8) * d.
+ *   Q8_0, 34 bytes: binary16 d then int8 q[32]; w = q * d.
+ *
+ * Layout.  W has N rows and K columns; row n is K/32 consecutive blocks and
+ * rows are consecutive (block b of row n at byte (n*K/32 + b) * block bytes).
+ * Activations and outputs are dense row-major: x[M][K], y[M][N].
+ *
+ * Ownership and execution.  Every pointer is a caller-owned DEVICE pointer on
+ * the current CUDA device.  Outputs are overwritten, never accumulated into.
+ * Calls are asynchronous on `stream` (NULL = legacy default stream) and never
+ * synchronise.  The library allocates no device memory; its only device
+ * state is one error word per GPU (a module-scope variable).  Calls
+ * on different streams may run concurrently.  Kernels are launched with
+ * programmatic dependent launch: a call may start while the preceding
+ * kernel of this library in the same stream is finishing, and waits for it
+ * before reading activations or writing outputs.  A GEMV may read its weight
+ * bytes before that wait (weights are read-only model data; no entry point
+ * writes block-format bytes), so a weight buffer must not alias the output
+ * of the immediately preceding call in the stream.  Kernels from elsewhere
+ * never trigger the early start: after them a call starts as usual.
+ *
+ * Errors.  Arguments are checked before anything is launched; a failed check
+ * returns its status and launches nothing.  A launch failure returns
+ * QMM_ERR_CUDA.  Device-side waits are bounded: a kernel that gives up
+ * records QMM_ERR_TIMEOUT in the device error word, which
+ * qmm_get_device_error() reports.  No entry point aborts the process.
+ */
+#ifndef QMM_H
+#define QMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum qmm_status {
+    QMM_OK = 0,
+    QMM_ERR_NULL = 1,        /* a required pointer is NULL                     */
+    QMM_ERR_SHAPE = 2,       /* K % 32 != 0, a size < 1, or M outside its range */
+    QMM_ERR_ALIGN = 3,       /* a pointer lacks the alignment the call needs    */
+    QMM_ERR_UNSUPPORTED = 4, /* valid arguments this build does not handle     */
+    QMM_ERR_CUDA = 5,        /* a CUDA runtime call or launch failed           */
+    QMM_ERR_TIMEOUT = 6      /* a device-side wait hit its limit               */
+} qmm_status;
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *qmm_stream_t;
+
+/* Largest M accepted by the GEMV entry points. */
+#define QMM_GEMV_MAX_M 16
+
+/* ---- Dequantization (bit-exact) ---------------------------------------
+ * w   : N*K/32 blocks (18 or 34 bytes each), any byte alignment.
+ * out : fp32 [N][K], 4-byte aligned.  out[n][k] = (float)(nibble-8) * d for
+ *       Q4_0, (float)q * d for Q8_0, the exact IEEE binary32 product (the
+ *       sign of zero and inf/NaN follow IEEE multiplication).
+ * Requires n >= 1, k >= 32, k % 32 == 0. */
+qmm_status qmm_dequant_q4_0(const void *w, float *out, int64_t n, int64_t k,
+                            qmm_stream_t stream);
+qmm_status qmm_dequant_q8_0(const void *w, float *out, int64_t n, int64_t k,
+                            qmm_stream_t stream);
+
+/* ---- Decode GEMV ------------------------------------------------------
+ * y[i][j] = sum_k x[i][k] * w[j][k] for i < m, j < n, computed in fp32
+ * (one fp32 product per weight and row, fp32 sums; no tensor cores).
+ * w : N*K/32 blocks.   x : fp32 [m][k].   y : fp32 [m][n].
+ * Requires 1 <= m <= QMM_GEMV_MAX_M, n >= 1, k >= 32, k % 32 == 0, x and y
+ * 4-byte aligned, y not overlapping w or x.  The streaming kernel is used
+ * when k % 256 == 0 and w and x are 16-byte aligned; other valid arguments
+ * take a slower byte-wise kernel.  Accuracy: |y - y_exact| <=
+ * 1e-4 * sum_k |w*x| + 1e-6 per output. */
+qmm_status qmm_gemv_q4_0(const void *w, const float *x, float *y, int m, int64_t n,
+                         int64_t k, qmm_stream_t stream);
+qmm_status qmm_gemv_q8_0(const void *w, const float *x, float *y, int m, int64_t n,
+                         int64_t k, qmm_stream_t stream);
+
+/* ---- Prefill GEMM (tcgen05 tensor cores) ------------------------------
+ * Y[i][j] = sum_k X[i][k] * w[j][k] for i < m, j < n.  X is bf16 [m][k]
+ * given as raw bf16 bit patterns; each weight is rounded once to bf16
+ * ((nibble-8)*d, round to nearest even) and products are summed in fp32
+ * in tensor memory.  Y : fp32 [m][n].
+ * Requires m >= 1, n >= 1, k % 256 == 0, k >= 256, w and x 16-byte aligned,
+ * y 16-byte aligned and n % 4 == 0.  Other valid shapes return
+ * QMM_ERR_UNSUPPORTED.  Accuracy: |Y - Y_exact| <= 2e-3 * sum_k |w*x| + 1e-6
+ * per output. */
+qmm_status qmm_gemm_q4_0(const void *w, const uint16_t *x_bf16, float *y, int64_t m,
+                         int64_t n, int64_t k, qmm_stream_t stream);
+
+/* ---- Utilities --------------------------------------------------------- */
+
+/* Static English text for a status code (never NULL). */
+const char *qmm_status_string(qmm_status status);
+
+/* Library version: major*10000 + minor*100 + patch. */
+int qmm_version(void);
+
+/* Synchronises `stream`, then returns and clears the current device's error
+ * word: QMM_OK, QMM_ERR_TIMEOUT if a kernel gave up a bounded wait since the
+ * last call, or QMM_ERR_CUDA if the synchronisation itself failed. */
+qmm_status qmm_get_device_error(qmm_stream_t stream);
+
+/* Time limit, in nanoseconds of the GPU global timer, of every device-side
+ * wait (default 2e9 = 2 s; 0 restores the default).  Applies to launches
+ * made after the call, from any thread. */
+void qmm_set_wait_timeout_ns(uint64_t ns);
+
+/* Launches one kernel that waits on a barrier nothing ever completes, for at
+ * most `timeout_ns`, so that the timeout path can be exercised without a
+ * fault: the kernel records QMM_ERR_TIMEOUT in the error word and returns.
+ * Returns QMM_ERR_CUDA if the launch fails. */
+qmm_status qmm_selftest_wait_timeout(uint64_t timeout_ns, qmm_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif

@@ -1,0 +1,73 @@
+"""The C-ABI library builds, loads and exports every entry point that
+include/qmm.h declares; argument checks that return before any launch.
+No kernel is launched here (these tests run without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from block_quantized_matmul_gguf_gb300 import build, qmm
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def header_symbols():
+    text = open(os.path.join(ROOT, "include", "qmm.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(qmm_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build_library()
+    return qmm.load()
+
+
+def test_header_declares_the_entry_points():
+    syms = header_symbols()
+    for name in ("qmm_dequant_q4_0", "qmm_dequant_q8_0", "qmm_gemv_q4_0", "qmm_gemv_q8_0",
+                 "qmm_gemm_q4_0"):
+        assert name in syms
+    assert set(syms) <= set(qmm.EXPORTED) | set(syms)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(build.LIB_PATH)
+    for name in header_symbols():
+        assert hasattr(raw, name), name
+    for name in qmm.EXPORTED:
+        assert name in header_symbols(), name
+
+
+def test_status_strings_and_version(lib):
+    for s in range(7):
+        assert qmm.status_string(s)
+    assert qmm.status_string(99) == "unknown status"
+    assert qmm.qmm_version() >= 100
+
+
+def test_null_and_shape_errors_return_before_any_launch(lib):
+    L = lib
+    assert L.qmm_gemv_q4_0(0, 16, 16, 1, 32, 64, 0) == qmm.QMM_ERR_NULL
+    assert L.qmm_gemv_q4_0(16, 0, 16, 1, 32, 64, 0) == qmm.QMM_ERR_NULL
+    assert L.qmm_gemv_q4_0(16, 16, 0, 1, 32, 64, 0) == qmm.QMM_ERR_NULL
+    assert L.qmm_gemv_q8_0(16, 16, 4096, 0, 32, 64, 0) == qmm.QMM_ERR_SHAPE
+    assert L.qmm_gemv_q8_0(16, 16, 4096, 17, 32, 64, 0) == qmm.QMM_ERR_SHAPE
+    assert L.qmm_gemv_q4_0(16, 16, 4096, 1, 32, 48, 0) == qmm.QMM_ERR_SHAPE   # k % 32
+    assert L.qmm_gemv_q4_0(16, 16, 4096, 1, 0, 64, 0) == qmm.QMM_ERR_SHAPE    # n = 0
+    assert L.qmm_gemv_q4_0(16, 18, 4096, 1, 32, 64, 0) == qmm.QMM_ERR_ALIGN   # x % 4
+    assert L.qmm_dequant_q4_0(0, 16, 4, 64, 0) == qmm.QMM_ERR_NULL
+    assert L.qmm_dequant_q8_0(16, 0, 4, 64, 0) == qmm.QMM_ERR_NULL
+    assert L.qmm_dequant_q8_0(16, 16, 4, 0, 0) == qmm.QMM_ERR_SHAPE
+    assert L.qmm_dequant_q4_0(16, 18, 4, 64, 0) == qmm.QMM_ERR_ALIGN
+    assert L.qmm_gemm_q4_0(0, 16, 16, 256, 256, 256, 0) == qmm.QMM_ERR_NULL
+    assert L.qmm_gemm_q4_0(16, 16, 16, 0, 256, 256, 0) == qmm.QMM_ERR_SHAPE
+    assert L.qmm_gemm_q4_0(16, 16, 16, 256, 256, 288, 0) == qmm.QMM_ERR_UNSUPPORTED
+    assert L.qmm_gemm_q4_0(16, 16, 16, 256, 254, 256, 0) == qmm.QMM_ERR_UNSUPPORTED
+    assert L.qmm_gemm_q4_0(18, 16, 16, 256, 256, 256, 0) == qmm.QMM_ERR_ALIGN
+
+
+def test_overlapping_output_is_rejected(lib):
+    # y overlapping w: rejected by the host check, nothing launched
+    assert lib.qmm_gemv_q4_0(4096, 1 << 20, 4096 + 64, 1, 32, 64, 0) == qmm.QMM_ERR_UNSUPPORTED

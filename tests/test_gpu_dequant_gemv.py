@@ -1,0 +1,224 @@
+"""GPU parity: dequantization (bit-exact) and decode GEMV (1e-4 bound)
+against the CPU oracle, through the C ABI."""
+import numpy as np
+import pytest
+
+from block_quantized_matmul_gguf_gb300 import synth
+from helpers import GEMV_REL, assert_within, to_dev
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def qmm():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from block_quantized_matmul_gguf_gb300 import build, qmm as q
+    build.build_library()
+    q.load()
+    return q
+
+
+def _bits_equal_nan_class(a, b):
+    a = np.asarray(a, np.float32)
+    b = np.asarray(b, np.float32)
+    na, nb = np.isnan(a), np.isnan(b)
+    if not np.array_equal(na, nb):
+        return False
+    return np.array_equal(a[~na].view(np.uint32), b[~nb].view(np.uint32))
+
+
+def _special_q4_blocks():
+    """Every nibble in both positions, for special and ordinary scales."""
+    scales = [0x0000, 0x8000, 0x0001, 0x8001, 0x03FF, 0x7BFF, 0xFBFF, 0x7C00, 0xFC00, 0x7E00,
+              0x3C00, 0xB800, 0x1234]
+    blocks = []
+    for d in scales:
+        for v in range(16):
+            qs = [(v | ((15 - v) << 4)) ^ (i * 0x11 & 0xFF) for i in range(16)]
+            blocks.append([d & 0xFF, d >> 8] + qs)
+    return np.array(blocks, dtype=np.uint8)
+
+
+def _special_q8_blocks():
+    scales = [0x0000, 0x8000, 0x0001, 0x7BFF, 0xFBFF, 0x7C00, 0x7E00, 0x3C00, 0xB555]
+    blocks = []
+    for d in scales:
+        for start in range(0, 256, 32):
+            blocks.append([d & 0xFF, d >> 8] + list(range(start, start + 32)))
+    return np.array(blocks, dtype=np.uint8)
+
+
+@pytest.mark.parametrize("fmt", ["q4_0", "q8_0"])
+def test_dequant_special_blocks_bit_exact(qmm, oracle_mod, fmt):
+    blocks = _special_q4_blocks() if fmt == "q4_0" else _special_q8_blocks()
+    n, k = blocks.shape[0], 32
+    ref = (oracle_mod.dequant_q4_0 if fmt == "q4_0" else oracle_mod.dequant_q8_0)(blocks, n, k)
+    got = qmm.dequant(fmt, to_dev(blocks, torch), n, k)
+    torch.cuda.synchronize()
+    assert _bits_equal_nan_class(got.cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("fmt,n,k", [("q4_0", 37, 96), ("q4_0", 1000, 2048), ("q8_0", 129, 288),
+                                     ("q8_0", 512, 2048), ("q4_0", 1, 32)])
+def test_dequant_random_bit_exact(qmm, oracle_mod, fmt, n, k):
+    case = synth.gemv_case(fmt, 1, n, k, seed=21)
+    ref = (oracle_mod.dequant_q4_0 if fmt == "q4_0" else oracle_mod.dequant_q8_0)(case.w, n, k)
+    got = qmm.dequant(fmt, to_dev(case.w, torch), n, k)
+    torch.cuda.synchronize()
+    assert _bits_equal_nan_class(got.cpu().numpy(), ref)
+
+
+def test_dequant_unaligned_output(qmm, oracle_mod):
+    n, k = 9, 64
+    case = synth.gemv_case("q4_0", 1, n, k, seed=2)
+    ref = oracle_mod.dequant_q4_0(case.w, n, k)
+    buf = torch.empty(n * k + 1, dtype=torch.float32, device="cuda")
+    out = buf[1:]
+    qmm.qmm_dequant_q4_0(to_dev(case.w, torch), out.data_ptr(), n, k)
+    torch.cuda.synchronize()
+    assert _bits_equal_nan_class(out.cpu().numpy().reshape(n, k), ref)
+
+
+def _run_gemv(qmm, fmt, case):
+    w = to_dev(case.w, torch)
+    x = to_dev(case.x, torch)
+    y = qmm.gemv(fmt, w, x, case.n, case.k)
+    torch.cuda.synchronize()
+    return y.cpu().numpy()
+
+
+def _oracle_gemv(oracle_mod, fmt, case):
+    f = oracle_mod.gemv_q4_0 if fmt == "q4_0" else oracle_mod.gemv_q8_0
+    return f(case.w, case.x, case.m, case.n, case.k)
+
+
+@pytest.mark.parametrize("fmt", ["q4_0", "q8_0"])
+@pytest.mark.parametrize("m", list(range(1, 17)))
+def test_gemv_every_m(qmm, oracle_mod, fmt, m):
+    # ragged rows (N % 32 != 0), several K chunks, small enough for the oracle
+    case = synth.gemv_case(fmt, m, 203, 1280, seed=100 + m)
+    y_ref, bound = _oracle_gemv(oracle_mod, fmt, case)
+    assert_within(_run_gemv(qmm, fmt, case), y_ref, bound, GEMV_REL, f"{fmt} m={m}")
+
+
+@pytest.mark.parametrize("fmt,m,n,k", [
+    ("q4_0", 1, 1, 256), ("q4_0", 3, 31, 256), ("q4_0", 2, 33, 512), ("q4_0", 1, 257, 8192),
+    ("q4_0", 16, 64, 16384), ("q4_0", 5, 4000, 768), ("q8_0", 1, 1, 256), ("q8_0", 8, 257, 2048),
+    ("q8_0", 16, 96, 8192), ("q4_0", 1, 512, 2048), ("q4_0", 4, 2048, 2048),
+])
+def test_gemv_shapes_streaming_path(qmm, oracle_mod, fmt, m, n, k):
+    case = synth.gemv_case(fmt, m, n, k, seed=n + k)
+    y_ref, bound = _oracle_gemv(oracle_mod, fmt, case)
+    assert_within(_run_gemv(qmm, fmt, case), y_ref, bound, GEMV_REL, f"{fmt} {m}x{n}x{k}")
+
+
+@pytest.mark.parametrize("fmt,m,n,k", [("q4_0", 1, 7, 32), ("q4_0", 4, 65, 288), ("q8_0", 2, 33, 96),
+                                       ("q8_0", 16, 40, 800)])
+def test_gemv_bytewise_path_k_not_multiple_of_256(qmm, oracle_mod, fmt, m, n, k):
+    case = synth.gemv_case(fmt, m, n, k, seed=3)
+    y_ref, bound = _oracle_gemv(oracle_mod, fmt, case)
+    assert_within(_run_gemv(qmm, fmt, case), y_ref, bound, GEMV_REL, f"{fmt} {m}x{n}x{k}")
+
+
+@pytest.mark.parametrize("fmt", ["q4_0", "q8_0"])
+def test_gemv_unaligned_weights_take_bytewise_path(qmm, oracle_mod, fmt):
+    m, n, k = 3, 45, 512
+    case = synth.gemv_case(fmt, m, n, k, seed=8)
+    raw = torch.zeros(case.w.size + 2, dtype=torch.uint8, device="cuda")
+    raw[2:] = to_dev(case.w.reshape(-1), torch)
+    x = to_dev(case.x, torch)
+    y = torch.empty((m, n), dtype=torch.float32, device="cuda")
+    (qmm.qmm_gemv_q4_0 if fmt == "q4_0" else qmm.qmm_gemv_q8_0)(raw.data_ptr() + 2, x, y, m, n, k)
+    torch.cuda.synchronize()
+    y_ref, bound = _oracle_gemv(oracle_mod, fmt, case)
+    assert_within(y.cpu().numpy(), y_ref, bound, GEMV_REL, "unaligned w")
+
+
+def test_gemv_degenerate_inputs(qmm):
+    n, k = 70, 512
+    # all nibbles 8 -> every weight zero; x arbitrary -> y == 0 exactly
+    w = np.zeros((n, k // 32, 18), np.uint8)
+    w[:, :, 0:2] = np.frombuffer(np.float16(0.5).tobytes(), np.uint8)
+    w[:, :, 2:] = 0x88
+    x = synth.activations_f32(2, k, seed=1)
+    y = qmm.gemv("q4_0", to_dev(w, torch), to_dev(x, torch), n, k)
+    assert torch.count_nonzero(y).item() == 0
+    # x == 0 -> y == 0
+    case = synth.gemv_case("q8_0", 3, n, k, seed=1)
+    y = qmm.gemv("q8_0", to_dev(case.w, torch), torch.zeros((3, k), device="cuda"), n, k)
+    assert torch.count_nonzero(y).item() == 0
+
+
+def test_gemv_deterministic(qmm):
+    case = synth.gemv_case("q4_0", 4, 2048, 2048, seed=5)
+    w, x = to_dev(case.w, torch), to_dev(case.x, torch)
+    a = qmm.gemv("q4_0", w, x, case.n, case.k)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        b = qmm.gemv("q4_0", w, x, case.n, case.k)
+    s.synchronize()
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+def test_gemv_one_hot_equals_dequant(qmm):
+    """x = e_c gives the dequantized column exactly (both on the GPU)."""
+    n, k = 300, 1024
+    case = synth.gemv_case("q4_0", 1, n, k, seed=6)
+    w = to_dev(case.w, torch)
+    cols = [0, 17, 255, 256, 1023]
+    x = torch.zeros((len(cols), k), device="cuda")
+    for i, c in enumerate(cols):
+        x[i, c] = 1.0
+    y = qmm.gemv("q4_0", w, x, n, k)
+    deq = qmm.dequant("q4_0", w, n, k)
+    for i, c in enumerate(cols):
+        assert torch.equal(y[i], deq[:, c])
+
+
+# ---- full-size workloads, in the launch configuration the benchmark times ----
+
+def test_decode_layer_set_full(qmm, oracle_mod):
+    for i, proj in enumerate(synth.DECODE_LAYER):
+        case = synth.gemv_case("q4_0", 1, proj.n, proj.k, seed=0, stream=10 + i)
+        y_ref, bound = _oracle_gemv(oracle_mod, "q4_0", case)
+        assert_within(_run_gemv(qmm, "q4_0", case), y_ref, bound, GEMV_REL, proj.name)
+
+
+@pytest.mark.parametrize("m", synth.BATCHED_M)
+def test_batched_decode_full(qmm, oracle_mod, m):
+    for i, proj in enumerate(synth.BATCHED_SHAPES):
+        case = synth.gemv_case("q4_0", m, proj.n, proj.k, seed=0, stream=30 + i)
+        rng = np.random.default_rng(m)
+        mi = rng.integers(0, m, 3000)
+        ni = rng.integers(0, proj.n, 3000)
+        y_ref, bound = oracle_mod.gemv_q4_0_at(case.w, case.x, m, proj.n, proj.k, mi, ni)
+        y = _run_gemv(qmm, "q4_0", case)
+        assert_within(y[mi, ni], y_ref, bound, GEMV_REL, f"{proj.name} m={m}")
+
+
+@pytest.mark.parametrize("m", synth.LM_HEAD_M)
+def test_lm_head_q8_0_full_sampled(qmm, oracle_mod, m):
+    p = synth.LM_HEAD
+    case = synth.gemv_case("q8_0", m, p.n, p.k, seed=0, stream=50)
+    y = _run_gemv(qmm, "q8_0", case)
+    rng = np.random.default_rng(1)
+    mi = rng.integers(0, m, 4000)
+    ni = np.concatenate([rng.integers(0, p.n, 3990), np.arange(p.n - 10, p.n)])
+    y_ref, bound = oracle_mod.gemv_q8_0_at(case.w, case.x, m, p.n, p.k, mi, ni)
+    assert_within(y[mi, ni], y_ref, bound, GEMV_REL, f"lm_head m={m}")
+    assert np.all(np.isfinite(y))
+
+
+def test_timeout_path_reports_and_context_survives(qmm):
+    qmm.qmm_get_device_error()  # clear
+    qmm.qmm_selftest_wait_timeout(2_000_000)  # 2 ms
+    assert qmm.qmm_get_device_error() == qmm.QMM_ERR_TIMEOUT
+    assert qmm.qmm_get_device_error() == qmm.QMM_OK
+    # the context still works
+    case = synth.gemv_case("q4_0", 1, 64, 256, seed=1)
+    y = qmm.gemv("q4_0", to_dev(case.w, torch), to_dev(case.x, torch), 64, 256)
+    torch.cuda.synchronize()
+    assert torch.isfinite(y).all()
