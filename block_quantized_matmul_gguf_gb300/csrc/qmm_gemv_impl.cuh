@@ -75,11 +75,19 @@ __device__ __forceinline__ float mag8(uint32_t v, uint32_t mask, uint32_t magic_
 
 __device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
 
+// Independent FMA chains per output row: at small M the rows alone do not
+// give the scheduler enough independent work, so each block's sum is split.
+template <int M>
+struct Chains {
+    static constexpr int value = M <= 2 ? 4 : (M <= 4 ? 2 : 1);
+};
+
 // One row chunk (8 Q4_0 blocks, 144 bytes at `src`) against the pre-scaled
 // activations `xs` (position 0 of the chunk for row 0; rows XS apart).
 template <int M>
 __device__ __forceinline__ void q4_0_chunk(const uint8_t *src, const float *xs, int XS,
                                            float (&tot)[M]) {
+    constexpr int CH = Chains<M>::value;
     uint32_t wd[36];
 #pragma unroll
     for (int t = 0; t < 9; ++t) {
@@ -106,9 +114,11 @@ __device__ __forceinline__ void q4_0_chunk(const uint8_t *src, const float *xs, 
             for (int i = 0; i < 4; ++i) q[i] = wd[base + 1 + i];
         }
         const float d = half_bits_to_float(dbits);
-        float2 acc[M];
+        float2 acc[M][CH];
 #pragma unroll
-        for (int m = 0; m < M; ++m) acc[m] = f2(0.0f, 0.0f);
+        for (int m = 0; m < M; ++m)
+#pragma unroll
+            for (int c = 0; c < CH; ++c) acc[m][c] = f2(0.0f, 0.0f);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const uint32_t v = q[i], u = v >> 16;
@@ -116,18 +126,24 @@ __device__ __forceinline__ void q4_0_chunk(const uint8_t *src, const float *xs, 
             const float2 p23 = __fadd2_rn(f2(mag(v, 0x000F0000u), mag(u, 0x00000F00u)), c23);
             const float2 p45 = __fadd2_rn(f2(mag(v, 0x000000F0u), mag(v, 0x0000F000u)), c45);
             const float2 p67 = __fadd2_rn(f2(mag(u, 0x000000F0u), mag(u, 0x0000F000u)), c45);
+            const int c = i % CH;
 #pragma unroll
             for (int m = 0; m < M; ++m) {
                 const float4 xa = lds128f(xs + m * XS + 32 * b + 4 * i);
                 const float4 xb = lds128f(xs + m * XS + 32 * b + 16 + 4 * i);
-                acc[m] = __ffma2_rn(p01, f2(xa.x, xa.y), acc[m]);
-                acc[m] = __ffma2_rn(p23, f2(xa.z, xa.w), acc[m]);
-                acc[m] = __ffma2_rn(p45, f2(xb.x, xb.y), acc[m]);
-                acc[m] = __ffma2_rn(p67, f2(xb.z, xb.w), acc[m]);
+                acc[m][c] = __ffma2_rn(p01, f2(xa.x, xa.y), acc[m][c]);
+                acc[m][c] = __ffma2_rn(p23, f2(xa.z, xa.w), acc[m][c]);
+                acc[m][c] = __ffma2_rn(p45, f2(xb.x, xb.y), acc[m][c]);
+                acc[m][c] = __ffma2_rn(p67, f2(xb.z, xb.w), acc[m][c]);
             }
         }
 #pragma unroll
-        for (int m = 0; m < M; ++m) tot[m] = fmaf(d, acc[m].x + acc[m].y, tot[m]);
+        for (int m = 0; m < M; ++m) {
+            float2 a = acc[m][0];
+#pragma unroll
+            for (int c = 1; c < CH; ++c) a = __fadd2_rn(a, acc[m][c]);
+            tot[m] = fmaf(d, a.x + a.y, tot[m]);
+        }
     }
 }
 
@@ -135,6 +151,7 @@ __device__ __forceinline__ void q4_0_chunk(const uint8_t *src, const float *xs, 
 template <int M>
 __device__ __forceinline__ void q8_0_chunk(const uint8_t *src, const float *xs, int XS,
                                            float (&tot)[M]) {
+    constexpr int CH = Chains<M>::value;
     uint32_t wd[68];
 #pragma unroll
     for (int t = 0; t < 17; ++t) {
@@ -159,9 +176,11 @@ __device__ __forceinline__ void q8_0_chunk(const uint8_t *src, const float *xs, 
             for (int i = 0; i < 8; ++i) q[i] = wd[base + 1 + i];
         }
         const float d = half_bits_to_float(dbits);
-        float2 acc[M];
+        float2 acc[M][CH];
 #pragma unroll
-        for (int m = 0; m < M; ++m) acc[m] = f2(0.0f, 0.0f);
+        for (int m = 0; m < M; ++m)
+#pragma unroll
+            for (int h = 0; h < CH; ++h) acc[m][h] = f2(0.0f, 0.0f);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const uint32_t v = q[i], u = v >> 16;
@@ -169,15 +188,21 @@ __device__ __forceinline__ void q8_0_chunk(const uint8_t *src, const float *xs, 
                 f2(mag8(v, 0x000000FFu, kMagic | 0x80u), mag8(v, 0x0000FF00u, kMagic | 0x8000u)), c);
             const float2 p23 = __fadd2_rn(
                 f2(mag8(u, 0x000000FFu, kMagic | 0x80u), mag8(u, 0x0000FF00u, kMagic | 0x8000u)), c);
+            const int h = i % CH;
 #pragma unroll
             for (int m = 0; m < M; ++m) {
                 const float4 xa = lds128f(xs + m * XS + 32 * b + 4 * i);
-                acc[m] = __ffma2_rn(p01, f2(xa.x, xa.y), acc[m]);
-                acc[m] = __ffma2_rn(p23, f2(xa.z, xa.w), acc[m]);
+                acc[m][h] = __ffma2_rn(p01, f2(xa.x, xa.y), acc[m][h]);
+                acc[m][h] = __ffma2_rn(p23, f2(xa.z, xa.w), acc[m][h]);
             }
         }
 #pragma unroll
-        for (int m = 0; m < M; ++m) tot[m] = fmaf(d, acc[m].x + acc[m].y, tot[m]);
+        for (int m = 0; m < M; ++m) {
+            float2 a = acc[m][0];
+#pragma unroll
+            for (int h = 1; h < CH; ++h) a = __fadd2_rn(a, acc[m][h]);
+            tot[m] = fmaf(d, a.x + a.y, tot[m]);
+        }
     }
 }
 
@@ -211,62 +236,63 @@ struct StreamParams {
     float *y;
     int n;            // rows of W
     int k;            // columns (multiple of 256)
-    int nw;           // warps per CTA
     int stages;       // ring depth per warp
-    int cpc;          // chunks per CTA (K range of one cluster rank)
+    int cpc;          // chunks per CTA (the K range of one cluster rank)
     int xs_chunks;    // chunks per activation slice
     LaunchCtx ctx;
 };
 
+// Grid: blockIdx.x = group * ksplit + rank, with a cluster of ksplit CTAs
+// along x.  Warp w of group g owns rows (g*nw + w)*32 .. +31; cluster rank r
+// owns chunks [r*cpc, (r+1)*cpc) of K.  Every warp streams all chunks of its
+// CTA's K range for its own rows.
 template <Fmt F, int M>
 __global__ void __launch_bounds__(128) gemv_stream_kernel(StreamParams p) {
     constexpr int CB = StreamFmt<F>::kChunkBytes;
     extern __shared__ __align__(128) uint8_t smem[];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
-    const int nw = p.nw, S = p.stages;
+    const int nw = blockDim.x >> 5;
+    const int S = p.stages;
     const uint32_t rank = cluster_ctarank();
     const uint32_t ksplit = cluster_nctarank();
-    const int tile = static_cast<int>(blockIdx.x / ksplit);
-    const int row0 = tile * kRowsPerCta;
+    const int group = static_cast<int>(blockIdx.x / ksplit);
+    const int row0 = (group * nw + warp) * kRowsPerCta;
     const int row = row0 + lane;
     const bool row_ok = row < p.n;
-    const int valid_rows = min(kRowsPerCta, p.n - row0);
+    const int valid_rows = max(0, min(kRowsPerCta, p.n - row0));
     const int XS = p.xs_chunks * kChunkK;
     const size_t rowbytes = static_cast<size_t>(p.k / kChunkK) * CB;
     const int c_begin = static_cast<int>(rank) * p.cpc;
+    const int cpc = p.cpc;
 
-    // shared memory: ring | xs | red | part | barriers
-    uint8_t *ring = smem;
-    float *xs = reinterpret_cast<float *>(ring + static_cast<size_t>(nw) * S * kRowsPerCta * CB);
-    float *red = xs + M * XS;
-    float *part = red + nw * M * kRowsPerCta;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(part + M * kRowsPerCta);
+    // shared memory: ring [nw][S][32 rows][CB] | xs [M][XS] | part [nw][M][32] | bars [nw][S]
+    uint8_t *my_ring = smem + static_cast<size_t>(warp) * S * kRowsPerCta * CB;
+    float *xs = reinterpret_cast<float *>(smem + static_cast<size_t>(nw) * S * kRowsPerCta * CB);
+    float *part = xs + M * XS;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(part + nw * M * kRowsPerCta);
+    uint64_t *my_bars = bars + warp * S;
 
     if (lane == 0)
-        for (int s = 0; s < S; ++s) mbar_init(&bars[warp * S + s], 1);
+        for (int s = 0; s < S; ++s) mbar_init(&my_bars[s], 1);
     fence_mbar_init();
     __syncthreads();
 
-    const int nmine = warp < p.cpc ? (p.cpc - warp + nw - 1) / nw : 0;
-    uint8_t *my_ring = ring + static_cast<size_t>(warp) * S * kRowsPerCta * CB;
-    const uint8_t *my_src = p.w + static_cast<size_t>(row_ok ? row : row0) * rowbytes;
-
-    auto issue = [&](int i) {
-        const int c = c_begin + warp + i * nw;
+    const uint8_t *my_src = p.w + static_cast<size_t>(row_ok ? row : 0) * rowbytes;
+    auto issue = [&](int i) {  // chunk i of this CTA's K range into stage i % S
         const int st = i % S;
-        if (lane == 0) mbar_arrive_expect_tx(&bars[warp * S + st], valid_rows * CB);
+        if (lane == 0) mbar_arrive_expect_tx(&my_bars[st], valid_rows * CB);
         __syncwarp();
         if (row_ok)
-            bulk_g2s(my_ring + (st * kRowsPerCta + lane) * CB, my_src + static_cast<size_t>(c) * CB,
-                     CB, &bars[warp * S + st]);
+            bulk_g2s(my_ring + (st * kRowsPerCta + lane) * CB,
+                     my_src + static_cast<size_t>(c_begin + i) * CB, CB, &my_bars[st]);
     };
     // The weight prefetch may start before the preceding kernel in the stream
     // has finished (programmatic dependent launch): weights are read-only
     // model data that no kernel of this library writes.  Activations are read
     // and outputs written only after the wait below.
     int issued = 0;
-    for (; issued < min(S, nmine); ++issued) issue(issued);
+    for (; issued < min(S, cpc); ++issued) issue(issued);
     pdl_wait();
     pdl_launch_dependents();
 
@@ -275,18 +301,18 @@ __global__ void __launch_bounds__(128) gemv_stream_kernel(StreamParams p) {
     for (int m = 0; m < M; ++m) tot[m] = 0.0f;
 
     bool failed = false;
-    int i = 0;         // next chunk (sequence index) of this warp
-    int consumed = 0;  // chunks whose copy completed
-    for (int s0 = 0; s0 < p.cpc; s0 += p.xs_chunks) {
-        const int s1 = min(p.cpc, s0 + p.xs_chunks);
-        __syncthreads();  // the previous slice is no longer read
+    int consumed = 0;
+    for (int s0 = 0; s0 < cpc; s0 += p.xs_chunks) {
+        const int s1 = min(cpc, s0 + p.xs_chunks);
+        if (s0 > 0) __syncthreads();  // the previous slice is no longer read
         {
             const int kx0 = (c_begin + s0) * kChunkK;
             const int nk4 = (s1 - s0) * (kChunkK / 4);
             for (int e = threadIdx.x; e < M * nk4; e += nw * 32) {
                 const int m = e / nk4;
                 const int kk = (e - m * nk4) * 4;
-                float4 v = __ldg(reinterpret_cast<const float4 *>(p.x + static_cast<size_t>(m) * p.k + kx0 + kk));
+                float4 v = __ldg(reinterpret_cast<const float4 *>(
+                    p.x + static_cast<size_t>(m) * p.k + kx0 + kk));
                 const int j = (kx0 + kk) & 31;
                 if constexpr (F == Fmt::Q4_0) {
                     v.x *= __int_as_float((127 - q4_0_shift(j + 0)) << 23);
@@ -301,55 +327,57 @@ __global__ void __launch_bounds__(128) gemv_stream_kernel(StreamParams p) {
             }
         }
         __syncthreads();
-        while (i < nmine && warp + i * nw < s1) {
+        for (int i = s0; i < s1; ++i) {
+            if (valid_rows == 0 || failed) continue;  // warp-uniform
             const int st = i % S;
             const uint32_t par = static_cast<uint32_t>(i / S) & 1u;
-            if (!failed && !mbar_wait(&bars[warp * S + st], par, p.ctx)) failed = true;
-            if (!failed) {
-                ++consumed;
-                const uint8_t *src = my_ring + (st * kRowsPerCta + lane) * CB;
-                const float *xc = xs + (warp + i * nw - s0) * kChunkK;
-                if constexpr (F == Fmt::Q4_0)
-                    q4_0_chunk<M>(src, xc, XS, tot);
-                else
-                    q8_0_chunk<M>(src, xc, XS, tot);
-                __syncwarp();
-                if (issued < nmine) {
-                    fence_proxy_async_smem();
-                    issue(issued);
-                    ++issued;
-                }
+            if (!mbar_wait(&my_bars[st], par, p.ctx)) {
+                failed = true;
+                continue;
             }
-            ++i;
+            ++consumed;
+            const uint8_t *src = my_ring + (st * kRowsPerCta + lane) * CB;
+            const float *xc = xs + (i - s0) * kChunkK;
+            if constexpr (F == Fmt::Q4_0)
+                q4_0_chunk<M>(src, xc, XS, tot);
+            else
+                q8_0_chunk<M>(src, xc, XS, tot);
+            __syncwarp();
+            if (issued < cpc) {
+                fence_proxy_async_smem();
+                issue(issued);
+                ++issued;
+            }
         }
     }
     if (failed) {
         // Let copies still in flight land before the CTA's shared memory is
         // released; each wait is again bounded.
         for (int j = consumed; j < issued; ++j)
-            mbar_wait(&bars[warp * S + (j % S)], static_cast<uint32_t>(j / S) & 1u, p.ctx);
+            mbar_wait(&my_bars[j % S], static_cast<uint32_t>(j / S) & 1u, p.ctx);
     }
 
-    // reduce over warps (fixed order), then over cluster ranks (rank order)
+    if (ksplit == 1) {
+        if (row_ok) {
 #pragma unroll
-    for (int m = 0; m < M; ++m) red[(warp * M + m) * kRowsPerCta + lane] = tot[m];
-    __syncthreads();
-    for (int t = threadIdx.x; t < M * kRowsPerCta; t += nw * 32) {
-        const int m = t / kRowsPerCta, r = t % kRowsPerCta;
-        float s = 0.0f;
-        for (int wv = 0; wv < nw; ++wv) s += red[(wv * M + m) * kRowsPerCta + r];
-        part[t] = s;
+            for (int m = 0; m < M; ++m) p.y[static_cast<size_t>(m) * p.n + row] = tot[m];
+        }
+        return;
     }
-    if (ksplit > 1) cluster_sync(); else __syncthreads();
-    if (rank == 0) {
-        for (int t = threadIdx.x; t < M * kRowsPerCta; t += nw * 32) {
-            const int m = t / kRowsPerCta, r = t % kRowsPerCta;
-            float s = part[t];
-            for (uint32_t q = 1; q < ksplit; ++q) s += ld_dsmem_f32(&part[t], q);
-            if (row0 + r < p.n) p.y[static_cast<size_t>(m) * p.n + row0 + r] = s;
+    // partial sums of the cluster's K ranges, added in rank order by rank 0
+    float *my_part = part + warp * M * kRowsPerCta;
+#pragma unroll
+    for (int m = 0; m < M; ++m) my_part[m * kRowsPerCta + lane] = tot[m];
+    cluster_sync();
+    if (rank == 0 && row_ok) {
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+            float s = tot[m];
+            for (uint32_t q = 1; q < ksplit; ++q) s += ld_dsmem_f32(&my_part[m * kRowsPerCta + lane], q);
+            p.y[static_cast<size_t>(m) * p.n + row] = s;
         }
     }
-    if (ksplit > 1) cluster_sync();
+    cluster_sync();  // peers keep their shared memory until rank 0 has read it
 }
 
 // Byte-wise fallback: one warp per row, lanes over blocks.
@@ -396,45 +424,62 @@ __global__ void __launch_bounds__(128) gemv_bytewise_kernel(const uint8_t *__res
     }
 }
 
+// Launch shape.  Units are (32-row tile, K range) pairs; the K dimension is
+// split over a cluster (ksplit CTAs) until there are enough units to give
+// every SM several resident warps, and warps per CTA share one activation
+// slice.  Rings hold only as many stages as a warp has chunks.
+struct StreamShape {
+    int ksplit, nw, stages, cpc, xs_chunks;
+    size_t smem;
+};
+
+template <Fmt F, int M>
+StreamShape stream_shape(int64_t n, int64_t k, int sms) {
+    constexpr int CB = StreamFmt<F>::kChunkBytes;
+    StreamShape sh;
+    const int64_t tiles = (n + kRowsPerCta - 1) / kRowsPerCta;
+    const int C = static_cast<int>(k / kChunkK);
+    const int64_t want_units = 8LL * sms;  // about eight resident row tiles per SM
+    sh.ksplit = 1;
+    while (sh.ksplit < 8 && tiles * sh.ksplit < want_units && C % (2 * sh.ksplit) == 0)
+        sh.ksplit *= 2;
+    sh.cpc = C / sh.ksplit;
+    // several warps per CTA when there are plenty of tiles (they share x')
+    const int64_t units = tiles * sh.ksplit;
+    sh.nw = 1;
+    while (sh.nw < 4 && units / (2 * sh.nw) >= 2LL * sms) sh.nw *= 2;
+    sh.stages = std::min(sh.cpc, F == Fmt::Q4_0 ? 4 : 3);
+    const int xs_budget = 32 * 1024;
+    sh.xs_chunks = std::max(1, std::min(sh.cpc, xs_budget / (M * kChunkK * 4)));
+    sh.smem = static_cast<size_t>(sh.nw) * sh.stages * kRowsPerCta * CB +
+              sizeof(float) * (static_cast<size_t>(M) * sh.xs_chunks * kChunkK +
+                               static_cast<size_t>(sh.nw) * M * kRowsPerCta) +
+              sizeof(uint64_t) * sh.nw * sh.stages;
+    return sh;
+}
+
 template <Fmt F, int M>
 cudaError_t launch_stream(const uint8_t *w, const float *x, float *y, int64_t n, int64_t k,
                           cudaStream_t stream, const LaunchCtx &ctx) {
-    constexpr int CB = StreamFmt<F>::kChunkBytes;
-    const int sms = device_sm_count();
-    const int tiles = static_cast<int>((n + kRowsPerCta - 1) / kRowsPerCta);
-    const int C = static_cast<int>(k / kChunkK);
-    int ksplit = 1;
-    while (ksplit < 8 && static_cast<int64_t>(tiles) * ksplit < 2LL * sms && C % (2 * ksplit) == 0)
-        ksplit *= 2;
-    const int cpc = C / ksplit;
-    const int nw = std::min(4, cpc);
-    const int stages = F == Fmt::Q4_0 ? 4 : 3;
-    const int xs_budget = 64 * 1024;
-    int xs_chunks = std::max(1, xs_budget / (M * kChunkK * 4));
-    xs_chunks = std::min(xs_chunks, cpc);
-    if (xs_chunks > nw) xs_chunks -= xs_chunks % nw;  // whole rounds of the warps per slice
+    const StreamShape sh = stream_shape<F, M>(n, k, device_sm_count());
+    const int64_t tiles = (n + kRowsPerCta - 1) / kRowsPerCta;
+    const int64_t groups = (tiles + sh.nw - 1) / sh.nw;
     StreamParams p;
     p.w = w;
     p.x = x;
     p.y = y;
     p.n = static_cast<int>(n);
     p.k = static_cast<int>(k);
-    p.nw = nw;
-    p.stages = stages;
-    p.cpc = cpc;
-    p.xs_chunks = xs_chunks;
+    p.stages = sh.stages;
+    p.cpc = sh.cpc;
+    p.xs_chunks = sh.xs_chunks;
     p.ctx = ctx;
-    const size_t smem = static_cast<size_t>(nw) * stages * kRowsPerCta * CB +
-                        sizeof(float) * (static_cast<size_t>(M) * xs_chunks * kChunkK +
-                                         static_cast<size_t>(nw) * M * kRowsPerCta +
-                                         M * kRowsPerCta) +
-                        sizeof(uint64_t) * nw * stages;
     auto kern = gemv_stream_kernel<F, M>;
     static int smem_limits[kMaxDevices] = {0};  // this instantiation's own cache
-    const cudaError_t e = ensure_smem(kern, smem, true, smem_limits);
+    const cudaError_t e = ensure_smem(kern, sh.smem, true, smem_limits);
     if (e != cudaSuccess) return e;
-    return launch_kernel(kern, dim3(static_cast<unsigned>(tiles * ksplit)), dim3(nw * 32), smem,
-                         stream, static_cast<unsigned>(ksplit), p);
+    return launch_kernel(kern, dim3(static_cast<unsigned>(groups * sh.ksplit)), dim3(sh.nw * 32),
+                         sh.smem, stream, static_cast<unsigned>(sh.ksplit), p);
 }
 
 template <Fmt F, int M>

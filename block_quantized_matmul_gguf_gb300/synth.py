@@ -208,13 +208,18 @@ class GemvCase:
     meta: dict = field(default_factory=dict)
 
 
-def gemv_case(fmt: str, m: int, n: int, k: int, seed: int = 0, stream: int = 0) -> GemvCase:
-    if fmt == "q4_0":
-        w = q4_0_weights(n, k, seed, 2 * stream)
-    elif fmt == "q8_0":
-        w = q8_0_weights(n, k, seed, 2 * stream)
-    else:
+def gemv_case(fmt: str, m: int, n: int, k: int, seed: int = 0, stream: int = 0,
+              weights: np.ndarray | None = None) -> GemvCase:
+    """Weights and activations of one GEMV problem.  The weights depend only on
+    (fmt, n, k, seed, stream), not on m; pass `weights` to reuse them."""
+    if fmt not in ("q4_0", "q8_0"):
         raise ValueError(fmt)
+    if weights is not None:
+        w = weights
+    elif fmt == "q4_0":
+        w = q4_0_weights(n, k, seed, 2 * stream)
+    else:
+        w = q8_0_weights(n, k, seed, 2 * stream)
     x = activations_f32(m, k, seed, 2 * stream + 1 + (1 << 20))
     return GemvCase(fmt, m, n, k, w, x)
 
