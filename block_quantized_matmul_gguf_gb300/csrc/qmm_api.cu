@@ -3,6 +3,8 @@
 #include "../../include/qmm.h"
 #include "qmm_internal.h"
 
+#include <cudaTypedefs.h>
+
 #include <atomic>
 #include <mutex>
 
@@ -105,6 +107,29 @@ qmm_status gemv(Fmt fmt, const void *w, const float *x, float *y, int m, int64_t
 }
 
 }  // namespace
+
+bool encode_tmap_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *base,
+                    uint64_t inner, uint64_t outer, uint64_t outer_stride_bytes,
+                    uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle) {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, []() {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {outer_stride_bytes};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, dtype, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 int current_device() {
     int dev = 0;

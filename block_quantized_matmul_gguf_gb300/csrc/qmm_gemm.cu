@@ -11,61 +11,64 @@
 // to bf16 (round to nearest even); products are summed in fp32 in tensor
 // memory.
 //
-// Structure (one persistent CTA per SM, 448 threads, warp-specialised):
-//   warp 0      producer: TMA loads of X tiles (128 x 64 bf16, 128-byte
-//               swizzle) and of raw Q4_0 tiles (256 rows x 144 bytes = 8
-//               blocks per row, no swizzle), each tracked by an mbarrier with
-//               a byte count.
-//   warps 2-9   dequantisers: thread t owns W row t of the tile; it reads its
-//               row's 144 raw bytes (conflict-free 16-byte loads), then for
-//               each of the four 64-wide K stages writes 64 bf16 weights into
-//               the B tile in the canonical K-major 128-byte-swizzled layout
-//               (16-byte chunk c of row r at chunk c ^ (r & 7)).
-//   warp 1      MMA issuer: one thread issues tcgen05.mma (M=128, N=256,
-//               K=16, kind::f16, bf16 x bf16 -> fp32) from the two shared-
-//               memory descriptors into one of two TMEM accumulators, and
-//               tcgen05.commit releases stages and hands accumulators over.
-//   warps 10-13 epilogue: tcgen05.ld of the 128 x 256 fp32 accumulator (warp
-//               w reads TMEM lanes 32*(w%4)..+31) and stores to Y; the second
-//               accumulator lets the next tile's MMAs run meanwhile.
+// Structure: persistent CTA pairs (thread-block clusters of 2), one CTA per
+// SM, 448 threads each, warp-specialised.  A pair computes a 256 x 256 tile
+// of Y with tcgen05.mma.cta_group::2 (M=256, N=256, K=16): each CTA holds 128
+// rows of X (the A operand) and 128 dequantised rows of W (its half of the B
+// operand), so each SM dequantises and stages half of B per tile.
+//   warp 0      producer (both CTAs): TMA loads of its X rows (128 x 64 bf16,
+//               128-byte swizzle; completion counted on the leader CTA's
+//               barrier) and of its raw Q4_0 rows (128 rows x 144 bytes).
+//   warps 2-9   dequantisers (both CTAs): thread t owns W row t % 128 and one
+//               of the two 32-weight blocks of each 64-wide K stage; it reads
+//               the row's 144 raw bytes (conflict-free 16-byte loads) and
+//               writes bf16 weights into the B tile in the canonical K-major
+//               128-byte-swizzled layout (16-byte chunk c of row r at chunk
+//               c ^ (r & 7)), then signals the leader.
+//   warp 1      MMA issuer (leader CTA only): one thread issues the pair's
+//               MMAs into one of two TMEM accumulators (2 x 256 columns);
+//               tcgen05.commit multicasts stage releases and accumulator
+//               hand-overs to both CTAs.
+//   warps 10-13 epilogue (both CTAs): tcgen05.ld of the CTA's 128 x 256 fp32
+//               accumulator (warp w reads TMEM lanes 32*(w%4)..+31) and stores
+//               to Y; the second accumulator lets the next tile's MMAs run
+//               meanwhile.
 // Every wait is bounded (GPU global timer).  On a timeout the CTA records the
-// error, sets a shared abort flag that makes every other wait give up at
-// once, lets its own TMA copies and MMAs finish (bounded waits), frees TMEM
-// and exits.
+// error, sets a shared abort flag that makes its other waits give up at once,
+// lets its own TMA copies and MMAs finish (bounded waits), keeps its shared
+// memory until the peer has drained (cluster barrier), frees TMEM and exits.
 #include "qmm_internal.h"
 
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
-#include <mutex>
+#include <algorithm>
 
 namespace qmm {
 namespace {
 
-constexpr int BM = 128;              // tokens per tile (MMA M)
-constexpr int BN = 256;              // weight rows per tile (MMA N)
+constexpr int BM = 128;              // X rows per CTA (MMA M = 2 * BM per pair)
+constexpr int BN = 256;              // W rows per pair tile (MMA N)
+constexpr int BN_CTA = BN / 2;       // W rows each CTA dequantises
 constexpr int BK = 64;               // K per operand stage (one 128-byte swizzle row)
 constexpr int UMMA_K = 16;           // K per tcgen05.mma (kind::f16)
 constexpr int RAW_K = 256;           // K per raw stage (8 Q4_0 blocks)
 constexpr int RAW_ROW_BYTES = 144;   // 8 blocks x 18 bytes
-constexpr int OP_STAGES = 3;
+constexpr int OP_STAGES = 5;
 constexpr int RAW_STAGES = 2;
-constexpr int X_STAGE_BYTES = BM * BK * 2;           // 16 KB
-constexpr int W_STAGE_BYTES = BN * BK * 2;           // 32 KB
-constexpr int RAW_STAGE_BYTES = BN * RAW_ROW_BYTES;  // 36 KB
+constexpr int X_STAGE_BYTES = BM * BK * 2;               // 16 KB
+constexpr int W_STAGE_BYTES = BN_CTA * BK * 2;           // 16 KB
+constexpr int RAW_STAGE_BYTES = BN_CTA * RAW_ROW_BYTES;  // 18 KB
 constexpr int NUM_ACC = 2;
-constexpr uint32_t TMEM_COLS = NUM_ACC * BN;         // 512 fp32 columns
+constexpr uint32_t TMEM_COLS = NUM_ACC * BN;             // 512 fp32 columns
 
 constexpr int WARP_PRODUCER = 0;
 constexpr int WARP_MMA = 1;
 constexpr int WARP_DEQ0 = 2;
-constexpr int NUM_DEQ_WARPS = BN / 32;               // 8
+constexpr int NUM_DEQ_WARPS = 8;                     // two threads per W row
 constexpr int WARP_EPI0 = WARP_DEQ0 + NUM_DEQ_WARPS;  // 10
 constexpr int NUM_EPI_WARPS = 4;
 constexpr int NUM_THREADS = (WARP_EPI0 + NUM_EPI_WARPS) * 32;  // 448
 
-static_assert(BN == NUM_DEQ_WARPS * 32, "one dequantiser thread per W row");
-static_assert(RAW_K % BK == 0, "raw stage covers whole operand stages");
+static_assert(NUM_DEQ_WARPS * 32 == 2 * BN_CTA, "two dequantiser threads per W row");
+static_assert(RAW_K % BK == 0 && BK == 2 * 32, "a K stage is two blocks");
 
 struct SmemLayout {
     static constexpr int x = 0;
@@ -80,12 +83,13 @@ struct SmemLayout {
     static constexpr int total = abort_flag + 4;
 };
 constexpr size_t kSmemBytes = SmemLayout::total + 1024;  // + alignment slack
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 struct GemmParams {
     float *y;
     int m, n, k;
-    int num_m_blocks;
-    int num_tiles;
+    int num_m_blocks;  // of 2*BM rows
+    int num_tiles;     // pair tiles
     LaunchCtx ctx;
 };
 
@@ -99,15 +103,57 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
-__device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem),
-                 "r"(ncols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+// X tile load whose completion is counted on a barrier that may live in the
+// peer CTA of the pair (the leader's).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map, int x,
+                                                 int y, uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster)
+        : "memory");
 }
 
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+// TMEM for the pair: executed by one warp in each CTA of the pair.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t slot_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_barrier() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+                 ::: "memory");
+}
+
+// Address of the same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t local, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx_cluster(uint32_t bar_cluster, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(
+                     bar_cluster),
+                 "r"(bytes)
                  : "memory");
 }
 
@@ -118,18 +164,22 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                          uint32_t idesc, uint32_t accumulate) {
+__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                               uint32_t idesc, uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
-__device__ __forceinline__ void umma_commit(uint32_t bar) {
+// Arrive (once each) on the barrier at this shared-memory offset in both CTAs
+// of the pair when all previously issued MMAs of this thread complete.
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
     asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+        "[%0], %1;" ::"r"(bar),
+        "h"(static_cast<unsigned short>(3))
         : "memory");
 }
 
@@ -159,10 +209,11 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
     return d;
 }
 
-// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major.
+// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major,
+// N = 256, M = 256 (the pair).
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
                             (static_cast<uint32_t>(BN >> 3) << 17) |
-                            (static_cast<uint32_t>(BM >> 4) << 24);
+                            (static_cast<uint32_t>((2 * BM) >> 4) << 24);
 
 __device__ __forceinline__ bool abort_set(const int *flag) {
     return *reinterpret_cast<const volatile int *>(flag) != 0;
@@ -292,23 +343,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const LaunchCtx ctx = p.ctx;
+    const uint32_t rank = cluster_rank();  // 0 = leader of the pair
+    const bool leader = rank == 0;
+    const int pair = static_cast<int>(blockIdx.x >> 1);
+    const int num_pairs = static_cast<int>(gridDim.x >> 1);
 
     auto bar = [&](int i) -> uint32_t { return sbase + SmemLayout::bars + 8u * i; };
-    auto x_full = [&](int s) { return bar(s); };
-    auto w_ready = [&](int s) { return bar(OP_STAGES + s); };
-    auto op_empty = [&](int s) { return bar(2 * OP_STAGES + s); };
+    auto x_full = [&](int s) { return bar(s); };                    // leader: 2 arrivals + bytes
+    auto w_ready = [&](int s) { return bar(OP_STAGES + s); };       // leader: 16 warps
+    auto op_empty = [&](int s) { return bar(2 * OP_STAGES + s); };  // both: MMA commit
     auto raw_full = [&](int r) { return bar(3 * OP_STAGES + r); };
     auto raw_empty = [&](int r) { return bar(3 * OP_STAGES + RAW_STAGES + r); };
-    auto acc_full = [&](int a) { return bar(3 * OP_STAGES + 2 * RAW_STAGES + a); };
-    auto acc_empty = [&](int a) { return bar(3 * OP_STAGES + 2 * RAW_STAGES + NUM_ACC + a); };
+    auto acc_full = [&](int a) { return bar(3 * OP_STAGES + 2 * RAW_STAGES + a); };  // both
+    auto acc_empty = [&](int a) {  // leader: 8 epilogue warps
+        return bar(3 * OP_STAGES + 2 * RAW_STAGES + NUM_ACC + a);
+    };
     const uint32_t final_bar = bar(SmemLayout::nbars - 1);
     int *abort_flag = reinterpret_cast<int *>(sgen + SmemLayout::abort_flag);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sgen + SmemLayout::tmem_slot);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < OP_STAGES; ++s) {
-            mbar_init_addr(x_full(s), 1);
-            mbar_init_addr(w_ready(s), NUM_DEQ_WARPS);
+            mbar_init_addr(x_full(s), 2);
+            mbar_init_addr(w_ready(s), 2 * NUM_DEQ_WARPS);
             mbar_init_addr(op_empty(s), 1);
         }
         for (int r = 0; r < RAW_STAGES; ++r) {
@@ -317,22 +374,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         for (int a = 0; a < NUM_ACC; ++a) {
             mbar_init_addr(acc_full(a), 1);
-            mbar_init_addr(acc_empty(a), NUM_EPI_WARPS);
+            mbar_init_addr(acc_empty(a), 2 * NUM_EPI_WARPS);
         }
         mbar_init_addr(final_bar, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == WARP_MMA) tmem_alloc(sbase + SmemLayout::tmem_slot, TMEM_COLS);
+    if (warp == WARP_MMA) tmem_alloc_pair(sbase + SmemLayout::tmem_slot, TMEM_COLS);
     tc_fence_before();
     __syncthreads();
+    cluster_barrier();  // the peer's barriers exist before anyone signals them
     tc_fence_after();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
 
     pdl_wait();
 
-    const int KB = p.k / BK;             // operand stages per tile
-    const int KR = p.k / RAW_K;          // raw stages per tile
+    const int KB = p.k / BK;     // operand stages per tile
+    const int KR = p.k / RAW_K;  // raw stages per tile
 
     if (warp == WARP_PRODUCER) {
         if (lane == 0) {
@@ -340,8 +398,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_w)) : "memory");
             uint32_t it = 0, rit = 0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+            for (int t = pair; ok && t < p.num_tiles; t += num_pairs) {
                 const int mb = t % p.num_m_blocks, nb = t / p.num_m_blocks;
+                const int xrow = mb * 2 * BM + static_cast<int>(rank) * BM;
+                const int wrow = nb * BN + static_cast<int>(rank) * BN_CTA;
                 for (int kb = 0; ok && kb < KB; ++kb) {
                     if (kb % (RAW_K / BK) == 0) {
                         const int r = rit % RAW_STAGES;
@@ -349,37 +409,41 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         if (!wait_or_abort(raw_empty(r), ph ^ 1u, abort_flag, ctx)) { ok = false; break; }
                         mbar_expect_tx_addr(raw_full(r), RAW_STAGE_BYTES);
                         tma_load_2d(sbase + SmemLayout::raw + r * RAW_STAGE_BYTES, &tmap_w,
-                                    (kb / (RAW_K / BK)) * RAW_ROW_BYTES, nb * BN, raw_full(r));
+                                    (kb / (RAW_K / BK)) * RAW_ROW_BYTES, wrow, raw_full(r));
                         ++rit;
                     }
                     const int s = it % OP_STAGES;
                     const uint32_t ph = (it / OP_STAGES) & 1u;
                     if (!wait_or_abort(op_empty(s), ph ^ 1u, abort_flag, ctx)) { ok = false; break; }
-                    mbar_expect_tx_addr(x_full(s), X_STAGE_BYTES);
-                    tma_load_2d(sbase + SmemLayout::x + s * X_STAGE_BYTES, &tmap_x, kb * BK,
-                                mb * BM, x_full(s));
+                    const uint32_t xf = map_to_rank(x_full(s), 0);
+                    mbar_expect_tx_cluster(xf, X_STAGE_BYTES);
+                    tma_load_2d_pair(sbase + SmemLayout::x + s * X_STAGE_BYTES, &tmap_x, kb * BK, xrow,
+                                     xf);
                     ++it;
                 }
             }
-            // let our own copies land before the CTA may exit
-            for (int s = 0; s < OP_STAGES; ++s) {
-                if (it > static_cast<uint32_t>(s)) {
-                    const uint32_t last = it - 1 - ((it - 1 - s) % OP_STAGES);
-                    wait_drain(x_full(s), (last / OP_STAGES) & 1u, ctx);
-                }
-            }
+            // let our own copies land before the CTA may exit: raw tiles on our
+            // barriers; X tiles either consumed (op_empty) or drained by the leader
             for (int r = 0; r < RAW_STAGES; ++r) {
                 if (rit > static_cast<uint32_t>(r)) {
                     const uint32_t last = rit - 1 - ((rit - 1 - r) % RAW_STAGES);
                     wait_drain(raw_full(r), (last / RAW_STAGES) & 1u, ctx);
                 }
             }
+            if (leader) {
+                for (int s = 0; s < OP_STAGES; ++s) {
+                    if (it > static_cast<uint32_t>(s)) {
+                        const uint32_t last = it - 1 - ((it - 1 - s) % OP_STAGES);
+                        wait_drain(x_full(s), (last / OP_STAGES) & 1u, ctx);
+                    }
+                }
+            }
         }
     } else if (warp == WARP_MMA) {
-        if (lane == 0) {
+        if (leader && lane == 0) {
             uint32_t it = 0, ait = 0;
             bool ok = true, issued = false;
-            for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+            for (int t = pair; ok && t < p.num_tiles; t += num_pairs) {
                 const int a = ait % NUM_ACC;
                 const uint32_t aph = (ait / NUM_ACC) & 1u;
                 if (!wait_or_abort(acc_empty(a), aph ^ 1u, abort_flag, ctx)) break;
@@ -396,34 +460,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                     for (int kk = 0; kk < BK / UMMA_K; ++kk) {
                         // advance 16 bf16 = 32 bytes along K inside the swizzle row
-                        umma_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, kIdesc,
-                                  (kb | kk) != 0 ? 1u : 0u);
+                        umma_bf16_pair(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, kIdesc,
+                                       (kb | kk) != 0 ? 1u : 0u);
                     }
                     issued = true;
-                    umma_commit(op_empty(s));
+                    umma_commit_pair(op_empty(s));
                     ++it;
                 }
                 if (!ok) break;
-                umma_commit(acc_full(a));
+                umma_commit_pair(acc_full(a));
                 ++ait;
             }
-            if (issued) {  // all MMAs of this thread complete before TMEM is freed
-                umma_commit(final_bar);
+            if (issued) {  // all MMAs of the pair complete before TMEM is freed
+                umma_commit_pair(final_bar);
                 wait_drain(final_bar, 0, ctx);
             }
         }
     } else if (warp < WARP_EPI0) {
-        // dequantisers: thread dt owns row dt of the W tile
+        // dequantisers: thread dt owns W row dt % 128, block (2*sub + half) of each K stage
         const int dt = (warp - WARP_DEQ0) * 32 + lane;
+        const int row = dt & (BN_CTA - 1);
+        const int half = dt >> 7;
+        const uint32_t w_ready_leader0 = map_to_rank(w_ready(0), 0);
         uint32_t it = 0, rit = 0;
         bool ok = true;
-        for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+        for (int t = pair; ok && t < p.num_tiles; t += num_pairs) {
             for (int kr = 0; ok && kr < KR; ++kr) {
                 const int r = rit % RAW_STAGES;
                 const uint32_t rph = (rit / RAW_STAGES) & 1u;
                 if (!warp_wait_or_abort(raw_full(r), rph, abort_flag, ctx)) { ok = false; break; }
                 uint32_t wd[36];
-                const uint8_t *src = sgen + SmemLayout::raw + r * RAW_STAGE_BYTES + dt * RAW_ROW_BYTES;
+                const uint8_t *src = sgen + SmemLayout::raw + r * RAW_STAGE_BYTES + row * RAW_ROW_BYTES;
 #pragma unroll
                 for (int q = 0; q < 9; ++q) {
                     const uint4 v = lds128(src + 16 * q);
@@ -440,19 +507,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const int s = it % OP_STAGES;
                     const uint32_t ph = (it / OP_STAGES) & 1u;
                     if (!warp_wait_or_abort(op_empty(s), ph ^ 1u, abort_flag, ctx)) { ok = false; break; }
-                    const uint32_t row_addr = sbase + SmemLayout::w + s * W_STAGE_BYTES + dt * 128;
-                    const uint32_t sw = static_cast<uint32_t>(dt & 7);
+                    const uint32_t row_addr = sbase + SmemLayout::w + s * W_STAGE_BYTES + row * 128;
+                    const uint32_t sw = static_cast<uint32_t>(row & 7);
+                    uint4 ch[4];
+                    // block 2*sub + half of the row chunk: K positions 32*half .. +31
+                    if (half == 0)
+                        dequant_block_bf16(wd, 2 * sub, ch);
+                    else
+                        dequant_block_bf16(wd, 2 * sub + 1, ch);
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        uint4 ch[4];
-                        dequant_block_bf16(wd, 2 * sub + h, ch);
-#pragma unroll
-                        for (int c = 0; c < 4; ++c)
-                            sts128(row_addr + (((4 * h + c) ^ sw) << 4), ch[c]);
-                    }
+                    for (int c = 0; c < 4; ++c)
+                        sts128(row_addr + (((4 * half + c) ^ sw) << 4), ch[c]);
                     fence_proxy_async_smem();  // generic writes -> visible to the tensor core
                     __syncwarp();
-                    if (lane == 0) mbar_arrive_addr(w_ready(s));
+                    if (lane == 0) mbar_arrive_cluster(w_ready_leader0 + 8u * s);
                     ++it;
                 }
             }
@@ -460,14 +528,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else {
         // epilogue
         const int q = warp & 3;  // TMEM lane quarter this warp may access
+        const uint32_t acc_empty_leader0 = map_to_rank(acc_empty(0), 0);
         uint32_t ait = 0;
-        for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+        for (int t = pair; t < p.num_tiles; t += num_pairs) {
             const int mb = t % p.num_m_blocks, nb = t / p.num_m_blocks;
             const int a = ait % NUM_ACC;
             const uint32_t aph = (ait / NUM_ACC) & 1u;
             if (!warp_wait_or_abort(acc_full(a), aph, abort_flag, ctx)) break;
             tc_fence_after();
-            const int row = mb * BM + q * 32 + lane;
+            const int row = mb * 2 * BM + static_cast<int>(rank) * BM + q * 32 + lane;
             float *yrow = p.y + static_cast<size_t>(row) * p.n + static_cast<size_t>(nb) * BN;
             const int ncols = min(BN, p.n - nb * BN);
 #pragma unroll 1
@@ -487,7 +556,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive_addr(acc_empty(a));
+            if (lane == 0) mbar_arrive_cluster(acc_empty_leader0 + 8u * a);
             ++ait;
         }
     }
@@ -495,69 +564,39 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     pdl_launch_dependents();
     tc_fence_before();
     __syncthreads();
+    cluster_barrier();  // the leader has drained; the peer's shared memory may go
     tc_fence_after();
-    if (warp == WARP_MMA) tmem_dealloc(tmem_base, TMEM_COLS);
-}
-
-// ---- host side -------------------------------------------------------------------
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, []() {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    return fn;
+    if (warp == WARP_MMA) tmem_dealloc_pair(tmem_base, TMEM_COLS);
 }
 
 }  // namespace
 
 cudaError_t launch_gemm_q4_0(const uint8_t *w, const uint16_t *x, float *y, int64_t m, int64_t n,
                              int64_t k, cudaStream_t stream, const LaunchCtx &ctx) {
-    auto enc = encode_fn();
-    if (!enc) return cudaErrorNotSupported;
     if (m > (1 << 30) || n > (1 << 30) || k > (1 << 24)) return cudaErrorInvalidValue;
     CUtensorMap tx, tw;
-    {
-        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(m)};
-        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(k) * 2};
-        const cuuint32_t box[2] = {BK, BM};
-        const cuuint32_t estr[2] = {1, 1};
-        if (enc(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(x), dims, strides,
-                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cudaErrorInvalidValue;
-    }
-    {
-        const cuuint64_t rowbytes = static_cast<cuuint64_t>(k / kQK) * kQ4_0Bytes;
-        const cuuint64_t dims[2] = {rowbytes, static_cast<cuuint64_t>(n)};
-        const cuuint64_t strides[1] = {rowbytes};
-        const cuuint32_t box[2] = {RAW_ROW_BYTES, BN};
-        const cuuint32_t estr[2] = {1, 1};
-        if (enc(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(w), dims, strides, box,
-                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cudaErrorInvalidValue;
-    }
+    if (!encode_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, k, m, k * 2, BK, BM,
+                        CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    const uint64_t rowbytes = static_cast<uint64_t>(k / kQK) * kQ4_0Bytes;
+    if (!encode_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, rowbytes, n, rowbytes,
+                        RAW_ROW_BYTES, BN_CTA))
+        return cudaErrorInvalidValue;
     GemmParams p;
     p.y = y;
     p.m = static_cast<int>(m);
     p.n = static_cast<int>(n);
     p.k = static_cast<int>(k);
-    p.num_m_blocks = static_cast<int>((m + BM - 1) / BM);
+    p.num_m_blocks = static_cast<int>((m + 2 * BM - 1) / (2 * BM));
     const int nnb = static_cast<int>((n + BN - 1) / BN);
     p.num_tiles = p.num_m_blocks * nnb;
     p.ctx = ctx;
     static int smem_limits[kMaxDevices] = {0};
-    cudaError_t e = ensure_smem(gemm_q4_0_kernel, kSmemBytes, false, smem_limits);
+    cudaError_t e = ensure_smem(gemm_q4_0_kernel, kSmemBytes, true, smem_limits);
     if (e != cudaSuccess) return e;
-    const int grid = std::min(p.num_tiles, device_sm_count());
-    return launch_kernel(gemm_q4_0_kernel, dim3(grid), dim3(NUM_THREADS), kSmemBytes, stream, 1,
-                         tx, tw, p);
+    const int pairs = std::max(1, std::min(p.num_tiles, device_sm_count() / 2));
+    return launch_kernel(gemm_q4_0_kernel, dim3(2 * pairs), dim3(NUM_THREADS), kSmemBytes, stream,
+                         2, tx, tw, p);
 }
 
 }  // namespace qmm

@@ -8,24 +8,27 @@
 // is about HBM and issue slots, not tensor cores.
 //
 // Streaming kernel (K % 256 == 0, 16-byte aligned w and x):
-//  * A CTA owns 32 rows; lane r of every warp owns row r.  The K dimension is
-//    cut into chunks of 256 weights (8 blocks: 144 bytes of Q4_0, 272 of
-//    Q8_0), which keeps every row chunk 16-byte aligned.  Warps take chunks
-//    round robin; small-N shapes also split K across a thread-block cluster
-//    and reduce through distributed shared memory (no global scratch, fixed
-//    summation order).
-//  * Each warp runs its own ring of S shared-memory stages.  Every lane
-//    issues one cp.async.bulk of its row's chunk; an mbarrier with a byte
-//    count tracks the stage.  Shared-memory rows are 144 (272) bytes apart,
-//    so the lanes' 16-byte reads hit distinct banks.
-//  * Activations are staged once per CTA slice in shared memory, pre-scaled
-//    by the power of two that matches where each nibble sits in its word
-//    (see below), and read as warp-wide broadcasts.
+//  * Lane r of a warp owns row r of a 32-row tile.  K is cut into chunks of
+//    256 weights (8 blocks: 144 bytes of Q4_0, 272 of Q8_0), which keeps
+//    every row chunk 16-byte aligned.  A warp streams the chunks of its K
+//    range through its own ring of shared-memory stages; warps never wait on
+//    one another.  Small-N shapes split K across a thread-block cluster and
+//    add the partial sums through distributed shared memory in rank order
+//    (no global scratch, deterministic).
+//  * One 2-D TMA load moves a warp's 32 rows x one chunk (4.6 KB Q4_0,
+//    8.7 KB Q8_0) and an mbarrier with a byte count tracks the stage (many
+//    small per-row bulk copies would be limited by the copy engine's
+//    per-request rate).  Rows sit 144 (272) bytes apart in shared memory, so
+//    the lanes' 16-byte reads hit distinct banks.
+//  * The CTA's slice of the activations (M rows x its K range) is copied
+//    into shared memory by bulk copies issued by one thread after the
+//    programmatic-launch wait; warps wait on its mbarrier and read x as
+//    warp-wide broadcasts.  No thread waits on another warp.
 //  * Decode without int->float conversions: OR-ing a nibble (or an offset
-//    byte) into the mantissa of 2^23 gives 2^23 + v*2^s exactly; one FADD of
-//    -(2^23 + 8*2^s) (Q4_0) or -(2^23 + 128*2^s) (Q8_0) leaves
-//    (nibble-8)*2^s or q*2^s exactly, and the product with x*2^-s is the
-//    exact w-free product (nibble-8)*x.  Adds and FMAs run as packed f32x2.
+//    byte) at bit s into the mantissa of 2^23 gives m = 2^23 + v*2^s exactly;
+//    one FMA m*2^-s - (2^23 + 8*2^s)*2^-s (Q4_0; +128 for Q8_0) leaves the
+//    exact integer nibble-8 (or q).  Both that FMA and the product with x run
+//    as packed f32x2 instructions, four independent chains at small M.
 //  * Per block: acc = sum_j (nibble_j - 8) * x_j in fp32, then y += d * acc.
 //
 // Byte-wise kernel: any K % 32 == 0 and any alignment; a warp per row.
@@ -35,40 +38,61 @@
 
 #include <algorithm>
 
+// Launch-shape knobs (defaults; a build may override them with -D).
+#ifndef QMM_GEMV_UNITS_PER_SM
+#define QMM_GEMV_UNITS_PER_SM 8   // target (row tile, K range) units per SM
+#endif
+#ifndef QMM_GEMV_MAX_KSPLIT
+#define QMM_GEMV_MAX_KSPLIT 8     // largest cluster along K
+#endif
+#ifndef QMM_GEMV_MAX_WARPS
+#define QMM_GEMV_MAX_WARPS 4      // warps (row tiles) per CTA
+#endif
+#ifndef QMM_GEMV_STAGES
+#define QMM_GEMV_STAGES 4         // ring depth per warp
+#endif
+#ifndef QMM_GEMV_X_BYTES
+#define QMM_GEMV_X_BYTES 65536    // activation slice per CTA (shared memory)
+#endif
+
 namespace qmm {
 namespace {
 
-constexpr int kRowsPerCta = 32;
+constexpr int kRowsPerWarp = 32;
 constexpr int kChunkK = 256;
 constexpr uint32_t kMagic = 0x4B000000u;  // 2^23
 
+// TMA view of the weight bytes: Q4_0 as uint8 (box 144 x 32), Q8_0 as
+// uint16 pairs (box 136 x 32; a box row may hold at most 256 elements).
 template <Fmt F>
 struct StreamFmt;
 template <>
 struct StreamFmt<Fmt::Q4_0> {
     static constexpr int kChunkBytes = 144;
+    static constexpr int kElemBytes = 1;
+    static constexpr CUtensorMapDataType kType = CU_TENSOR_MAP_DATA_TYPE_UINT8;
 };
 template <>
 struct StreamFmt<Fmt::Q8_0> {
     static constexpr int kChunkBytes = 272;
+    static constexpr int kElemBytes = 2;
+    static constexpr CUtensorMapDataType kType = CU_TENSOR_MAP_DATA_TYPE_UINT16;
 };
 
-// Power-of-two exponent s by which position j (0..31) of a block is
-// pre-scaled (x' = x * 2^-s).  Q4_0: a qs word holds positions
-// 4i..4i+3 (low nibbles, bits 0,8,16,24) and 16+4i..19+4i (high nibbles,
-// bits 4,12,20,28); bits 0-19 are used in place, bits 20-31 after >> 16.
-__device__ __forceinline__ int q4_0_shift(int j) {
-    const int t = j & 3;
-    if (j < 16) return t == 0 ? 0 : (t == 2 ? 16 : 8);
-    return (t & 1) ? 12 : 4;
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
+                                            uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, "
+        "{%2, %3}], [%4];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+        : "memory");
 }
-// Q8_0: bytes 0 and 2 of a word are used at bits 0-7 (s = 0), bytes 1 and 3
-// at bits 8-15 (s = 8).
 
+// m = 2^23 + (v & mask) as a float: the nibble (byte) lands in the mantissa.
 __device__ __forceinline__ float mag(uint32_t v, uint32_t mask) {
     return __uint_as_float((v & mask) | kMagic);
 }
-// Offset byte for Q8_0: ((v ^ 0x80 at the byte's top bit) & mask) | 2^23.
+// Q8_0 byte with its sign bit flipped (q + 128) in the mantissa of 2^23.
 __device__ __forceinline__ float mag8(uint32_t v, uint32_t mask, uint32_t magic_flip) {
     return __uint_as_float((mask & (v ^ magic_flip)) | (~mask & magic_flip));
 }
@@ -82,10 +106,14 @@ struct Chains {
     static constexpr int value = M <= 2 ? 4 : (M <= 4 ? 2 : 1);
 };
 
-// One row chunk (8 Q4_0 blocks, 144 bytes at `src`) against the pre-scaled
-// activations `xs` (position 0 of the chunk for row 0; rows XS apart).
+// One row chunk (8 Q4_0 blocks, 144 bytes at `src`) against activations
+// `xk` in shared memory (position 0 of the chunk for row 0; rows XS apart).
+//
+// A qs word v holds weights 4i..4i+3 (low nibbles, bits 0,8,16,24) and
+// 16+4i..19+4i (high nibbles, bits 4,12,20,28); bits 0-19 are used in place
+// and bits 20-31 after u = v >> 16, so the nibble sits at s in {0,4,8,12,16}.
 template <int M>
-__device__ __forceinline__ void q4_0_chunk(const uint8_t *src, const float *xs, int XS,
+__device__ __forceinline__ void q4_0_chunk(const uint8_t *src, const float *xk, int XS,
                                            float (&tot)[M]) {
     constexpr int CH = Chains<M>::value;
     uint32_t wd[36];
@@ -97,9 +125,10 @@ __device__ __forceinline__ void q4_0_chunk(const uint8_t *src, const float *xs, 
         wd[4 * t + 2] = v.z;
         wd[4 * t + 3] = v.w;
     }
-    const float2 c01 = f2(-8388616.0f, -8390656.0f);  // -(2^23 + 8*2^s), s = 0, 8
-    const float2 c23 = f2(-8912896.0f, -8390656.0f);  // s = 16, 8
-    const float2 c45 = f2(-8388736.0f, -8421376.0f);  // s = 4, 12
+    // (m - (2^23 + 8*2^s)) * 2^-s = m*2^-s - (2^23*2^-s + 8): exact nibble-8
+    const float2 s01 = f2(1.0f, 0.00390625f), b01 = f2(-8388616.0f, -32776.0f);           // s = 0, 8
+    const float2 s23 = f2(1.52587890625e-05f, 0.00390625f), b23 = f2(-136.0f, -32776.0f); // s = 16, 8
+    const float2 s45 = f2(0.0625f, 0.000244140625f), b45 = f2(-524296.0f, -2056.0f);      // s = 4, 12
 #pragma unroll
     for (int b = 0; b < 8; ++b) {
         const int base = (18 * b) >> 2;
@@ -122,15 +151,15 @@ __device__ __forceinline__ void q4_0_chunk(const uint8_t *src, const float *xs, 
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const uint32_t v = q[i], u = v >> 16;
-            const float2 p01 = __fadd2_rn(f2(mag(v, 0x0000000Fu), mag(v, 0x00000F00u)), c01);
-            const float2 p23 = __fadd2_rn(f2(mag(v, 0x000F0000u), mag(u, 0x00000F00u)), c23);
-            const float2 p45 = __fadd2_rn(f2(mag(v, 0x000000F0u), mag(v, 0x0000F000u)), c45);
-            const float2 p67 = __fadd2_rn(f2(mag(u, 0x000000F0u), mag(u, 0x0000F000u)), c45);
+            const float2 p01 = __ffma2_rn(f2(mag(v, 0x0000000Fu), mag(v, 0x00000F00u)), s01, b01);
+            const float2 p23 = __ffma2_rn(f2(mag(v, 0x000F0000u), mag(u, 0x00000F00u)), s23, b23);
+            const float2 p45 = __ffma2_rn(f2(mag(v, 0x000000F0u), mag(v, 0x0000F000u)), s45, b45);
+            const float2 p67 = __ffma2_rn(f2(mag(u, 0x000000F0u), mag(u, 0x0000F000u)), s45, b45);
             const int c = i % CH;
 #pragma unroll
             for (int m = 0; m < M; ++m) {
-                const float4 xa = lds128f(xs + m * XS + 32 * b + 4 * i);
-                const float4 xb = lds128f(xs + m * XS + 32 * b + 16 + 4 * i);
+                const float4 xa = lds128f(xk + m * XS + 32 * b + 4 * i);
+                const float4 xb = lds128f(xk + m * XS + 32 * b + 16 + 4 * i);
                 acc[m][c] = __ffma2_rn(p01, f2(xa.x, xa.y), acc[m][c]);
                 acc[m][c] = __ffma2_rn(p23, f2(xa.z, xa.w), acc[m][c]);
                 acc[m][c] = __ffma2_rn(p45, f2(xb.x, xb.y), acc[m][c]);
@@ -147,9 +176,10 @@ __device__ __forceinline__ void q4_0_chunk(const uint8_t *src, const float *xs, 
     }
 }
 
-// One row chunk of 8 Q8_0 blocks (272 bytes).
+// One row chunk of 8 Q8_0 blocks (272 bytes).  Bytes 0 and 2 of a word are
+// used at bits 0-7 (s = 0), bytes 1 and 3 at bits 8-15 (s = 8).
 template <int M>
-__device__ __forceinline__ void q8_0_chunk(const uint8_t *src, const float *xs, int XS,
+__device__ __forceinline__ void q8_0_chunk(const uint8_t *src, const float *xk, int XS,
                                            float (&tot)[M]) {
     constexpr int CH = Chains<M>::value;
     uint32_t wd[68];
@@ -161,7 +191,8 @@ __device__ __forceinline__ void q8_0_chunk(const uint8_t *src, const float *xs, 
         wd[4 * t + 2] = v.z;
         wd[4 * t + 3] = v.w;
     }
-    const float2 c = f2(-8388736.0f, -8421376.0f);  // -(2^23 + 128*2^s), s = 0, 8
+    // (m - (2^23 + 128*2^s)) * 2^-s: exact q
+    const float2 sc = f2(1.0f, 0.00390625f), bc = f2(-8388736.0f, -32896.0f);
 #pragma unroll
     for (int b = 0; b < 8; ++b) {
         const int base = (34 * b) >> 2;
@@ -184,14 +215,14 @@ __device__ __forceinline__ void q8_0_chunk(const uint8_t *src, const float *xs, 
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const uint32_t v = q[i], u = v >> 16;
-            const float2 p01 = __fadd2_rn(
-                f2(mag8(v, 0x000000FFu, kMagic | 0x80u), mag8(v, 0x0000FF00u, kMagic | 0x8000u)), c);
-            const float2 p23 = __fadd2_rn(
-                f2(mag8(u, 0x000000FFu, kMagic | 0x80u), mag8(u, 0x0000FF00u, kMagic | 0x8000u)), c);
+            const float2 p01 = __ffma2_rn(
+                f2(mag8(v, 0x000000FFu, kMagic | 0x80u), mag8(v, 0x0000FF00u, kMagic | 0x8000u)), sc, bc);
+            const float2 p23 = __ffma2_rn(
+                f2(mag8(u, 0x000000FFu, kMagic | 0x80u), mag8(u, 0x0000FF00u, kMagic | 0x8000u)), sc, bc);
             const int h = i % CH;
 #pragma unroll
             for (int m = 0; m < M; ++m) {
-                const float4 xa = lds128f(xs + m * XS + 32 * b + 4 * i);
+                const float4 xa = lds128f(xk + m * XS + 32 * b + 4 * i);
                 acc[m][h] = __ffma2_rn(p01, f2(xa.x, xa.y), acc[m][h]);
                 acc[m][h] = __ffma2_rn(p23, f2(xa.z, xa.w), acc[m][h]);
             }
@@ -231,25 +262,26 @@ __device__ __forceinline__ float ld_dsmem_f32(const float *local, uint32_t rank)
 }
 
 struct StreamParams {
-    const uint8_t *w;
     const float *x;
     float *y;
     int n;            // rows of W
     int k;            // columns (multiple of 256)
     int stages;       // ring depth per warp
     int cpc;          // chunks per CTA (the K range of one cluster rank)
-    int xs_chunks;    // chunks per activation slice
     LaunchCtx ctx;
 };
 
 // Grid: blockIdx.x = group * ksplit + rank, with a cluster of ksplit CTAs
 // along x.  Warp w of group g owns rows (g*nw + w)*32 .. +31; cluster rank r
 // owns chunks [r*cpc, (r+1)*cpc) of K.  Every warp streams all chunks of its
-// CTA's K range for its own rows.
+// CTA's K range for its own rows, independently of the other warps.
 template <Fmt F, int M>
-__global__ void __launch_bounds__(128) gemv_stream_kernel(StreamParams p) {
+__global__ void __launch_bounds__(128)
+    gemv_stream_kernel(const __grid_constant__ CUtensorMap wmap, StreamParams p) {
     constexpr int CB = StreamFmt<F>::kChunkBytes;
-    extern __shared__ __align__(128) uint8_t smem[];
+    extern __shared__ __align__(128) uint8_t smem_dyn[];
+    // TMA destinations: 128-byte aligned (the launch adds 128 bytes of slack)
+    uint8_t *smem = smem_dyn + ((128u - (smem_addr(smem_dyn) & 127u)) & 127u);
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int nw = blockDim.x >> 5;
@@ -257,92 +289,84 @@ __global__ void __launch_bounds__(128) gemv_stream_kernel(StreamParams p) {
     const uint32_t rank = cluster_ctarank();
     const uint32_t ksplit = cluster_nctarank();
     const int group = static_cast<int>(blockIdx.x / ksplit);
-    const int row0 = (group * nw + warp) * kRowsPerCta;
+    const int row0 = (group * nw + warp) * kRowsPerWarp;
     const int row = row0 + lane;
     const bool row_ok = row < p.n;
-    const int valid_rows = max(0, min(kRowsPerCta, p.n - row0));
-    const int XS = p.xs_chunks * kChunkK;
-    const size_t rowbytes = static_cast<size_t>(p.k / kChunkK) * CB;
+    const bool warp_active = row0 < p.n;  // warp-uniform
     const int c_begin = static_cast<int>(rank) * p.cpc;
     const int cpc = p.cpc;
 
-    // shared memory: ring [nw][S][32 rows][CB] | xs [M][XS] | part [nw][M][32] | bars [nw][S]
-    uint8_t *my_ring = smem + static_cast<size_t>(warp) * S * kRowsPerCta * CB;
-    float *xs = reinterpret_cast<float *>(smem + static_cast<size_t>(nw) * S * kRowsPerCta * CB);
+    const int XS = cpc * kChunkK;  // activation floats per row in shared memory
+
+    // shared memory: ring [nw][S][32 rows][CB] | xs [M][XS] | part [nw][M][32] |
+    //                bars [nw][S] | xbar
+    uint8_t *my_ring = smem + static_cast<size_t>(warp) * S * kRowsPerWarp * CB;
+    float *xs = reinterpret_cast<float *>(smem + static_cast<size_t>(nw) * S * kRowsPerWarp * CB);
     float *part = xs + M * XS;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(part + nw * M * kRowsPerCta);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(part + nw * M * kRowsPerWarp);
     uint64_t *my_bars = bars + warp * S;
+    uint64_t *xbar = bars + nw * S;
 
-    if (lane == 0)
+    if (lane == 0) {
+        if (warp == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&wmap)) : "memory");
+            mbar_init(xbar, 1);
+        }
         for (int s = 0; s < S; ++s) mbar_init(&my_bars[s], 1);
-    fence_mbar_init();
-    __syncthreads();
+        fence_mbar_init();
+    }
+    __syncthreads();  // barriers initialised before any thread waits on them
 
-    const uint8_t *my_src = p.w + static_cast<size_t>(row_ok ? row : 0) * rowbytes;
     auto issue = [&](int i) {  // chunk i of this CTA's K range into stage i % S
-        const int st = i % S;
-        if (lane == 0) mbar_arrive_expect_tx(&my_bars[st], valid_rows * CB);
-        __syncwarp();
-        if (row_ok)
-            bulk_g2s(my_ring + (st * kRowsPerCta + lane) * CB,
-                     my_src + static_cast<size_t>(c_begin + i) * CB, CB, &my_bars[st]);
+        if (lane == 0) {
+            const int st = i % S;
+            // full box bytes: rows past N are zero-filled and still counted
+            mbar_arrive_expect_tx(&my_bars[st], kRowsPerWarp * CB);
+            tma_load_2d(my_ring + st * kRowsPerWarp * CB, &wmap,
+                        (c_begin + i) * (CB / StreamFmt<F>::kElemBytes), row0, &my_bars[st]);
+        }
     };
     // The weight prefetch may start before the preceding kernel in the stream
     // has finished (programmatic dependent launch): weights are read-only
     // model data that no kernel of this library writes.  Activations are read
     // and outputs written only after the wait below.
     int issued = 0;
-    for (; issued < min(S, cpc); ++issued) issue(issued);
+    if (warp_active)
+        for (; issued < min(S, cpc); ++issued) issue(issued);
     pdl_wait();
+    if (threadIdx.x == 0) {  // activations: one bulk copy per row m of the K range
+        mbar_arrive_expect_tx(xbar, static_cast<uint32_t>(M * XS * sizeof(float)));
+#pragma unroll
+        for (int m = 0; m < M; ++m)
+            bulk_g2s(xs + m * XS, p.x + static_cast<size_t>(m) * p.k + c_begin * kChunkK,
+                     static_cast<uint32_t>(XS * sizeof(float)), xbar);
+    }
     pdl_launch_dependents();
 
     float tot[M];
 #pragma unroll
     for (int m = 0; m < M; ++m) tot[m] = 0.0f;
 
-    bool failed = false;
     int consumed = 0;
-    for (int s0 = 0; s0 < cpc; s0 += p.xs_chunks) {
-        const int s1 = min(cpc, s0 + p.xs_chunks);
-        if (s0 > 0) __syncthreads();  // the previous slice is no longer read
-        {
-            const int kx0 = (c_begin + s0) * kChunkK;
-            const int nk4 = (s1 - s0) * (kChunkK / 4);
-            for (int e = threadIdx.x; e < M * nk4; e += nw * 32) {
-                const int m = e / nk4;
-                const int kk = (e - m * nk4) * 4;
-                float4 v = __ldg(reinterpret_cast<const float4 *>(
-                    p.x + static_cast<size_t>(m) * p.k + kx0 + kk));
-                const int j = (kx0 + kk) & 31;
-                if constexpr (F == Fmt::Q4_0) {
-                    v.x *= __int_as_float((127 - q4_0_shift(j + 0)) << 23);
-                    v.y *= __int_as_float((127 - q4_0_shift(j + 1)) << 23);
-                    v.z *= __int_as_float((127 - q4_0_shift(j + 2)) << 23);
-                    v.w *= __int_as_float((127 - q4_0_shift(j + 3)) << 23);
-                } else {
-                    v.y *= 0.00390625f;  // 2^-8 for odd positions
-                    v.w *= 0.00390625f;
-                }
-                *reinterpret_cast<float4 *>(xs + m * XS + kk) = v;
-            }
-        }
-        __syncthreads();
-        for (int i = s0; i < s1; ++i) {
-            if (valid_rows == 0 || failed) continue;  // warp-uniform
+    // every warp waits for the activations (so none exits with the copy in flight)
+    const bool x_ok = mbar_wait(xbar, 0, p.ctx);
+    bool failed = !x_ok;
+    if (warp_active) {
+        for (int i = 0; i < cpc && !failed; ++i) {
             const int st = i % S;
             const uint32_t par = static_cast<uint32_t>(i / S) & 1u;
             if (!mbar_wait(&my_bars[st], par, p.ctx)) {
                 failed = true;
-                continue;
+                break;
             }
             ++consumed;
-            const uint8_t *src = my_ring + (st * kRowsPerCta + lane) * CB;
-            const float *xc = xs + (i - s0) * kChunkK;
+            const uint8_t *src = my_ring + (st * kRowsPerWarp + lane) * CB;
+            const float *xk = xs + i * kChunkK;
             if constexpr (F == Fmt::Q4_0)
-                q4_0_chunk<M>(src, xc, XS, tot);
+                q4_0_chunk<M>(src, xk, XS, tot);
             else
-                q8_0_chunk<M>(src, xc, XS, tot);
-            __syncwarp();
+                q8_0_chunk<M>(src, xk, XS, tot);
+            __syncwarp();  // every lane is done reading the stage
             if (issued < cpc) {
                 fence_proxy_async_smem();
                 issue(issued);
@@ -353,6 +377,7 @@ __global__ void __launch_bounds__(128) gemv_stream_kernel(StreamParams p) {
     if (failed) {
         // Let copies still in flight land before the CTA's shared memory is
         // released; each wait is again bounded.
+        if (!x_ok) mbar_wait(xbar, 0, p.ctx);
         for (int j = consumed; j < issued; ++j)
             mbar_wait(&my_bars[j % S], static_cast<uint32_t>(j / S) & 1u, p.ctx);
     }
@@ -365,15 +390,15 @@ __global__ void __launch_bounds__(128) gemv_stream_kernel(StreamParams p) {
         return;
     }
     // partial sums of the cluster's K ranges, added in rank order by rank 0
-    float *my_part = part + warp * M * kRowsPerCta;
+    float *my_part = part + warp * M * kRowsPerWarp;
 #pragma unroll
-    for (int m = 0; m < M; ++m) my_part[m * kRowsPerCta + lane] = tot[m];
+    for (int m = 0; m < M; ++m) my_part[m * kRowsPerWarp + lane] = tot[m];
     cluster_sync();
     if (rank == 0 && row_ok) {
 #pragma unroll
         for (int m = 0; m < M; ++m) {
             float s = tot[m];
-            for (uint32_t q = 1; q < ksplit; ++q) s += ld_dsmem_f32(&my_part[m * kRowsPerCta + lane], q);
+            for (uint32_t q = 1; q < ksplit; ++q) s += ld_dsmem_f32(&my_part[m * kRowsPerWarp + lane], q);
             p.y[static_cast<size_t>(m) * p.n + row] = s;
         }
     }
@@ -424,12 +449,12 @@ __global__ void __launch_bounds__(128) gemv_bytewise_kernel(const uint8_t *__res
     }
 }
 
-// Launch shape.  Units are (32-row tile, K range) pairs; the K dimension is
-// split over a cluster (ksplit CTAs) until there are enough units to give
-// every SM several resident warps, and warps per CTA share one activation
-// slice.  Rings hold only as many stages as a warp has chunks.
+// Launch shape.  Units are (32-row tile, K range) pairs; K is split over a
+// cluster (ksplit CTAs) until there are enough units to give every SM
+// several resident warps.  Rings hold only as many stages as a warp has
+// chunks.
 struct StreamShape {
-    int ksplit, nw, stages, cpc, xs_chunks;
+    int ksplit, nw, stages, cpc;
     size_t smem;
 };
 
@@ -437,24 +462,26 @@ template <Fmt F, int M>
 StreamShape stream_shape(int64_t n, int64_t k, int sms) {
     constexpr int CB = StreamFmt<F>::kChunkBytes;
     StreamShape sh;
-    const int64_t tiles = (n + kRowsPerCta - 1) / kRowsPerCta;
+    const int64_t tiles = (n + kRowsPerWarp - 1) / kRowsPerWarp;
     const int C = static_cast<int>(k / kChunkK);
-    const int64_t want_units = 8LL * sms;  // about eight resident row tiles per SM
+    const int64_t want_units = static_cast<int64_t>(QMM_GEMV_UNITS_PER_SM) * sms;
     sh.ksplit = 1;
-    while (sh.ksplit < 8 && tiles * sh.ksplit < want_units && C % (2 * sh.ksplit) == 0)
+    while (sh.ksplit < QMM_GEMV_MAX_KSPLIT && tiles * sh.ksplit < want_units &&
+           C % (2 * sh.ksplit) == 0)
+        sh.ksplit *= 2;
+    // the CTA's activation slice (M rows x K range) must fit its budget
+    while (sh.ksplit < QMM_GEMV_MAX_KSPLIT && C % (2 * sh.ksplit) == 0 &&
+           static_cast<int64_t>(M) * (k / sh.ksplit) * 4 > QMM_GEMV_X_BYTES)
         sh.ksplit *= 2;
     sh.cpc = C / sh.ksplit;
-    // several warps per CTA when there are plenty of tiles (they share x')
     const int64_t units = tiles * sh.ksplit;
     sh.nw = 1;
-    while (sh.nw < 4 && units / (2 * sh.nw) >= 2LL * sms) sh.nw *= 2;
-    sh.stages = std::min(sh.cpc, F == Fmt::Q4_0 ? 4 : 3);
-    const int xs_budget = 32 * 1024;
-    sh.xs_chunks = std::max(1, std::min(sh.cpc, xs_budget / (M * kChunkK * 4)));
-    sh.smem = static_cast<size_t>(sh.nw) * sh.stages * kRowsPerCta * CB +
-              sizeof(float) * (static_cast<size_t>(M) * sh.xs_chunks * kChunkK +
-                               static_cast<size_t>(sh.nw) * M * kRowsPerCta) +
-              sizeof(uint64_t) * sh.nw * sh.stages;
+    while (sh.nw < QMM_GEMV_MAX_WARPS && units / (2 * sh.nw) >= 2LL * sms) sh.nw *= 2;
+    sh.stages = std::min(sh.cpc, QMM_GEMV_STAGES);
+    sh.smem = static_cast<size_t>(sh.nw) * sh.stages * kRowsPerWarp * CB +
+              sizeof(float) * (static_cast<size_t>(M) * sh.cpc * kChunkK +
+                               static_cast<size_t>(sh.nw) * M * kRowsPerWarp) +
+              sizeof(uint64_t) * (sh.nw * sh.stages + 1) + 128;
     return sh;
 }
 
@@ -462,24 +489,28 @@ template <Fmt F, int M>
 cudaError_t launch_stream(const uint8_t *w, const float *x, float *y, int64_t n, int64_t k,
                           cudaStream_t stream, const LaunchCtx &ctx) {
     const StreamShape sh = stream_shape<F, M>(n, k, device_sm_count());
-    const int64_t tiles = (n + kRowsPerCta - 1) / kRowsPerCta;
+    const int64_t tiles = (n + kRowsPerWarp - 1) / kRowsPerWarp;
     const int64_t groups = (tiles + sh.nw - 1) / sh.nw;
+    CUtensorMap wmap;
+    const uint64_t rowbytes = static_cast<uint64_t>(k / kChunkK) * StreamFmt<F>::kChunkBytes;
+    constexpr int EB = StreamFmt<F>::kElemBytes;
+    if (!encode_tmap_2d(&wmap, StreamFmt<F>::kType, w, rowbytes / EB, n, rowbytes,
+                        StreamFmt<F>::kChunkBytes / EB, kRowsPerWarp))
+        return cudaErrorInvalidValue;
     StreamParams p;
-    p.w = w;
     p.x = x;
     p.y = y;
     p.n = static_cast<int>(n);
     p.k = static_cast<int>(k);
     p.stages = sh.stages;
     p.cpc = sh.cpc;
-    p.xs_chunks = sh.xs_chunks;
     p.ctx = ctx;
     auto kern = gemv_stream_kernel<F, M>;
     static int smem_limits[kMaxDevices] = {0};  // this instantiation's own cache
     const cudaError_t e = ensure_smem(kern, sh.smem, true, smem_limits);
     if (e != cudaSuccess) return e;
     return launch_kernel(kern, dim3(static_cast<unsigned>(groups * sh.ksplit)), dim3(sh.nw * 32),
-                         sh.smem, stream, static_cast<unsigned>(sh.ksplit), p);
+                         sh.smem, stream, static_cast<unsigned>(sh.ksplit), wmap, p);
 }
 
 template <Fmt F, int M>

@@ -7,6 +7,8 @@
 
 #include <cuda_runtime.h>
 
+#include <cuda.h>
+
 #include "qmm_device.cuh"
 
 namespace qmm {
@@ -73,6 +75,14 @@ cudaError_t ensure_smem(Kernel kernel, size_t bytes, bool cluster, int (&limits)
     if (e == cudaSuccess) __atomic_store_n(&limits[dev], static_cast<int>(bytes), __ATOMIC_RELEASE);
     return e;
 }
+
+// Encode a 2-D tiled TMA descriptor (no swizzle unless given): dims
+// {inner, outer} elements, outer stride in bytes, box {box_inner, box_outer}.
+// Returns false if the driver entry point is missing or rejects the shape.
+bool encode_tmap_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *base,
+                    uint64_t inner, uint64_t outer, uint64_t outer_stride_bytes,
+                    uint32_t box_inner, uint32_t box_outer,
+                    CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_NONE);
 
 cudaError_t launch_dequant(Fmt fmt, const uint8_t *w, float *out, int64_t n, int64_t k,
                            cudaStream_t stream, const LaunchCtx &ctx);
