@@ -76,8 +76,8 @@ struct SmemLayout {
     static constexpr int raw = w + OP_STAGES * W_STAGE_BYTES;
     static constexpr int bars = raw + RAW_STAGES * RAW_STAGE_BYTES;
     // barriers: x_full, w_ready, op_empty [OP_STAGES]; raw_full, raw_empty
-    // [RAW_STAGES]; acc_full, acc_empty [NUM_ACC]; final
-    static constexpr int nbars = 3 * OP_STAGES + 2 * RAW_STAGES + 2 * NUM_ACC + 1;
+    // [RAW_STAGES]; acc_full, acc_empty [NUM_ACC]; final; w_local [OP_STAGES]
+    static constexpr int nbars = 4 * OP_STAGES + 2 * RAW_STAGES + 2 * NUM_ACC + 1;
     static constexpr int tmem_slot = bars + nbars * 8;
     static constexpr int abort_flag = tmem_slot + 4;
     static constexpr int total = abort_flag + 4;
@@ -150,8 +150,9 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
                  : "memory");
 }
 
+// Announces bytes a TMA load will deliver; publishes no data, so relaxed.
 __device__ __forceinline__ void mbar_expect_tx_cluster(uint32_t bar_cluster, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(
+    asm volatile("mbarrier.arrive.expect_tx.relaxed.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(
                      bar_cluster),
                  "r"(bytes)
                  : "memory");
@@ -226,6 +227,34 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, int
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 0; it < (1u << 30); ++it) {
         if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 15u) == 15u) {
+            if (abort_set(flag)) return false;
+            if (global_timer_ns() - t0 > ctx.timeout_ns) break;
+        }
+    }
+    *reinterpret_cast<volatile int *>(flag) = 1;
+    record_error(ctx, kDevErrTimeout);
+    return false;
+}
+
+// Wait whose acquire covers releases made by threads of the peer CTA.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar_addr, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2; "
+        "selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(bar_addr), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool wait_or_abort_cluster(uint32_t bar, uint32_t parity, int *flag,
+                                                      const LaunchCtx &ctx) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 0; it < (1u << 30); ++it) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
         if ((it & 15u) == 15u) {
             if (abort_set(flag)) return false;
             if (global_timer_ns() - t0 > ctx.timeout_ns) break;
@@ -358,15 +387,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     auto acc_empty = [&](int a) {  // leader: 8 epilogue warps
         return bar(3 * OP_STAGES + 2 * RAW_STAGES + NUM_ACC + a);
     };
-    const uint32_t final_bar = bar(SmemLayout::nbars - 1);
+    const uint32_t final_bar = bar(3 * OP_STAGES + 2 * RAW_STAGES + 2 * NUM_ACC);
+    // peer CTA: its dequantisers' stage-done signal, forwarded once to the leader
+    auto w_local = [&](int s) { return bar(3 * OP_STAGES + 2 * RAW_STAGES + 2 * NUM_ACC + 1 + s); };
     int *abort_flag = reinterpret_cast<int *>(sgen + SmemLayout::abort_flag);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sgen + SmemLayout::tmem_slot);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < OP_STAGES; ++s) {
             mbar_init_addr(x_full(s), 2);
-            mbar_init_addr(w_ready(s), 2 * NUM_DEQ_WARPS);
+            mbar_init_addr(w_ready(s), NUM_DEQ_WARPS + 1);  // own warps + the peer's forward
             mbar_init_addr(op_empty(s), 1);
+            mbar_init_addr(w_local(s), NUM_DEQ_WARPS);
         }
         for (int r = 0; r < RAW_STAGES; ++r) {
             mbar_init_addr(raw_full(r), 1);
@@ -446,14 +478,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int t = pair; ok && t < p.num_tiles; t += num_pairs) {
                 const int a = ait % NUM_ACC;
                 const uint32_t aph = (ait / NUM_ACC) & 1u;
-                if (!wait_or_abort(acc_empty(a), aph ^ 1u, abort_flag, ctx)) break;
+                if (!wait_or_abort_cluster(acc_empty(a), aph ^ 1u, abort_flag, ctx)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + a * BN;
                 for (int kb = 0; kb < KB; ++kb) {
                     const int s = it % OP_STAGES;
                     const uint32_t ph = (it / OP_STAGES) & 1u;
-                    if (!wait_or_abort(x_full(s), ph, abort_flag, ctx) ||
-                        !wait_or_abort(w_ready(s), ph, abort_flag, ctx)) { ok = false; break; }
+                    if (!wait_or_abort_cluster(x_full(s), ph, abort_flag, ctx) ||
+                        !wait_or_abort_cluster(w_ready(s), ph, abort_flag, ctx)) { ok = false; break; }
                     tc_fence_after();
                     const uint64_t adesc = sw128_desc(sbase + SmemLayout::x + s * X_STAGE_BYTES);
                     const uint64_t bdesc = sw128_desc(sbase + SmemLayout::w + s * W_STAGE_BYTES);
@@ -475,13 +507,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 umma_commit_pair(final_bar);
                 wait_drain(final_bar, 0, ctx);
             }
+        } else if (!leader && lane == 0) {
+            // forward "stage written" once per stage: a cluster-scope release
+            // by one thread instead of one per dequantiser warp
+            const uint32_t w_ready_leader0 = map_to_rank(w_ready(0), 0);
+            uint32_t it = 0;
+            bool ok = true;
+            for (int t = pair; ok && t < p.num_tiles; t += num_pairs) {
+                for (int kb = 0; kb < KB; ++kb) {
+                    const int s = it % OP_STAGES;
+                    const uint32_t ph = (it / OP_STAGES) & 1u;
+                    if (!wait_or_abort(w_local(s), ph, abort_flag, ctx)) { ok = false; break; }
+                    mbar_arrive_cluster(w_ready_leader0 + 8u * s);
+                    ++it;
+                }
+            }
         }
     } else if (warp < WARP_EPI0) {
         // dequantisers: thread dt owns W row dt % 128, block (2*sub + half) of each K stage
         const int dt = (warp - WARP_DEQ0) * 32 + lane;
         const int row = dt & (BN_CTA - 1);
         const int half = dt >> 7;
-        const uint32_t w_ready_leader0 = map_to_rank(w_ready(0), 0);
+        // leader: arrive on its own w_ready; peer: on its w_local (forwarded)
+        const uint32_t done0 = leader ? w_ready(0) : w_local(0);
         uint32_t it = 0, rit = 0;
         bool ok = true;
         for (int t = pair; ok && t < p.num_tiles; t += num_pairs) {
@@ -520,7 +568,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         sts128(row_addr + (((4 * half + c) ^ sw) << 4), ch[c]);
                     fence_proxy_async_smem();  // generic writes -> visible to the tensor core
                     __syncwarp();
-                    if (lane == 0) mbar_arrive_cluster(w_ready_leader0 + 8u * s);
+                    if (lane == 0) mbar_arrive_addr(done0 + 8u * s);
                     ++it;
                 }
             }

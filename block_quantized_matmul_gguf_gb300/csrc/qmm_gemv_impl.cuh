@@ -10,11 +10,12 @@
 // Streaming kernel (K % 256 == 0, 16-byte aligned w and x):
 //  * Lane r of a warp owns row r of a 32-row tile.  K is cut into chunks of
 //    256 weights (8 blocks: 144 bytes of Q4_0, 272 of Q8_0), which keeps
-//    every row chunk 16-byte aligned.  A warp streams the chunks of its K
-//    range through its own ring of shared-memory stages; warps never wait on
-//    one another.  Small-N shapes split K across a thread-block cluster and
-//    add the partial sums through distributed shared memory in rank order
-//    (no global scratch, deterministic).
+//    every row chunk 16-byte aligned.  A tile's K range is split over kw
+//    warps of a CTA (partial sums added through shared memory) and, for
+//    small N, over a thread-block cluster of ksplit CTAs (partials pushed
+//    into rank 0's shared memory with remote stores, one cluster barrier,
+//    added in rank order).  No global scratch; the summation order is fixed.
+//  * A warp streams its chunks through its own ring of shared-memory stages.
 //  * One 2-D TMA load moves a warp's 32 rows x one chunk (4.6 KB Q4_0,
 //    8.7 KB Q8_0) and an mbarrier with a byte count tracks the stage (many
 //    small per-row bulk copies would be limited by the copy engine's
@@ -39,17 +40,26 @@
 #include <algorithm>
 
 // Launch-shape knobs (defaults; a build may override them with -D).
-#ifndef QMM_GEMV_UNITS_PER_SM
-#define QMM_GEMV_UNITS_PER_SM 8   // target (row tile, K range) units per SM
+#ifndef QMM_GEMV_WARPS_PER_SM
+#define QMM_GEMV_WARPS_PER_SM 10  // target resident warps per SM (work units)
 #endif
 #ifndef QMM_GEMV_MAX_KSPLIT
 #define QMM_GEMV_MAX_KSPLIT 8     // largest cluster along K
 #endif
-#ifndef QMM_GEMV_MAX_WARPS
-#define QMM_GEMV_MAX_WARPS 4      // warps (row tiles) per CTA
+#ifndef QMM_GEMV_MAX_KW
+#define QMM_GEMV_MAX_KW 8         // largest K split across the warps of a CTA
+#endif
+#ifndef QMM_GEMV_MIN_WARPS
+#define QMM_GEMV_MIN_WARPS 4      // warps per CTA when tiles allow
 #endif
 #ifndef QMM_GEMV_STAGES
 #define QMM_GEMV_STAGES 4         // ring depth per warp
+#endif
+#ifndef QMM_GEMV_L4_UNITS
+#define QMM_GEMV_L4_UNITS 0       // (32-row tile x chunk) units up to which 4 lanes share a row
+#endif
+#ifndef QMM_GEMV_L2_UNITS
+#define QMM_GEMV_L2_UNITS 1024    // ... and up to which 2 lanes share a row
 #endif
 #ifndef QMM_GEMV_X_BYTES
 #define QMM_GEMV_X_BYTES 65536    // activation slice per CTA (shared memory)
@@ -58,7 +68,6 @@
 namespace qmm {
 namespace {
 
-constexpr int kRowsPerWarp = 32;
 constexpr int kChunkK = 256;
 constexpr uint32_t kMagic = 0x4B000000u;  // 2^23
 
@@ -99,6 +108,34 @@ __device__ __forceinline__ float mag8(uint32_t v, uint32_t mask, uint32_t magic_
 
 __device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
 
+// Loads this lane's share of a row chunk: `words` 32-bit words from a
+// portion aligned to 16, 8 or 4 bytes (one, two or four lanes per row).
+template <int L, int WORDS>
+__device__ __forceinline__ void load_portion(const uint8_t *src, uint32_t (&wd)[WORDS]) {
+    if constexpr (L == 1) {
+#pragma unroll
+        for (int t = 0; t < WORDS / 4; ++t) {
+            const uint4 v = lds128(src + 16 * t);
+            wd[4 * t + 0] = v.x;
+            wd[4 * t + 1] = v.y;
+            wd[4 * t + 2] = v.z;
+            wd[4 * t + 3] = v.w;
+        }
+    } else if constexpr (L == 2) {
+#pragma unroll
+        for (int t = 0; t < WORDS / 2; ++t) {
+            uint32_t a, b;
+            asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(a), "=r"(b) : "r"(smem_addr(src + 8 * t)));
+            wd[2 * t + 0] = a;
+            wd[2 * t + 1] = b;
+        }
+    } else {
+#pragma unroll
+        for (int t = 0; t < WORDS; ++t)
+            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(wd[t]) : "r"(smem_addr(src + 4 * t)));
+    }
+}
+
 // Independent FMA chains per output row: at small M the rows alone do not
 // give the scheduler enough independent work, so each block's sum is split.
 template <int M>
@@ -106,31 +143,26 @@ struct Chains {
     static constexpr int value = M <= 2 ? 4 : (M <= 4 ? 2 : 1);
 };
 
-// One row chunk (8 Q4_0 blocks, 144 bytes at `src`) against activations
-// `xk` in shared memory (position 0 of the chunk for row 0; rows XS apart).
+// This lane's share (8/L consecutive Q4_0 blocks, 144/L bytes at `src`) of
+// a row chunk against activations `xk` in shared memory (position 0 of the
+// share for row 0; rows XS apart).
 //
 // A qs word v holds weights 4i..4i+3 (low nibbles, bits 0,8,16,24) and
 // 16+4i..19+4i (high nibbles, bits 4,12,20,28); bits 0-19 are used in place
 // and bits 20-31 after u = v >> 16, so the nibble sits at s in {0,4,8,12,16}.
-template <int M>
+template <int M, int L>
 __device__ __forceinline__ void q4_0_chunk(const uint8_t *src, const float *xk, int XS,
                                            float (&tot)[M]) {
     constexpr int CH = Chains<M>::value;
-    uint32_t wd[36];
-#pragma unroll
-    for (int t = 0; t < 9; ++t) {
-        const uint4 v = lds128(src + 16 * t);
-        wd[4 * t + 0] = v.x;
-        wd[4 * t + 1] = v.y;
-        wd[4 * t + 2] = v.z;
-        wd[4 * t + 3] = v.w;
-    }
+    constexpr int NB = 8 / L;
+    uint32_t wd[36 / L];
+    load_portion<L>(src, wd);
     // (m - (2^23 + 8*2^s)) * 2^-s = m*2^-s - (2^23*2^-s + 8): exact nibble-8
     const float2 s01 = f2(1.0f, 0.00390625f), b01 = f2(-8388616.0f, -32776.0f);           // s = 0, 8
     const float2 s23 = f2(1.52587890625e-05f, 0.00390625f), b23 = f2(-136.0f, -32776.0f); // s = 16, 8
     const float2 s45 = f2(0.0625f, 0.000244140625f), b45 = f2(-524296.0f, -2056.0f);      // s = 4, 12
 #pragma unroll
-    for (int b = 0; b < 8; ++b) {
+    for (int b = 0; b < NB; ++b) {
         const int base = (18 * b) >> 2;
         uint32_t dbits, q[4];
         if ((b & 1) == 0) {  // block starts on a word: d low half, qs shifted by 2 bytes
@@ -176,25 +208,20 @@ __device__ __forceinline__ void q4_0_chunk(const uint8_t *src, const float *xk, 
     }
 }
 
-// One row chunk of 8 Q8_0 blocks (272 bytes).  Bytes 0 and 2 of a word are
-// used at bits 0-7 (s = 0), bytes 1 and 3 at bits 8-15 (s = 8).
-template <int M>
+// This lane's share (8/L consecutive Q8_0 blocks, 272/L bytes) of a row
+// chunk.  Bytes 0 and 2 of a word are used at bits 0-7 (s = 0), bytes 1 and
+// 3 at bits 8-15 (s = 8).
+template <int M, int L>
 __device__ __forceinline__ void q8_0_chunk(const uint8_t *src, const float *xk, int XS,
                                            float (&tot)[M]) {
     constexpr int CH = Chains<M>::value;
-    uint32_t wd[68];
-#pragma unroll
-    for (int t = 0; t < 17; ++t) {
-        const uint4 v = lds128(src + 16 * t);
-        wd[4 * t + 0] = v.x;
-        wd[4 * t + 1] = v.y;
-        wd[4 * t + 2] = v.z;
-        wd[4 * t + 3] = v.w;
-    }
+    constexpr int NB = 8 / L;
+    uint32_t wd[68 / L];
+    load_portion<L>(src, wd);
     // (m - (2^23 + 128*2^s)) * 2^-s: exact q
     const float2 sc = f2(1.0f, 0.00390625f), bc = f2(-8388736.0f, -32896.0f);
 #pragma unroll
-    for (int b = 0; b < 8; ++b) {
+    for (int b = 0; b < NB; ++b) {
         const int base = (34 * b) >> 2;
         uint32_t dbits, q[8];
         if ((b & 1) == 0) {
@@ -251,14 +278,13 @@ __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
                  ::: "memory");
 }
-__device__ __forceinline__ float ld_dsmem_f32(const float *local, uint32_t rank) {
+
+__device__ __forceinline__ void st_dsmem_f32(const float *local, uint32_t rank, float v) {
     uint32_t remote;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
                  : "=r"(remote)
                  : "r"(smem_addr(local)), "r"(rank));
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-    return v;
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
 }
 
 struct StreamParams {
@@ -266,19 +292,21 @@ struct StreamParams {
     float *y;
     int n;            // rows of W
     int k;            // columns (multiple of 256)
+    int rw;           // row tiles per CTA
+    int kw;           // warps sharing one row tile (K split inside the CTA)
+    int cpw;          // chunks per warp
     int stages;       // ring depth per warp
-    int cpc;          // chunks per CTA (the K range of one cluster rank)
     LaunchCtx ctx;
 };
 
-// Grid: blockIdx.x = group * ksplit + rank, with a cluster of ksplit CTAs
-// along x.  Warp w of group g owns rows (g*nw + w)*32 .. +31; cluster rank r
-// owns chunks [r*cpc, (r+1)*cpc) of K.  Every warp streams all chunks of its
-// CTA's K range for its own rows, independently of the other warps.
-template <Fmt F, int M>
-__global__ void __launch_bounds__(128)
+// Grid: blockIdx.x = group * ksplit + rank (cluster of ksplit CTAs along x).
+// Warp w of a CTA owns row tile group*rw + w / kw and the (w % kw)-th part of
+// the CTA's K range; cluster rank r owns the r-th part of K.
+template <Fmt F, int M, int L>
+__global__ void __launch_bounds__(256)
     gemv_stream_kernel(const __grid_constant__ CUtensorMap wmap, StreamParams p) {
     constexpr int CB = StreamFmt<F>::kChunkBytes;
+    constexpr int kRowsPerWarp = 32 / L;  // L lanes share a row
     extern __shared__ __align__(128) uint8_t smem_dyn[];
     // TMA destinations: 128-byte aligned (the launch adds 128 bytes of slack)
     uint8_t *smem = smem_dyn + ((128u - (smem_addr(smem_dyn) & 127u)) & 127u);
@@ -286,24 +314,30 @@ __global__ void __launch_bounds__(128)
     const int warp = threadIdx.x >> 5;
     const int nw = blockDim.x >> 5;
     const int S = p.stages;
+    const int kw = p.kw, cpw = p.cpw;
     const uint32_t rank = cluster_ctarank();
     const uint32_t ksplit = cluster_nctarank();
     const int group = static_cast<int>(blockIdx.x / ksplit);
-    const int row0 = (group * nw + warp) * kRowsPerWarp;
-    const int row = row0 + lane;
+    const int tile_in_cta = warp / kw;
+    const int kpart = warp % kw;
+    const int row0 = (group * p.rw + tile_in_cta) * kRowsPerWarp;
+    const int r = lane / L;  // row within the warp's tile
+    const int h = lane % L;  // this lane's share of each chunk
+    const int row = row0 + r;
     const bool row_ok = row < p.n;
     const bool warp_active = row0 < p.n;  // warp-uniform
-    const int c_begin = static_cast<int>(rank) * p.cpc;
-    const int cpc = p.cpc;
+    const int cta_chunks = kw * cpw;
+    const int cta_c0 = static_cast<int>(rank) * cta_chunks;  // first chunk of the CTA
+    const int w_c0 = kpart * cpw;                            // first chunk of the warp, CTA-relative
+    const int XS = cta_chunks * kChunkK;  // activation floats per row in shared memory
 
-    const int XS = cpc * kChunkK;  // activation floats per row in shared memory
-
-    // shared memory: ring [nw][S][32 rows][CB] | xs [M][XS] | part [nw][M][32] |
-    //                bars [nw][S] | xbar
+    // shared memory: ring [nw][S][32 rows][CB] | xs [M][XS] | red [nw][M][32] |
+    //                part [ksplit][rw][M][32] (rank 0 only) | bars [nw][S] | xbar
     uint8_t *my_ring = smem + static_cast<size_t>(warp) * S * kRowsPerWarp * CB;
     float *xs = reinterpret_cast<float *>(smem + static_cast<size_t>(nw) * S * kRowsPerWarp * CB);
-    float *part = xs + M * XS;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(part + nw * M * kRowsPerWarp);
+    float *red = xs + M * XS;
+    float *part = red + nw * M * kRowsPerWarp;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(part + ksplit * p.rw * M * kRowsPerWarp);
     uint64_t *my_bars = bars + warp * S;
     uint64_t *xbar = bars + nw * S;
 
@@ -317,13 +351,13 @@ __global__ void __launch_bounds__(128)
     }
     __syncthreads();  // barriers initialised before any thread waits on them
 
-    auto issue = [&](int i) {  // chunk i of this CTA's K range into stage i % S
+    auto issue = [&](int i) {  // chunk i of this warp into stage i % S
         if (lane == 0) {
             const int st = i % S;
             // full box bytes: rows past N are zero-filled and still counted
             mbar_arrive_expect_tx(&my_bars[st], kRowsPerWarp * CB);
             tma_load_2d(my_ring + st * kRowsPerWarp * CB, &wmap,
-                        (c_begin + i) * (CB / StreamFmt<F>::kElemBytes), row0, &my_bars[st]);
+                        (cta_c0 + w_c0 + i) * (CB / StreamFmt<F>::kElemBytes), row0, &my_bars[st]);
         }
     };
     // The weight prefetch may start before the preceding kernel in the stream
@@ -332,13 +366,13 @@ __global__ void __launch_bounds__(128)
     // and outputs written only after the wait below.
     int issued = 0;
     if (warp_active)
-        for (; issued < min(S, cpc); ++issued) issue(issued);
+        for (; issued < min(S, cpw); ++issued) issue(issued);
     pdl_wait();
-    if (threadIdx.x == 0) {  // activations: one bulk copy per row m of the K range
+    if (threadIdx.x == 0) {  // activations: one bulk copy per row m of the CTA's K range
         mbar_arrive_expect_tx(xbar, static_cast<uint32_t>(M * XS * sizeof(float)));
 #pragma unroll
         for (int m = 0; m < M; ++m)
-            bulk_g2s(xs + m * XS, p.x + static_cast<size_t>(m) * p.k + c_begin * kChunkK,
+            bulk_g2s(xs + m * XS, p.x + static_cast<size_t>(m) * p.k + cta_c0 * kChunkK,
                      static_cast<uint32_t>(XS * sizeof(float)), xbar);
     }
     pdl_launch_dependents();
@@ -352,7 +386,7 @@ __global__ void __launch_bounds__(128)
     const bool x_ok = mbar_wait(xbar, 0, p.ctx);
     bool failed = !x_ok;
     if (warp_active) {
-        for (int i = 0; i < cpc && !failed; ++i) {
+        for (int i = 0; i < cpw && !failed; ++i) {
             const int st = i % S;
             const uint32_t par = static_cast<uint32_t>(i / S) & 1u;
             if (!mbar_wait(&my_bars[st], par, p.ctx)) {
@@ -360,14 +394,14 @@ __global__ void __launch_bounds__(128)
                 break;
             }
             ++consumed;
-            const uint8_t *src = my_ring + (st * kRowsPerWarp + lane) * CB;
-            const float *xk = xs + i * kChunkK;
+            const uint8_t *src = my_ring + (st * kRowsPerWarp + r) * CB + h * (CB / L);
+            const float *xk = xs + (w_c0 + i) * kChunkK + h * (kChunkK / L);
             if constexpr (F == Fmt::Q4_0)
-                q4_0_chunk<M>(src, xk, XS, tot);
+                q4_0_chunk<M, L>(src, xk, XS, tot);
             else
-                q8_0_chunk<M>(src, xk, XS, tot);
+                q8_0_chunk<M, L>(src, xk, XS, tot);
             __syncwarp();  // every lane is done reading the stage
-            if (issued < cpc) {
+            if (issued < cpw) {
                 fence_proxy_async_smem();
                 issue(issued);
                 ++issued;
@@ -382,27 +416,50 @@ __global__ void __launch_bounds__(128)
             mbar_wait(&my_bars[j % S], static_cast<uint32_t>(j / S) & 1u, p.ctx);
     }
 
+    // 0) the L lanes of a row add their shares (every lane ends with the sum)
+#pragma unroll
+    for (int off = 1; off < L; off <<= 1) {
+#pragma unroll
+        for (int m = 0; m < M; ++m) tot[m] += __shfl_xor_sync(0xFFFFFFFFu, tot[m], off);
+    }
+    const bool writer = h == 0;
+    // 1) K parts inside the CTA: warps kpart > 0 hand their sums to kpart 0
+    if (kw > 1) {
+        if (kpart > 0 && writer) {
+#pragma unroll
+            for (int m = 0; m < M; ++m) red[(warp * M + m) * kRowsPerWarp + r] = tot[m];
+        }
+        __syncthreads();
+        if (kpart == 0) {
+            for (int q = 1; q < kw; ++q) {
+#pragma unroll
+                for (int m = 0; m < M; ++m) tot[m] += red[((warp + q) * M + m) * kRowsPerWarp + r];
+            }
+        }
+    }
+    // 2) K parts across the cluster: ranks push into rank 0, which adds in rank order
     if (ksplit == 1) {
-        if (row_ok) {
+        if (kpart == 0 && writer && row_ok) {
 #pragma unroll
             for (int m = 0; m < M; ++m) p.y[static_cast<size_t>(m) * p.n + row] = tot[m];
         }
         return;
     }
-    // partial sums of the cluster's K ranges, added in rank order by rank 0
-    float *my_part = part + warp * M * kRowsPerWarp;
+    if (kpart == 0 && writer) {
+        float *slot = part + ((rank * p.rw + tile_in_cta) * M) * kRowsPerWarp;
 #pragma unroll
-    for (int m = 0; m < M; ++m) my_part[m * kRowsPerWarp + lane] = tot[m];
+        for (int m = 0; m < M; ++m) st_dsmem_f32(slot + m * kRowsPerWarp + r, 0, tot[m]);
+    }
     cluster_sync();
-    if (rank == 0 && row_ok) {
+    if (rank == 0 && kpart == 0 && writer && row_ok) {
 #pragma unroll
         for (int m = 0; m < M; ++m) {
-            float s = tot[m];
-            for (uint32_t q = 1; q < ksplit; ++q) s += ld_dsmem_f32(&my_part[m * kRowsPerWarp + lane], q);
+            float s = 0.0f;
+            for (uint32_t q = 0; q < ksplit; ++q)
+                s += part[((q * p.rw + tile_in_cta) * M + m) * kRowsPerWarp + r];
             p.y[static_cast<size_t>(m) * p.n + row] = s;
         }
     }
-    cluster_sync();  // peers keep their shared memory until rank 0 has read it
 }
 
 // Byte-wise fallback: one warp per row, lanes over blocks.
@@ -449,48 +506,60 @@ __global__ void __launch_bounds__(128) gemv_bytewise_kernel(const uint8_t *__res
     }
 }
 
-// Launch shape.  Units are (32-row tile, K range) pairs; K is split over a
-// cluster (ksplit CTAs) until there are enough units to give every SM
-// several resident warps.  Rings hold only as many stages as a warp has
-// chunks.
+// Launch shape.  g = kw * ksplit K parts per 32-row tile, the smallest
+// power of two giving about QMM_GEMV_WARPS_PER_SM warps per SM (at most one
+// part per chunk).  Parts go to warps of one CTA first (cheap reduction),
+// then to a cluster; CTAs hold rw tiles when kw alone gives few warps.  The
+// CTA's activation slice must fit its shared-memory budget.
 struct StreamShape {
-    int ksplit, nw, stages, cpc;
+    int ksplit, kw, rw, cpw, stages;
     size_t smem;
 };
 
-template <Fmt F, int M>
+template <Fmt F, int M, int L>
 StreamShape stream_shape(int64_t n, int64_t k, int sms) {
     constexpr int CB = StreamFmt<F>::kChunkBytes;
+    constexpr int kRowsPerWarp = 32 / L;
     StreamShape sh;
     const int64_t tiles = (n + kRowsPerWarp - 1) / kRowsPerWarp;
     const int C = static_cast<int>(k / kChunkK);
-    const int64_t want_units = static_cast<int64_t>(QMM_GEMV_UNITS_PER_SM) * sms;
-    sh.ksplit = 1;
-    while (sh.ksplit < QMM_GEMV_MAX_KSPLIT && tiles * sh.ksplit < want_units &&
-           C % (2 * sh.ksplit) == 0)
+    const int64_t want = static_cast<int64_t>(QMM_GEMV_WARPS_PER_SM) * sms;
+    int g = 1;
+    while (g < C && C % (2 * g) == 0 && tiles * g < want &&
+           g < QMM_GEMV_MAX_KW * QMM_GEMV_MAX_KSPLIT)
+        g *= 2;
+    sh.kw = std::min(g, QMM_GEMV_MAX_KW);
+    sh.ksplit = g / sh.kw;
+    // the CTA's activation slice (M rows x its K range) must fit the budget
+    while (sh.ksplit < QMM_GEMV_MAX_KSPLIT && (C / sh.ksplit) % 2 == 0 && sh.kw > 1 &&
+           static_cast<int64_t>(M) * (k / sh.ksplit) * 4 > QMM_GEMV_X_BYTES) {
         sh.ksplit *= 2;
-    // the CTA's activation slice (M rows x K range) must fit its budget
-    while (sh.ksplit < QMM_GEMV_MAX_KSPLIT && C % (2 * sh.ksplit) == 0 &&
+        sh.kw /= 2;
+    }
+    while (sh.ksplit < QMM_GEMV_MAX_KSPLIT && (C / sh.ksplit) % 2 == 0 &&
            static_cast<int64_t>(M) * (k / sh.ksplit) * 4 > QMM_GEMV_X_BYTES)
         sh.ksplit *= 2;
-    sh.cpc = C / sh.ksplit;
-    const int64_t units = tiles * sh.ksplit;
-    sh.nw = 1;
-    while (sh.nw < QMM_GEMV_MAX_WARPS && units / (2 * sh.nw) >= 2LL * sms) sh.nw *= 2;
-    sh.stages = std::min(sh.cpc, QMM_GEMV_STAGES);
-    sh.smem = static_cast<size_t>(sh.nw) * sh.stages * kRowsPerWarp * CB +
-              sizeof(float) * (static_cast<size_t>(M) * sh.cpc * kChunkK +
-                               static_cast<size_t>(sh.nw) * M * kRowsPerWarp) +
-              sizeof(uint64_t) * (sh.nw * sh.stages + 1) + 128;
+    sh.cpw = C / (sh.kw * sh.ksplit);
+    sh.rw = 1;
+    while (sh.rw * sh.kw < QMM_GEMV_MIN_WARPS && tiles >= 2LL * sh.rw * sms) sh.rw *= 2;
+    sh.stages = std::min(sh.cpw, QMM_GEMV_STAGES);
+    const int nw = sh.rw * sh.kw;
+    const int cta_chunks = sh.kw * sh.cpw;
+    sh.smem = static_cast<size_t>(nw) * sh.stages * kRowsPerWarp * CB +
+              sizeof(float) * (static_cast<size_t>(M) * cta_chunks * kChunkK +
+                               static_cast<size_t>(nw) * M * kRowsPerWarp +
+                               static_cast<size_t>(sh.ksplit) * sh.rw * M * kRowsPerWarp) +
+              sizeof(uint64_t) * (nw * sh.stages + 1) + 128;
     return sh;
 }
 
-template <Fmt F, int M>
+template <Fmt F, int M, int L>
 cudaError_t launch_stream(const uint8_t *w, const float *x, float *y, int64_t n, int64_t k,
                           cudaStream_t stream, const LaunchCtx &ctx) {
-    const StreamShape sh = stream_shape<F, M>(n, k, device_sm_count());
+    constexpr int kRowsPerWarp = 32 / L;
+    const StreamShape sh = stream_shape<F, M, L>(n, k, device_sm_count());
     const int64_t tiles = (n + kRowsPerWarp - 1) / kRowsPerWarp;
-    const int64_t groups = (tiles + sh.nw - 1) / sh.nw;
+    const int64_t groups = (tiles + sh.rw - 1) / sh.rw;
     CUtensorMap wmap;
     const uint64_t rowbytes = static_cast<uint64_t>(k / kChunkK) * StreamFmt<F>::kChunkBytes;
     constexpr int EB = StreamFmt<F>::kElemBytes;
@@ -502,23 +571,34 @@ cudaError_t launch_stream(const uint8_t *w, const float *x, float *y, int64_t n,
     p.y = y;
     p.n = static_cast<int>(n);
     p.k = static_cast<int>(k);
+    p.rw = sh.rw;
+    p.kw = sh.kw;
+    p.cpw = sh.cpw;
     p.stages = sh.stages;
-    p.cpc = sh.cpc;
     p.ctx = ctx;
-    auto kern = gemv_stream_kernel<F, M>;
+    auto kern = gemv_stream_kernel<F, M, L>;
     static int smem_limits[kMaxDevices] = {0};  // this instantiation's own cache
     const cudaError_t e = ensure_smem(kern, sh.smem, true, smem_limits);
     if (e != cudaSuccess) return e;
-    return launch_kernel(kern, dim3(static_cast<unsigned>(groups * sh.ksplit)), dim3(sh.nw * 32),
-                         sh.smem, stream, static_cast<unsigned>(sh.ksplit), wmap, p);
+    return launch_kernel(kern, dim3(static_cast<unsigned>(groups * sh.ksplit)),
+                         dim3(sh.rw * sh.kw * 32), sh.smem, stream,
+                         static_cast<unsigned>(sh.ksplit), wmap, p);
 }
 
 template <Fmt F, int M>
 cudaError_t launch_m(const uint8_t *w, const float *x, float *y, int64_t n, int64_t k,
                      cudaStream_t stream, const LaunchCtx &ctx) {
     const bool aligned = ((reinterpret_cast<uintptr_t>(w) | reinterpret_cast<uintptr_t>(x)) & 15) == 0;
-    if (k % kChunkK == 0 && aligned && n <= (1LL << 30) && k <= (1LL << 24))
-        return launch_stream<F, M>(w, x, y, n, k, stream, ctx);
+    if (k % kChunkK == 0 && aligned && n <= (1LL << 30) && k <= (1LL << 24)) {
+        // Lanes per row: small problems at small M are latency bound, so more
+        // lanes share each row chunk; large or wide-M problems keep one.
+        if constexpr (M <= 4) {
+            const int64_t units = ((n + 31) / 32) * (k / kChunkK);
+            if (units <= QMM_GEMV_L4_UNITS) return launch_stream<F, M, 4>(w, x, y, n, k, stream, ctx);
+            if (units <= QMM_GEMV_L2_UNITS) return launch_stream<F, M, 2>(w, x, y, n, k, stream, ctx);
+        }
+        return launch_stream<F, M, 1>(w, x, y, n, k, stream, ctx);
+    }
     const unsigned grid = static_cast<unsigned>((n + 3) / 4);
     return launch_kernel(gemv_bytewise_kernel<F, M>, dim3(grid), dim3(128), 0, stream, 1, w, x, y,
                          n, k, ctx);
