@@ -16,7 +16,7 @@ barrier and a device synchronise on both sides, max over ranks.  SM clocks
 and throttle reasons are sampled with nvidia-smi during the timed region.
 
 `e2e` repeats the step through the public API with host buffers: each step
-copies its activations from pinned host memory, runs the seven calls and
+copies its activations from pinned host memory, runs the step's calls and
 copies the outputs back (weights stay resident: they are the model).
 
 `--impl reference` times the CPU oracle (the plain C definition) on the
@@ -282,35 +282,55 @@ def capture(torch, stream, body):
     return g
 
 
+# The decode layer's GEMV calls in dependency order: q, k and v read the
+# same normed hidden state (one grouped call), o reads the attention output,
+# gate and up read the same FFN input (one grouped call), down reads their
+# activation.  Each group is one launch.
+DECODE_GROUPS = (("q", "k", "v"), ("o",), ("gate", "up"), ("down",))
+
+
 class DecodeLayer:
-    """Seven Q4_0 projections, M = 1, R rotating weight replicas."""
+    """GEMV groups over R rotating weight replicas; a group's projections
+    share one activation matrix and run as one call."""
 
     def __init__(self, torch, qmm, l2_bytes, stream, m=1, projections=synth.DECODE_LAYER,
-                 stream_base=10, fmt="q4_0", weights=None):
+                 stream_base=10, fmt="q4_0", weights=None, groups=None):
         self.torch, self.qmm, self.m, self.fmt = torch, qmm, m, fmt
         self.projs = projections
         self.cases = [synth.gemv_case(fmt, m, p.n, p.k, seed=0, stream=stream_base + i,
                                       weights=None if weights is None else weights[i])
                       for i, p in enumerate(projections)]
+        names = [p.name for p in projections]
+        if groups is None:
+            groups = tuple((nm,) for nm in names)
+        self.groups = [[names.index(nm) for nm in g] for g in groups]
         bb = 18 if fmt == "q4_0" else 34
         self.step_bytes = sum(p.n * (p.k // 32) * bb for p in projections)
-        self.launches_per_step = len(projections)
+        self.launches_per_step = len(self.groups)
         self.R = replicas_for(self.step_bytes, l2_bytes)
         dev = torch.device("cuda")
         base = [torch.from_numpy(c.w.reshape(-1)).to(dev) for c in self.cases]
         self.W = [[b.clone() for b in base] for _ in range(self.R)]
         del base
-        self.X = [torch.from_numpy(c.x).to(dev) for c in self.cases]
+        # one activation matrix per group (the first member's synthetic x)
+        self.X = [torch.from_numpy(self.cases[g[0]].x).to(dev) for g in self.groups]
         self.Y = [torch.empty((m, p.n), dtype=torch.float32, device=dev) for p in projections]
         self.stream = stream
         self.fn = qmm.qmm_gemv_q4_0 if fmt == "q4_0" else qmm.qmm_gemv_q8_0
+        self.fn_multi = qmm.qmm_gemv_q4_0_multi if fmt == "q4_0" else qmm.qmm_gemv_q8_0_multi
         self.full = capture(torch, stream, lambda: [self.step(r) for r in range(self.R)])
         self.single = [None] * self.R
 
     def step(self, r):
         s = self.stream.cuda_stream
-        for i, p in enumerate(self.projs):
-            self.fn(self.W[r][i], self.X[i], self.Y[i], self.m, p.n, p.k, s)
+        for gi, g in enumerate(self.groups):
+            k = self.projs[g[0]].k
+            if len(g) == 1:
+                i = g[0]
+                self.fn(self.W[r][i], self.X[gi], self.Y[i], self.m, self.projs[i].n, k, s)
+            else:
+                self.fn_multi([(self.W[r][i], self.Y[i], self.projs[i].n) for i in g],
+                              self.X[gi], self.m, k, s)
 
     def run_steps(self, k):
         """Exactly k steps, rotating replicas from replica 0."""
@@ -324,8 +344,8 @@ class DecodeLayer:
 
 def measure_e2e(torch, qmm, layer: DecodeLayer, steps: int, dist):
     """Same step through the public API with host buffers: pinned host x ->
-    device, seven calls, device y -> pinned host, every step."""
-    xs_host = [torch.from_numpy(c.x).pin_memory() for c in layer.cases]
+    device, the step's calls, device y -> pinned host, every step."""
+    xs_host = [torch.from_numpy(layer.cases[g[0]].x).pin_memory() for g in layer.groups]
     ys_host = [torch.empty(y.shape, dtype=torch.float32).pin_memory() for y in layer.Y]
     h2d = sum(x.numel() * 4 for x in xs_host)
     d2h = sum(y.numel() * 4 for y in ys_host)
@@ -459,7 +479,7 @@ def run_ours(args, dist):
     stream = torch.cuda.Stream()
     timer = Timer(torch, stream)
 
-    layer = DecodeLayer(torch, qmm, l2, stream)
+    layer = DecodeLayer(torch, qmm, l2, stream, groups=DECODE_GROUPS)
     warm = max(3, args.warmup)
     layer.run_steps(warm)
     torch.cuda.synchronize()
@@ -500,7 +520,8 @@ def run_ours(args, dist):
         "config": {
             "workload": "Q4_0 decode-layer GEMV set, M=1: q 2048->2048, k 2048->512, "
                         "v 2048->512, o 2048->2048, gate 2048->8192, up 2048->8192, "
-                        "down 8192->2048 (34,209,792 weight bytes per step)",
+                        "down 8192->2048 (34,209,792 weight bytes per step), as 4 dependent "
+                        "calls: q+k+v grouped (shared x), o, gate+up grouped, down",
             "weight_bytes_per_step": layer.step_bytes,
             "launches_per_step": layer.launches_per_step,
             "replicas": layer.R,
@@ -525,8 +546,8 @@ def run_ours(args, dist):
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps,
-                "path": "pinned host x -> device, 7 C-ABI calls via ctypes, device y -> "
-                        "pinned host, per step; host wall clock"},
+                "path": "pinned host x -> device, the step's 4 C-ABI calls via ctypes, device "
+                        "y -> pinned host, per step; host wall clock"},
         "gpu_launches": args.steps * layer.launches_per_step,
     }
     del layer

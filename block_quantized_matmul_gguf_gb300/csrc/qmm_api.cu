@@ -89,20 +89,36 @@ qmm_status dequant(Fmt fmt, const void *w, float *out, int64_t n, int64_t k,
                                     reinterpret_cast<cudaStream_t>(stream), ctx));
 }
 
-qmm_status gemv(Fmt fmt, const void *w, const float *x, float *y, int m, int64_t n, int64_t k,
+qmm_status gemv(Fmt fmt, const qmm_gemv_out *outs, int count, const float *x, int m, int64_t k,
                 qmm_stream_t stream) {
-    qmm_status s = check_wk(w, n, k);
-    if (s != QMM_OK) return s;
-    if (!x || !y) return QMM_ERR_NULL;
+    if (!outs || !x) return QMM_ERR_NULL;
+    if (count < 1 || count > QMM_GEMV_MAX_OUTPUTS) return QMM_ERR_SHAPE;
     if (m < 1 || m > QMM_GEMV_MAX_M) return QMM_ERR_SHAPE;
-    if (!aligned(x, 4) || !aligned(y, 4)) return QMM_ERR_ALIGN;
-    const size_t wbytes = static_cast<size_t>(n) * (k / kQK) * block_bytes(fmt);
-    const size_t ybytes = sizeof(float) * static_cast<size_t>(m) * n;
-    if (overlaps(y, ybytes, w, wbytes) || overlaps(y, ybytes, x, sizeof(float) * m * k))
-        return QMM_ERR_UNSUPPORTED;
+    if (!aligned(x, 4)) return QMM_ERR_ALIGN;
+    GemvProblem probs[QMM_GEMV_MAX_OUTPUTS];
+    for (int i = 0; i < count; ++i) {
+        const qmm_status s = check_wk(outs[i].w, outs[i].n, k);
+        if (s != QMM_OK) return s;
+        if (!outs[i].y) return QMM_ERR_NULL;
+        if (!aligned(outs[i].y, 4)) return QMM_ERR_ALIGN;
+        probs[i] = GemvProblem{outs[i].w, outs[i].y, outs[i].n};
+    }
+    // no output may overlap an input or another output
+    const size_t xbytes = sizeof(float) * static_cast<size_t>(m) * k;
+    for (int i = 0; i < count; ++i) {
+        const size_t ybytes = sizeof(float) * static_cast<size_t>(m) * outs[i].n;
+        if (overlaps(outs[i].y, ybytes, x, xbytes)) return QMM_ERR_UNSUPPORTED;
+        for (int j = 0; j < count; ++j) {
+            const size_t wbytes = static_cast<size_t>(outs[j].n) * (k / kQK) * block_bytes(fmt);
+            if (overlaps(outs[i].y, ybytes, outs[j].w, wbytes)) return QMM_ERR_UNSUPPORTED;
+            if (j != i && overlaps(outs[i].y, ybytes, outs[j].y,
+                                   sizeof(float) * static_cast<size_t>(m) * outs[j].n))
+                return QMM_ERR_UNSUPPORTED;
+        }
+    }
     LaunchCtx ctx;
     if (!make_ctx(&ctx)) return QMM_ERR_CUDA;
-    return from_cuda(launch_gemv(fmt, static_cast<const uint8_t *>(w), x, y, m, n, k,
+    return from_cuda(launch_gemv(fmt, probs, count, x, m, k,
                                  reinterpret_cast<cudaStream_t>(stream), ctx));
 }
 
@@ -174,12 +190,24 @@ qmm_status qmm_dequant_q8_0(const void *w, float *out, int64_t n, int64_t k,
 
 qmm_status qmm_gemv_q4_0(const void *w, const float *x, float *y, int m, int64_t n, int64_t k,
                          qmm_stream_t stream) {
-    return gemv(Fmt::Q4_0, w, x, y, m, n, k, stream);
+    const qmm_gemv_out one = {w, y, n};
+    return gemv(Fmt::Q4_0, &one, 1, x, m, k, stream);
 }
 
 qmm_status qmm_gemv_q8_0(const void *w, const float *x, float *y, int m, int64_t n, int64_t k,
                          qmm_stream_t stream) {
-    return gemv(Fmt::Q8_0, w, x, y, m, n, k, stream);
+    const qmm_gemv_out one = {w, y, n};
+    return gemv(Fmt::Q8_0, &one, 1, x, m, k, stream);
+}
+
+qmm_status qmm_gemv_q4_0_multi(const qmm_gemv_out *outs, int count, const float *x, int m,
+                               int64_t k, qmm_stream_t stream) {
+    return gemv(Fmt::Q4_0, outs, count, x, m, k, stream);
+}
+
+qmm_status qmm_gemv_q8_0_multi(const qmm_gemv_out *outs, int count, const float *x, int m,
+                               int64_t k, qmm_stream_t stream) {
+    return gemv(Fmt::Q8_0, outs, count, x, m, k, stream);
 }
 
 qmm_status qmm_gemm_q4_0(const void *w, const uint16_t *x_bf16, float *y, int64_t m, int64_t n,

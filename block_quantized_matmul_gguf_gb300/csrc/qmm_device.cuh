@@ -110,21 +110,15 @@ __device__ __forceinline__ void bulk_g2s(void *dst_smem, const void *src_gmem, u
         : "memory");
 }
 
-// ---- small loads -------------------------------------------------------------
+// ---- shared-memory loads --------------------------------------------------------
+// Plain C++ accesses (not volatile asm), so the compiler may schedule them
+// early; the "memory" clobber of every barrier wait keeps them after it.
 __device__ __forceinline__ uint4 lds128(const void *p) {
-    uint4 v;
-    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(smem_addr(p)));
-    return v;
+    return *reinterpret_cast<const uint4 *>(p);
 }
 
 __device__ __forceinline__ float4 lds128f(const float *p) {
-    float4 v;
-    asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(smem_addr(p)));
-    return v;
+    return *reinterpret_cast<const float4 *>(p);
 }
 
 // binary16 bit pattern -> fp32 (exact for every pattern; hardware convert).

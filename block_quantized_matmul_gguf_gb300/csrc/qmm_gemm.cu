@@ -51,8 +51,17 @@ constexpr int BK = 64;               // K per operand stage (one 128-byte swizzl
 constexpr int UMMA_K = 16;           // K per tcgen05.mma (kind::f16)
 constexpr int RAW_K = 256;           // K per raw stage (8 Q4_0 blocks)
 constexpr int RAW_ROW_BYTES = 144;   // 8 blocks x 18 bytes
-constexpr int OP_STAGES = 5;
-constexpr int RAW_STAGES = 2;
+#ifndef QMM_GEMM_OP_STAGES
+#define QMM_GEMM_OP_STAGES 5
+#endif
+#ifndef QMM_GEMM_RAW_STAGES
+#define QMM_GEMM_RAW_STAGES 2
+#endif
+#ifndef QMM_GEMM_DEQ_WARPS
+#define QMM_GEMM_DEQ_WARPS 8  // 8: a thread decodes one block per K stage; 16: half a block
+#endif
+constexpr int OP_STAGES = QMM_GEMM_OP_STAGES;
+constexpr int RAW_STAGES = QMM_GEMM_RAW_STAGES;
 constexpr int X_STAGE_BYTES = BM * BK * 2;               // 16 KB
 constexpr int W_STAGE_BYTES = BN_CTA * BK * 2;           // 16 KB
 constexpr int RAW_STAGE_BYTES = BN_CTA * RAW_ROW_BYTES;  // 18 KB
@@ -62,12 +71,14 @@ constexpr uint32_t TMEM_COLS = NUM_ACC * BN;             // 512 fp32 columns
 constexpr int WARP_PRODUCER = 0;
 constexpr int WARP_MMA = 1;
 constexpr int WARP_DEQ0 = 2;
-constexpr int NUM_DEQ_WARPS = 8;                     // two threads per W row
+constexpr int NUM_DEQ_WARPS = QMM_GEMM_DEQ_WARPS;     // 2 or 4 threads per W row
 constexpr int WARP_EPI0 = WARP_DEQ0 + NUM_DEQ_WARPS;  // 10
 constexpr int NUM_EPI_WARPS = 4;
 constexpr int NUM_THREADS = (WARP_EPI0 + NUM_EPI_WARPS) * 32;  // 448
 
-static_assert(NUM_DEQ_WARPS * 32 == 2 * BN_CTA, "two dequantiser threads per W row");
+static_assert(NUM_DEQ_WARPS * 32 == 2 * BN_CTA || NUM_DEQ_WARPS * 32 == 4 * BN_CTA,
+              "two or four dequantiser threads per W row");
+constexpr int DEQ_PER_ROW = NUM_DEQ_WARPS * 32 / BN_CTA;
 static_assert(RAW_K % BK == 0 && BK == 2 * 32, "a K stage is two blocks");
 
 struct SmemLayout {
@@ -316,10 +327,13 @@ __device__ __forceinline__ uint32_t w_pair(float ma, float mb, float2 c, float2 
     return pack_bf16x2(w.x, w.y);
 }
 
-// Dequantise Q4_0 block `b` (0..7) of a 144-byte row chunk held in wd[36]
-// into 32 bf16 values = four 16-byte chunks q[0..3] (K order).
-__device__ __forceinline__ void dequant_block_bf16(const uint32_t (&wd)[36], int b,
-                                                   uint4 (&out)[4]) {
+// Dequantise qs words [I0, I0 + NI) of Q4_0 block `b` (0..7) of a 144-byte
+// row chunk held in wd[36].  Word i holds weights 4i..4i+3 (low nibbles) and
+// 16+4i..19+4i (high nibbles); out[0..NI/2) are the low 16-byte chunks
+// (K 8*I0/2 ..), out[NI/2..NI) the high ones (K 16 + ...).
+template <int I0, int NI>
+__device__ __forceinline__ void dequant_words_bf16(const uint32_t (&wd)[36], int b,
+                                                   uint4 (&out)[NI]) {
     const int base = (18 * b) >> 2;
     uint32_t dbits, q[4];
     if ((b & 1) == 0) {
@@ -338,28 +352,25 @@ __device__ __forceinline__ void dequant_block_bf16(const uint32_t (&wd)[36], int
     const float2 c168 = make_float2(-8912896.0f, -8390656.0f); // s = 16, 8
     const float2 c412 = make_float2(-8388736.0f, -8421376.0f); // s = 4, 12
     const float2 d08 = make_float2(d, d8), d168 = make_float2(d16, d8), d412 = make_float2(d4, d12);
-    uint32_t lo[8], hi[8];
+    uint32_t lo[2 * NI], hi[2 * NI];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const uint32_t v = q[i], u = v >> 16;
+    for (int j = 0; j < NI; ++j) {
+        const uint32_t v = q[I0 + j], u = v >> 16;
         // low nibbles: weights 4i .. 4i+3
-        lo[2 * i + 0] = w_pair(mag(v, 0x0000000Fu), mag(v, 0x00000F00u), c08, d08);
-        lo[2 * i + 1] = w_pair(mag(v, 0x000F0000u), mag(u, 0x00000F00u), c168, d168);
+        lo[2 * j + 0] = w_pair(mag(v, 0x0000000Fu), mag(v, 0x00000F00u), c08, d08);
+        lo[2 * j + 1] = w_pair(mag(v, 0x000F0000u), mag(u, 0x00000F00u), c168, d168);
         // high nibbles: weights 16+4i .. 19+4i
-        hi[2 * i + 0] = w_pair(mag(v, 0x000000F0u), mag(v, 0x0000F000u), c412, d412);
-        hi[2 * i + 1] = w_pair(mag(u, 0x000000F0u), mag(u, 0x0000F000u), c412, d412);
+        hi[2 * j + 0] = w_pair(mag(v, 0x000000F0u), mag(v, 0x0000F000u), c412, d412);
+        hi[2 * j + 1] = w_pair(mag(u, 0x000000F0u), mag(u, 0x0000F000u), c412, d412);
     }
-    out[0] = make_uint4(lo[0], lo[1], lo[2], lo[3]);  // k 0..7
-    out[1] = make_uint4(lo[4], lo[5], lo[6], lo[7]);  // k 8..15
-    out[2] = make_uint4(hi[0], hi[1], hi[2], hi[3]);  // k 16..23
-    out[3] = make_uint4(hi[4], hi[5], hi[6], hi[7]);  // k 24..31
+#pragma unroll
+    for (int c = 0; c < NI / 2; ++c) {
+        out[c] = make_uint4(lo[4 * c], lo[4 * c + 1], lo[4 * c + 2], lo[4 * c + 3]);
+        out[NI / 2 + c] = make_uint4(hi[4 * c], hi[4 * c + 1], hi[4 * c + 2], hi[4 * c + 3]);
+    }
 }
 
-__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
-    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y),
-                 "r"(v.z), "r"(v.w)
-                 : "memory");
-}
+
 
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_q4_0_kernel(const __grid_constant__ CUtensorMap tmap_x,
@@ -524,10 +535,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
         }
     } else if (warp < WARP_EPI0) {
-        // dequantisers: thread dt owns W row dt % 128, block (2*sub + half) of each K stage
+        // dequantisers: thread dt owns W row dt % 128 and, of each 64-wide K
+        // stage, block (2*sub + half) -- all of it (2 threads per row) or the
+        // qs words 2*wh, 2*wh+1 of it (4 threads per row)
         const int dt = (warp - WARP_DEQ0) * 32 + lane;
         const int row = dt & (BN_CTA - 1);
-        const int half = dt >> 7;
+        const int part = dt >> 7;  // warp-uniform
+        const int half = DEQ_PER_ROW == 2 ? part : (part >> 1);
+        const int wh = DEQ_PER_ROW == 2 ? 0 : (part & 1);
         // leader: arrive on its own w_ready; peer: on its w_local (forwarded)
         const uint32_t done0 = leader ? w_ready(0) : w_local(0);
         uint32_t it = 0, rit = 0;
@@ -555,17 +570,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const int s = it % OP_STAGES;
                     const uint32_t ph = (it / OP_STAGES) & 1u;
                     if (!warp_wait_or_abort(op_empty(s), ph ^ 1u, abort_flag, ctx)) { ok = false; break; }
-                    const uint32_t row_addr = sbase + SmemLayout::w + s * W_STAGE_BYTES + row * 128;
+                    uint8_t *row_ptr = sgen + SmemLayout::w + s * W_STAGE_BYTES + row * 128;
                     const uint32_t sw = static_cast<uint32_t>(row & 7);
-                    uint4 ch[4];
                     // block 2*sub + half of the row chunk: K positions 32*half .. +31
-                    if (half == 0)
-                        dequant_block_bf16(wd, 2 * sub, ch);
-                    else
-                        dequant_block_bf16(wd, 2 * sub + 1, ch);
+                    if constexpr (DEQ_PER_ROW == 2) {
+                        uint4 ch[4];
+                        if (half == 0)
+                            dequant_words_bf16<0, 4>(wd, 2 * sub, ch);
+                        else
+                            dequant_words_bf16<0, 4>(wd, 2 * sub + 1, ch);
 #pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        sts128(row_addr + (((4 * half + c) ^ sw) << 4), ch[c]);
+                        for (int c = 0; c < 4; ++c)
+                            *reinterpret_cast<uint4 *>(row_ptr + (((4 * half + c) ^ sw) << 4)) = ch[c];
+                    } else {
+                        // words 2*wh, 2*wh+1: chunk wh (low nibbles) and 2 + wh (high)
+                        uint4 ch[2];
+                        const int b = 2 * sub + half;
+                        if (wh == 0) {
+                            if (half == 0) dequant_words_bf16<0, 2>(wd, 2 * sub, ch);
+                            else dequant_words_bf16<0, 2>(wd, 2 * sub + 1, ch);
+                        } else {
+                            if (half == 0) dequant_words_bf16<2, 2>(wd, 2 * sub, ch);
+                            else dequant_words_bf16<2, 2>(wd, 2 * sub + 1, ch);
+                        }
+                        (void)b;
+                        *reinterpret_cast<uint4 *>(row_ptr + (((4 * half + wh) ^ sw) << 4)) = ch[0];
+                        *reinterpret_cast<uint4 *>(row_ptr + (((4 * half + 2 + wh) ^ sw) << 4)) = ch[1];
+                    }
                     fence_proxy_async_smem();  // generic writes -> visible to the tensor core
                     __syncwarp();
                     if (lane == 0) mbar_arrive_addr(done0 + 8u * s);

@@ -68,6 +68,8 @@
 namespace qmm {
 namespace {
 
+constexpr int kMaxGemvProblems = 4;
+
 constexpr int kChunkK = 256;
 constexpr uint32_t kMagic = 0x4B000000u;  // 2^23
 
@@ -124,15 +126,13 @@ __device__ __forceinline__ void load_portion(const uint8_t *src, uint32_t (&wd)[
     } else if constexpr (L == 2) {
 #pragma unroll
         for (int t = 0; t < WORDS / 2; ++t) {
-            uint32_t a, b;
-            asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(a), "=r"(b) : "r"(smem_addr(src + 8 * t)));
-            wd[2 * t + 0] = a;
-            wd[2 * t + 1] = b;
+            const uint2 v = *reinterpret_cast<const uint2 *>(src + 8 * t);
+            wd[2 * t + 0] = v.x;
+            wd[2 * t + 1] = v.y;
         }
     } else {
 #pragma unroll
-        for (int t = 0; t < WORDS; ++t)
-            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(wd[t]) : "r"(smem_addr(src + 4 * t)));
+        for (int t = 0; t < WORDS; ++t) wd[t] = *reinterpret_cast<const uint32_t *>(src + 4 * t);
     }
 }
 
@@ -287,10 +287,18 @@ __device__ __forceinline__ void st_dsmem_f32(const float *local, uint32_t rank, 
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
 }
 
+// Up to kMaxGemvProblems weight matrices that share the activations x (and
+// K), e.g. the q/k/v or gate/up projections of a decode layer, in one launch.
+struct StreamMaps {
+    CUtensorMap m[kMaxGemvProblems];
+};
+
 struct StreamParams {
     const float *x;
-    float *y;
-    int n;            // rows of W
+    float *y[kMaxGemvProblems];
+    int n[kMaxGemvProblems];                  // rows of each W
+    int group_begin[kMaxGemvProblems + 1];    // first CTA group of each problem
+    int count;                                // problems
     int k;            // columns (multiple of 256)
     int rw;           // row tiles per CTA
     int kw;           // warps sharing one row tile (K split inside the CTA)
@@ -304,7 +312,7 @@ struct StreamParams {
 // the CTA's K range; cluster rank r owns the r-th part of K.
 template <Fmt F, int M, int L>
 __global__ void __launch_bounds__(256)
-    gemv_stream_kernel(const __grid_constant__ CUtensorMap wmap, StreamParams p) {
+    gemv_stream_kernel(const __grid_constant__ StreamMaps maps, StreamParams p) {
     constexpr int CB = StreamFmt<F>::kChunkBytes;
     constexpr int kRowsPerWarp = 32 / L;  // L lanes share a row
     extern __shared__ __align__(128) uint8_t smem_dyn[];
@@ -317,15 +325,21 @@ __global__ void __launch_bounds__(256)
     const int kw = p.kw, cpw = p.cpw;
     const uint32_t rank = cluster_ctarank();
     const uint32_t ksplit = cluster_nctarank();
-    const int group = static_cast<int>(blockIdx.x / ksplit);
+    const int gg = static_cast<int>(blockIdx.x / ksplit);  // CTA group over all problems
+    int prob = 0;
+    while (prob + 1 < p.count && gg >= p.group_begin[prob + 1]) ++prob;
+    const int group = gg - p.group_begin[prob];
+    const int n_rows = p.n[prob];
+    float *const y = p.y[prob];
+    const CUtensorMap *wmap = &maps.m[prob];
     const int tile_in_cta = warp / kw;
     const int kpart = warp % kw;
     const int row0 = (group * p.rw + tile_in_cta) * kRowsPerWarp;
     const int r = lane / L;  // row within the warp's tile
     const int h = lane % L;  // this lane's share of each chunk
     const int row = row0 + r;
-    const bool row_ok = row < p.n;
-    const bool warp_active = row0 < p.n;  // warp-uniform
+    const bool row_ok = row < n_rows;
+    const bool warp_active = row0 < n_rows;  // warp-uniform
     const int cta_chunks = kw * cpw;
     const int cta_c0 = static_cast<int>(rank) * cta_chunks;  // first chunk of the CTA
     const int w_c0 = kpart * cpw;                            // first chunk of the warp, CTA-relative
@@ -343,7 +357,7 @@ __global__ void __launch_bounds__(256)
 
     if (lane == 0) {
         if (warp == 0) {
-            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&wmap)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(wmap)) : "memory");
             mbar_init(xbar, 1);
         }
         for (int s = 0; s < S; ++s) mbar_init(&my_bars[s], 1);
@@ -356,7 +370,7 @@ __global__ void __launch_bounds__(256)
             const int st = i % S;
             // full box bytes: rows past N are zero-filled and still counted
             mbar_arrive_expect_tx(&my_bars[st], kRowsPerWarp * CB);
-            tma_load_2d(my_ring + st * kRowsPerWarp * CB, &wmap,
+            tma_load_2d(my_ring + st * kRowsPerWarp * CB, wmap,
                         (cta_c0 + w_c0 + i) * (CB / StreamFmt<F>::kElemBytes), row0, &my_bars[st]);
         }
     };
@@ -441,7 +455,7 @@ __global__ void __launch_bounds__(256)
     if (ksplit == 1) {
         if (kpart == 0 && writer && row_ok) {
 #pragma unroll
-            for (int m = 0; m < M; ++m) p.y[static_cast<size_t>(m) * p.n + row] = tot[m];
+            for (int m = 0; m < M; ++m) y[static_cast<size_t>(m) * n_rows + row] = tot[m];
         }
         return;
     }
@@ -457,7 +471,7 @@ __global__ void __launch_bounds__(256)
             float s = 0.0f;
             for (uint32_t q = 0; q < ksplit; ++q)
                 s += part[((q * p.rw + tile_in_cta) * M + m) * kRowsPerWarp + r];
-            p.y[static_cast<size_t>(m) * p.n + row] = s;
+            y[static_cast<size_t>(m) * n_rows + row] = s;
         }
     }
 }
@@ -517,11 +531,10 @@ struct StreamShape {
 };
 
 template <Fmt F, int M, int L>
-StreamShape stream_shape(int64_t n, int64_t k, int sms) {
+StreamShape stream_shape(int64_t tiles, int64_t k, int sms) {
     constexpr int CB = StreamFmt<F>::kChunkBytes;
     constexpr int kRowsPerWarp = 32 / L;
     StreamShape sh;
-    const int64_t tiles = (n + kRowsPerWarp - 1) / kRowsPerWarp;
     const int C = static_cast<int>(k / kChunkK);
     const int64_t want = static_cast<int64_t>(QMM_GEMV_WARPS_PER_SM) * sms;
     int g = 1;
@@ -553,63 +566,91 @@ StreamShape stream_shape(int64_t n, int64_t k, int sms) {
     return sh;
 }
 
+// One launch over `count` problems sharing x: problem i has weights
+// probs[i].w (probs[i].n rows) and output probs[i].y.
 template <Fmt F, int M, int L>
-cudaError_t launch_stream(const uint8_t *w, const float *x, float *y, int64_t n, int64_t k,
+cudaError_t launch_stream(const GemvProblem *probs, int count, const float *x, int64_t k,
                           cudaStream_t stream, const LaunchCtx &ctx) {
     constexpr int kRowsPerWarp = 32 / L;
-    const StreamShape sh = stream_shape<F, M, L>(n, k, device_sm_count());
-    const int64_t tiles = (n + kRowsPerWarp - 1) / kRowsPerWarp;
-    const int64_t groups = (tiles + sh.rw - 1) / sh.rw;
-    CUtensorMap wmap;
-    const uint64_t rowbytes = static_cast<uint64_t>(k / kChunkK) * StreamFmt<F>::kChunkBytes;
-    constexpr int EB = StreamFmt<F>::kElemBytes;
-    if (!encode_tmap_2d(&wmap, StreamFmt<F>::kType, w, rowbytes / EB, n, rowbytes,
-                        StreamFmt<F>::kChunkBytes / EB, kRowsPerWarp))
-        return cudaErrorInvalidValue;
+    int64_t tiles = 0;
+    for (int i = 0; i < count; ++i) tiles += (probs[i].n + kRowsPerWarp - 1) / kRowsPerWarp;
+    const StreamShape sh = stream_shape<F, M, L>(tiles, k, device_sm_count());
+    StreamMaps maps;
     StreamParams p;
     p.x = x;
-    p.y = y;
-    p.n = static_cast<int>(n);
     p.k = static_cast<int>(k);
+    p.count = count;
     p.rw = sh.rw;
     p.kw = sh.kw;
     p.cpw = sh.cpw;
     p.stages = sh.stages;
     p.ctx = ctx;
+    const uint64_t rowbytes = static_cast<uint64_t>(k / kChunkK) * StreamFmt<F>::kChunkBytes;
+    constexpr int EB = StreamFmt<F>::kElemBytes;
+    int64_t groups = 0;
+    for (int i = 0; i < kMaxGemvProblems; ++i) {
+        if (i < count) {
+            if (!encode_tmap_2d(&maps.m[i], StreamFmt<F>::kType, probs[i].w, rowbytes / EB,
+                                probs[i].n, rowbytes, StreamFmt<F>::kChunkBytes / EB,
+                                kRowsPerWarp))
+                return cudaErrorInvalidValue;
+            p.y[i] = probs[i].y;
+            p.n[i] = static_cast<int>(probs[i].n);
+            p.group_begin[i] = static_cast<int>(groups);
+            const int64_t t = (probs[i].n + kRowsPerWarp - 1) / kRowsPerWarp;
+            groups += (t + sh.rw - 1) / sh.rw;
+        } else {
+            maps.m[i] = maps.m[0];
+            p.y[i] = nullptr;
+            p.n[i] = 0;
+            p.group_begin[i] = static_cast<int>(groups);
+        }
+    }
+    p.group_begin[kMaxGemvProblems] = static_cast<int>(groups);
     auto kern = gemv_stream_kernel<F, M, L>;
     static int smem_limits[kMaxDevices] = {0};  // this instantiation's own cache
     const cudaError_t e = ensure_smem(kern, sh.smem, true, smem_limits);
     if (e != cudaSuccess) return e;
     return launch_kernel(kern, dim3(static_cast<unsigned>(groups * sh.ksplit)),
                          dim3(sh.rw * sh.kw * 32), sh.smem, stream,
-                         static_cast<unsigned>(sh.ksplit), wmap, p);
+                         static_cast<unsigned>(sh.ksplit), maps, p);
 }
 
 template <Fmt F, int M>
-cudaError_t launch_m(const uint8_t *w, const float *x, float *y, int64_t n, int64_t k,
+cudaError_t launch_m(const GemvProblem *probs, int count, const float *x, int64_t k,
                      cudaStream_t stream, const LaunchCtx &ctx) {
-    const bool aligned = ((reinterpret_cast<uintptr_t>(w) | reinterpret_cast<uintptr_t>(x)) & 15) == 0;
-    if (k % kChunkK == 0 && aligned && n <= (1LL << 30) && k <= (1LL << 24)) {
+    bool aligned = (reinterpret_cast<uintptr_t>(x) & 15) == 0;
+    int64_t units = 0;
+    for (int i = 0; i < count; ++i) {
+        aligned = aligned && (reinterpret_cast<uintptr_t>(probs[i].w) & 15) == 0 &&
+                  probs[i].n <= (1LL << 30);
+        units += ((probs[i].n + 31) / 32) * (k / kChunkK);
+    }
+    if (k % kChunkK == 0 && aligned && k <= (1LL << 24)) {
         // Lanes per row: small problems at small M are latency bound, so more
         // lanes share each row chunk; large or wide-M problems keep one.
         if constexpr (M <= 4) {
-            const int64_t units = ((n + 31) / 32) * (k / kChunkK);
-            if (units <= QMM_GEMV_L4_UNITS) return launch_stream<F, M, 4>(w, x, y, n, k, stream, ctx);
-            if (units <= QMM_GEMV_L2_UNITS) return launch_stream<F, M, 2>(w, x, y, n, k, stream, ctx);
+            if (units <= QMM_GEMV_L4_UNITS) return launch_stream<F, M, 4>(probs, count, x, k, stream, ctx);
+            if (units <= QMM_GEMV_L2_UNITS) return launch_stream<F, M, 2>(probs, count, x, k, stream, ctx);
         }
-        return launch_stream<F, M, 1>(w, x, y, n, k, stream, ctx);
+        return launch_stream<F, M, 1>(probs, count, x, k, stream, ctx);
     }
-    const unsigned grid = static_cast<unsigned>((n + 3) / 4);
-    return launch_kernel(gemv_bytewise_kernel<F, M>, dim3(grid), dim3(128), 0, stream, 1, w, x, y,
-                         n, k, ctx);
+    for (int i = 0; i < count; ++i) {  // byte-wise kernel, one launch per problem
+        const unsigned grid = static_cast<unsigned>((probs[i].n + 3) / 4);
+        const cudaError_t e = launch_kernel(gemv_bytewise_kernel<F, M>, dim3(grid), dim3(128), 0,
+                                            stream, 1, static_cast<const uint8_t *>(probs[i].w),
+                                            x, probs[i].y, probs[i].n, k, ctx);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 template <Fmt F>
-cudaError_t launch_fmt(const uint8_t *w, const float *x, float *y, int m, int64_t n, int64_t k,
+cudaError_t launch_fmt(const GemvProblem *probs, int count, const float *x, int m, int64_t k,
                        cudaStream_t s, const LaunchCtx &ctx) {
     switch (m) {
 #define QMM_CASE(MM) \
-    case MM: return launch_m<F, MM>(w, x, y, n, k, s, ctx);
+    case MM: return launch_m<F, MM>(probs, count, x, k, s, ctx);
         QMM_CASE(1) QMM_CASE(2) QMM_CASE(3) QMM_CASE(4) QMM_CASE(5) QMM_CASE(6) QMM_CASE(7)
         QMM_CASE(8) QMM_CASE(9) QMM_CASE(10) QMM_CASE(11) QMM_CASE(12) QMM_CASE(13)
         QMM_CASE(14) QMM_CASE(15) QMM_CASE(16)

@@ -5,9 +5,9 @@
 
 namespace qmm {
 
-cudaError_t launch_gemv_q8_0(const uint8_t *w, const float *x, float *y, int m, int64_t n,
+cudaError_t launch_gemv_q8_0(const GemvProblem *probs, int count, const float *x, int m,
                              int64_t k, cudaStream_t stream, const LaunchCtx &ctx) {
-    return launch_fmt<Fmt::Q8_0>(w, x, y, m, n, k, stream, ctx);
+    return launch_fmt<Fmt::Q8_0>(probs, count, x, m, k, stream, ctx);
 }
 
 }  // namespace qmm

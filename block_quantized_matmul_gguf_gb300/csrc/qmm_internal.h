@@ -87,15 +87,25 @@ bool encode_tmap_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *bas
 cudaError_t launch_dequant(Fmt fmt, const uint8_t *w, float *out, int64_t n, int64_t k,
                            cudaStream_t stream, const LaunchCtx &ctx);
 
-cudaError_t launch_gemv_q4_0(const uint8_t *w, const float *x, float *y, int m, int64_t n,
+// One weight matrix of a GEMV call: w (n rows of blocks) applied to the
+// call's shared activations, written to y [m][n].
+struct GemvProblem {
+    const void *w;
+    float *y;
+    int64_t n;
+};
+
+// GEMV over `count` (1..4) problems that share x [m][k]; one launch when the
+// streaming kernel applies.
+cudaError_t launch_gemv_q4_0(const GemvProblem *probs, int count, const float *x, int m,
                              int64_t k, cudaStream_t stream, const LaunchCtx &ctx);
-cudaError_t launch_gemv_q8_0(const uint8_t *w, const float *x, float *y, int m, int64_t n,
+cudaError_t launch_gemv_q8_0(const GemvProblem *probs, int count, const float *x, int m,
                              int64_t k, cudaStream_t stream, const LaunchCtx &ctx);
 
-inline cudaError_t launch_gemv(Fmt fmt, const uint8_t *w, const float *x, float *y, int m,
-                               int64_t n, int64_t k, cudaStream_t stream, const LaunchCtx &ctx) {
-    return fmt == Fmt::Q4_0 ? launch_gemv_q4_0(w, x, y, m, n, k, stream, ctx)
-                            : launch_gemv_q8_0(w, x, y, m, n, k, stream, ctx);
+inline cudaError_t launch_gemv(Fmt fmt, const GemvProblem *probs, int count, const float *x,
+                               int m, int64_t k, cudaStream_t stream, const LaunchCtx &ctx) {
+    return fmt == Fmt::Q4_0 ? launch_gemv_q4_0(probs, count, x, m, k, stream, ctx)
+                            : launch_gemv_q8_0(probs, count, x, m, k, stream, ctx);
 }
 
 cudaError_t launch_gemm_q4_0(const uint8_t *w, const uint16_t *x, float *y, int64_t m,

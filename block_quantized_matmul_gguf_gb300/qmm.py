@@ -24,11 +24,19 @@ QMM_ERR_CUDA = 5
 QMM_ERR_TIMEOUT = 6
 QMM_GEMV_MAX_M = 16
 
+QMM_GEMV_MAX_OUTPUTS = 4
+
 EXPORTED = (
     "qmm_dequant_q4_0", "qmm_dequant_q8_0", "qmm_gemv_q4_0", "qmm_gemv_q8_0",
+    "qmm_gemv_q4_0_multi", "qmm_gemv_q8_0_multi",
     "qmm_gemm_q4_0", "qmm_status_string", "qmm_version", "qmm_get_device_error",
     "qmm_set_wait_timeout_ns", "qmm_selftest_wait_timeout",
 )
+
+
+class GemvOut(ctypes.Structure):
+    """struct qmm_gemv_out: one weight matrix and its output."""
+    _fields_ = [("w", ctypes.c_void_p), ("y", ctypes.c_void_p), ("n", ctypes.c_int64)]
 
 
 class QmmError(RuntimeError):
@@ -62,6 +70,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         "qmm_gemv_q4_0": [P, P, P, I32, I64, I64, P],
         "qmm_gemv_q8_0": [P, P, P, I32, I64, I64, P],
         "qmm_gemm_q4_0": [P, P, P, I64, I64, I64, P],
+        "qmm_gemv_q4_0_multi": [ctypes.POINTER(GemvOut), I32, P, I32, I64, P],
+        "qmm_gemv_q8_0_multi": [ctypes.POINTER(GemvOut), I32, P, I32, I64, P],
         "qmm_get_device_error": [P],
         "qmm_selftest_wait_timeout": [U64, P],
     }
@@ -131,6 +141,26 @@ def qmm_gemv_q4_0(w, x, y, m: int, n: int, k: int, stream=None) -> None:
 def qmm_gemv_q8_0(w, x, y, m: int, n: int, k: int, stream=None) -> None:
     _check(load().qmm_gemv_q8_0(_ptr(w), _ptr(x), _ptr(y), m, n, k, _stream(stream)),
            "qmm_gemv_q8_0")
+
+
+def _outs(outs):
+    arr = (GemvOut * max(1, len(outs)))()
+    for i, (w, y, n) in enumerate(outs):
+        arr[i].w = _ptr(w)
+        arr[i].y = _ptr(y)
+        arr[i].n = int(n)
+    return arr
+
+
+def qmm_gemv_q4_0_multi(outs, x, m: int, k: int, stream=None) -> None:
+    """outs: sequence of (w, y, n) sharing the activations x [m][k]."""
+    _check(load().qmm_gemv_q4_0_multi(_outs(outs), len(outs), _ptr(x), m, k, _stream(stream)),
+           "qmm_gemv_q4_0_multi")
+
+
+def qmm_gemv_q8_0_multi(outs, x, m: int, k: int, stream=None) -> None:
+    _check(load().qmm_gemv_q8_0_multi(_outs(outs), len(outs), _ptr(x), m, k, _stream(stream)),
+           "qmm_gemv_q8_0_multi")
 
 
 def qmm_gemm_q4_0(w, x_bf16, y, m: int, n: int, k: int, stream=None) -> None:

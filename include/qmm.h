@@ -93,6 +93,30 @@ qmm_status qmm_gemv_q4_0(const void *w, const float *x, float *y, int m, int64_t
 qmm_status qmm_gemv_q8_0(const void *w, const float *x, float *y, int m, int64_t n,
                          int64_t k, qmm_stream_t stream);
 
+/* ---- Grouped decode GEMV -----------------------------------------------
+ * Several weight matrices applied to the same activations in one launch:
+ * the q/k/v (or gate/up) projections of a layer read one hidden state, and
+ * the packed QKV / fused FFN paths of "Add generated quant-kernel JIT and
+ * accelerate Gemma4, BGE-M3, and GLiNER2" (second revision, "Summary") batch
+ * such projections.  Output i is y_i[r][j] = sum_k x[r][k] * w_i[j][k] for
+ * r < m, j < n_i; each output is computed exactly as by qmm_gemv_q4_0 /
+ * qmm_gemv_q8_0 on its own (same arithmetic, same accuracy bound).
+ * outs : host array of `count` (1..QMM_GEMV_MAX_OUTPUTS) descriptors read
+ *        during the call; each w and y is a device pointer as above.
+ * Requires what the single call requires for every output, and no output
+ * may overlap x, any weight buffer or another output. */
+#define QMM_GEMV_MAX_OUTPUTS 4
+typedef struct qmm_gemv_out {
+    const void *w; /* N_i*K/32 blocks */
+    float *y;      /* fp32 [m][n] */
+    int64_t n;     /* rows of w_i */
+} qmm_gemv_out;
+
+qmm_status qmm_gemv_q4_0_multi(const qmm_gemv_out *outs, int count, const float *x, int m,
+                               int64_t k, qmm_stream_t stream);
+qmm_status qmm_gemv_q8_0_multi(const qmm_gemv_out *outs, int count, const float *x, int m,
+                               int64_t k, qmm_stream_t stream);
+
 /* ---- Prefill GEMM (tcgen05 tensor cores) ------------------------------
  * Y[i][j] = sum_k X[i][k] * w[j][k] for i < m, j < n.  X is bf16 [m][k]
  * given as raw bf16 bit patterns; each weight is rounded once to bf16

@@ -27,7 +27,7 @@ def lib():
 def test_header_declares_the_entry_points():
     syms = header_symbols()
     for name in ("qmm_dequant_q4_0", "qmm_dequant_q8_0", "qmm_gemv_q4_0", "qmm_gemv_q8_0",
-                 "qmm_gemm_q4_0"):
+                 "qmm_gemv_q4_0_multi", "qmm_gemv_q8_0_multi", "qmm_gemm_q4_0"):
         assert name in syms
     assert set(syms) <= set(qmm.EXPORTED) | set(syms)
 
@@ -71,3 +71,18 @@ def test_null_and_shape_errors_return_before_any_launch(lib):
 def test_overlapping_output_is_rejected(lib):
     # y overlapping w: rejected by the host check, nothing launched
     assert lib.qmm_gemv_q4_0(4096, 1 << 20, 4096 + 64, 1, 32, 64, 0) == qmm.QMM_ERR_UNSUPPORTED
+
+
+def test_multi_argument_checks(lib):
+    import ctypes
+    Out = qmm.GemvOut
+    arr = (Out * 2)()
+    arr[0].w, arr[0].y, arr[0].n = 16, 4096, 32
+    arr[1].w, arr[1].y, arr[1].n = 16, 0, 32
+    assert lib.qmm_gemv_q4_0_multi(arr, 2, 16, 1, 64, 0) == qmm.QMM_ERR_NULL      # y NULL
+    assert lib.qmm_gemv_q4_0_multi(arr, 0, 16, 1, 64, 0) == qmm.QMM_ERR_SHAPE     # count 0
+    assert lib.qmm_gemv_q4_0_multi(arr, 5, 16, 1, 64, 0) == qmm.QMM_ERR_SHAPE     # count 5
+    assert lib.qmm_gemv_q8_0_multi(None, 1, 16, 1, 64, 0) == qmm.QMM_ERR_NULL
+    arr[1].y = 8192
+    assert lib.qmm_gemv_q4_0_multi(arr, 2, 16, 1, 48, 0) == qmm.QMM_ERR_SHAPE     # k % 32
+    assert lib.qmm_gemv_q4_0_multi(arr, 2, 16, 17, 64, 0) == qmm.QMM_ERR_SHAPE    # m

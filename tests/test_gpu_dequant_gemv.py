@@ -222,3 +222,53 @@ def test_timeout_path_reports_and_context_survives(qmm):
     y = qmm.gemv("q4_0", to_dev(case.w, torch), to_dev(case.x, torch), 64, 256)
     torch.cuda.synchronize()
     assert torch.isfinite(y).all()
+
+
+# ---- grouped GEMV: several weight matrices sharing x in one launch ----
+
+@pytest.mark.parametrize("fmt", ["q4_0", "q8_0"])
+@pytest.mark.parametrize("m", [1, 2, 5, 16])
+def test_gemv_multi_matches_oracle(qmm, oracle_mod, fmt, m):
+    k = 2048
+    ns = [2048, 512, 512] if fmt == "q4_0" else [1000, 96]
+    x = synth.activations_f32(m, k, seed=60 + m)
+    ws = [(synth.q4_0_weights if fmt == "q4_0" else synth.q8_0_weights)(n, k, seed=61, stream=i)
+          for i, n in enumerate(ns)]
+    xd = to_dev(x, torch)
+    ys = [torch.empty((m, n), dtype=torch.float32, device="cuda") for n in ns]
+    outs = [(to_dev(w, torch), y, n) for w, y, n in zip(ws, ys, ns)]
+    (qmm.qmm_gemv_q4_0_multi if fmt == "q4_0" else qmm.qmm_gemv_q8_0_multi)(outs, xd, m, k)
+    torch.cuda.synchronize()
+    f = oracle_mod.gemv_q4_0 if fmt == "q4_0" else oracle_mod.gemv_q8_0
+    for w, y, n in zip(ws, ys, ns):
+        y_ref, bound = f(w, x, m, n, k)
+        assert_within(y.cpu().numpy(), y_ref, bound, GEMV_REL, f"multi {fmt} m={m} n={n}")
+
+
+def test_gemv_multi_decode_qkv_and_gate_up_full(qmm, oracle_mod):
+    """The decode layer's grouped calls: q+k+v and gate+up, at full size."""
+    k = 2048
+    x = synth.activations_f32(1, k, seed=70)
+    xd = to_dev(x, torch)
+    for group in (("q", "k", "v"), ("gate", "up")):
+        projs = [p for p in synth.DECODE_LAYER if p.name in group]
+        ws = [synth.q4_0_weights(p.n, p.k, seed=71, stream=i) for i, p in enumerate(projs)]
+        ys = [torch.empty((1, p.n), dtype=torch.float32, device="cuda") for p in projs]
+        qmm.qmm_gemv_q4_0_multi([(to_dev(w, torch), y, p.n) for w, y, p in zip(ws, ys, projs)], xd, 1, k)
+        torch.cuda.synchronize()
+        for w, y, p in zip(ws, ys, projs):
+            y_ref, bound = oracle_mod.gemv_q4_0(w, x, 1, p.n, k)
+            assert_within(y.cpu().numpy(), y_ref, bound, GEMV_REL, f"multi {p.name}")
+
+
+def test_gemv_multi_rejects_overlap_and_count(qmm):
+    k, n = 256, 64
+    w = torch.zeros(n * (k // 32) * 18, dtype=torch.uint8, device="cuda")
+    x = torch.zeros((1, k), device="cuda")
+    y = torch.empty((1, 2 * n), device="cuda")
+    with pytest.raises(qmm.QmmError) as e:
+        qmm.qmm_gemv_q4_0_multi([(w, y, n), (w, y.view(-1)[8:], n)], x, 1, k)  # outputs overlap
+    assert e.value.status == qmm.QMM_ERR_UNSUPPORTED
+    with pytest.raises(qmm.QmmError) as e:
+        qmm.qmm_gemv_q4_0_multi([(w, y, n)] * 5, x, 1, k)
+    assert e.value.status == qmm.QMM_ERR_SHAPE
