@@ -55,11 +55,14 @@
 #ifndef QMM_GEMV_STAGES
 #define QMM_GEMV_STAGES 4         // ring depth per warp
 #endif
-#ifndef QMM_GEMV_L4_UNITS
-#define QMM_GEMV_L4_UNITS 0       // (32-row tile x chunk) units up to which 4 lanes share a row
-#endif
 #ifndef QMM_GEMV_L2_UNITS
-#define QMM_GEMV_L2_UNITS 1024    // ... and up to which 2 lanes share a row
+#define QMM_GEMV_L2_UNITS 1024    // (32-row tile x chunk) units up to which 2 lanes share a row
+#endif
+#ifndef QMM_GEMV_R2_MAX_M
+#define QMM_GEMV_R2_MAX_M 4       // largest M at which a lane owns two weight rows
+#endif
+#ifndef QMM_GEMV_R_SMALL
+#define QMM_GEMV_R_SMALL 1        // rows per lane for the small (two lanes per row) case
 #endif
 #ifndef QMM_GEMV_X_BYTES
 #define QMM_GEMV_X_BYTES 65536    // activation slice per CTA (shared memory)
@@ -69,6 +72,7 @@ namespace qmm {
 namespace {
 
 constexpr int kMaxGemvProblems = 4;
+constexpr size_t kGemvSmemCap = 200 * 1024;  // dynamic shared memory per CTA
 
 constexpr int kChunkK = 256;
 constexpr uint32_t kMagic = 0x4B000000u;  // 2^23
@@ -138,25 +142,27 @@ __device__ __forceinline__ void load_portion(const uint8_t *src, uint32_t (&wd)[
 
 // Independent FMA chains per output row: at small M the rows alone do not
 // give the scheduler enough independent work, so each block's sum is split.
-template <int M>
+template <int ROWS>
 struct Chains {
-    static constexpr int value = M <= 2 ? 4 : (M <= 4 ? 2 : 1);
+    static constexpr int value = ROWS <= 2 ? 4 : (ROWS <= 4 ? 2 : 1);
 };
 
-// This lane's share (8/L consecutive Q4_0 blocks, 144/L bytes at `src`) of
-// a row chunk against activations `xk` in shared memory (position 0 of the
-// share for row 0; rows XS apart).
+// R rows' shares (8/L consecutive Q4_0 blocks, 144/L bytes each; row j at
+// src + j*rstride) of a row chunk, against activations `xk` in shared memory
+// (position 0 of the share for activation row 0; rows XS apart).  Each
+// activation value is loaded once and used for all R weight rows.
 //
 // A qs word v holds weights 4i..4i+3 (low nibbles, bits 0,8,16,24) and
 // 16+4i..19+4i (high nibbles, bits 4,12,20,28); bits 0-19 are used in place
 // and bits 20-31 after u = v >> 16, so the nibble sits at s in {0,4,8,12,16}.
-template <int M, int L>
-__device__ __forceinline__ void q4_0_chunk(const uint8_t *src, const float *xk, int XS,
-                                           float (&tot)[M]) {
-    constexpr int CH = Chains<M>::value;
+template <int M, int L, int R>
+__device__ __forceinline__ void q4_0_chunk(const uint8_t *src, int rstride, const float *xk,
+                                           int XS, float (&tot)[R][M]) {
+    constexpr int CH = Chains<M * R>::value;
     constexpr int NB = 8 / L;
-    uint32_t wd[36 / L];
-    load_portion<L>(src, wd);
+    uint32_t wd[R][36 / L];
+#pragma unroll
+    for (int j = 0; j < R; ++j) load_portion<L>(src + j * rstride, wd[j]);
     // (m - (2^23 + 8*2^s)) * 2^-s = m*2^-s - (2^23*2^-s + 8): exact nibble-8
     const float2 s01 = f2(1.0f, 0.00390625f), b01 = f2(-8388616.0f, -32776.0f);           // s = 0, 8
     const float2 s23 = f2(1.52587890625e-05f, 0.00390625f), b23 = f2(-136.0f, -32776.0f); // s = 16, 8
@@ -164,102 +170,218 @@ __device__ __forceinline__ void q4_0_chunk(const uint8_t *src, const float *xk, 
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
         const int base = (18 * b) >> 2;
-        uint32_t dbits, q[4];
-        if ((b & 1) == 0) {  // block starts on a word: d low half, qs shifted by 2 bytes
-            dbits = wd[base] & 0xFFFFu;
+        uint32_t q[R][4];
+        float d[R];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) q[i] = __byte_perm(wd[base + i], wd[base + i + 1], 0x5432);
-        } else {  // block starts 2 bytes into a word: d high half, qs aligned
-            dbits = wd[base] >> 16;
+        for (int j = 0; j < R; ++j) {
+            uint32_t dbits;
+            if ((b & 1) == 0) {  // block starts on a word: d low half, qs shifted by 2 bytes
+                dbits = wd[j][base] & 0xFFFFu;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) q[i] = wd[base + 1 + i];
+                for (int i = 0; i < 4; ++i)
+                    q[j][i] = __byte_perm(wd[j][base + i], wd[j][base + i + 1], 0x5432);
+            } else {  // block starts 2 bytes into a word: d high half, qs aligned
+                dbits = wd[j][base] >> 16;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) q[j][i] = wd[j][base + 1 + i];
+            }
+            d[j] = half_bits_to_float(dbits);
         }
-        const float d = half_bits_to_float(dbits);
-        float2 acc[M][CH];
+        float2 acc[R][M][CH];
 #pragma unroll
-        for (int m = 0; m < M; ++m)
+        for (int j = 0; j < R; ++j)
 #pragma unroll
-            for (int c = 0; c < CH; ++c) acc[m][c] = f2(0.0f, 0.0f);
+            for (int m = 0; m < M; ++m)
+#pragma unroll
+                for (int c = 0; c < CH; ++c) acc[j][m][c] = f2(0.0f, 0.0f);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const uint32_t v = q[i], u = v >> 16;
-            const float2 p01 = __ffma2_rn(f2(mag(v, 0x0000000Fu), mag(v, 0x00000F00u)), s01, b01);
-            const float2 p23 = __ffma2_rn(f2(mag(v, 0x000F0000u), mag(u, 0x00000F00u)), s23, b23);
-            const float2 p45 = __ffma2_rn(f2(mag(v, 0x000000F0u), mag(v, 0x0000F000u)), s45, b45);
-            const float2 p67 = __ffma2_rn(f2(mag(u, 0x000000F0u), mag(u, 0x0000F000u)), s45, b45);
-            const int c = i % CH;
+            float4 xa[M], xb[M];
 #pragma unroll
             for (int m = 0; m < M; ++m) {
-                const float4 xa = lds128f(xk + m * XS + 32 * b + 4 * i);
-                const float4 xb = lds128f(xk + m * XS + 32 * b + 16 + 4 * i);
-                acc[m][c] = __ffma2_rn(p01, f2(xa.x, xa.y), acc[m][c]);
-                acc[m][c] = __ffma2_rn(p23, f2(xa.z, xa.w), acc[m][c]);
-                acc[m][c] = __ffma2_rn(p45, f2(xb.x, xb.y), acc[m][c]);
-                acc[m][c] = __ffma2_rn(p67, f2(xb.z, xb.w), acc[m][c]);
+                xa[m] = lds128f(xk + m * XS + 32 * b + 4 * i);
+                xb[m] = lds128f(xk + m * XS + 32 * b + 16 + 4 * i);
+            }
+            const int c = i % CH;
+#pragma unroll
+            for (int j = 0; j < R; ++j) {
+                const uint32_t v = q[j][i], u = v >> 16;
+                const float2 p01 = __ffma2_rn(f2(mag(v, 0x0000000Fu), mag(v, 0x00000F00u)), s01, b01);
+                const float2 p23 = __ffma2_rn(f2(mag(v, 0x000F0000u), mag(u, 0x00000F00u)), s23, b23);
+                const float2 p45 = __ffma2_rn(f2(mag(v, 0x000000F0u), mag(v, 0x0000F000u)), s45, b45);
+                const float2 p67 = __ffma2_rn(f2(mag(u, 0x000000F0u), mag(u, 0x0000F000u)), s45, b45);
+#pragma unroll
+                for (int m = 0; m < M; ++m) {
+                    acc[j][m][c] = __ffma2_rn(p01, f2(xa[m].x, xa[m].y), acc[j][m][c]);
+                    acc[j][m][c] = __ffma2_rn(p23, f2(xa[m].z, xa[m].w), acc[j][m][c]);
+                    acc[j][m][c] = __ffma2_rn(p45, f2(xb[m].x, xb[m].y), acc[j][m][c]);
+                    acc[j][m][c] = __ffma2_rn(p67, f2(xb[m].z, xb[m].w), acc[j][m][c]);
+                }
             }
         }
 #pragma unroll
-        for (int m = 0; m < M; ++m) {
-            float2 a = acc[m][0];
+        for (int j = 0; j < R; ++j)
 #pragma unroll
-            for (int c = 1; c < CH; ++c) a = __fadd2_rn(a, acc[m][c]);
-            tot[m] = fmaf(d, a.x + a.y, tot[m]);
-        }
+            for (int m = 0; m < M; ++m) {
+                float2 a = acc[j][m][0];
+#pragma unroll
+                for (int c = 1; c < CH; ++c) a = __fadd2_rn(a, acc[j][m][c]);
+                tot[j][m] = fmaf(d[j], a.x + a.y, tot[j][m]);
+            }
     }
 }
 
-// This lane's share (8/L consecutive Q8_0 blocks, 272/L bytes) of a row
+// R rows' shares (8/L consecutive Q8_0 blocks, 272/L bytes each) of a row
 // chunk.  Bytes 0 and 2 of a word are used at bits 0-7 (s = 0), bytes 1 and
 // 3 at bits 8-15 (s = 8).
-template <int M, int L>
-__device__ __forceinline__ void q8_0_chunk(const uint8_t *src, const float *xk, int XS,
-                                           float (&tot)[M]) {
-    constexpr int CH = Chains<M>::value;
+template <int M, int L, int R>
+__device__ __forceinline__ void q8_0_chunk(const uint8_t *src, int rstride, const float *xk,
+                                           int XS, float (&tot)[R][M]) {
+    constexpr int CH = Chains<M * R>::value;
     constexpr int NB = 8 / L;
-    uint32_t wd[68 / L];
-    load_portion<L>(src, wd);
+    uint32_t wd[R][68 / L];
+#pragma unroll
+    for (int j = 0; j < R; ++j) load_portion<L>(src + j * rstride, wd[j]);
     // (m - (2^23 + 128*2^s)) * 2^-s: exact q
     const float2 sc = f2(1.0f, 0.00390625f), bc = f2(-8388736.0f, -32896.0f);
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
         const int base = (34 * b) >> 2;
-        uint32_t dbits, q[8];
-        if ((b & 1) == 0) {
-            dbits = wd[base] & 0xFFFFu;
+        float d[R];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) q[i] = __byte_perm(wd[base + i], wd[base + i + 1], 0x5432);
-        } else {
-            dbits = wd[base] >> 16;
+        for (int j = 0; j < R; ++j)
+            d[j] = half_bits_to_float((b & 1) == 0 ? (wd[j][base] & 0xFFFFu) : (wd[j][base] >> 16));
+        float2 acc[R][M][CH];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) q[i] = wd[base + 1 + i];
-        }
-        const float d = half_bits_to_float(dbits);
-        float2 acc[M][CH];
+        for (int j = 0; j < R; ++j)
 #pragma unroll
-        for (int m = 0; m < M; ++m)
+            for (int m = 0; m < M; ++m)
 #pragma unroll
-            for (int h = 0; h < CH; ++h) acc[m][h] = f2(0.0f, 0.0f);
+                for (int h = 0; h < CH; ++h) acc[j][m][h] = f2(0.0f, 0.0f);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const uint32_t v = q[i], u = v >> 16;
-            const float2 p01 = __ffma2_rn(
-                f2(mag8(v, 0x000000FFu, kMagic | 0x80u), mag8(v, 0x0000FF00u, kMagic | 0x8000u)), sc, bc);
-            const float2 p23 = __ffma2_rn(
-                f2(mag8(u, 0x000000FFu, kMagic | 0x80u), mag8(u, 0x0000FF00u, kMagic | 0x8000u)), sc, bc);
+            float4 xa[M];
+#pragma unroll
+            for (int m = 0; m < M; ++m) xa[m] = lds128f(xk + m * XS + 32 * b + 4 * i);
             const int h = i % CH;
 #pragma unroll
-            for (int m = 0; m < M; ++m) {
-                const float4 xa = lds128f(xk + m * XS + 32 * b + 4 * i);
-                acc[m][h] = __ffma2_rn(p01, f2(xa.x, xa.y), acc[m][h]);
-                acc[m][h] = __ffma2_rn(p23, f2(xa.z, xa.w), acc[m][h]);
+            for (int j = 0; j < R; ++j) {
+                const uint32_t v = (b & 1) == 0 ? __byte_perm(wd[j][base + i], wd[j][base + i + 1], 0x5432)
+                                                : wd[j][base + 1 + i];
+                const uint32_t u = v >> 16;
+                const float2 p01 = __ffma2_rn(
+                    f2(mag8(v, 0x000000FFu, kMagic | 0x80u), mag8(v, 0x0000FF00u, kMagic | 0x8000u)), sc, bc);
+                const float2 p23 = __ffma2_rn(
+                    f2(mag8(u, 0x000000FFu, kMagic | 0x80u), mag8(u, 0x0000FF00u, kMagic | 0x8000u)), sc, bc);
+#pragma unroll
+                for (int m = 0; m < M; ++m) {
+                    acc[j][m][h] = __ffma2_rn(p01, f2(xa[m].x, xa[m].y), acc[j][m][h]);
+                    acc[j][m][h] = __ffma2_rn(p23, f2(xa[m].z, xa[m].w), acc[j][m][h]);
+                }
             }
         }
 #pragma unroll
-        for (int m = 0; m < M; ++m) {
-            float2 a = acc[m][0];
+        for (int j = 0; j < R; ++j)
 #pragma unroll
-            for (int h = 1; h < CH; ++h) a = __fadd2_rn(a, acc[m][h]);
-            tot[m] = fmaf(d, a.x + a.y, tot[m]);
+            for (int m = 0; m < M; ++m) {
+                float2 a = acc[j][m][0];
+#pragma unroll
+                for (int h = 1; h < CH; ++h) a = __fadd2_rn(a, acc[j][m][h]);
+                tot[j][m] = fmaf(d[j], a.x + a.y, tot[j][m]);
+            }
+    }
+}
+
+
+// Wide-M forms (one lane per row, one row per lane): a runtime loop over
+// block pairs, each pair's 36 (Q4_0) or 68 (Q8_0) bytes read from shared
+// memory as words.  The arithmetic is that of q4_0_chunk / q8_0_chunk; the
+// loop keeps the code (and build time) small where FMAs, not loads, bound
+// the kernel.
+template <int M>
+__device__ __forceinline__ void q4_0_chunk_wide(const uint8_t *src, const float *xk, int XS,
+                                                float (&tot)[1][M]) {
+    const float2 s01 = f2(1.0f, 0.00390625f), b01 = f2(-8388616.0f, -32776.0f);
+    const float2 s23 = f2(1.52587890625e-05f, 0.00390625f), b23 = f2(-136.0f, -32776.0f);
+    const float2 s45 = f2(0.0625f, 0.000244140625f), b45 = f2(-524296.0f, -2056.0f);
+#pragma unroll 1
+    for (int bp = 0; bp < 4; ++bp) {
+        uint32_t wd[9];
+#pragma unroll
+        for (int t = 0; t < 9; ++t) wd[t] = *reinterpret_cast<const uint32_t *>(src + 36 * bp + 4 * t);
+#pragma unroll
+        for (int hb = 0; hb < 2; ++hb) {
+            const int b = 2 * bp + hb;
+            uint32_t q[4], dbits;
+            if (hb == 0) {
+                dbits = wd[0] & 0xFFFFu;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) q[i] = __byte_perm(wd[i], wd[i + 1], 0x5432);
+            } else {
+                dbits = wd[4] >> 16;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) q[i] = wd[5 + i];
+            }
+            const float d = half_bits_to_float(dbits);
+            float2 acc[M];
+#pragma unroll
+            for (int m = 0; m < M; ++m) acc[m] = f2(0.0f, 0.0f);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t v = q[i], u = v >> 16;
+                const float2 p01 = __ffma2_rn(f2(mag(v, 0x0000000Fu), mag(v, 0x00000F00u)), s01, b01);
+                const float2 p23 = __ffma2_rn(f2(mag(v, 0x000F0000u), mag(u, 0x00000F00u)), s23, b23);
+                const float2 p45 = __ffma2_rn(f2(mag(v, 0x000000F0u), mag(v, 0x0000F000u)), s45, b45);
+                const float2 p67 = __ffma2_rn(f2(mag(u, 0x000000F0u), mag(u, 0x0000F000u)), s45, b45);
+#pragma unroll
+                for (int m = 0; m < M; ++m) {
+                    const float4 xa = lds128f(xk + m * XS + 32 * b + 4 * i);
+                    const float4 xb = lds128f(xk + m * XS + 32 * b + 16 + 4 * i);
+                    acc[m] = __ffma2_rn(p01, f2(xa.x, xa.y), acc[m]);
+                    acc[m] = __ffma2_rn(p23, f2(xa.z, xa.w), acc[m]);
+                    acc[m] = __ffma2_rn(p45, f2(xb.x, xb.y), acc[m]);
+                    acc[m] = __ffma2_rn(p67, f2(xb.z, xb.w), acc[m]);
+                }
+            }
+#pragma unroll
+            for (int m = 0; m < M; ++m) tot[0][m] = fmaf(d, acc[m].x + acc[m].y, tot[0][m]);
+        }
+    }
+}
+
+template <int M>
+__device__ __forceinline__ void q8_0_chunk_wide(const uint8_t *src, const float *xk, int XS,
+                                                float (&tot)[1][M]) {
+    const float2 sc = f2(1.0f, 0.00390625f), bc = f2(-8388736.0f, -32896.0f);
+#pragma unroll 1
+    for (int bp = 0; bp < 4; ++bp) {
+        uint32_t wd[17];
+#pragma unroll
+        for (int t = 0; t < 17; ++t) wd[t] = *reinterpret_cast<const uint32_t *>(src + 68 * bp + 4 * t);
+#pragma unroll
+        for (int hb = 0; hb < 2; ++hb) {
+            const int b = 2 * bp + hb;
+            const float d = half_bits_to_float(hb == 0 ? (wd[0] & 0xFFFFu) : (wd[8] >> 16));
+            float2 acc[M];
+#pragma unroll
+            for (int m = 0; m < M; ++m) acc[m] = f2(0.0f, 0.0f);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t v = hb == 0 ? __byte_perm(wd[i], wd[i + 1], 0x5432) : wd[9 + i];
+                const uint32_t u = v >> 16;
+                const float2 p01 = __ffma2_rn(
+                    f2(mag8(v, 0x000000FFu, kMagic | 0x80u), mag8(v, 0x0000FF00u, kMagic | 0x8000u)), sc, bc);
+                const float2 p23 = __ffma2_rn(
+                    f2(mag8(u, 0x000000FFu, kMagic | 0x80u), mag8(u, 0x0000FF00u, kMagic | 0x8000u)), sc, bc);
+#pragma unroll
+                for (int m = 0; m < M; ++m) {
+                    const float4 xa = lds128f(xk + m * XS + 32 * b + 4 * i);
+                    acc[m] = __ffma2_rn(p01, f2(xa.x, xa.y), acc[m]);
+                    acc[m] = __ffma2_rn(p23, f2(xa.z, xa.w), acc[m]);
+                }
+            }
+#pragma unroll
+            for (int m = 0; m < M; ++m) tot[0][m] = fmaf(d, acc[m].x + acc[m].y, tot[0][m]);
         }
     }
 }
@@ -310,11 +432,12 @@ struct StreamParams {
 // Grid: blockIdx.x = group * ksplit + rank (cluster of ksplit CTAs along x).
 // Warp w of a CTA owns row tile group*rw + w / kw and the (w % kw)-th part of
 // the CTA's K range; cluster rank r owns the r-th part of K.
-template <Fmt F, int M, int L>
+template <Fmt F, int M, int L, int R>
 __global__ void __launch_bounds__(256)
     gemv_stream_kernel(const __grid_constant__ StreamMaps maps, StreamParams p) {
     constexpr int CB = StreamFmt<F>::kChunkBytes;
-    constexpr int kRowsPerWarp = 32 / L;  // L lanes share a row
+    constexpr int kLaneRows = 32 / L;                 // rows covered by one pass of the lanes
+    constexpr int kRowsPerWarp = kLaneRows * R;       // L lanes share a row; a lane owns R rows
     extern __shared__ __align__(128) uint8_t smem_dyn[];
     // TMA destinations: 128-byte aligned (the launch adds 128 bytes of slack)
     uint8_t *smem = smem_dyn + ((128u - (smem_addr(smem_dyn) & 127u)) & 127u);
@@ -335,10 +458,8 @@ __global__ void __launch_bounds__(256)
     const int tile_in_cta = warp / kw;
     const int kpart = warp % kw;
     const int row0 = (group * p.rw + tile_in_cta) * kRowsPerWarp;
-    const int r = lane / L;  // row within the warp's tile
+    const int r = lane / L;  // rows r, r + 32/L, ... of the warp's tile
     const int h = lane % L;  // this lane's share of each chunk
-    const int row = row0 + r;
-    const bool row_ok = row < n_rows;
     const bool warp_active = row0 < n_rows;  // warp-uniform
     const int cta_chunks = kw * cpw;
     const int cta_c0 = static_cast<int>(rank) * cta_chunks;  // first chunk of the CTA
@@ -391,9 +512,11 @@ __global__ void __launch_bounds__(256)
     }
     pdl_launch_dependents();
 
-    float tot[M];
+    float tot[R][M];
 #pragma unroll
-    for (int m = 0; m < M; ++m) tot[m] = 0.0f;
+    for (int j = 0; j < R; ++j)
+#pragma unroll
+        for (int m = 0; m < M; ++m) tot[j][m] = 0.0f;
 
     int consumed = 0;
     // every warp waits for the activations (so none exits with the copy in flight)
@@ -410,10 +533,16 @@ __global__ void __launch_bounds__(256)
             ++consumed;
             const uint8_t *src = my_ring + (st * kRowsPerWarp + r) * CB + h * (CB / L);
             const float *xk = xs + (w_c0 + i) * kChunkK + h * (kChunkK / L);
-            if constexpr (F == Fmt::Q4_0)
-                q4_0_chunk<M, L>(src, xk, XS, tot);
-            else
-                q8_0_chunk<M, L>(src, xk, XS, tot);
+            if constexpr (M > QMM_GEMV_R2_MAX_M && L == 1 && R == 1) {
+                if constexpr (F == Fmt::Q4_0)
+                    q4_0_chunk_wide<M>(src, xk, XS, tot);
+                else
+                    q8_0_chunk_wide<M>(src, xk, XS, tot);
+            } else if constexpr (F == Fmt::Q4_0) {
+                q4_0_chunk<M, L, R>(src, kLaneRows * CB, xk, XS, tot);
+            } else {
+                q8_0_chunk<M, L, R>(src, kLaneRows * CB, xk, XS, tot);
+            }
             __syncwarp();  // every lane is done reading the stage
             if (issued < cpw) {
                 fence_proxy_async_smem();
@@ -434,44 +563,66 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
     for (int off = 1; off < L; off <<= 1) {
 #pragma unroll
-        for (int m = 0; m < M; ++m) tot[m] += __shfl_xor_sync(0xFFFFFFFFu, tot[m], off);
+        for (int j = 0; j < R; ++j)
+#pragma unroll
+            for (int m = 0; m < M; ++m) tot[j][m] += __shfl_xor_sync(0xFFFFFFFFu, tot[j][m], off);
     }
     const bool writer = h == 0;
     // 1) K parts inside the CTA: warps kpart > 0 hand their sums to kpart 0
     if (kw > 1) {
         if (kpart > 0 && writer) {
 #pragma unroll
-            for (int m = 0; m < M; ++m) red[(warp * M + m) * kRowsPerWarp + r] = tot[m];
+            for (int j = 0; j < R; ++j)
+#pragma unroll
+                for (int m = 0; m < M; ++m)
+                    red[(warp * M + m) * kRowsPerWarp + j * kLaneRows + r] = tot[j][m];
         }
         __syncthreads();
         if (kpart == 0) {
             for (int q = 1; q < kw; ++q) {
 #pragma unroll
-                for (int m = 0; m < M; ++m) tot[m] += red[((warp + q) * M + m) * kRowsPerWarp + r];
+                for (int j = 0; j < R; ++j)
+#pragma unroll
+                    for (int m = 0; m < M; ++m)
+                        tot[j][m] += red[((warp + q) * M + m) * kRowsPerWarp + j * kLaneRows + r];
             }
         }
     }
     // 2) K parts across the cluster: ranks push into rank 0, which adds in rank order
     if (ksplit == 1) {
-        if (kpart == 0 && writer && row_ok) {
+        if (kpart == 0 && writer) {
 #pragma unroll
-            for (int m = 0; m < M; ++m) y[static_cast<size_t>(m) * n_rows + row] = tot[m];
+            for (int j = 0; j < R; ++j) {
+                const int row = row0 + j * kLaneRows + r;
+                if (row < n_rows) {
+#pragma unroll
+                    for (int m = 0; m < M; ++m) y[static_cast<size_t>(m) * n_rows + row] = tot[j][m];
+                }
+            }
         }
         return;
     }
     if (kpart == 0 && writer) {
         float *slot = part + ((rank * p.rw + tile_in_cta) * M) * kRowsPerWarp;
 #pragma unroll
-        for (int m = 0; m < M; ++m) st_dsmem_f32(slot + m * kRowsPerWarp + r, 0, tot[m]);
+        for (int j = 0; j < R; ++j)
+#pragma unroll
+            for (int m = 0; m < M; ++m)
+                st_dsmem_f32(slot + m * kRowsPerWarp + j * kLaneRows + r, 0, tot[j][m]);
     }
     cluster_sync();
-    if (rank == 0 && kpart == 0 && writer && row_ok) {
+    if (rank == 0 && kpart == 0 && writer) {
 #pragma unroll
-        for (int m = 0; m < M; ++m) {
-            float s = 0.0f;
-            for (uint32_t q = 0; q < ksplit; ++q)
-                s += part[((q * p.rw + tile_in_cta) * M + m) * kRowsPerWarp + r];
-            y[static_cast<size_t>(m) * n_rows + row] = s;
+        for (int j = 0; j < R; ++j) {
+            const int row = row0 + j * kLaneRows + r;
+            if (row >= n_rows) continue;
+#pragma unroll
+            for (int m = 0; m < M; ++m) {
+                float s = 0.0f;
+                for (uint32_t q = 0; q < ksplit; ++q)
+                    s += part[((q * p.rw + tile_in_cta) * M + m) * kRowsPerWarp + j * kLaneRows + r];
+                y[static_cast<size_t>(m) * n_rows + row] = s;
+            }
         }
     }
 }
@@ -530,10 +681,10 @@ struct StreamShape {
     size_t smem;
 };
 
-template <Fmt F, int M, int L>
+template <Fmt F, int M, int L, int R>
 StreamShape stream_shape(int64_t tiles, int64_t k, int sms) {
     constexpr int CB = StreamFmt<F>::kChunkBytes;
-    constexpr int kRowsPerWarp = 32 / L;
+    constexpr int kRowsPerWarp = 32 / L * R;
     StreamShape sh;
     const int C = static_cast<int>(k / kChunkK);
     const int64_t want = static_cast<int64_t>(QMM_GEMV_WARPS_PER_SM) * sms;
@@ -556,25 +707,33 @@ StreamShape stream_shape(int64_t tiles, int64_t k, int sms) {
     sh.rw = 1;
     while (sh.rw * sh.kw < QMM_GEMV_MIN_WARPS && tiles >= 2LL * sh.rw * sms) sh.rw *= 2;
     sh.stages = std::min(sh.cpw, QMM_GEMV_STAGES);
-    const int nw = sh.rw * sh.kw;
-    const int cta_chunks = sh.kw * sh.cpw;
-    sh.smem = static_cast<size_t>(nw) * sh.stages * kRowsPerWarp * CB +
-              sizeof(float) * (static_cast<size_t>(M) * cta_chunks * kChunkK +
-                               static_cast<size_t>(nw) * M * kRowsPerWarp +
-                               static_cast<size_t>(sh.ksplit) * sh.rw * M * kRowsPerWarp) +
-              sizeof(uint64_t) * (nw * sh.stages + 1) + 128;
+    auto smem_of = [&](const StreamShape &t) {
+        const int nw = t.rw * t.kw;
+        const int cta_chunks = t.kw * t.cpw;
+        return static_cast<size_t>(nw) * t.stages * kRowsPerWarp * CB +
+               sizeof(float) * (static_cast<size_t>(M) * cta_chunks * kChunkK +
+                                static_cast<size_t>(nw) * M * kRowsPerWarp +
+                                static_cast<size_t>(t.ksplit) * t.rw * M * kRowsPerWarp) +
+               sizeof(uint64_t) * (nw * t.stages + 1) + 128;
+    };
+    // fit the shared-memory budget: shallower rings, then fewer tiles per CTA
+    while (smem_of(sh) > kGemvSmemCap && sh.stages > 2) --sh.stages;
+    while (smem_of(sh) > kGemvSmemCap && sh.rw > 1) sh.rw /= 2;
+    while (smem_of(sh) > kGemvSmemCap && sh.stages > 1) --sh.stages;
+    sh.smem = smem_of(sh);
     return sh;
 }
 
 // One launch over `count` problems sharing x: problem i has weights
 // probs[i].w (probs[i].n rows) and output probs[i].y.
-template <Fmt F, int M, int L>
+template <Fmt F, int M, int L, int R>
 cudaError_t launch_stream(const GemvProblem *probs, int count, const float *x, int64_t k,
                           cudaStream_t stream, const LaunchCtx &ctx) {
-    constexpr int kRowsPerWarp = 32 / L;
+    constexpr int kRowsPerWarp = 32 / L * R;
     int64_t tiles = 0;
     for (int i = 0; i < count; ++i) tiles += (probs[i].n + kRowsPerWarp - 1) / kRowsPerWarp;
-    const StreamShape sh = stream_shape<F, M, L>(tiles, k, device_sm_count());
+    const StreamShape sh = stream_shape<F, M, L, R>(tiles, k, device_sm_count());
+    if (sh.smem > kGemvSmemCap) return cudaErrorInvalidConfiguration;
     StreamMaps maps;
     StreamParams p;
     p.x = x;
@@ -607,7 +766,7 @@ cudaError_t launch_stream(const GemvProblem *probs, int count, const float *x, i
         }
     }
     p.group_begin[kMaxGemvProblems] = static_cast<int>(groups);
-    auto kern = gemv_stream_kernel<F, M, L>;
+    auto kern = gemv_stream_kernel<F, M, L, R>;
     static int smem_limits[kMaxDevices] = {0};  // this instantiation's own cache
     const cudaError_t e = ensure_smem(kern, sh.smem, true, smem_limits);
     if (e != cudaSuccess) return e;
@@ -629,11 +788,13 @@ cudaError_t launch_m(const GemvProblem *probs, int count, const float *x, int64_
     if (k % kChunkK == 0 && aligned && k <= (1LL << 24)) {
         // Lanes per row: small problems at small M are latency bound, so more
         // lanes share each row chunk; large or wide-M problems keep one.
-        if constexpr (M <= 4) {
-            if (units <= QMM_GEMV_L4_UNITS) return launch_stream<F, M, 4>(probs, count, x, k, stream, ctx);
-            if (units <= QMM_GEMV_L2_UNITS) return launch_stream<F, M, 2>(probs, count, x, k, stream, ctx);
+        // Rows per lane: at small M each activation load feeds two weight rows.
+        if constexpr (M <= QMM_GEMV_R2_MAX_M) {
+            if (units <= QMM_GEMV_L2_UNITS) return launch_stream<F, M, 2, QMM_GEMV_R_SMALL>(probs, count, x, k, stream, ctx);
+            return launch_stream<F, M, 1, 2>(probs, count, x, k, stream, ctx);
+        } else {
+            return launch_stream<F, M, 1, 1>(probs, count, x, k, stream, ctx);
         }
-        return launch_stream<F, M, 1>(probs, count, x, k, stream, ctx);
     }
     for (int i = 0; i < count; ++i) {  // byte-wise kernel, one launch per problem
         const unsigned grid = static_cast<unsigned>((probs[i].n + 3) / 4);
@@ -645,17 +806,16 @@ cudaError_t launch_m(const GemvProblem *probs, int count, const float *x, int64_
     return cudaSuccess;
 }
 
-template <Fmt F>
-cudaError_t launch_fmt(const GemvProblem *probs, int count, const float *x, int m, int64_t k,
-                       cudaStream_t s, const LaunchCtx &ctx) {
-    switch (m) {
-#define QMM_CASE(MM) \
-    case MM: return launch_m<F, MM>(probs, count, x, k, s, ctx);
-        QMM_CASE(1) QMM_CASE(2) QMM_CASE(3) QMM_CASE(4) QMM_CASE(5) QMM_CASE(6) QMM_CASE(7)
-        QMM_CASE(8) QMM_CASE(9) QMM_CASE(10) QMM_CASE(11) QMM_CASE(12) QMM_CASE(13)
-        QMM_CASE(14) QMM_CASE(15) QMM_CASE(16)
-#undef QMM_CASE
-        default: return cudaErrorInvalidValue;
+// Dispatch of m in [LO, HI] (one translation unit per range builds in
+// parallel with the others).
+template <Fmt F, int LO, int HI>
+cudaError_t launch_m_range(const GemvProblem *probs, int count, const float *x, int m, int64_t k,
+                           cudaStream_t s, const LaunchCtx &ctx) {
+    if constexpr (LO > HI) {
+        return cudaErrorInvalidValue;
+    } else {
+        if (m == LO) return launch_m<F, LO>(probs, count, x, k, s, ctx);
+        return launch_m_range<F, LO + 1, HI>(probs, count, x, m, k, s, ctx);
     }
 }
 

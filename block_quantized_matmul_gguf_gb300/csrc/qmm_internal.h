@@ -96,16 +96,36 @@ struct GemvProblem {
 };
 
 // GEMV over `count` (1..4) problems that share x [m][k]; one launch when the
-// streaming kernel applies.
-cudaError_t launch_gemv_q4_0(const GemvProblem *probs, int count, const float *x, int m,
-                             int64_t k, cudaStream_t stream, const LaunchCtx &ctx);
-cudaError_t launch_gemv_q8_0(const GemvProblem *probs, int count, const float *x, int m,
-                             int64_t k, cudaStream_t stream, const LaunchCtx &ctx);
+// streaming kernel applies.  Implemented per format and range of m.
+cudaError_t launch_gemv_q4_0_m1_2(const GemvProblem *probs, int count, const float *x, int m,
+                                  int64_t k, cudaStream_t stream, const LaunchCtx &ctx);
+cudaError_t launch_gemv_q4_0_m3_4(const GemvProblem *probs, int count, const float *x, int m,
+                                  int64_t k, cudaStream_t stream, const LaunchCtx &ctx);
+cudaError_t launch_gemv_q4_0_m5_10(const GemvProblem *probs, int count, const float *x, int m,
+                                  int64_t k, cudaStream_t stream, const LaunchCtx &ctx);
+cudaError_t launch_gemv_q4_0_m11_16(const GemvProblem *probs, int count, const float *x, int m,
+                                  int64_t k, cudaStream_t stream, const LaunchCtx &ctx);
+cudaError_t launch_gemv_q8_0_m1_2(const GemvProblem *probs, int count, const float *x, int m,
+                                  int64_t k, cudaStream_t stream, const LaunchCtx &ctx);
+cudaError_t launch_gemv_q8_0_m3_4(const GemvProblem *probs, int count, const float *x, int m,
+                                  int64_t k, cudaStream_t stream, const LaunchCtx &ctx);
+cudaError_t launch_gemv_q8_0_m5_10(const GemvProblem *probs, int count, const float *x, int m,
+                                  int64_t k, cudaStream_t stream, const LaunchCtx &ctx);
+cudaError_t launch_gemv_q8_0_m11_16(const GemvProblem *probs, int count, const float *x, int m,
+                                  int64_t k, cudaStream_t stream, const LaunchCtx &ctx);
 
 inline cudaError_t launch_gemv(Fmt fmt, const GemvProblem *probs, int count, const float *x,
                                int m, int64_t k, cudaStream_t stream, const LaunchCtx &ctx) {
-    return fmt == Fmt::Q4_0 ? launch_gemv_q4_0(probs, count, x, m, k, stream, ctx)
-                            : launch_gemv_q8_0(probs, count, x, m, k, stream, ctx);
+    if (fmt == Fmt::Q4_0) {
+        if (m <= 2) return launch_gemv_q4_0_m1_2(probs, count, x, m, k, stream, ctx);
+        if (m <= 4) return launch_gemv_q4_0_m3_4(probs, count, x, m, k, stream, ctx);
+        if (m <= 10) return launch_gemv_q4_0_m5_10(probs, count, x, m, k, stream, ctx);
+        return launch_gemv_q4_0_m11_16(probs, count, x, m, k, stream, ctx);
+    }
+    if (m <= 2) return launch_gemv_q8_0_m1_2(probs, count, x, m, k, stream, ctx);
+    if (m <= 4) return launch_gemv_q8_0_m3_4(probs, count, x, m, k, stream, ctx);
+    if (m <= 10) return launch_gemv_q8_0_m5_10(probs, count, x, m, k, stream, ctx);
+    return launch_gemv_q8_0_m11_16(probs, count, x, m, k, stream, ctx);
 }
 
 cudaError_t launch_gemm_q4_0(const uint8_t *w, const uint16_t *x, float *y, int64_t m,
