@@ -12,27 +12,37 @@
 // memory.
 //
 // Structure: persistent CTA pairs (thread-block clusters of 2), one CTA per
-// SM, 448 threads each, warp-specialised.  A pair computes a 256 x 256 tile
-// of Y with tcgen05.mma.cta_group::2 (M=256, N=256, K=16): each CTA holds 128
-// rows of X (the A operand) and 128 dequantised rows of W (its half of the B
-// operand), so each SM dequantises and stages half of B per tile.
-//   warp 0      producer (both CTAs): TMA loads of its X rows (128 x 64 bf16,
-//               128-byte swizzle; completion counted on the leader CTA's
-//               barrier) and of its raw Q4_0 rows (128 rows x 144 bytes).
-//   warps 2-9   dequantisers (both CTAs): thread t owns W row t % 128 and one
-//               of the two 32-weight blocks of each 64-wide K stage; it reads
-//               the row's 144 raw bytes (conflict-free 16-byte loads) and
-//               writes bf16 weights into the B tile in the canonical K-major
-//               128-byte-swizzled layout (16-byte chunk c of row r at chunk
-//               c ^ (r & 7)), then signals the leader.
-//   warp 1      MMA issuer (leader CTA only): one thread issues the pair's
-//               MMAs into one of two TMEM accumulators (2 x 256 columns);
-//               tcgen05.commit multicasts stage releases and accumulator
-//               hand-overs to both CTAs.
+// SM, 448 threads each, warp-specialised.  A pair computes a tile of
+// 256 weight rows x 256 tokens as Y^T = W . X^T with
+// tcgen05.mma.cta_group::2 (M=256 weight rows, N=256 tokens, K=16): the A
+// operand (dequantised W, bf16) is in tensor memory, written there by the
+// dequantiser warps with tcgen05.st straight from registers; the B operand
+// (X, bf16) is in shared memory, loaded by TMA.  Each CTA holds 128 weight
+// rows in its TMEM and 128 tokens of X in its shared memory.  Writing the
+// weights to tensor memory instead of shared memory avoids both the shared-
+// memory traffic of a dequantised B tile and the generic-to-async proxy
+// fence that shared-memory writes need before the tensor core may read
+// them (about 1.6k cycles per fence and warp on this part).
+//   warp 0      producers (both CTAs): lane 0 loads X tiles (128 tokens x
+//               64 bf16, 128-byte swizzle; completion counted on the leader
+//               CTA's barrier), lane 1 loads raw Q4_0 tiles (128 rows x 144
+//               bytes = 8 blocks per row).
+//   warps 2-9   dequantisers (both CTAs): warp w owns TMEM lanes (weight
+//               rows) 32*(w%4)..+31 and one of the two 32-weight blocks of
+//               each 64-wide K stage; it forms bf16((nibble-8)*d) and writes
+//               16 columns of the stage's A slot with tcgen05.st.
+//   warp 1      MMA issuer (leader CTA): one thread issues the pair's MMAs
+//               into the 256-column accumulator and releases X stages, A
+//               slots and the accumulator with multicast tcgen05.commit.
+//               Every dequantiser warp of both CTAs reports a written A slot
+//               on the leader's barrier with a CTA-scope (not cluster-scope)
+//               release arrive: the TMEM data is complete once tcgen05.wait::st
+//               returns, and a cluster-scope release costs about 1k cycles per
+//               arrive on this part, which serialised the pipeline when one
+//               peer thread forwarded every stage.
 //   warps 10-13 epilogue (both CTAs): tcgen05.ld of the CTA's 128 x 256 fp32
-//               accumulator (warp w reads TMEM lanes 32*(w%4)..+31) and stores
-//               to Y; the second accumulator lets the next tile's MMAs run
-//               meanwhile.
+//               accumulator; lane i holds weight row i, so each store of a
+//               warp writes 32 consecutive outputs of one token (coalesced).
 // Every wait is bounded (GPU global timer).  On a timeout the CTA records the
 // error, sets a shared abort flag that makes its other waits give up at once,
 // lets its own TMA copies and MMAs finish (bounded waits), keeps its shared
@@ -44,51 +54,67 @@
 namespace qmm {
 namespace {
 
-constexpr int BM = 128;              // X rows per CTA (MMA M = 2 * BM per pair)
-constexpr int BN = 256;              // W rows per pair tile (MMA N)
-constexpr int BN_CTA = BN / 2;       // W rows each CTA dequantises
-constexpr int BK = 64;               // K per operand stage (one 128-byte swizzle row)
+#ifndef QMM_GEMM_STAGES
+#define QMM_GEMM_STAGES 8
+#endif
+#ifndef QMM_GEMM_LOOKAHEAD_KK
+#define QMM_GEMM_LOOKAHEAD_KK 1
+#endif
+#ifndef QMM_GEMM_GROUP
+#define QMM_GEMM_GROUP 4
+#endif
+#ifndef QMM_GEMM_RAW_STAGES
+#define QMM_GEMM_RAW_STAGES 3
+#endif
+constexpr int BW = 128;              // weight rows per CTA (MMA M = 2 * BW per pair)
+constexpr int BT = 256;              // tokens per pair tile (MMA N); 128 per CTA
+constexpr int BT_CTA = BT / 2;
+constexpr int BK = 64;               // K per stage (one 128-byte swizzle row of X)
 constexpr int UMMA_K = 16;           // K per tcgen05.mma (kind::f16)
 constexpr int RAW_K = 256;           // K per raw stage (8 Q4_0 blocks)
 constexpr int RAW_ROW_BYTES = 144;   // 8 blocks x 18 bytes
-#ifndef QMM_GEMM_OP_STAGES
-#define QMM_GEMM_OP_STAGES 5
-#endif
-#ifndef QMM_GEMM_RAW_STAGES
-#define QMM_GEMM_RAW_STAGES 2
-#endif
-#ifndef QMM_GEMM_DEQ_WARPS
-#define QMM_GEMM_DEQ_WARPS 8  // 8: a thread decodes one block per K stage; 16: half a block
-#endif
-constexpr int OP_STAGES = QMM_GEMM_OP_STAGES;
+constexpr int STAGES = QMM_GEMM_STAGES;  // K stages in flight (X in shared memory, A in TMEM)
+constexpr int LOOKAHEAD_KK = QMM_GEMM_LOOKAHEAD_KK;
+// Stages are announced to the MMA thread in groups: one "full" barrier per
+// GROUP consecutive stages, so the issuing thread waits once per 4*GROUP MMAs.
+// Under the integer/fp32 load of the dequantiser warps on the same SM, each
+// wait delays the issue stream by a couple of hundred cycles; one wait per
+// 16 MMAs hides that behind the MMAs still queued.  Slots are still released
+// one stage at a time.
+constexpr int GROUP = QMM_GEMM_GROUP;
+constexpr int NGROUPS = STAGES / GROUP;
+static_assert(STAGES % GROUP == 0, "whole groups in the ring");
+static_assert((256 / BK) % GROUP == 0, "k % 256 == 0 makes every tile a whole number of groups");
 constexpr int RAW_STAGES = QMM_GEMM_RAW_STAGES;
-constexpr int X_STAGE_BYTES = BM * BK * 2;               // 16 KB
-constexpr int W_STAGE_BYTES = BN_CTA * BK * 2;           // 16 KB
-constexpr int RAW_STAGE_BYTES = BN_CTA * RAW_ROW_BYTES;  // 18 KB
-constexpr int NUM_ACC = 2;
-constexpr uint32_t TMEM_COLS = NUM_ACC * BN;             // 512 fp32 columns
+constexpr int X_STAGE_BYTES = BT_CTA * BK * 2;           // 16 KB
+constexpr int RAW_STAGE_BYTES = BW * RAW_ROW_BYTES;      // 18 KB
+constexpr uint32_t D_COLS = BT;                          // fp32 accumulator columns
+constexpr uint32_t A_COLS = BK / 2;                      // bf16 pairs per row per stage
+constexpr uint32_t TMEM_COLS = 512;
+static_assert(D_COLS + STAGES * A_COLS <= TMEM_COLS, "tensor memory budget");
+static_assert(LOOKAHEAD_KK >= 0 && LOOKAHEAD_KK < BK / 16, "look-ahead point within a stage");
 
 constexpr int WARP_PRODUCER = 0;
 constexpr int WARP_MMA = 1;
 constexpr int WARP_DEQ0 = 2;
-constexpr int NUM_DEQ_WARPS = QMM_GEMM_DEQ_WARPS;     // 2 or 4 threads per W row
+constexpr int NUM_DEQ_WARPS = 8;                     // 4 lane quarters x 2 blocks per stage
 constexpr int WARP_EPI0 = WARP_DEQ0 + NUM_DEQ_WARPS;  // 10
-constexpr int NUM_EPI_WARPS = 4;
-constexpr int NUM_THREADS = (WARP_EPI0 + NUM_EPI_WARPS) * 32;  // 448
+#ifndef QMM_GEMM_EPI_WARPS
+#define QMM_GEMM_EPI_WARPS 8
+#endif
+constexpr int NUM_EPI_WARPS = QMM_GEMM_EPI_WARPS;  // 4 or 8: one or two per lane quarter
+static_assert(NUM_EPI_WARPS == 4 || NUM_EPI_WARPS == 8, "epilogue warps");
+constexpr int NUM_THREADS = (WARP_EPI0 + NUM_EPI_WARPS) * 32;  // 448 or 576
 
-static_assert(NUM_DEQ_WARPS * 32 == 2 * BN_CTA || NUM_DEQ_WARPS * 32 == 4 * BN_CTA,
-              "two or four dequantiser threads per W row");
-constexpr int DEQ_PER_ROW = NUM_DEQ_WARPS * 32 / BN_CTA;
 static_assert(RAW_K % BK == 0 && BK == 2 * 32, "a K stage is two blocks");
 
 struct SmemLayout {
     static constexpr int x = 0;
-    static constexpr int w = x + OP_STAGES * X_STAGE_BYTES;
-    static constexpr int raw = w + OP_STAGES * W_STAGE_BYTES;
+    static constexpr int raw = x + STAGES * X_STAGE_BYTES;
     static constexpr int bars = raw + RAW_STAGES * RAW_STAGE_BYTES;
-    // barriers: x_full, w_ready, op_empty [OP_STAGES]; raw_full, raw_empty
-    // [RAW_STAGES]; acc_full, acc_empty [NUM_ACC]; final; w_local [OP_STAGES]
-    static constexpr int nbars = 4 * OP_STAGES + 2 * RAW_STAGES + 2 * NUM_ACC + 1;
+    // barriers: full [NGROUPS], empty [STAGES]; raw_full, raw_empty
+    // [RAW_STAGES]; d_full, d_empty, final
+    static constexpr int nbars = NGROUPS + STAGES + 2 * RAW_STAGES + 3;
     static constexpr int tmem_slot = bars + nbars * 8;
     static constexpr int abort_flag = tmem_slot + 4;
     static constexpr int total = abort_flag + 4;
@@ -99,7 +125,7 @@ static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 struct GemmParams {
     float *y;
     int m, n, k;
-    int num_m_blocks;  // of 2*BM rows
+    int num_t_blocks;  // token blocks of BT
     int num_tiles;     // pair tiles
     LaunchCtx ctx;
 };
@@ -156,6 +182,11 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t local, uint32_t rank) {
     return r;
 }
 
+// Arrive on a barrier of either CTA of the pair (CTA-scope release).
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster) {
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
                  : "memory");
@@ -176,13 +207,29 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                               uint32_t idesc, uint32_t accumulate) {
+// D (TMEM) += A (TMEM, both CTAs' halves) x B (shared-memory descriptor).
+__device__ __forceinline__ void umma_bf16_pair_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                                  uint32_t idesc, uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
+}
+
+// 16 consecutive 32-bit TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_st_16cols(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+        "r"(v[15])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 // Arrive (once each) on the barrier at this shared-memory offset in both CTAs
@@ -222,10 +269,10 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
 }
 
 // Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major,
-// N = 256, M = 256 (the pair).
+// N = 256 tokens, M = 256 weight rows (the pair).
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
-                            (static_cast<uint32_t>(BN >> 3) << 17) |
-                            (static_cast<uint32_t>((2 * BM) >> 4) << 24);
+                            (static_cast<uint32_t>(BT >> 3) << 17) |
+                            (static_cast<uint32_t>((2 * BW) >> 4) << 24);
 
 __device__ __forceinline__ bool abort_set(const int *flag) {
     return *reinterpret_cast<const volatile int *>(flag) != 0;
@@ -372,6 +419,15 @@ __device__ __forceinline__ void dequant_words_bf16(const uint32_t (&wd)[36], int
 
 
 
+#ifndef QMM_GEMM_WAIT_CLUSTER
+#define QMM_GEMM_WAIT_CLUSTER 0
+#endif
+#if QMM_GEMM_WAIT_CLUSTER
+#define MMA_WAIT wait_or_abort_cluster
+#else
+#define MMA_WAIT wait_or_abort
+#endif
+
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_q4_0_kernel(const __grid_constant__ CUtensorMap tmap_x,
                      const __grid_constant__ CUtensorMap tmap_w, GemmParams p) {
@@ -389,36 +445,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int num_pairs = static_cast<int>(gridDim.x >> 1);
 
     auto bar = [&](int i) -> uint32_t { return sbase + SmemLayout::bars + 8u * i; };
-    auto x_full = [&](int s) { return bar(s); };                    // leader: 2 arrivals + bytes
-    auto w_ready = [&](int s) { return bar(OP_STAGES + s); };       // leader: 16 warps
-    auto op_empty = [&](int s) { return bar(2 * OP_STAGES + s); };  // both: MMA commit
-    auto raw_full = [&](int r) { return bar(3 * OP_STAGES + r); };
-    auto raw_empty = [&](int r) { return bar(3 * OP_STAGES + RAW_STAGES + r); };
-    auto acc_full = [&](int a) { return bar(3 * OP_STAGES + 2 * RAW_STAGES + a); };  // both
-    auto acc_empty = [&](int a) {  // leader: 8 epilogue warps
-        return bar(3 * OP_STAGES + 2 * RAW_STAGES + NUM_ACC + a);
-    };
-    const uint32_t final_bar = bar(3 * OP_STAGES + 2 * RAW_STAGES + 2 * NUM_ACC);
-    // peer CTA: its dequantisers' stage-done signal, forwarded once to the leader
-    auto w_local = [&](int s) { return bar(3 * OP_STAGES + 2 * RAW_STAGES + 2 * NUM_ACC + 1 + s); };
+    // full(g): leader only; for each stage of group g, both X producers
+    // (expect_tx + bytes) and the 16 dequantiser warps of the pair.
+    // empty(s): both CTAs; multicast commit once the stage's MMAs are done.
+    // Stage index i (counted over the pair's whole sequence) uses slot
+    // i % STAGES and group barrier (i / GROUP) % NGROUPS, whose phase is
+    // i / STAGES.
+    auto full = [&](uint32_t i) { return bar(static_cast<int>((i / GROUP) % NGROUPS)); };
+    auto empty = [&](int s) { return bar(NGROUPS + s); };
+    auto raw_full = [&](int r) { return bar(NGROUPS + STAGES + r); };
+    auto raw_empty = [&](int r) { return bar(NGROUPS + STAGES + RAW_STAGES + r); };
+    const uint32_t d_full = bar(NGROUPS + STAGES + 2 * RAW_STAGES);       // both
+    const uint32_t d_empty = bar(NGROUPS + STAGES + 2 * RAW_STAGES + 1);  // leader: 8
+    const uint32_t final_bar = bar(NGROUPS + STAGES + 2 * RAW_STAGES + 2);
     int *abort_flag = reinterpret_cast<int *>(sgen + SmemLayout::abort_flag);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sgen + SmemLayout::tmem_slot);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < OP_STAGES; ++s) {
-            mbar_init_addr(x_full(s), 2);
-            mbar_init_addr(w_ready(s), NUM_DEQ_WARPS + 1);  // own warps + the peer's forward
-            mbar_init_addr(op_empty(s), 1);
-            mbar_init_addr(w_local(s), NUM_DEQ_WARPS);
-        }
+        for (int g = 0; g < NGROUPS; ++g) mbar_init_addr(bar(g), GROUP * (2 + 2 * NUM_DEQ_WARPS));
+        for (int s = 0; s < STAGES; ++s) mbar_init_addr(empty(s), 1);
         for (int r = 0; r < RAW_STAGES; ++r) {
             mbar_init_addr(raw_full(r), 1);
             mbar_init_addr(raw_empty(r), NUM_DEQ_WARPS);
         }
-        for (int a = 0; a < NUM_ACC; ++a) {
-            mbar_init_addr(acc_full(a), 1);
-            mbar_init_addr(acc_empty(a), 2 * NUM_EPI_WARPS);
-        }
+        mbar_init_addr(d_full, 1);
+        mbar_init_addr(d_empty, 2 * NUM_EPI_WARPS);
         mbar_init_addr(final_bar, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -429,214 +480,192 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     cluster_barrier();  // the peer's barriers exist before anyone signals them
     tc_fence_after();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
+    const uint32_t a_col0 = D_COLS;  // A slots follow the accumulator
 
     pdl_wait();
 
-    const int KB = p.k / BK;     // operand stages per tile
+    const int KB = p.k / BK;     // K stages per tile
     const int KR = p.k / RAW_K;  // raw stages per tile
 
     if (warp == WARP_PRODUCER) {
         if (lane == 0) {
+            // X tiles: this CTA's 128 tokens of the pair tile
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_x)) : "memory");
-            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_w)) : "memory");
-            uint32_t it = 0, rit = 0;
+            uint32_t it = 0;
             bool ok = true;
             for (int t = pair; ok && t < p.num_tiles; t += num_pairs) {
-                const int mb = t % p.num_m_blocks, nb = t / p.num_m_blocks;
-                const int xrow = mb * 2 * BM + static_cast<int>(rank) * BM;
-                const int wrow = nb * BN + static_cast<int>(rank) * BN_CTA;
-                for (int kb = 0; ok && kb < KB; ++kb) {
-                    if (kb % (RAW_K / BK) == 0) {
-                        const int r = rit % RAW_STAGES;
-                        const uint32_t ph = (rit / RAW_STAGES) & 1u;
-                        if (!wait_or_abort(raw_empty(r), ph ^ 1u, abort_flag, ctx)) { ok = false; break; }
-                        mbar_expect_tx_addr(raw_full(r), RAW_STAGE_BYTES);
-                        tma_load_2d(sbase + SmemLayout::raw + r * RAW_STAGE_BYTES, &tmap_w,
-                                    (kb / (RAW_K / BK)) * RAW_ROW_BYTES, wrow, raw_full(r));
-                        ++rit;
-                    }
-                    const int s = it % OP_STAGES;
-                    const uint32_t ph = (it / OP_STAGES) & 1u;
-                    if (!wait_or_abort(op_empty(s), ph ^ 1u, abort_flag, ctx)) { ok = false; break; }
-                    const uint32_t xf = map_to_rank(x_full(s), 0);
+                const int tb = t % p.num_t_blocks;
+                const int xrow = tb * BT + static_cast<int>(rank) * BT_CTA;
+                for (int kb = 0; kb < KB; ++kb) {
+                    const int s = it % STAGES;
+                    const uint32_t ph = (it / STAGES) & 1u;
+                    if (!wait_or_abort(empty(s), ph ^ 1u, abort_flag, ctx)) { ok = false; break; }
+                    const uint32_t xf = map_to_rank(full(it), 0);
                     mbar_expect_tx_cluster(xf, X_STAGE_BYTES);
-                    tma_load_2d_pair(sbase + SmemLayout::x + s * X_STAGE_BYTES, &tmap_x, kb * BK, xrow,
-                                     xf);
+                    tma_load_2d_pair(sbase + SmemLayout::x + s * X_STAGE_BYTES, &tmap_x, kb * BK, xrow, xf);
                     ++it;
                 }
             }
-            // let our own copies land before the CTA may exit: raw tiles on our
-            // barriers; X tiles either consumed (op_empty) or drained by the leader
+            if (leader) {  // X copies of both CTAs complete on the leader's barriers
+                for (int s = 0; s < STAGES; ++s) {
+                    if (it > static_cast<uint32_t>(s)) {
+                        const uint32_t last = it - 1 - ((it - 1 - s) % STAGES);
+                        wait_drain(full(last), (last / STAGES) & 1u, ctx);
+                    }
+                }
+            }
+        } else if (lane == 1) {
+            // raw weight tiles: this CTA's 128 weight rows
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_w)) : "memory");
+            uint32_t rit = 0;
+            bool ok = true;
+            for (int t = pair; ok && t < p.num_tiles; t += num_pairs) {
+                const int wb = t / p.num_t_blocks;
+                const int wrow = wb * 2 * BW + static_cast<int>(rank) * BW;
+                for (int kr = 0; kr < KR; ++kr) {
+                    const int r = rit % RAW_STAGES;
+                    const uint32_t ph = (rit / RAW_STAGES) & 1u;
+                    if (!wait_or_abort(raw_empty(r), ph ^ 1u, abort_flag, ctx)) { ok = false; break; }
+                    mbar_expect_tx_addr(raw_full(r), RAW_STAGE_BYTES);
+                    tma_load_2d(sbase + SmemLayout::raw + r * RAW_STAGE_BYTES, &tmap_w, kr * RAW_ROW_BYTES,
+                                wrow, raw_full(r));
+                    ++rit;
+                }
+            }
             for (int r = 0; r < RAW_STAGES; ++r) {
                 if (rit > static_cast<uint32_t>(r)) {
                     const uint32_t last = rit - 1 - ((rit - 1 - r) % RAW_STAGES);
                     wait_drain(raw_full(r), (last / RAW_STAGES) & 1u, ctx);
                 }
             }
-            if (leader) {
-                for (int s = 0; s < OP_STAGES; ++s) {
-                    if (it > static_cast<uint32_t>(s)) {
-                        const uint32_t last = it - 1 - ((it - 1 - s) % OP_STAGES);
-                        wait_drain(x_full(s), (last / OP_STAGES) & 1u, ctx);
-                    }
-                }
-            }
         }
     } else if (warp == WARP_MMA) {
         if (leader && lane == 0) {
-            uint32_t it = 0, ait = 0;
-            bool ok = true, issued = false;
-            for (int t = pair; ok && t < p.num_tiles; t += num_pairs) {
-                const int a = ait % NUM_ACC;
-                const uint32_t aph = (ait / NUM_ACC) & 1u;
-                if (!wait_or_abort_cluster(acc_empty(a), aph ^ 1u, abort_flag, ctx)) break;
+            // one flat sequence of K stages over this pair's tiles; the wait
+            // for stage g+1 is placed after MMA LOOKAHEAD_KK of stage g, so
+            // that its latency overlaps the MMAs still queued in the pipe
+            const uint32_t my_tiles =
+                pair < p.num_tiles ? static_cast<uint32_t>((p.num_tiles - pair + num_pairs - 1) / num_pairs) : 0u;
+            const uint32_t total = my_tiles * static_cast<uint32_t>(KB);
+            uint32_t tiles_done = 0;
+            bool issued = false;
+            bool ok = total == 0 || MMA_WAIT(full(0u), 0u, abort_flag, ctx);
+            for (uint32_t g = 0; ok && g < total; ++g) {
+                const uint32_t kb = g % static_cast<uint32_t>(KB);
+                const int s = static_cast<int>(g % STAGES);
+                if (kb == 0 && !wait_or_abort_cluster(d_empty, (tiles_done & 1u) ^ 1u, abort_flag, ctx))
+                    break;
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + a * BN;
-                for (int kb = 0; kb < KB; ++kb) {
-                    const int s = it % OP_STAGES;
-                    const uint32_t ph = (it / OP_STAGES) & 1u;
-                    if (!wait_or_abort_cluster(x_full(s), ph, abort_flag, ctx) ||
-                        !wait_or_abort_cluster(w_ready(s), ph, abort_flag, ctx)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint64_t adesc = sw128_desc(sbase + SmemLayout::x + s * X_STAGE_BYTES);
-                    const uint64_t bdesc = sw128_desc(sbase + SmemLayout::w + s * W_STAGE_BYTES);
+                const uint64_t bdesc = sw128_desc(sbase + SmemLayout::x + s * X_STAGE_BYTES);
+                const uint32_t a_tmem = tmem_base + a_col0 + s * A_COLS;
 #pragma unroll
-                    for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                        // advance 16 bf16 = 32 bytes along K inside the swizzle row
-                        umma_bf16_pair(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, kIdesc,
-                                       (kb | kk) != 0 ? 1u : 0u);
+                for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                    // K step kk: 8 TMEM columns of A, 32 bytes along the swizzle row of B
+                    umma_bf16_pair_ta(tmem_base, a_tmem + (UMMA_K / 2) * kk, bdesc + 2 * kk, kIdesc,
+                                      (kb | static_cast<uint32_t>(kk)) != 0 ? 1u : 0u);
+                    if (kk == LOOKAHEAD_KK && (g + 1) % GROUP == 0 && g + 1 < total) {
+                        const uint32_t g1 = g + 1;  // first stage of the next group
+                        ok = MMA_WAIT(full(g1), (g1 / STAGES) & 1u, abort_flag, ctx);
                     }
-                    issued = true;
-                    umma_commit_pair(op_empty(s));
-                    ++it;
                 }
-                if (!ok) break;
-                umma_commit_pair(acc_full(a));
-                ++ait;
+                issued = true;
+                umma_commit_pair(empty(s));
+                if (kb + 1 == static_cast<uint32_t>(KB)) {
+                    umma_commit_pair(d_full);
+                    ++tiles_done;
+                }
             }
             if (issued) {  // all MMAs of the pair complete before TMEM is freed
                 umma_commit_pair(final_bar);
                 wait_drain(final_bar, 0, ctx);
             }
-        } else if (!leader && lane == 0) {
-            // forward "stage written" once per stage: a cluster-scope release
-            // by one thread instead of one per dequantiser warp
-            const uint32_t w_ready_leader0 = map_to_rank(w_ready(0), 0);
-            uint32_t it = 0;
-            bool ok = true;
-            for (int t = pair; ok && t < p.num_tiles; t += num_pairs) {
-                for (int kb = 0; kb < KB; ++kb) {
-                    const int s = it % OP_STAGES;
-                    const uint32_t ph = (it / OP_STAGES) & 1u;
-                    if (!wait_or_abort(w_local(s), ph, abort_flag, ctx)) { ok = false; break; }
-                    mbar_arrive_cluster(w_ready_leader0 + 8u * s);
-                    ++it;
-                }
-            }
         }
     } else if (warp < WARP_EPI0) {
-        // dequantisers: thread dt owns W row dt % 128 and, of each 64-wide K
-        // stage, block (2*sub + half) -- all of it (2 threads per row) or the
-        // qs words 2*wh, 2*wh+1 of it (4 threads per row)
-        const int dt = (warp - WARP_DEQ0) * 32 + lane;
-        const int row = dt & (BN_CTA - 1);
-        const int part = dt >> 7;  // warp-uniform
-        const int half = DEQ_PER_ROW == 2 ? part : (part >> 1);
-        const int wh = DEQ_PER_ROW == 2 ? 0 : (part & 1);
-        // leader: arrive on its own w_ready; peer: on its w_local (forwarded)
-        const uint32_t done0 = leader ? w_ready(0) : w_local(0);
+        // dequantisers: warp w writes TMEM lanes 32*(w%4)..+31 (its weight rows)
+        // and block `half` (K 32*half..+31) of every 64-wide K stage
+        const int q = warp & 3;
+        const int half = (warp - WARP_DEQ0) >> 2;  // warp-uniform
+        const int row = q * 32 + lane;             // weight row within the CTA's 128
+        const uint32_t full_leader0 = map_to_rank(bar(0), 0);
+        const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + a_col0 +
+                                   static_cast<uint32_t>(half * 16);
         uint32_t it = 0, rit = 0;
         bool ok = true;
         for (int t = pair; ok && t < p.num_tiles; t += num_pairs) {
             for (int kr = 0; ok && kr < KR; ++kr) {
                 const int r = rit % RAW_STAGES;
-                const uint32_t rph = (rit / RAW_STAGES) & 1u;
-                if (!warp_wait_or_abort(raw_full(r), rph, abort_flag, ctx)) { ok = false; break; }
+                if (!warp_wait_or_abort(raw_full(r), (rit / RAW_STAGES) & 1u, abort_flag, ctx)) {
+                    ok = false;
+                    break;
+                }
                 uint32_t wd[36];
                 const uint8_t *src = sgen + SmemLayout::raw + r * RAW_STAGE_BYTES + row * RAW_ROW_BYTES;
 #pragma unroll
-                for (int q = 0; q < 9; ++q) {
-                    const uint4 v = lds128(src + 16 * q);
-                    wd[4 * q + 0] = v.x;
-                    wd[4 * q + 1] = v.y;
-                    wd[4 * q + 2] = v.z;
-                    wd[4 * q + 3] = v.w;
+                for (int qq = 0; qq < 9; ++qq) {
+                    const uint4 v = lds128(src + 16 * qq);
+                    wd[4 * qq + 0] = v.x;
+                    wd[4 * qq + 1] = v.y;
+                    wd[4 * qq + 2] = v.z;
+                    wd[4 * qq + 3] = v.w;
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive_addr(raw_empty(r));
                 ++rit;
 #pragma unroll
                 for (int sub = 0; sub < RAW_K / BK; ++sub) {
-                    const int s = it % OP_STAGES;
-                    const uint32_t ph = (it / OP_STAGES) & 1u;
-                    if (!warp_wait_or_abort(op_empty(s), ph ^ 1u, abort_flag, ctx)) { ok = false; break; }
-                    uint8_t *row_ptr = sgen + SmemLayout::w + s * W_STAGE_BYTES + row * 128;
-                    const uint32_t sw = static_cast<uint32_t>(row & 7);
-                    // block 2*sub + half of the row chunk: K positions 32*half .. +31
-                    if constexpr (DEQ_PER_ROW == 2) {
-                        uint4 ch[4];
-                        if (half == 0)
-                            dequant_words_bf16<0, 4>(wd, 2 * sub, ch);
-                        else
-                            dequant_words_bf16<0, 4>(wd, 2 * sub + 1, ch);
-#pragma unroll
-                        for (int c = 0; c < 4; ++c)
-                            *reinterpret_cast<uint4 *>(row_ptr + (((4 * half + c) ^ sw) << 4)) = ch[c];
-                    } else {
-                        // words 2*wh, 2*wh+1: chunk wh (low nibbles) and 2 + wh (high)
-                        uint4 ch[2];
-                        const int b = 2 * sub + half;
-                        if (wh == 0) {
-                            if (half == 0) dequant_words_bf16<0, 2>(wd, 2 * sub, ch);
-                            else dequant_words_bf16<0, 2>(wd, 2 * sub + 1, ch);
-                        } else {
-                            if (half == 0) dequant_words_bf16<2, 2>(wd, 2 * sub, ch);
-                            else dequant_words_bf16<2, 2>(wd, 2 * sub + 1, ch);
-                        }
-                        (void)b;
-                        *reinterpret_cast<uint4 *>(row_ptr + (((4 * half + wh) ^ sw) << 4)) = ch[0];
-                        *reinterpret_cast<uint4 *>(row_ptr + (((4 * half + 2 + wh) ^ sw) << 4)) = ch[1];
+                    const int s = it % STAGES;
+                    if (!warp_wait_or_abort(empty(s), ((it / STAGES) & 1u) ^ 1u, abort_flag, ctx)) {
+                        ok = false;
+                        break;
                     }
-                    fence_proxy_async_smem();  // generic writes -> visible to the tensor core
+                    tc_fence_after();
+                    uint4 ch[4];
+                    if (half == 0)
+                        dequant_words_bf16<0, 4>(wd, 2 * sub, ch);
+                    else
+                        dequant_words_bf16<0, 4>(wd, 2 * sub + 1, ch);
+                    const uint32_t v[16] = {ch[0].x, ch[0].y, ch[0].z, ch[0].w, ch[1].x, ch[1].y,
+                                            ch[1].z, ch[1].w, ch[2].x, ch[2].y, ch[2].z, ch[2].w,
+                                            ch[3].x, ch[3].y, ch[3].z, ch[3].w};
+                    tmem_st_16cols(lane_base + s * A_COLS, v);
+                    tmem_wait_st();
+                    tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive_addr(done0 + 8u * s);
+                    if (lane == 0) mbar_arrive_remote(full_leader0 + 8u * ((it / GROUP) % NGROUPS));
                     ++it;
                 }
             }
         }
     } else {
-        // epilogue
-        const int q = warp & 3;  // TMEM lane quarter this warp may access
-        const uint32_t acc_empty_leader0 = map_to_rank(acc_empty(0), 0);
-        uint32_t ait = 0;
+        // epilogue: lane i of warp quarter q holds weight row 32q+i; columns are tokens
+        const int q = warp & 3;
+        constexpr int CPW = (BT / 32) / (NUM_EPI_WARPS / 4);    // 32-column chunks per warp
+        const int c0 = ((warp - WARP_EPI0) >> 2) * CPW;
+        const uint32_t d_empty_leader = map_to_rank(d_empty, 0);
+        uint32_t tiles_done = 0;
         for (int t = pair; t < p.num_tiles; t += num_pairs) {
-            const int mb = t % p.num_m_blocks, nb = t / p.num_m_blocks;
-            const int a = ait % NUM_ACC;
-            const uint32_t aph = (ait / NUM_ACC) & 1u;
-            if (!warp_wait_or_abort(acc_full(a), aph, abort_flag, ctx)) break;
+            const int tb = t % p.num_t_blocks, wb = t / p.num_t_blocks;
+            if (!warp_wait_or_abort(d_full, tiles_done & 1u, abort_flag, ctx)) break;
             tc_fence_after();
-            const int row = mb * 2 * BM + static_cast<int>(rank) * BM + q * 32 + lane;
-            float *yrow = p.y + static_cast<size_t>(row) * p.n + static_cast<size_t>(nb) * BN;
-            const int ncols = min(BN, p.n - nb * BN);
+            const int n = wb * 2 * BW + static_cast<int>(rank) * BW + q * 32 + lane;
+            const bool n_ok = n < p.n;
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
+            for (int c = c0; c < c0 + CPW; ++c) {
                 uint32_t v[32];
-                tmem_ld_32cols(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + a * BN + c * 32, v);
-                if (row < p.m) {
+                tmem_ld_32cols(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + c * 32, v);
+                // column j of the accumulator is token tb*BT + j: the leader's 128 tokens
+                // then the peer's 128
+                const int m0 = tb * BT + c * 32;
+                if (n_ok) {
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const int col = c * 32 + 4 * j;
-                        if (col < ncols)
-                            *reinterpret_cast<float4 *>(yrow + col) =
-                                make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                            __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
-                    }
+                    for (int j = 0; j < 32; ++j)
+                        if (m0 + j < p.m) p.y[static_cast<size_t>(m0 + j) * p.n + n] = __uint_as_float(v[j]);
                 }
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(acc_empty_leader0 + 8u * a);
-            ++ait;
+            if (lane == 0) mbar_arrive_cluster(d_empty_leader);
+            ++tiles_done;
         }
     }
 
@@ -654,21 +683,21 @@ cudaError_t launch_gemm_q4_0(const uint8_t *w, const uint16_t *x, float *y, int6
                              int64_t k, cudaStream_t stream, const LaunchCtx &ctx) {
     if (m > (1 << 30) || n > (1 << 30) || k > (1 << 24)) return cudaErrorInvalidValue;
     CUtensorMap tx, tw;
-    if (!encode_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, k, m, k * 2, BK, BM,
+    if (!encode_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, k, m, k * 2, BK, BT_CTA,
                         CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     const uint64_t rowbytes = static_cast<uint64_t>(k / kQK) * kQ4_0Bytes;
     if (!encode_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, rowbytes, n, rowbytes,
-                        RAW_ROW_BYTES, BN_CTA))
+                        RAW_ROW_BYTES, BW))
         return cudaErrorInvalidValue;
     GemmParams p;
     p.y = y;
     p.m = static_cast<int>(m);
     p.n = static_cast<int>(n);
     p.k = static_cast<int>(k);
-    p.num_m_blocks = static_cast<int>((m + 2 * BM - 1) / (2 * BM));
-    const int nnb = static_cast<int>((n + BN - 1) / BN);
-    p.num_tiles = p.num_m_blocks * nnb;
+    p.num_t_blocks = static_cast<int>((m + BT - 1) / BT);
+    const int nwb = static_cast<int>((n + 2 * BW - 1) / (2 * BW));
+    p.num_tiles = p.num_t_blocks * nwb;
     p.ctx = ctx;
     static int smem_limits[kMaxDevices] = {0};
     cudaError_t e = ensure_smem(gemm_q4_0_kernel, kSmemBytes, true, smem_limits);
