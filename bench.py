@@ -65,7 +65,8 @@ def parse_args(argv=None):
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--profile", default=None, metavar="CASE",
                     help="no timing: run CASE a few times for a profiler and exit. CASE is "
-                         "decode (one decode-layer step), gemv:FMT:M:N:K, dequant:FMT:N:K "
+                         "decode_grouped (the timed decode step), decode (seven separate calls), "
+                         "gemv:FMT:M:N:K, dequant:FMT:N:K "
                          "or gemm:M:N:K")
     ap.add_argument("--profile-launches", type=int, default=3)
     return ap.parse_args(argv)
@@ -79,7 +80,20 @@ def run_profile(args):
     dev = torch.device("cuda:0")
     parts = args.profile.split(":")
     reps = args.profile_launches
-    if parts[0] == "decode":
+    if parts[0] == "decode_grouped":
+        # the timed step: q+k+v (shared x), o, gate+up (shared x), down
+        cases = [synth.gemv_case("q4_0", 1, p.n, p.k, seed=0, stream=10 + i)
+                 for i, p in enumerate(synth.DECODE_LAYER)]
+        names = [p.name for p in synth.DECODE_LAYER]
+        W = [torch.from_numpy(c.w).to(dev) for c in cases]
+        Y = [torch.empty((1, c.n), dtype=torch.float32, device=dev) for c in cases]
+        groups = [[names.index(nm) for nm in g] for g in DECODE_GROUPS]
+        X = [torch.from_numpy(cases[g[0]].x).to(dev) for g in groups]
+        for _ in range(reps):
+            for g, x in zip(groups, X):
+                qmm.qmm_gemv_q4_0_multi([(W[i], Y[i], cases[i].n) for i in g], x, 1,
+                                        cases[g[0]].k)
+    elif parts[0] == "decode":
         cases = [synth.gemv_case("q4_0", 1, p.n, p.k, seed=0, stream=10 + i)
                  for i, p in enumerate(synth.DECODE_LAYER)]
         W = [torch.from_numpy(c.w).to(dev) for c in cases]

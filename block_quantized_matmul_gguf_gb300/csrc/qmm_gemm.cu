@@ -127,6 +127,7 @@ struct GemmParams {
     int m, n, k;
     int num_t_blocks;  // token blocks of BT
     int num_tiles;     // pair tiles
+    uint32_t magic;    // 0x4B000000 (2^23)
     LaunchCtx ctx;
 };
 
@@ -355,8 +356,11 @@ __device__ __forceinline__ void mbar_expect_tx_addr(uint32_t bar, uint32_t bytes
                  : "memory");
 }
 
-__device__ __forceinline__ float mag(uint32_t v, uint32_t mask) {
-    return __uint_as_float((v & mask) | 0x4B000000u);
+// 2^23 + (v & mask) as a float.  `magic` (0x4B000000) comes from the kernel
+// parameters so that it sits in a register: with the mask and the magic both
+// immediates the compiler splits the extraction into two LOP3.
+__device__ __forceinline__ float mag(uint32_t v, uint32_t mask, uint32_t magic) {
+    return __uint_as_float((v & mask) | magic);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -379,7 +383,7 @@ __device__ __forceinline__ uint32_t w_pair(float ma, float mb, float2 c, float2 
 // 16+4i..19+4i (high nibbles); out[0..NI/2) are the low 16-byte chunks
 // (K 8*I0/2 ..), out[NI/2..NI) the high ones (K 16 + ...).
 template <int I0, int NI>
-__device__ __forceinline__ void dequant_words_bf16(const uint32_t (&wd)[36], int b,
+__device__ __forceinline__ void dequant_words_bf16(const uint32_t (&wd)[36], int b, uint32_t magic,
                                                    uint4 (&out)[NI]) {
     const int base = (18 * b) >> 2;
     uint32_t dbits, q[4];
@@ -404,11 +408,11 @@ __device__ __forceinline__ void dequant_words_bf16(const uint32_t (&wd)[36], int
     for (int j = 0; j < NI; ++j) {
         const uint32_t v = q[I0 + j], u = v >> 16;
         // low nibbles: weights 4i .. 4i+3
-        lo[2 * j + 0] = w_pair(mag(v, 0x0000000Fu), mag(v, 0x00000F00u), c08, d08);
-        lo[2 * j + 1] = w_pair(mag(v, 0x000F0000u), mag(u, 0x00000F00u), c168, d168);
+        lo[2 * j + 0] = w_pair(mag(v, 0x0000000Fu, magic), mag(v, 0x00000F00u, magic), c08, d08);
+        lo[2 * j + 1] = w_pair(mag(v, 0x000F0000u, magic), mag(u, 0x00000F00u, magic), c168, d168);
         // high nibbles: weights 16+4i .. 19+4i
-        hi[2 * j + 0] = w_pair(mag(v, 0x000000F0u), mag(v, 0x0000F000u), c412, d412);
-        hi[2 * j + 1] = w_pair(mag(u, 0x000000F0u), mag(u, 0x0000F000u), c412, d412);
+        hi[2 * j + 0] = w_pair(mag(v, 0x000000F0u, magic), mag(v, 0x0000F000u, magic), c412, d412);
+        hi[2 * j + 1] = w_pair(mag(u, 0x000000F0u, magic), mag(u, 0x0000F000u, magic), c412, d412);
     }
 #pragma unroll
     for (int c = 0; c < NI / 2; ++c) {
@@ -621,9 +625,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     tc_fence_after();
                     uint4 ch[4];
                     if (half == 0)
-                        dequant_words_bf16<0, 4>(wd, 2 * sub, ch);
+                        dequant_words_bf16<0, 4>(wd, 2 * sub, p.magic, ch);
                     else
-                        dequant_words_bf16<0, 4>(wd, 2 * sub + 1, ch);
+                        dequant_words_bf16<0, 4>(wd, 2 * sub + 1, p.magic, ch);
                     const uint32_t v[16] = {ch[0].x, ch[0].y, ch[0].z, ch[0].w, ch[1].x, ch[1].y,
                                             ch[1].z, ch[1].w, ch[2].x, ch[2].y, ch[2].z, ch[2].w,
                                             ch[3].x, ch[3].y, ch[3].z, ch[3].w};
@@ -698,6 +702,7 @@ cudaError_t launch_gemm_q4_0(const uint8_t *w, const uint16_t *x, float *y, int6
     p.num_t_blocks = static_cast<int>((m + BT - 1) / BT);
     const int nwb = static_cast<int>((n + 2 * BW - 1) / (2 * BW));
     p.num_tiles = p.num_t_blocks * nwb;
+    p.magic = 0x4B000000u;
     p.ctx = ctx;
     static int smem_limits[kMaxDevices] = {0};
     cudaError_t e = ensure_smem(gemm_q4_0_kernel, kSmemBytes, true, smem_limits);

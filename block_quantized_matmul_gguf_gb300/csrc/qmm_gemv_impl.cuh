@@ -50,7 +50,7 @@
 #define QMM_GEMV_MAX_KW 8         // largest K split across the warps of a CTA
 #endif
 #ifndef QMM_GEMV_MIN_WARPS
-#define QMM_GEMV_MIN_WARPS 4      // warps per CTA when tiles allow
+#define QMM_GEMV_MIN_WARPS 8      // warps per CTA when tiles allow
 #endif
 #ifndef QMM_GEMV_STAGES
 #define QMM_GEMV_STAGES 4         // ring depth per warp
@@ -63,6 +63,9 @@
 #endif
 #ifndef QMM_GEMV_R_SMALL
 #define QMM_GEMV_R_SMALL 1        // rows per lane for the small (two lanes per row) case
+#endif
+#ifndef QMM_GEMV_PROXY_FENCE
+#define QMM_GEMV_PROXY_FENCE 0    // 1: fence.proxy.async before refilling a stage (not needed)
 #endif
 #ifndef QMM_GEMV_X_BYTES
 #define QMM_GEMV_X_BYTES 65536    // activation slice per CTA (shared memory)
@@ -104,10 +107,23 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
 }
 
 // m = 2^23 + (v & mask) as a float: the nibble (byte) lands in the mantissa.
-__device__ __forceinline__ float mag(uint32_t v, uint32_t mask) {
+// `magic` is 2^23's bit pattern, passed in at run time: with the mask and the
+// magic both compile-time immediates the compiler emits two LOP3 per
+// extraction (a SASS LOP3 takes one immediate); with the magic in a register
+// it is one.
+#ifndef QMM_MAGIC_PARAM
+#define QMM_MAGIC_PARAM 1
+#endif
+__device__ __forceinline__ float mag(uint32_t v, uint32_t mask, uint32_t magic) {
+#if QMM_MAGIC_PARAM
+    return __uint_as_float((v & mask) | magic);
+#else
+    (void)magic;
     return __uint_as_float((v & mask) | kMagic);
+#endif
 }
-// Q8_0 byte with its sign bit flipped (q + 128) in the mantissa of 2^23.
+// Q8_0 byte with its sign bit flipped (q + 128) in the mantissa of 2^23;
+// magic_flip = 2^23's pattern with the byte's top bit set.
 __device__ __forceinline__ float mag8(uint32_t v, uint32_t mask, uint32_t magic_flip) {
     return __uint_as_float((mask & (v ^ magic_flip)) | (~mask & magic_flip));
 }
@@ -157,7 +173,7 @@ struct Chains {
 // and bits 20-31 after u = v >> 16, so the nibble sits at s in {0,4,8,12,16}.
 template <int M, int L, int R>
 __device__ __forceinline__ void q4_0_chunk(const uint8_t *src, int rstride, const float *xk,
-                                           int XS, float (&tot)[R][M]) {
+                                           int XS, uint32_t magic, float (&tot)[R][M]) {
     constexpr int CH = Chains<M * R>::value;
     constexpr int NB = 8 / L;
     uint32_t wd[R][36 / L];
@@ -206,10 +222,10 @@ __device__ __forceinline__ void q4_0_chunk(const uint8_t *src, int rstride, cons
 #pragma unroll
             for (int j = 0; j < R; ++j) {
                 const uint32_t v = q[j][i], u = v >> 16;
-                const float2 p01 = __ffma2_rn(f2(mag(v, 0x0000000Fu), mag(v, 0x00000F00u)), s01, b01);
-                const float2 p23 = __ffma2_rn(f2(mag(v, 0x000F0000u), mag(u, 0x00000F00u)), s23, b23);
-                const float2 p45 = __ffma2_rn(f2(mag(v, 0x000000F0u), mag(v, 0x0000F000u)), s45, b45);
-                const float2 p67 = __ffma2_rn(f2(mag(u, 0x000000F0u), mag(u, 0x0000F000u)), s45, b45);
+                const float2 p01 = __ffma2_rn(f2(mag(v, 0x0000000Fu, magic), mag(v, 0x00000F00u, magic)), s01, b01);
+                const float2 p23 = __ffma2_rn(f2(mag(v, 0x000F0000u, magic), mag(u, 0x00000F00u, magic)), s23, b23);
+                const float2 p45 = __ffma2_rn(f2(mag(v, 0x000000F0u, magic), mag(v, 0x0000F000u, magic)), s45, b45);
+                const float2 p67 = __ffma2_rn(f2(mag(u, 0x000000F0u, magic), mag(u, 0x0000F000u, magic)), s45, b45);
 #pragma unroll
                 for (int m = 0; m < M; ++m) {
                     acc[j][m][c] = __ffma2_rn(p01, f2(xa[m].x, xa[m].y), acc[j][m][c]);
@@ -236,7 +252,7 @@ __device__ __forceinline__ void q4_0_chunk(const uint8_t *src, int rstride, cons
 // 3 at bits 8-15 (s = 8).
 template <int M, int L, int R>
 __device__ __forceinline__ void q8_0_chunk(const uint8_t *src, int rstride, const float *xk,
-                                           int XS, float (&tot)[R][M]) {
+                                           int XS, uint32_t magic, float (&tot)[R][M]) {
     constexpr int CH = Chains<M * R>::value;
     constexpr int NB = 8 / L;
     uint32_t wd[R][68 / L];
@@ -244,6 +260,10 @@ __device__ __forceinline__ void q8_0_chunk(const uint8_t *src, int rstride, cons
     for (int j = 0; j < R; ++j) load_portion<L>(src + j * rstride, wd[j]);
     // (m - (2^23 + 128*2^s)) * 2^-s: exact q
     const float2 sc = f2(1.0f, 0.00390625f), bc = f2(-8388736.0f, -32896.0f);
+    // compile-time constants here: for the byte path the compiler's own
+    // immediate form measured faster than a register operand
+    (void)magic;
+    constexpr uint32_t mf0 = kMagic | 0x80u, mf1 = kMagic | 0x8000u;
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
         const int base = (34 * b) >> 2;
@@ -270,9 +290,9 @@ __device__ __forceinline__ void q8_0_chunk(const uint8_t *src, int rstride, cons
                                                 : wd[j][base + 1 + i];
                 const uint32_t u = v >> 16;
                 const float2 p01 = __ffma2_rn(
-                    f2(mag8(v, 0x000000FFu, kMagic | 0x80u), mag8(v, 0x0000FF00u, kMagic | 0x8000u)), sc, bc);
+                    f2(mag8(v, 0x000000FFu, mf0), mag8(v, 0x0000FF00u, mf1)), sc, bc);
                 const float2 p23 = __ffma2_rn(
-                    f2(mag8(u, 0x000000FFu, kMagic | 0x80u), mag8(u, 0x0000FF00u, kMagic | 0x8000u)), sc, bc);
+                    f2(mag8(u, 0x000000FFu, mf0), mag8(u, 0x0000FF00u, mf1)), sc, bc);
 #pragma unroll
                 for (int m = 0; m < M; ++m) {
                     acc[j][m][h] = __ffma2_rn(p01, f2(xa[m].x, xa[m].y), acc[j][m][h]);
@@ -300,7 +320,7 @@ __device__ __forceinline__ void q8_0_chunk(const uint8_t *src, int rstride, cons
 // the kernel.
 template <int M>
 __device__ __forceinline__ void q4_0_chunk_wide(const uint8_t *src, const float *xk, int XS,
-                                                float (&tot)[1][M]) {
+                                                uint32_t magic, float (&tot)[1][M]) {
     const float2 s01 = f2(1.0f, 0.00390625f), b01 = f2(-8388616.0f, -32776.0f);
     const float2 s23 = f2(1.52587890625e-05f, 0.00390625f), b23 = f2(-136.0f, -32776.0f);
     const float2 s45 = f2(0.0625f, 0.000244140625f), b45 = f2(-524296.0f, -2056.0f);
@@ -329,10 +349,10 @@ __device__ __forceinline__ void q4_0_chunk_wide(const uint8_t *src, const float 
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const uint32_t v = q[i], u = v >> 16;
-                const float2 p01 = __ffma2_rn(f2(mag(v, 0x0000000Fu), mag(v, 0x00000F00u)), s01, b01);
-                const float2 p23 = __ffma2_rn(f2(mag(v, 0x000F0000u), mag(u, 0x00000F00u)), s23, b23);
-                const float2 p45 = __ffma2_rn(f2(mag(v, 0x000000F0u), mag(v, 0x0000F000u)), s45, b45);
-                const float2 p67 = __ffma2_rn(f2(mag(u, 0x000000F0u), mag(u, 0x0000F000u)), s45, b45);
+                const float2 p01 = __ffma2_rn(f2(mag(v, 0x0000000Fu, magic), mag(v, 0x00000F00u, magic)), s01, b01);
+                const float2 p23 = __ffma2_rn(f2(mag(v, 0x000F0000u, magic), mag(u, 0x00000F00u, magic)), s23, b23);
+                const float2 p45 = __ffma2_rn(f2(mag(v, 0x000000F0u, magic), mag(v, 0x0000F000u, magic)), s45, b45);
+                const float2 p67 = __ffma2_rn(f2(mag(u, 0x000000F0u, magic), mag(u, 0x0000F000u, magic)), s45, b45);
 #pragma unroll
                 for (int m = 0; m < M; ++m) {
                     const float4 xa = lds128f(xk + m * XS + 32 * b + 4 * i);
@@ -351,8 +371,12 @@ __device__ __forceinline__ void q4_0_chunk_wide(const uint8_t *src, const float 
 
 template <int M>
 __device__ __forceinline__ void q8_0_chunk_wide(const uint8_t *src, const float *xk, int XS,
-                                                float (&tot)[1][M]) {
+                                                uint32_t magic, float (&tot)[1][M]) {
     const float2 sc = f2(1.0f, 0.00390625f), bc = f2(-8388736.0f, -32896.0f);
+    // compile-time constants here: for the byte path the compiler's own
+    // immediate form measured faster than a register operand
+    (void)magic;
+    constexpr uint32_t mf0 = kMagic | 0x80u, mf1 = kMagic | 0x8000u;
 #pragma unroll 1
     for (int bp = 0; bp < 4; ++bp) {
         uint32_t wd[17];
@@ -370,9 +394,9 @@ __device__ __forceinline__ void q8_0_chunk_wide(const uint8_t *src, const float 
                 const uint32_t v = hb == 0 ? __byte_perm(wd[i], wd[i + 1], 0x5432) : wd[9 + i];
                 const uint32_t u = v >> 16;
                 const float2 p01 = __ffma2_rn(
-                    f2(mag8(v, 0x000000FFu, kMagic | 0x80u), mag8(v, 0x0000FF00u, kMagic | 0x8000u)), sc, bc);
+                    f2(mag8(v, 0x000000FFu, mf0), mag8(v, 0x0000FF00u, mf1)), sc, bc);
                 const float2 p23 = __ffma2_rn(
-                    f2(mag8(u, 0x000000FFu, kMagic | 0x80u), mag8(u, 0x0000FF00u, kMagic | 0x8000u)), sc, bc);
+                    f2(mag8(u, 0x000000FFu, mf0), mag8(u, 0x0000FF00u, mf1)), sc, bc);
 #pragma unroll
                 for (int m = 0; m < M; ++m) {
                     const float4 xa = lds128f(xk + m * XS + 32 * b + 4 * i);
@@ -426,14 +450,18 @@ struct StreamParams {
     int kw;           // warps sharing one row tile (K split inside the CTA)
     int cpw;          // chunks per warp
     int stages;       // ring depth per warp
+    uint32_t magic;   // 0x4B000000 (2^23), kept in a register by the kernel
     LaunchCtx ctx;
 };
 
 // Grid: blockIdx.x = group * ksplit + rank (cluster of ksplit CTAs along x).
 // Warp w of a CTA owns row tile group*rw + w / kw and the (w % kw)-th part of
 // the CTA's K range; cluster rank r owns the r-th part of K.
+#ifndef QMM_GEMV_MAX_THREADS
+#define QMM_GEMV_MAX_THREADS 256
+#endif
 template <Fmt F, int M, int L, int R>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(QMM_GEMV_MAX_THREADS)
     gemv_stream_kernel(const __grid_constant__ StreamMaps maps, StreamParams p) {
     constexpr int CB = StreamFmt<F>::kChunkBytes;
     constexpr int kLaneRows = 32 / L;                 // rows covered by one pass of the lanes
@@ -535,17 +563,23 @@ __global__ void __launch_bounds__(256)
             const float *xk = xs + (w_c0 + i) * kChunkK + h * (kChunkK / L);
             if constexpr (M > QMM_GEMV_R2_MAX_M && L == 1 && R == 1) {
                 if constexpr (F == Fmt::Q4_0)
-                    q4_0_chunk_wide<M>(src, xk, XS, tot);
+                    q4_0_chunk_wide<M>(src, xk, XS, p.magic, tot);
                 else
-                    q8_0_chunk_wide<M>(src, xk, XS, tot);
+                    q8_0_chunk_wide<M>(src, xk, XS, p.magic, tot);
             } else if constexpr (F == Fmt::Q4_0) {
-                q4_0_chunk<M, L, R>(src, kLaneRows * CB, xk, XS, tot);
+                q4_0_chunk<M, L, R>(src, kLaneRows * CB, xk, XS, p.magic, tot);
             } else {
-                q8_0_chunk<M, L, R>(src, kLaneRows * CB, xk, XS, tot);
+                q8_0_chunk<M, L, R>(src, kLaneRows * CB, xk, XS, p.magic, tot);
             }
             __syncwarp();  // every lane is done reading the stage
             if (issued < cpw) {
+#if QMM_GEMV_PROXY_FENCE
                 fence_proxy_async_smem();
+#endif
+                // The stage was only read (its values are already in registers
+                // and used), so the TMA write that refills it needs no proxy
+                // fence: a write-after-read through the async proxy is ordered
+                // by the warp's own program order and __syncwarp.
                 issue(issued);
                 ++issued;
             }
@@ -743,6 +777,7 @@ cudaError_t launch_stream(const GemvProblem *probs, int count, const float *x, i
     p.kw = sh.kw;
     p.cpw = sh.cpw;
     p.stages = sh.stages;
+    p.magic = kMagic;
     p.ctx = ctx;
     const uint64_t rowbytes = static_cast<uint64_t>(k / kChunkK) * StreamFmt<F>::kChunkBytes;
     constexpr int EB = StreamFmt<F>::kElemBytes;
