@@ -75,7 +75,12 @@ namespace qmm {
 namespace {
 
 constexpr int kMaxGemvProblems = 4;
-constexpr size_t kGemvSmemCap = 200 * 1024;  // dynamic shared memory per CTA
+#ifndef QMM_GEMV_SMEM_CAP
+#define QMM_GEMV_SMEM_CAP (224 * 1024)  // below the 227 KB per-CTA limit
+#endif
+constexpr size_t kGemvSmemCap = QMM_GEMV_SMEM_CAP;  // dynamic shared memory per CTA
+// launch_stream's "no launch shape fits" answer (the caller falls back)
+constexpr cudaError_t kShapeTooLarge = cudaErrorInvalidConfiguration;
 
 constexpr int kChunkK = 256;
 constexpr uint32_t kMagic = 0x4B000000u;  // 2^23
@@ -767,7 +772,7 @@ cudaError_t launch_stream(const GemvProblem *probs, int count, const float *x, i
     int64_t tiles = 0;
     for (int i = 0; i < count; ++i) tiles += (probs[i].n + kRowsPerWarp - 1) / kRowsPerWarp;
     const StreamShape sh = stream_shape<F, M, L, R>(tiles, k, device_sm_count());
-    if (sh.smem > kGemvSmemCap) return cudaErrorInvalidConfiguration;
+    if (sh.smem > kGemvSmemCap) return kShapeTooLarge;  // nothing launched
     StreamMaps maps;
     StreamParams p;
     p.x = x;
@@ -824,12 +829,19 @@ cudaError_t launch_m(const GemvProblem *probs, int count, const float *x, int64_
         // Lanes per row: small problems at small M are latency bound, so more
         // lanes share each row chunk; large or wide-M problems keep one.
         // Rows per lane: at small M each activation load feeds two weight rows.
+        // A shape whose activation slice cannot fit shared memory even at the
+        // largest cluster split (very large K at large M) is refused before
+        // any launch and takes the byte-wise kernel below.
+        cudaError_t e;
         if constexpr (M <= QMM_GEMV_R2_MAX_M) {
-            if (units <= QMM_GEMV_L2_UNITS) return launch_stream<F, M, 2, QMM_GEMV_R_SMALL>(probs, count, x, k, stream, ctx);
-            return launch_stream<F, M, 1, 2>(probs, count, x, k, stream, ctx);
+            if (units <= QMM_GEMV_L2_UNITS)
+                e = launch_stream<F, M, 2, QMM_GEMV_R_SMALL>(probs, count, x, k, stream, ctx);
+            else
+                e = launch_stream<F, M, 1, 2>(probs, count, x, k, stream, ctx);
         } else {
-            return launch_stream<F, M, 1, 1>(probs, count, x, k, stream, ctx);
+            e = launch_stream<F, M, 1, 1>(probs, count, x, k, stream, ctx);
         }
+        if (e != kShapeTooLarge) return e;
     }
     for (int i = 0; i < count; ++i) {  // byte-wise kernel, one launch per problem
         const unsigned grid = static_cast<unsigned>((probs[i].n + 3) / 4);

@@ -272,3 +272,66 @@ def test_gemv_multi_rejects_overlap_and_count(qmm):
     with pytest.raises(qmm.QmmError) as e:
         qmm.qmm_gemv_q4_0_multi([(w, y, n)] * 5, x, 1, k)
     assert e.value.status == qmm.QMM_ERR_SHAPE
+
+
+# ---- M = 1, K % 2048 == 0: the row-balanced kernel (one CTA per SM, whole rows) ----
+
+@pytest.mark.parametrize("n,k", [(1, 2048), (100, 2048), (151, 2048), (152, 2048), (153, 2048),
+                                 (1000, 2048), (3001, 4096), (777, 8192), (300, 16384),
+                                 (20000, 2048), (22000, 2048)])
+def test_gemv_m1_row_balanced_shapes(qmm, oracle_mod, n, k):
+    # ragged and tiny N around the SM count, K in 1..8 segments of 2048, and
+    # N just inside / outside the shared-memory budget (the latter falls back
+    # to the streaming kernel)
+    case = synth.gemv_case("q4_0", 1, n, k, seed=n * 7 + k)
+    if n * k > 8_000_000:
+        rng = np.random.default_rng(n)
+        ni = rng.integers(0, n, 4000)
+        mi = np.zeros_like(ni)
+        y_ref, bound = oracle_mod.gemv_q4_0_at(case.w, case.x, 1, n, k, mi, ni)
+        assert_within(_run_gemv(qmm, "q4_0", case)[mi, ni], y_ref, bound, GEMV_REL, f"1x{n}x{k}")
+    else:
+        y_ref, bound = _oracle_gemv(oracle_mod, "q4_0", case)
+        assert_within(_run_gemv(qmm, "q4_0", case), y_ref, bound, GEMV_REL, f"1x{n}x{k}")
+
+
+@pytest.mark.parametrize("k,ns", [(2048, [5, 300, 1500, 7]), (8192, [100, 60]), (4096, [1, 151, 2])])
+def test_gemv_m1_multi_rows_straddle_ctas(qmm, oracle_mod, k, ns):
+    """Grouped problems whose boundaries fall inside a CTA's row range."""
+    x = synth.activations_f32(1, k, seed=80)
+    ws = [synth.q4_0_weights(n, k, seed=81, stream=i) for i, n in enumerate(ns)]
+    ys = [torch.full((1, n), float("nan"), dtype=torch.float32, device="cuda") for n in ns]
+    qmm.qmm_gemv_q4_0_multi([(to_dev(w, torch), y, n) for w, y, n in zip(ws, ys, ns)],
+                            to_dev(x, torch), 1, k)
+    torch.cuda.synchronize()
+    for w, y, n in zip(ws, ys, ns):
+        y_ref, bound = oracle_mod.gemv_q4_0(w, x, 1, n, k)
+        assert_within(y.cpu().numpy(), y_ref, bound, GEMV_REL, f"multi k={k} n={n}")
+
+
+def test_gemv_m1_one_hot_and_determinism(qmm):
+    """x = e_c gives the dequantized column exactly; repeated calls are bitwise equal."""
+    n, k = 1000, 4096
+    case = synth.gemv_case("q4_0", 1, n, k, seed=9)
+    w = to_dev(case.w, torch)
+    deq = qmm.dequant("q4_0", w, n, k)
+    for c in (0, 63, 64, 2047, 2048, 4095):
+        x = torch.zeros((1, k), device="cuda")
+        x[0, c] = 1.0
+        y = qmm.gemv("q4_0", w, x, n, k)
+        assert torch.equal(y[0], deq[:, c]), c
+    x = to_dev(case.x, torch)
+    a = qmm.gemv("q4_0", w, x, n, k)
+    b = qmm.gemv("q4_0", w, x, n, k)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+@pytest.mark.parametrize("fmt,m,n,k", [("q4_0", 16, 40, 65536), ("q8_0", 8, 33, 32768),
+                                       ("q4_0", 10, 70, 32768)])
+def test_gemv_very_large_k_falls_back_correctly(qmm, oracle_mod, fmt, m, n, k):
+    """Activation slices too large for shared memory at any cluster split take
+    the byte-wise kernel: still correct, never an error status."""
+    case = synth.gemv_case(fmt, m, n, k, seed=m + n)
+    y_ref, bound = _oracle_gemv(oracle_mod, fmt, case)
+    assert_within(_run_gemv(qmm, fmt, case), y_ref, bound, GEMV_REL, f"{fmt} {m}x{n}x{k}")
