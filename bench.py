@@ -407,13 +407,20 @@ def run_secondary(torch, qmm, l2, stream, timer, peaks):
         layer.run_steps(layer.R)
         el = timer.run(lambda: layer.run_steps(steps))
         gbs = layer.step_bytes * steps / el / 1e9
+        resident = layer.R * layer.step_bytes
         out[name] = {"gbs": round(gbs, 1), "frac_hbm": round(gbs / hbm, 4),
                      "us_per_call": round(el / steps / len(projs) * 1e6, 3),
-                     "replicas": layer.R}
+                     "replicas": layer.R,
+                     "l2": ("weights rotate through %d replicas (%.0f MB, %s L2)"
+                            % (layer.R, resident / 1e6, "larger than" if resident > l2 else
+                               "smaller than: L2-resident, not an HBM figure"))}
         del layer
         torch.cuda.empty_cache()
 
     gemv_entry("q4_0_gemv_256x1024_m1", "q4_0", 1, (synth.SINGLE_SMALL,), 90)
+    # the decode step's projections one at a time (separate dependent calls)
+    for i, p in enumerate(synth.DECODE_LAYER):
+        gemv_entry(f"q4_0_decode_{p.name}_{p.n}x{p.k}_m1", "q4_0", 1, (p,), 10 + i)
     for m in synth.BATCHED_M:
         for i, p in enumerate(synth.BATCHED_SHAPES):
             gemv_entry(f"q4_0_gemv_{p.n}x{p.k}_m{m}", "q4_0", m, (p,), 30 + i)
@@ -448,10 +455,29 @@ def measure_gemm(torch, qmm, l2, stream, timer, peaks):
             gf.replay()
             times.append(timer.run(g.replay))
         t = statistics.median(times)
-        tfl = 2.0 * m * p.n * p.k / t / 1e12
+        q = statistics.quantiles(times, n=10)
+        flops = 2.0 * m * p.n * p.k
+        tfl = flops / t / 1e12
         res[f"q4_0_gemm_{m}x{p.n}x{p.k}"] = {
             "tflops": round(tfl, 1), "frac_bf16_peak": round(tfl / peaks["bf16_tflops"], 4),
-            "us": round(t * 1e6, 2), "l2": "flushed (2x L2 write) before each timed launch"}
+            "us": round(t * 1e6, 2), "us_p10": round(q[0] * 1e6, 2), "us_p90": round(q[-1] * 1e6, 2),
+            "l2": "flushed (2x L2 write) before each timed launch"}
+        # practical ceiling of the same contraction: cuBLAS bf16 with the
+        # weights already dense bf16 (no dequantization), same flush and timing
+        Wd = torch.randn((p.n, p.k), device=dev).to(torch.bfloat16)
+        Xd = torch.randn((m, p.k), device=dev).to(torch.bfloat16)
+        gc = capture(torch, stream, lambda: torch.matmul(Xd, Wd.t()))
+        tc = []
+        for _ in range(20):
+            gf.replay()
+            tc.append(timer.run(gc.replay))
+        tcm = statistics.median(tc)
+        res[f"cublas_bf16_dense_{m}x{p.n}x{p.k}"] = {
+            "tflops": round(flops / tcm / 1e12, 1),
+            "frac_bf16_peak": round(flops / tcm / 1e12 / peaks["bf16_tflops"], 4),
+            "us": round(tcm * 1e6, 2),
+            "what": "torch.matmul bf16 x bf16 -> bf16 of dense weights: a practical ceiling, not this library"}
+        del Wd, Xd, gc
     return res
 
 
@@ -473,10 +499,25 @@ def cpu_baseline(seconds: float):
         el = time.perf_counter() - t0
         if el >= seconds:
             break
-    return {"value": round(step_bytes * passes / el / 1e9, 4), "unit": "GB/s", "cores": cores,
+    value = step_bytes * passes / el / 1e9
+    # the same oracle on one thread, a shorter sample
+    oracle.set_threads(1)
+    passes1 = 0
+    t0 = time.perf_counter()
+    while True:
+        for c in cases:
+            oracle.gemv_q4_0(c.w, c.x, c.m, c.n, c.k)
+        passes1 += 1
+        el1 = time.perf_counter() - t0
+        if el1 >= seconds / 4:
+            break
+    oracle.set_threads(cores)
+    return {"value": round(value, 4), "unit": "GB/s", "cores": cores,
             "kind": "oracle",
             "sample": f"{passes} full passes of the decode-layer set (M=1, 7 Q4_0 projections) "
-                      f"in {el:.1f} s, binary64 C oracle, {cores} OpenMP threads"}
+                      f"in {el:.1f} s, binary64 C oracle, {cores} OpenMP threads",
+            "single_thread": {"value": round(step_bytes * passes1 / el1 / 1e9, 4), "unit": "GB/s",
+                              "sample": f"{passes1} passes in {el1:.1f} s on 1 thread"}}
 
 
 # ----------------------------------------------------------------- arms
