@@ -411,9 +411,9 @@ def run_secondary(torch, qmm, l2, stream, timer, peaks):
         out[name] = {"gbs": round(gbs, 1), "frac_hbm": round(gbs / hbm, 4),
                      "us_per_call": round(el / steps / len(projs) * 1e6, 3),
                      "replicas": layer.R,
-                     "l2": ("weights rotate through %d replicas (%.0f MB, %s L2)"
-                            % (layer.R, resident / 1e6, "larger than" if resident > l2 else
-                               "smaller than: L2-resident, not an HBM figure"))}
+                     "l2": ("weights rotate through %d replicas (%.0f MB, %s)"
+                            % (layer.R, resident / 1e6, "larger than L2" if resident > l2 else
+                               "smaller than L2: L2-resident, not an HBM figure"))}
         del layer
         torch.cuda.empty_cache()
 

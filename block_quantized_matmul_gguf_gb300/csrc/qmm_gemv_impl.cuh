@@ -61,6 +61,9 @@
 #ifndef QMM_GEMV_R2_MAX_M
 #define QMM_GEMV_R2_MAX_M 4       // largest M at which a lane owns two weight rows
 #endif
+#ifndef QMM_GEMV_R_WIDE_MAX_M
+#define QMM_GEMV_R_WIDE_MAX_M 10  // above R2_MAX_M, two rows per lane up to this M, then one
+#endif
 #ifndef QMM_GEMV_R_SMALL
 #define QMM_GEMV_R_SMALL 1        // rows per lane for the small (two lanes per row) case
 #endif
@@ -323,60 +326,80 @@ __device__ __forceinline__ void q8_0_chunk(const uint8_t *src, int rstride, cons
 // memory as words.  The arithmetic is that of q4_0_chunk / q8_0_chunk; the
 // loop keeps the code (and build time) small where FMAs, not loads, bound
 // the kernel.
-template <int M>
-__device__ __forceinline__ void q4_0_chunk_wide(const uint8_t *src, const float *xk, int XS,
-                                                uint32_t magic, float (&tot)[1][M]) {
+template <int M, int R>
+__device__ __forceinline__ void q4_0_chunk_wide(const uint8_t *src, int rstride, const float *xk,
+                                                int XS, uint32_t magic, float (&tot)[R][M]) {
     const float2 s01 = f2(1.0f, 0.00390625f), b01 = f2(-8388616.0f, -32776.0f);
     const float2 s23 = f2(1.52587890625e-05f, 0.00390625f), b23 = f2(-136.0f, -32776.0f);
     const float2 s45 = f2(0.0625f, 0.000244140625f), b45 = f2(-524296.0f, -2056.0f);
 #pragma unroll 1
     for (int bp = 0; bp < 4; ++bp) {
-        uint32_t wd[9];
+        uint32_t wd[R][9];
 #pragma unroll
-        for (int t = 0; t < 9; ++t) wd[t] = *reinterpret_cast<const uint32_t *>(src + 36 * bp + 4 * t);
+        for (int j = 0; j < R; ++j)
+#pragma unroll
+            for (int t = 0; t < 9; ++t)
+                wd[j][t] = *reinterpret_cast<const uint32_t *>(src + j * rstride + 36 * bp + 4 * t);
 #pragma unroll
         for (int hb = 0; hb < 2; ++hb) {
             const int b = 2 * bp + hb;
-            uint32_t q[4], dbits;
-            if (hb == 0) {
-                dbits = wd[0] & 0xFFFFu;
+            uint32_t q[R][4];
+            float d[R];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) q[i] = __byte_perm(wd[i], wd[i + 1], 0x5432);
-            } else {
-                dbits = wd[4] >> 16;
+            for (int j = 0; j < R; ++j) {
+                uint32_t dbits;
+                if (hb == 0) {
+                    dbits = wd[j][0] & 0xFFFFu;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) q[i] = wd[5 + i];
+                    for (int i = 0; i < 4; ++i) q[j][i] = __byte_perm(wd[j][i], wd[j][i + 1], 0x5432);
+                } else {
+                    dbits = wd[j][4] >> 16;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) q[j][i] = wd[j][5 + i];
+                }
+                d[j] = half_bits_to_float(dbits);
             }
-            const float d = half_bits_to_float(dbits);
-            float2 acc[M];
+            float2 acc[R][M];
 #pragma unroll
-            for (int m = 0; m < M; ++m) acc[m] = f2(0.0f, 0.0f);
+            for (int j = 0; j < R; ++j)
+#pragma unroll
+                for (int m = 0; m < M; ++m) acc[j][m] = f2(0.0f, 0.0f);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const uint32_t v = q[i], u = v >> 16;
-                const float2 p01 = __ffma2_rn(f2(mag(v, 0x0000000Fu, magic), mag(v, 0x00000F00u, magic)), s01, b01);
-                const float2 p23 = __ffma2_rn(f2(mag(v, 0x000F0000u, magic), mag(u, 0x00000F00u, magic)), s23, b23);
-                const float2 p45 = __ffma2_rn(f2(mag(v, 0x000000F0u, magic), mag(v, 0x0000F000u, magic)), s45, b45);
-                const float2 p67 = __ffma2_rn(f2(mag(u, 0x000000F0u, magic), mag(u, 0x0000F000u, magic)), s45, b45);
+                float2 p01[R], p23[R], p45[R], p67[R];
+#pragma unroll
+                for (int j = 0; j < R; ++j) {
+                    const uint32_t v = q[j][i], u = v >> 16;
+                    p01[j] = __ffma2_rn(f2(mag(v, 0x0000000Fu, magic), mag(v, 0x00000F00u, magic)), s01, b01);
+                    p23[j] = __ffma2_rn(f2(mag(v, 0x000F0000u, magic), mag(u, 0x00000F00u, magic)), s23, b23);
+                    p45[j] = __ffma2_rn(f2(mag(v, 0x000000F0u, magic), mag(v, 0x0000F000u, magic)), s45, b45);
+                    p67[j] = __ffma2_rn(f2(mag(u, 0x000000F0u, magic), mag(u, 0x0000F000u, magic)), s45, b45);
+                }
 #pragma unroll
                 for (int m = 0; m < M; ++m) {
+                    // each activation load feeds all R rows
                     const float4 xa = lds128f(xk + m * XS + 32 * b + 4 * i);
                     const float4 xb = lds128f(xk + m * XS + 32 * b + 16 + 4 * i);
-                    acc[m] = __ffma2_rn(p01, f2(xa.x, xa.y), acc[m]);
-                    acc[m] = __ffma2_rn(p23, f2(xa.z, xa.w), acc[m]);
-                    acc[m] = __ffma2_rn(p45, f2(xb.x, xb.y), acc[m]);
-                    acc[m] = __ffma2_rn(p67, f2(xb.z, xb.w), acc[m]);
+#pragma unroll
+                    for (int j = 0; j < R; ++j) {
+                        acc[j][m] = __ffma2_rn(p01[j], f2(xa.x, xa.y), acc[j][m]);
+                        acc[j][m] = __ffma2_rn(p23[j], f2(xa.z, xa.w), acc[j][m]);
+                        acc[j][m] = __ffma2_rn(p45[j], f2(xb.x, xb.y), acc[j][m]);
+                        acc[j][m] = __ffma2_rn(p67[j], f2(xb.z, xb.w), acc[j][m]);
+                    }
                 }
             }
 #pragma unroll
-            for (int m = 0; m < M; ++m) tot[0][m] = fmaf(d, acc[m].x + acc[m].y, tot[0][m]);
+            for (int j = 0; j < R; ++j)
+#pragma unroll
+                for (int m = 0; m < M; ++m) tot[j][m] = fmaf(d[j], acc[j][m].x + acc[j][m].y, tot[j][m]);
         }
     }
 }
 
-template <int M>
-__device__ __forceinline__ void q8_0_chunk_wide(const uint8_t *src, const float *xk, int XS,
-                                                uint32_t magic, float (&tot)[1][M]) {
+template <int M, int R>
+__device__ __forceinline__ void q8_0_chunk_wide(const uint8_t *src, int rstride, const float *xk,
+                                                int XS, uint32_t magic, float (&tot)[R][M]) {
     const float2 sc = f2(1.0f, 0.00390625f), bc = f2(-8388736.0f, -32896.0f);
     // compile-time constants here: for the byte path the compiler's own
     // immediate form measured faster than a register operand
@@ -384,33 +407,48 @@ __device__ __forceinline__ void q8_0_chunk_wide(const uint8_t *src, const float 
     constexpr uint32_t mf0 = kMagic | 0x80u, mf1 = kMagic | 0x8000u;
 #pragma unroll 1
     for (int bp = 0; bp < 4; ++bp) {
-        uint32_t wd[17];
+        uint32_t wd[R][17];
 #pragma unroll
-        for (int t = 0; t < 17; ++t) wd[t] = *reinterpret_cast<const uint32_t *>(src + 68 * bp + 4 * t);
+        for (int j = 0; j < R; ++j)
+#pragma unroll
+            for (int t = 0; t < 17; ++t)
+                wd[j][t] = *reinterpret_cast<const uint32_t *>(src + j * rstride + 68 * bp + 4 * t);
 #pragma unroll
         for (int hb = 0; hb < 2; ++hb) {
             const int b = 2 * bp + hb;
-            const float d = half_bits_to_float(hb == 0 ? (wd[0] & 0xFFFFu) : (wd[8] >> 16));
-            float2 acc[M];
+            float d[R];
 #pragma unroll
-            for (int m = 0; m < M; ++m) acc[m] = f2(0.0f, 0.0f);
+            for (int j = 0; j < R; ++j)
+                d[j] = half_bits_to_float(hb == 0 ? (wd[j][0] & 0xFFFFu) : (wd[j][8] >> 16));
+            float2 acc[R][M];
+#pragma unroll
+            for (int j = 0; j < R; ++j)
+#pragma unroll
+                for (int m = 0; m < M; ++m) acc[j][m] = f2(0.0f, 0.0f);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                const uint32_t v = hb == 0 ? __byte_perm(wd[i], wd[i + 1], 0x5432) : wd[9 + i];
-                const uint32_t u = v >> 16;
-                const float2 p01 = __ffma2_rn(
-                    f2(mag8(v, 0x000000FFu, mf0), mag8(v, 0x0000FF00u, mf1)), sc, bc);
-                const float2 p23 = __ffma2_rn(
-                    f2(mag8(u, 0x000000FFu, mf0), mag8(u, 0x0000FF00u, mf1)), sc, bc);
+                float2 p01[R], p23[R];
+#pragma unroll
+                for (int j = 0; j < R; ++j) {
+                    const uint32_t v = hb == 0 ? __byte_perm(wd[j][i], wd[j][i + 1], 0x5432) : wd[j][9 + i];
+                    const uint32_t u = v >> 16;
+                    p01[j] = __ffma2_rn(f2(mag8(v, 0x000000FFu, mf0), mag8(v, 0x0000FF00u, mf1)), sc, bc);
+                    p23[j] = __ffma2_rn(f2(mag8(u, 0x000000FFu, mf0), mag8(u, 0x0000FF00u, mf1)), sc, bc);
+                }
 #pragma unroll
                 for (int m = 0; m < M; ++m) {
                     const float4 xa = lds128f(xk + m * XS + 32 * b + 4 * i);
-                    acc[m] = __ffma2_rn(p01, f2(xa.x, xa.y), acc[m]);
-                    acc[m] = __ffma2_rn(p23, f2(xa.z, xa.w), acc[m]);
+#pragma unroll
+                    for (int j = 0; j < R; ++j) {
+                        acc[j][m] = __ffma2_rn(p01[j], f2(xa.x, xa.y), acc[j][m]);
+                        acc[j][m] = __ffma2_rn(p23[j], f2(xa.z, xa.w), acc[j][m]);
+                    }
                 }
             }
 #pragma unroll
-            for (int m = 0; m < M; ++m) tot[0][m] = fmaf(d, acc[m].x + acc[m].y, tot[0][m]);
+            for (int j = 0; j < R; ++j)
+#pragma unroll
+                for (int m = 0; m < M; ++m) tot[j][m] = fmaf(d[j], acc[j][m].x + acc[j][m].y, tot[j][m]);
         }
     }
 }
@@ -566,11 +604,11 @@ __global__ void __launch_bounds__(QMM_GEMV_MAX_THREADS)
             ++consumed;
             const uint8_t *src = my_ring + (st * kRowsPerWarp + r) * CB + h * (CB / L);
             const float *xk = xs + (w_c0 + i) * kChunkK + h * (kChunkK / L);
-            if constexpr (M > QMM_GEMV_R2_MAX_M && L == 1 && R == 1) {
+            if constexpr (M > QMM_GEMV_R2_MAX_M && L == 1) {
                 if constexpr (F == Fmt::Q4_0)
-                    q4_0_chunk_wide<M>(src, xk, XS, p.magic, tot);
+                    q4_0_chunk_wide<M, R>(src, kLaneRows * CB, xk, XS, p.magic, tot);
                 else
-                    q8_0_chunk_wide<M>(src, xk, XS, p.magic, tot);
+                    q8_0_chunk_wide<M, R>(src, kLaneRows * CB, xk, XS, p.magic, tot);
             } else if constexpr (F == Fmt::Q4_0) {
                 q4_0_chunk<M, L, R>(src, kLaneRows * CB, xk, XS, p.magic, tot);
             } else {
@@ -755,10 +793,22 @@ StreamShape stream_shape(int64_t tiles, int64_t k, int sms) {
                                 static_cast<size_t>(t.ksplit) * t.rw * M * kRowsPerWarp) +
                sizeof(uint64_t) * (nw * t.stages + 1) + 128;
     };
-    // fit the shared-memory budget: shallower rings, then fewer tiles per CTA
+    // fit the shared-memory budget: shallower rings, then fewer tiles per CTA,
+    // then a wider cluster split (halves the activation slice), then K parts
+    // moved from the CTA's warps to the cluster (halves the ring as well)
     while (smem_of(sh) > kGemvSmemCap && sh.stages > 2) --sh.stages;
     while (smem_of(sh) > kGemvSmemCap && sh.rw > 1) sh.rw /= 2;
     while (smem_of(sh) > kGemvSmemCap && sh.stages > 1) --sh.stages;
+    while (smem_of(sh) > kGemvSmemCap && sh.ksplit < QMM_GEMV_MAX_KSPLIT &&
+           C % (2 * sh.kw * sh.ksplit) == 0) {
+        sh.ksplit *= 2;
+        sh.cpw = C / (sh.kw * sh.ksplit);
+        sh.stages = std::min(sh.stages, sh.cpw);
+    }
+    while (smem_of(sh) > kGemvSmemCap && sh.kw > 1 && sh.ksplit < QMM_GEMV_MAX_KSPLIT) {
+        sh.kw /= 2;
+        sh.ksplit *= 2;
+    }
     sh.smem = smem_of(sh);
     return sh;
 }
@@ -839,7 +889,15 @@ cudaError_t launch_m(const GemvProblem *probs, int count, const float *x, int64_
             else
                 e = launch_stream<F, M, 1, 2>(probs, count, x, k, stream, ctx);
         } else {
-            e = launch_stream<F, M, 1, 1>(probs, count, x, k, stream, ctx);
+            // the activation loads bound wide M; two rows per lane halve them per
+            // FMA until the accumulators crowd the registers (M > 10); where
+            // their shared memory does not fit, one row per lane
+            if constexpr (M <= QMM_GEMV_R_WIDE_MAX_M) {
+                e = launch_stream<F, M, 1, 2>(probs, count, x, k, stream, ctx);
+                if (e == kShapeTooLarge) e = launch_stream<F, M, 1, 1>(probs, count, x, k, stream, ctx);
+            } else {
+                e = launch_stream<F, M, 1, 1>(probs, count, x, k, stream, ctx);
+            }
         }
         if (e != kShapeTooLarge) return e;
     }

@@ -335,3 +335,13 @@ def test_gemv_very_large_k_falls_back_correctly(qmm, oracle_mod, fmt, m, n, k):
     case = synth.gemv_case(fmt, m, n, k, seed=m + n)
     y_ref, bound = _oracle_gemv(oracle_mod, fmt, case)
     assert_within(_run_gemv(qmm, fmt, case), y_ref, bound, GEMV_REL, f"{fmt} {m}x{n}x{k}")
+
+
+@pytest.mark.parametrize("fmt,m,n,k", [("q8_0", 8, 300, 8192), ("q8_0", 9, 70, 16384),
+                                       ("q4_0", 6, 1000, 2048), ("q4_0", 10, 257, 4096)])
+def test_gemv_wide_m_two_rows_per_lane_and_its_fallback(qmm, oracle_mod, fmt, m, n, k):
+    """M = 5..10 uses two weight rows per lane; shapes whose shared memory does
+    not fit that form fall back to one row per lane (Q8_0 at K = 16384)."""
+    case = synth.gemv_case(fmt, m, n, k, seed=m * 13 + n)
+    y_ref, bound = _oracle_gemv(oracle_mod, fmt, case)
+    assert_within(_run_gemv(qmm, fmt, case), y_ref, bound, GEMV_REL, f"{fmt} {m}x{n}x{k}")
