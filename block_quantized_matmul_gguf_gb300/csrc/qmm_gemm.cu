@@ -12,7 +12,7 @@
 // memory.
 //
 // Structure: persistent CTA pairs (thread-block clusters of 2), one CTA per
-// SM, 448 threads each, warp-specialised.  A pair computes a tile of
+// SM, 576 threads each, warp-specialised.  A pair computes a tile of
 // 256 weight rows x 256 tokens as Y^T = W . X^T with
 // tcgen05.mma.cta_group::2 (M=256 weight rows, N=256 tokens, K=16): the A
 // operand (dequantised W, bf16) is in tensor memory, written there by the
@@ -34,15 +34,19 @@
 //   warp 1      MMA issuer (leader CTA): one thread issues the pair's MMAs
 //               into the 256-column accumulator and releases X stages, A
 //               slots and the accumulator with multicast tcgen05.commit.
+//               X stages and A slots are announced to it per group of four
+//               K stages (one wait per 16 MMAs): under the dequantisers'
+//               integer load a per-stage wait delayed the issue stream.
 //               Every dequantiser warp of both CTAs reports a written A slot
 //               on the leader's barrier with a CTA-scope (not cluster-scope)
 //               release arrive: the TMEM data is complete once tcgen05.wait::st
 //               returns, and a cluster-scope release costs about 1k cycles per
 //               arrive on this part, which serialised the pipeline when one
 //               peer thread forwarded every stage.
-//   warps 10-13 epilogue (both CTAs): tcgen05.ld of the CTA's 128 x 256 fp32
-//               accumulator; lane i holds weight row i, so each store of a
-//               warp writes 32 consecutive outputs of one token (coalesced).
+//   warps 10-17 epilogue (both CTAs): tcgen05.ld of the CTA's 128 x 256 fp32
+//               accumulator, two warps per lane quarter (half the columns
+//               each); lane i holds weight row i, so each store of a warp
+//               writes 32 consecutive outputs of one token (coalesced).
 // Every wait is bounded (GPU global timer).  On a timeout the CTA records the
 // error, sets a shared abort flag that makes its other waits give up at once,
 // lets its own TMA copies and MMAs finish (bounded waits), keeps its shared

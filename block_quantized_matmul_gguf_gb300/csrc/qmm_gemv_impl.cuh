@@ -8,8 +8,10 @@
 // is about HBM and issue slots, not tensor cores.
 //
 // Streaming kernel (K % 256 == 0, 16-byte aligned w and x):
-//  * Lane r of a warp owns row r of a 32-row tile.  K is cut into chunks of
-//    256 weights (8 blocks: 144 bytes of Q4_0, 272 of Q8_0), which keeps
+//  * Lane r of a warp owns row r of a 32-row tile; for small problems two
+//    lanes share a row (half a chunk each), and at M <= 10 a lane owns two
+//    rows, so that each activation load feeds both.  K is cut into chunks
+//    of 256 weights (8 blocks: 144 bytes of Q4_0, 272 of Q8_0), which keeps
 //    every row chunk 16-byte aligned.  A tile's K range is split over kw
 //    warps of a CTA (partial sums added through shared memory) and, for
 //    small N, over a thread-block cluster of ksplit CTAs (partials pushed
@@ -32,7 +34,9 @@
 //    as packed f32x2 instructions, four independent chains at small M.
 //  * Per block: acc = sum_j (nibble_j - 8) * x_j in fp32, then y += d * acc.
 //
-// Byte-wise kernel: any K % 32 == 0 and any alignment; a warp per row.
+// Byte-wise kernel: any K % 32 == 0 and any alignment, and the shapes whose
+// activation slice does not fit shared memory at any cluster split; a warp
+// per row.
 #pragma once
 
 #include "qmm_internal.h"
