@@ -89,6 +89,10 @@ constexpr size_t kGemvSmemCap = QMM_GEMV_SMEM_CAP;  // dynamic shared memory per
 // launch_stream's "no launch shape fits" answer (the caller falls back)
 constexpr cudaError_t kShapeTooLarge = cudaErrorInvalidConfiguration;
 
+static_assert((QMM_GEMV_MAX_KW & (QMM_GEMV_MAX_KW - 1)) == 0 &&
+                  (QMM_GEMV_MAX_KSPLIT & (QMM_GEMV_MAX_KSPLIT - 1)) == 0,
+              "K parts per CTA and per cluster are powers of two (the kernel shifts by them)");
+
 constexpr int kChunkK = 256;
 constexpr uint32_t kMagic = 0x4B000000u;  // 2^23
 
@@ -523,15 +527,25 @@ __global__ void __launch_bounds__(QMM_GEMV_MAX_THREADS)
     const int kw = p.kw, cpw = p.cpw;
     const uint32_t rank = cluster_ctarank();
     const uint32_t ksplit = cluster_nctarank();
-    const int gg = static_cast<int>(blockIdx.x / ksplit);  // CTA group over all problems
-    int prob = 0;
-    while (prob + 1 < p.count && gg >= p.group_begin[prob + 1]) ++prob;
-    const int group = gg - p.group_begin[prob];
-    const int n_rows = p.n[prob];
-    float *const y = p.y[prob];
+    // kw and ksplit are powers of two: shifts instead of run-time divisions
+    const int gg = static_cast<int>(blockIdx.x >> (__ffs(static_cast<int>(ksplit)) - 1));  // CTA group
+    // this CTA's problem, picked with unrolled selects (indexing the
+    // parameter arrays with a run-time index would copy them to local memory)
+    int prob = 0, gbegin = p.group_begin[0], n_rows = p.n[0];
+    float *y = p.y[0];
+#pragma unroll
+    for (int i = 1; i < kMaxGemvProblems; ++i) {
+        if (i < p.count && gg >= p.group_begin[i]) {
+            prob = i;
+            gbegin = p.group_begin[i];
+            n_rows = p.n[i];
+            y = p.y[i];
+        }
+    }
+    const int group = gg - gbegin;
     const CUtensorMap *wmap = &maps.m[prob];
-    const int tile_in_cta = warp / kw;
-    const int kpart = warp % kw;
+    const int tile_in_cta = warp >> (__ffs(kw) - 1);
+    const int kpart = warp & (kw - 1);
     const int row0 = (group * p.rw + tile_in_cta) * kRowsPerWarp;
     const int r = lane / L;  // rows r, r + 32/L, ... of the warp's tile
     const int h = lane % L;  // this lane's share of each chunk
@@ -561,9 +575,8 @@ __global__ void __launch_bounds__(QMM_GEMV_MAX_THREADS)
     }
     __syncthreads();  // barriers initialised before any thread waits on them
 
-    auto issue = [&](int i) {  // chunk i of this warp into stage i % S
+    auto issue = [&](int st, int i) {  // chunk i of this warp into stage st (= i % S)
         if (lane == 0) {
-            const int st = i % S;
             // full box bytes: rows past N are zero-filled and still counted
             mbar_arrive_expect_tx(&my_bars[st], kRowsPerWarp * CB);
             tma_load_2d(my_ring + st * kRowsPerWarp * CB, wmap,
@@ -576,7 +589,7 @@ __global__ void __launch_bounds__(QMM_GEMV_MAX_THREADS)
     // and outputs written only after the wait below.
     int issued = 0;
     if (warp_active)
-        for (; issued < min(S, cpw); ++issued) issue(issued);
+        for (; issued < min(S, cpw); ++issued) issue(issued, issued);
     pdl_wait();
     if (threadIdx.x == 0) {  // activations: one bulk copy per row m of the CTA's K range
         mbar_arrive_expect_tx(xbar, static_cast<uint32_t>(M * XS * sizeof(float)));
@@ -598,9 +611,9 @@ __global__ void __launch_bounds__(QMM_GEMV_MAX_THREADS)
     const bool x_ok = mbar_wait(xbar, 0, p.ctx);
     bool failed = !x_ok;
     if (warp_active) {
+        int st = 0;         // i % S, kept incrementally (S is a run-time value)
+        uint32_t par = 0;   // (i / S) & 1
         for (int i = 0; i < cpw && !failed; ++i) {
-            const int st = i % S;
-            const uint32_t par = static_cast<uint32_t>(i / S) & 1u;
             if (!mbar_wait(&my_bars[st], par, p.ctx)) {
                 failed = true;
                 break;
@@ -627,8 +640,12 @@ __global__ void __launch_bounds__(QMM_GEMV_MAX_THREADS)
                 // and used), so the TMA write that refills it needs no proxy
                 // fence: a write-after-read through the async proxy is ordered
                 // by the warp's own program order and __syncwarp.
-                issue(issued);
+                issue(st, issued);  // issued == i + S: the stage just read
                 ++issued;
+            }
+            if (++st == S) {
+                st = 0;
+                par ^= 1u;
             }
         }
     }
