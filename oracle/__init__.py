@@ -66,6 +66,8 @@ def _load():
                  "qmm_oracle_gemm_q4_0_at"):
         getattr(lib, name).argtypes = [P, P, I64, P, P, I64, P, P]
         getattr(lib, name).restype = None
+    lib.qmm_oracle_geglu_q4_0.argtypes = [P, P, P, I64, I64, I64, P, P, P, P, P]
+    lib.qmm_oracle_geglu_q4_0.restype = None
     lib.qmm_oracle_set_threads.argtypes = [ctypes.c_int]
     lib.qmm_oracle_set_threads.restype = None
     lib.qmm_oracle_get_threads.argtypes = []
@@ -179,3 +181,16 @@ def gemv_q8_0_at(w, x, m, n, k, mi, ni):
 def gemm_q4_0_at(w, x_bf16_bits, m, n, k, mi, ni):
     return _product_at("qmm_oracle_gemm_q4_0_at", w, x_bf16_bits, m, n, k, mi, ni,
                        Q4_0_BYTES, np.uint16)
+
+
+def geglu_q4_0(wg, wu, x, m, n, k):
+    """(h, g, u, bound_g, bound_u), each binary64 [m][n]:
+    g = x . Wg^T, u = x . Wu^T (Q4_0), h = gelu_tanh(g) * u."""
+    wg = _blocks(wg, n, k, Q4_0_BYTES)
+    wu = _blocks(wu, n, k, Q4_0_BYTES)
+    x = np.ascontiguousarray(x, dtype=np.float32).reshape(-1)
+    if x.size != m * k:
+        raise ValueError(f"activation buffer has {x.size} values, expected {m * k}")
+    outs = [np.empty((m, n), dtype=np.float64) for _ in range(5)]
+    _load().qmm_oracle_geglu_q4_0(_ptr(wg), _ptr(wu), _ptr(x), m, n, k, *[_ptr(o) for o in outs])
+    return tuple(outs)

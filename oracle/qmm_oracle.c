@@ -184,3 +184,27 @@ void qmm_oracle_gemm_q4_0_at(const uint8_t *w, const uint16_t *x_bf16, int64_t k
                              double *y, double *bound) {
     product_at(w, x_bf16, k, mi, ni, count, y, bound, q4_0_weight, Q4_0_BYTES, act_bf16);
 }
+
+/* GELU, tanh form, in binary64 (libm tanh). */
+static double gelu_tanh(double z) {
+    const double c = sqrt(2.0 / 3.14159265358979323846);
+    return 0.5 * z * (1.0 + tanh(c * (z + 0.044715 * z * z * z)));
+}
+
+void qmm_oracle_geglu_q4_0(const uint8_t *wg, const uint8_t *wu, const float *x, int64_t m,
+                           int64_t n, int64_t k, double *h, double *g, double *u,
+                           double *bound_g, double *bound_u) {
+    int64_t total = m * n;
+#pragma omp parallel for schedule(dynamic, 16) num_threads(qmm_oracle_get_threads())
+    for (int64_t i = 0; i < total; i++) {
+        int64_t mi = i / n, ni = i % n;
+        double gv, uv, bg, bu;
+        dot(wg, x, k, mi, ni, q4_0_weight, Q4_0_BYTES, act_f32, &gv, &bg);
+        dot(wu, x, k, mi, ni, q4_0_weight, Q4_0_BYTES, act_f32, &uv, &bu);
+        h[i] = gelu_tanh(gv) * uv;
+        if (g) g[i] = gv;
+        if (u) u[i] = uv;
+        if (bound_g) bound_g[i] = bg;
+        if (bound_u) bound_u[i] = bu;
+    }
+}

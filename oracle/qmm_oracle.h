@@ -77,6 +77,19 @@ void qmm_oracle_gemm_q4_0_at(const uint8_t *w, const uint16_t *x_bf16, int64_t k
                              const int64_t *mi, const int64_t *ni, int64_t count,
                              double *y, double *bound);
 
+/* Gated feed-forward input (GeGLU): the fused FFN paths of "Add generated
+ * quant-kernel JIT and accelerate Gemma4, BGE-M3, and GLiNER2" (section
+ * "Summary").  The pages do not name the activation; the reading taken is
+ * the Gemma family's GELU in its tanh form, applied to the gate:
+ *   g = x . Wg^T,  u = x . Wu^T  (Q4_0 weights, fp32 x, binary64 sums),
+ *   h[m][n] = gelu(g[m][n]) * u[m][n],
+ *   gelu(z) = z/2 * (1 + tanh(sqrt(2/pi) * (z + 0.044715 z^3))).
+ * h, g, u, bound_g, bound_u are binary64 [M][N]; the bounds are those of the
+ * two products (sum_k |w*x|).  Any output pointer but h may be NULL. */
+void qmm_oracle_geglu_q4_0(const uint8_t *wg, const uint8_t *wu, const float *x, int64_t m,
+                           int64_t n, int64_t k, double *h, double *g, double *u,
+                           double *bound_g, double *bound_u);
+
 /* Host threads used by the loops over outputs (OpenMP); <=0 means all. */
 void qmm_oracle_set_threads(int nthreads);
 int qmm_oracle_get_threads(void);

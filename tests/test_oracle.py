@@ -399,3 +399,61 @@ def test_bf16_rounding_is_nearest_even():
     big = synth.activations_f32(1, 1 << 16, seed=3).reshape(-1)
     ref = torch.from_numpy(big).to(torch.bfloat16).view(torch.int16).numpy().astype(np.uint16)
     assert np.array_equal(synth.f32_to_bf16_bits(big), ref)
+
+
+# ---- GeGLU feed-forward input: h = gelu_tanh(x.Wg^T) * (x.Wu^T) ----
+
+def _one_block_rows(nibbles, scales):
+    """Q4_0 rows of one block each: weight 0 (low nibble of qs[0]) = nibbles[i],
+    every other weight nibble 8 (zero); d = scales[i] (rounded to binary16)."""
+    rows = []
+    for v, d in zip(nibbles, scales):
+        blk = np.zeros(18, dtype=np.uint8)
+        blk[0:2] = np.frombuffer(np.float16(d).tobytes(), np.uint8)
+        blk[2:] = 0x88
+        blk[2] = 0x80 | v  # weight 0 = v, weight 16 = 8
+        rows.append(blk)
+    return np.stack(rows)
+
+
+def test_geglu_activation_matches_torch_gelu_tanh(oracle_mod):
+    """One-hot x = e_0 makes g = (v-8)*d and u = 1, so h = gelu(g): checked
+    against torch's own float64 GELU (tanh form), an independent routine."""
+    torch = pytest.importorskip("torch")
+    vals, ds = [], []
+    for d in (0.25, 1.0, 3.0, 100.0, 1e-3):
+        for v in range(16):
+            vals.append(v)
+            ds.append(d)
+    n, k = len(vals), 32
+    wg = _one_block_rows(vals, ds)
+    wu = _one_block_rows([9] * n, [1.0] * n)  # u = 1 exactly
+    x = np.zeros((1, k), dtype=np.float32)
+    x[0, 0] = 1.0
+    h, g, u, bg, bu = oracle_mod.geglu_q4_0(wg, wu, x, 1, n, k)
+    g_want = np.array([(v - 8) * float(np.float16(d)) for v, d in zip(vals, ds)])
+    assert np.array_equal(g[0], g_want) and np.all(u == 1.0)
+    want = torch.nn.functional.gelu(torch.from_numpy(g_want), approximate="tanh").numpy()
+    np.testing.assert_allclose(h[0], want, rtol=1e-13, atol=1e-300)
+    assert h[0][vals.index(8)] == 0.0          # gelu(0) = 0
+    assert np.all(bg[0] == np.abs(g_want)) and np.all(bu[0] == 1.0)
+
+
+def test_geglu_composes_the_pinned_products(oracle_mod):
+    """h = gelu(g) * u with g, u the (pinned) GEMV of the gate and up weights:
+    the activation is on the gate operand, and the product is elementwise."""
+    torch = pytest.importorskip("torch")
+    m, n, k = 3, 37, 256
+    wg = synth.q4_0_weights(n, k, seed=11)
+    wu = synth.q4_0_weights(n, k, seed=12)
+    x = synth.activations_f32(m, k, seed=13)
+    h, g, u, bg, bu = oracle_mod.geglu_q4_0(wg, wu, x, m, n, k)
+    g_ref, bg_ref = oracle_mod.gemv_q4_0(wg, x, m, n, k)
+    u_ref, bu_ref = oracle_mod.gemv_q4_0(wu, x, m, n, k)
+    assert np.array_equal(g, g_ref) and np.array_equal(u, u_ref)
+    assert np.array_equal(bg, bg_ref) and np.array_equal(bu, bu_ref)
+    want = torch.nn.functional.gelu(torch.from_numpy(g_ref), approximate="tanh").numpy() * u_ref
+    np.testing.assert_allclose(h, want, rtol=1e-13, atol=1e-300)
+    # swapping the roles of gate and up gives a different result
+    h_sw = oracle_mod.geglu_q4_0(wu, wg, x, m, n, k)[0]
+    assert not np.allclose(h_sw, h, rtol=1e-3)
