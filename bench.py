@@ -66,7 +66,7 @@ def parse_args(argv=None):
     ap.add_argument("--profile", default=None, metavar="CASE",
                     help="no timing: run CASE a few times for a profiler and exit. CASE is "
                          "decode_grouped (the timed decode step), decode (seven separate calls), "
-                         "gemv:FMT:M:N:K, dequant:FMT:N:K "
+                         "gemv:FMT:M:N:K, geglu:M:N:K, dequant:FMT:N:K "
                          "or gemm:M:N:K")
     ap.add_argument("--profile-launches", type=int, default=3)
     return ap.parse_args(argv)
@@ -93,6 +93,13 @@ def run_profile(args):
             for g, x in zip(groups, X):
                 qmm.qmm_gemv_q4_0_multi([(W[i], Y[i], cases[i].n) for i in g], x, 1,
                                         cases[g[0]].k)
+    elif parts[0] == "geglu":
+        m, n, k = int(parts[1]), int(parts[2]), int(parts[3])
+        wg = torch.from_numpy(synth.q4_0_weights(n, k, seed=0, stream=14)).to(dev)
+        wu = torch.from_numpy(synth.q4_0_weights(n, k, seed=0, stream=15)).to(dev)
+        x = torch.from_numpy(synth.activations_f32(m, k, seed=0, stream=16)).to(dev)
+        for _ in range(reps):
+            qmm.geglu_q4_0(wg, wu, x, n, k)
     elif parts[0] == "decode":
         cases = [synth.gemv_case("q4_0", 1, p.n, p.k, seed=0, stream=10 + i)
                  for i, p in enumerate(synth.DECODE_LAYER)]
@@ -395,21 +402,22 @@ def run_secondary(torch, qmm, l2, stream, timer, peaks):
 
     weight_cache = {}
 
-    def gemv_entry(name, fmt, m, projs, base):
+    def gemv_entry(name, fmt, m, projs, base, grouped=False):
         key = (fmt, base, tuple((p.n, p.k) for p in projs))
         if key not in weight_cache:
             weight_cache.clear()
             weight_cache[key] = [synth.gemv_case(fmt, 1, p.n, p.k, seed=0, stream=base + i).w
                                  for i, p in enumerate(projs)]
         layer = DecodeLayer(torch, qmm, l2, stream, m=m, projections=projs, stream_base=base,
-                            fmt=fmt, weights=weight_cache[key])
+                            fmt=fmt, weights=weight_cache[key],
+                            groups=(tuple(p.name for p in projs),) if grouped else None)
         steps = max(layer.R, (2000 // layer.R) * layer.R)
         layer.run_steps(layer.R)
         el = timer.run(lambda: layer.run_steps(steps))
         gbs = layer.step_bytes * steps / el / 1e9
         resident = layer.R * layer.step_bytes
         out[name] = {"gbs": round(gbs, 1), "frac_hbm": round(gbs / hbm, 4),
-                     "us_per_call": round(el / steps / len(projs) * 1e6, 3),
+                     "us_per_call": round(el / steps / layer.launches_per_step * 1e6, 3),
                      "replicas": layer.R,
                      "l2": ("weights rotate through %d replicas (%.0f MB, %s)"
                             % (layer.R, resident / 1e6, "larger than L2" if resident > l2 else
@@ -426,11 +434,54 @@ def run_secondary(torch, qmm, l2, stream, timer, peaks):
             gemv_entry(f"q4_0_gemv_{p.n}x{p.k}_m{m}", "q4_0", m, (p,), 30 + i)
     for m in synth.LM_HEAD_M:
         gemv_entry(f"q8_0_lm_head_262144x2048_m{m}", "q8_0", m, (synth.LM_HEAD,), 50)
+    # the feed-forward input: gate and up as one grouped call (two outputs
+    # written) against the fused GeGLU call (h = gelu(g) * u written)
+    ffn = tuple(p for p in synth.DECODE_LAYER if p.name in ("gate", "up"))
+    for m in (1, 8):
+        gemv_entry(f"q4_0_decode_gate_up_grouped_m{m}", "q4_0", m, ffn, 14, grouped=True)
+        try:
+            out.update(measure_geglu(torch, qmm, l2, stream, timer, hbm, ffn, m))
+        except Exception as e:  # noqa: BLE001 - reported, not hidden
+            out[f"q4_0_decode_ffn_geglu_m{m}"] = {"error": str(e)[:200]}
     try:
         out.update(measure_gemm(torch, qmm, l2, stream, timer, peaks))
     except Exception as e:  # noqa: BLE001 - reported, not hidden
         out["q4_0_gemm"] = {"error": str(e)[:200]}
     return out
+
+
+def measure_geglu(torch, qmm, l2, stream, timer, hbm, ffn, m):
+    """Fused GeGLU decode call over rotating replicas of the gate/up pair."""
+    gate, up = ffn
+    n, k = gate.n, gate.k
+    dev = torch.device("cuda")
+    wg = torch.from_numpy(synth.q4_0_weights(n, k, seed=0, stream=14)).to(dev)
+    wu = torch.from_numpy(synth.q4_0_weights(n, k, seed=0, stream=15)).to(dev)
+    pair_bytes = 2 * wg.numel()
+    R = replicas_for(pair_bytes, l2)
+    WG = [wg.clone() for _ in range(R)]
+    WU = [wu.clone() for _ in range(R)]
+    del wg, wu
+    x = torch.from_numpy(synth.activations_f32(m, k, seed=0, stream=16)).to(dev)
+    h = torch.empty((m, n), dtype=torch.float32, device=dev)
+    s = stream.cuda_stream
+
+    def body():
+        for r in range(R):
+            qmm.qmm_gemv_q4_0_geglu(WG[r], WU[r], x, h, m, n, k, s)
+
+    g = capture(torch, stream, body)
+    reps = max(1, 2000 // R)
+    g.replay()
+    el = timer.run(lambda: [g.replay() for _ in range(reps)])
+    calls = reps * R
+    gbs = pair_bytes * calls / el / 1e9
+    return {f"q4_0_decode_ffn_geglu_m{m}": {
+        "gbs": round(gbs, 1), "frac_hbm": round(gbs / hbm, 4),
+        "us_per_call": round(el / calls * 1e6, 3), "replicas": R,
+        "what": "h = gelu_tanh(x.Wg^T) * (x.Wu^T), gate and up %dx%d Q4_0, one launch" % (n, k),
+        "l2": "weights rotate through %d replicas (%.0f MB, larger than L2)"
+              % (R, R * pair_bytes / 1e6)}}
 
 
 def measure_gemm(torch, qmm, l2, stream, timer, peaks):

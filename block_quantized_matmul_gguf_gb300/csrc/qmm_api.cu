@@ -210,6 +210,25 @@ qmm_status qmm_gemv_q8_0_multi(const qmm_gemv_out *outs, int count, const float 
     return gemv(Fmt::Q8_0, outs, count, x, m, k, stream);
 }
 
+qmm_status qmm_gemv_q4_0_geglu(const void *wg, const void *wu, const float *x, float *h, int m,
+                               int64_t n, int64_t k, qmm_stream_t stream) {
+    qmm_status s = check_wk(wg, n, k);
+    if (s == QMM_OK) s = check_wk(wu, n, k);
+    if (s != QMM_OK) return s;
+    if (!x || !h) return QMM_ERR_NULL;
+    if (m < 1 || m > QMM_GEMV_MAX_M) return QMM_ERR_SHAPE;
+    if (!aligned(x, 4) || !aligned(h, 4)) return QMM_ERR_ALIGN;
+    const size_t hbytes = sizeof(float) * static_cast<size_t>(m) * n;
+    const size_t wbytes = static_cast<size_t>(n) * (k / kQK) * kQ4_0Bytes;
+    if (overlaps(h, hbytes, x, sizeof(float) * static_cast<size_t>(m) * k) ||
+        overlaps(h, hbytes, wg, wbytes) || overlaps(h, hbytes, wu, wbytes))
+        return QMM_ERR_UNSUPPORTED;
+    LaunchCtx ctx;
+    if (!make_ctx(&ctx)) return QMM_ERR_CUDA;
+    const GemvProblem gate_up[2] = {{wg, h, n}, {wu, nullptr, n}};
+    return from_cuda(launch_geglu_q4_0(gate_up, x, m, k, reinterpret_cast<cudaStream_t>(stream), ctx));
+}
+
 qmm_status qmm_gemm_q4_0(const void *w, const uint16_t *x_bf16, float *y, int64_t m, int64_t n,
                          int64_t k, qmm_stream_t stream) {
     qmm_status s = check_wk(w, n, k);

@@ -505,18 +505,34 @@ struct StreamParams {
     LaunchCtx ctx;
 };
 
+// GeGLU feed-forward input h = gelu(g) * u, g = x.Wg^T, u = x.Wu^T (the
+// tanh form of the GELU, evaluated as z * sigmoid(2a) with
+// a = sqrt(2/pi) * (z + 0.044715 z^3), which equals z/2 * (1 + tanh(a))
+// and has no cancellation for negative z).
+__device__ __forceinline__ float gelu_tanh(float z) {
+    const float a = 0.7978845608028654f * fmaf(0.044715f * z, z * z, z);
+    return z / (1.0f + expf(-2.0f * a));
+}
+
 // Grid: blockIdx.x = group * ksplit + rank (cluster of ksplit CTAs along x).
 // Warp w of a CTA owns row tile group*rw + w / kw and the (w % kw)-th part of
 // the CTA's K range; cluster rank r owns the r-th part of K.
+//
+// G (GeGLU): one problem whose gate and up weights are maps.m[0] and
+// maps.m[1].  A lane's two rows (R == 2) are gate row and up row of the same
+// output: a stage holds the gate box (32/L rows) followed by the up box, the
+// lane's two sums meet in registers and the writer stores gelu(g) * u.
 #ifndef QMM_GEMV_MAX_THREADS
 #define QMM_GEMV_MAX_THREADS 256
 #endif
-template <Fmt F, int M, int L, int R>
+template <Fmt F, int M, int L, int R, bool G = false>
 __global__ void __launch_bounds__(QMM_GEMV_MAX_THREADS)
     gemv_stream_kernel(const __grid_constant__ StreamMaps maps, StreamParams p) {
+    static_assert(!G || R == 2, "GeGLU pairs the gate and up rows of one output in a lane");
     constexpr int CB = StreamFmt<F>::kChunkBytes;
     constexpr int kLaneRows = 32 / L;                 // rows covered by one pass of the lanes
     constexpr int kRowsPerWarp = kLaneRows * R;       // L lanes share a row; a lane owns R rows
+    constexpr int kTileRows = G ? kLaneRows : kRowsPerWarp;  // output rows of a warp's tile
     extern __shared__ __align__(128) uint8_t smem_dyn[];
     // TMA destinations: 128-byte aligned (the launch adds 128 bytes of slack)
     uint8_t *smem = smem_dyn + ((128u - (smem_addr(smem_dyn) & 127u)) & 127u);
@@ -546,7 +562,7 @@ __global__ void __launch_bounds__(QMM_GEMV_MAX_THREADS)
     const CUtensorMap *wmap = &maps.m[prob];
     const int tile_in_cta = warp >> (__ffs(kw) - 1);
     const int kpart = warp & (kw - 1);
-    const int row0 = (group * p.rw + tile_in_cta) * kRowsPerWarp;
+    const int row0 = (group * p.rw + tile_in_cta) * kTileRows;
     const int r = lane / L;  // rows r, r + 32/L, ... of the warp's tile
     const int h = lane % L;  // this lane's share of each chunk
     const bool warp_active = row0 < n_rows;  // warp-uniform
@@ -568,6 +584,9 @@ __global__ void __launch_bounds__(QMM_GEMV_MAX_THREADS)
     if (lane == 0) {
         if (warp == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(wmap)) : "memory");
+            if constexpr (G)
+                asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&maps.m[1]))
+                             : "memory");
             mbar_init(xbar, 1);
         }
         for (int s = 0; s < S; ++s) mbar_init(&my_bars[s], 1);
@@ -579,8 +598,11 @@ __global__ void __launch_bounds__(QMM_GEMV_MAX_THREADS)
         if (lane == 0) {
             // full box bytes: rows past N are zero-filled and still counted
             mbar_arrive_expect_tx(&my_bars[st], kRowsPerWarp * CB);
-            tma_load_2d(my_ring + st * kRowsPerWarp * CB, wmap,
-                        (cta_c0 + w_c0 + i) * (CB / StreamFmt<F>::kElemBytes), row0, &my_bars[st]);
+            const int cx = (cta_c0 + w_c0 + i) * (CB / StreamFmt<F>::kElemBytes);
+            tma_load_2d(my_ring + st * kRowsPerWarp * CB, wmap, cx, row0, &my_bars[st]);
+            if constexpr (G)  // the up rows of the same outputs, after the gate box
+                tma_load_2d(my_ring + (st * kRowsPerWarp + kLaneRows) * CB, &maps.m[1], cx, row0,
+                            &my_bars[st]);
         }
     };
     // The weight prefetch may start before the preceding kernel in the stream
@@ -689,12 +711,22 @@ __global__ void __launch_bounds__(QMM_GEMV_MAX_THREADS)
     // 2) K parts across the cluster: ranks push into rank 0, which adds in rank order
     if (ksplit == 1) {
         if (kpart == 0 && writer) {
-#pragma unroll
-            for (int j = 0; j < R; ++j) {
-                const int row = row0 + j * kLaneRows + r;
+            if constexpr (G) {
+                const int row = row0 + r;
                 if (row < n_rows) {
 #pragma unroll
-                    for (int m = 0; m < M; ++m) y[static_cast<size_t>(m) * n_rows + row] = tot[j][m];
+                    for (int m = 0; m < M; ++m)
+                        y[static_cast<size_t>(m) * n_rows + row] = gelu_tanh(tot[0][m]) * tot[1][m];
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < R; ++j) {
+                    const int row = row0 + j * kLaneRows + r;
+                    if (row < n_rows) {
+#pragma unroll
+                        for (int m = 0; m < M; ++m)
+                            y[static_cast<size_t>(m) * n_rows + row] = tot[j][m];
+                    }
                 }
             }
         }
@@ -709,7 +741,22 @@ __global__ void __launch_bounds__(QMM_GEMV_MAX_THREADS)
                 st_dsmem_f32(slot + m * kRowsPerWarp + j * kLaneRows + r, 0, tot[j][m]);
     }
     cluster_sync();
-    if (rank == 0 && kpart == 0 && writer) {
+    if (rank == 0 && kpart == 0 && writer && G) {
+        const int row = row0 + r;
+        if (row < n_rows) {
+#pragma unroll
+            for (int m = 0; m < M; ++m) {
+                float s[R];
+#pragma unroll
+                for (int j = 0; j < R; ++j) {
+                    s[j] = 0.0f;
+                    for (uint32_t q = 0; q < ksplit; ++q)
+                        s[j] += part[((q * p.rw + tile_in_cta) * M + m) * kRowsPerWarp + j * kLaneRows + r];
+                }
+                y[static_cast<size_t>(m) * n_rows + row] = gelu_tanh(s[0]) * s[1];
+            }
+        }
+    } else if (rank == 0 && kpart == 0 && writer) {
 #pragma unroll
         for (int j = 0; j < R; ++j) {
             const int row = row0 + j * kLaneRows + r;
@@ -727,18 +774,11 @@ __global__ void __launch_bounds__(QMM_GEMV_MAX_THREADS)
 
 // Byte-wise fallback: one warp per row, lanes over blocks.
 template <Fmt F, int M>
-__global__ void __launch_bounds__(128) gemv_bytewise_kernel(const uint8_t *__restrict__ w,
-                                                           const float *__restrict__ x,
-                                                           float *__restrict__ y, int64_t n,
-                                                           int64_t k, LaunchCtx ctx) {
+__device__ __forceinline__ void bytewise_row(const uint8_t *__restrict__ w,
+                                             const float *__restrict__ x, int64_t row, int64_t k,
+                                             int lane, float (&acc)[M]) {
     constexpr int kBB = F == Fmt::Q4_0 ? kQ4_0Bytes : kQ8_0Bytes;
-    pdl_wait();
-    pdl_launch_dependents();
-    const int lane = threadIdx.x & 31;
-    const int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (row >= n) return;
     const int64_t nb = k / kQK;
-    float acc[M];
 #pragma unroll
     for (int m = 0; m < M; ++m) acc[m] = 0.0f;
     for (int64_t b = lane; b < nb; b += 32) {
@@ -762,10 +802,33 @@ __global__ void __launch_bounds__(128) gemv_bytewise_kernel(const uint8_t *__res
         for (int m = 0; m < M; ++m) acc[m] = fmaf(d, part[m], acc[m]);
     }
 #pragma unroll
-    for (int m = 0; m < M; ++m) {
-        float v = acc[m];
-        for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
-        if (lane == 0) y[m * n + row] = v;
+    for (int m = 0; m < M; ++m)
+        for (int off = 16; off > 0; off >>= 1) acc[m] += __shfl_xor_sync(0xFFFFFFFFu, acc[m], off);
+}
+
+// y[m][row] = x[m] . w[row]; G (GeGLU): y[m][row] = gelu(x[m] . w[row]) * (x[m] . w2[row]).
+template <Fmt F, int M, bool G = false>
+__global__ void __launch_bounds__(128) gemv_bytewise_kernel(const uint8_t *__restrict__ w,
+                                                           const uint8_t *__restrict__ w2,
+                                                           const float *__restrict__ x,
+                                                           float *__restrict__ y, int64_t n,
+                                                           int64_t k, LaunchCtx ctx) {
+    pdl_wait();
+    pdl_launch_dependents();
+    const int lane = threadIdx.x & 31;
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (row >= n) return;
+    float acc[M];
+    bytewise_row<F, M>(w, x, row, k, lane, acc);
+    if constexpr (G) {
+        float up[M];
+        bytewise_row<F, M>(w2, x, row, k, lane, up);
+#pragma unroll
+        for (int m = 0; m < M; ++m) acc[m] = gelu_tanh(acc[m]) * up[m];
+    }
+    if (lane == 0) {
+#pragma unroll
+        for (int m = 0; m < M; ++m) y[m * n + row] = acc[m];
     }
 }
 
@@ -835,20 +898,24 @@ StreamShape stream_shape(int64_t tiles, int64_t k, int sms) {
 }
 
 // One launch over `count` problems sharing x: problem i has weights
-// probs[i].w (probs[i].n rows) and output probs[i].y.
-template <Fmt F, int M, int L, int R>
+// probs[i].w (probs[i].n rows) and output probs[i].y.  G (GeGLU): count == 2,
+// probs[0] the gate weights and the output h, probs[1] the up weights (same
+// n); one problem of n outputs whose tiles read both.
+template <Fmt F, int M, int L, int R, bool G = false>
 cudaError_t launch_stream(const GemvProblem *probs, int count, const float *x, int64_t k,
                           cudaStream_t stream, const LaunchCtx &ctx) {
     constexpr int kRowsPerWarp = 32 / L * R;
+    constexpr int kTileRows = G ? 32 / L : kRowsPerWarp;  // output rows of a tile
+    constexpr int kBoxRows = G ? 32 / L : kRowsPerWarp;   // rows of one TMA box
     int64_t tiles = 0;
-    for (int i = 0; i < count; ++i) tiles += (probs[i].n + kRowsPerWarp - 1) / kRowsPerWarp;
+    for (int i = 0; i < (G ? 1 : count); ++i) tiles += (probs[i].n + kTileRows - 1) / kTileRows;
     const StreamShape sh = stream_shape<F, M, L, R>(tiles, k, device_sm_count());
     if (sh.smem > kGemvSmemCap) return kShapeTooLarge;  // nothing launched
     StreamMaps maps;
     StreamParams p;
     p.x = x;
     p.k = static_cast<int>(k);
-    p.count = count;
+    p.count = G ? 1 : count;
     p.rw = sh.rw;
     p.kw = sh.kw;
     p.cpw = sh.cpw;
@@ -861,23 +928,25 @@ cudaError_t launch_stream(const GemvProblem *probs, int count, const float *x, i
     for (int i = 0; i < kMaxGemvProblems; ++i) {
         if (i < count) {
             if (!encode_tmap_2d(&maps.m[i], StreamFmt<F>::kType, probs[i].w, rowbytes / EB,
-                                probs[i].n, rowbytes, StreamFmt<F>::kChunkBytes / EB,
-                                kRowsPerWarp))
+                                probs[i].n, rowbytes, StreamFmt<F>::kChunkBytes / EB, kBoxRows))
                 return cudaErrorInvalidValue;
+        } else {
+            maps.m[i] = maps.m[0];
+        }
+        if (i < p.count) {
             p.y[i] = probs[i].y;
             p.n[i] = static_cast<int>(probs[i].n);
             p.group_begin[i] = static_cast<int>(groups);
-            const int64_t t = (probs[i].n + kRowsPerWarp - 1) / kRowsPerWarp;
+            const int64_t t = (probs[i].n + kTileRows - 1) / kTileRows;
             groups += (t + sh.rw - 1) / sh.rw;
         } else {
-            maps.m[i] = maps.m[0];
             p.y[i] = nullptr;
             p.n[i] = 0;
             p.group_begin[i] = static_cast<int>(groups);
         }
     }
     p.group_begin[kMaxGemvProblems] = static_cast<int>(groups);
-    auto kern = gemv_stream_kernel<F, M, L, R>;
+    auto kern = gemv_stream_kernel<F, M, L, R, G>;
     static int smem_limits[kMaxDevices] = {0};  // this instantiation's own cache
     const cudaError_t e = ensure_smem(kern, sh.smem, true, smem_limits);
     if (e != cudaSuccess) return e;
@@ -886,7 +955,7 @@ cudaError_t launch_stream(const GemvProblem *probs, int count, const float *x, i
                          static_cast<unsigned>(sh.ksplit), maps, p);
 }
 
-template <Fmt F, int M>
+template <Fmt F, int M, bool G = false>
 cudaError_t launch_m(const GemvProblem *probs, int count, const float *x, int64_t k,
                      cudaStream_t stream, const LaunchCtx &ctx) {
     bool aligned = (reinterpret_cast<uintptr_t>(x) & 15) == 0;
@@ -904,7 +973,17 @@ cudaError_t launch_m(const GemvProblem *probs, int count, const float *x, int64_
         // largest cluster split (very large K at large M) is refused before
         // any launch and takes the byte-wise kernel below.
         cudaError_t e;
-        if constexpr (M <= QMM_GEMV_R2_MAX_M) {
+        if constexpr (G) {
+            // GeGLU: a lane always owns the gate row and the up row of an output
+            if constexpr (M <= QMM_GEMV_R2_MAX_M) {
+                if (units <= QMM_GEMV_L2_UNITS)
+                    e = launch_stream<F, M, 2, 2, true>(probs, count, x, k, stream, ctx);
+                else
+                    e = launch_stream<F, M, 1, 2, true>(probs, count, x, k, stream, ctx);
+            } else {
+                e = launch_stream<F, M, 1, 2, true>(probs, count, x, k, stream, ctx);
+            }
+        } else if constexpr (M <= QMM_GEMV_R2_MAX_M) {
             if (units <= QMM_GEMV_L2_UNITS)
                 e = launch_stream<F, M, 2, QMM_GEMV_R_SMALL>(probs, count, x, k, stream, ctx);
             else
@@ -922,26 +1001,35 @@ cudaError_t launch_m(const GemvProblem *probs, int count, const float *x, int64_
         }
         if (e != kShapeTooLarge) return e;
     }
-    for (int i = 0; i < count; ++i) {  // byte-wise kernel, one launch per problem
-        const unsigned grid = static_cast<unsigned>((probs[i].n + 3) / 4);
-        const cudaError_t e = launch_kernel(gemv_bytewise_kernel<F, M>, dim3(grid), dim3(128), 0,
-                                            stream, 1, static_cast<const uint8_t *>(probs[i].w),
-                                            x, probs[i].y, probs[i].n, k, ctx);
-        if (e != cudaSuccess) return e;
+    if constexpr (G) {  // byte-wise GeGLU: both rows of an output in one warp
+        const unsigned grid = static_cast<unsigned>((probs[0].n + 3) / 4);
+        return launch_kernel(gemv_bytewise_kernel<F, M, true>, dim3(grid), dim3(128), 0, stream, 1,
+                             static_cast<const uint8_t *>(probs[0].w),
+                             static_cast<const uint8_t *>(probs[1].w), x, probs[0].y, probs[0].n,
+                             k, ctx);
+    } else {
+        for (int i = 0; i < count; ++i) {  // byte-wise kernel, one launch per problem
+            const unsigned grid = static_cast<unsigned>((probs[i].n + 3) / 4);
+            const cudaError_t e = launch_kernel(
+                gemv_bytewise_kernel<F, M>, dim3(grid), dim3(128), 0, stream, 1,
+                static_cast<const uint8_t *>(probs[i].w), static_cast<const uint8_t *>(nullptr), x,
+                probs[i].y, probs[i].n, k, ctx);
+            if (e != cudaSuccess) return e;
+        }
+        return cudaSuccess;
     }
-    return cudaSuccess;
 }
 
 // Dispatch of m in [LO, HI] (one translation unit per range builds in
 // parallel with the others).
-template <Fmt F, int LO, int HI>
+template <Fmt F, int LO, int HI, bool G = false>
 cudaError_t launch_m_range(const GemvProblem *probs, int count, const float *x, int m, int64_t k,
                            cudaStream_t s, const LaunchCtx &ctx) {
     if constexpr (LO > HI) {
         return cudaErrorInvalidValue;
     } else {
-        if (m == LO) return launch_m<F, LO>(probs, count, x, k, s, ctx);
-        return launch_m_range<F, LO + 1, HI>(probs, count, x, m, k, s, ctx);
+        if (m == LO) return launch_m<F, LO, G>(probs, count, x, k, s, ctx);
+        return launch_m_range<F, LO + 1, HI, G>(probs, count, x, m, k, s, ctx);
     }
 }
 

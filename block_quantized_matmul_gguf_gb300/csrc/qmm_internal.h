@@ -128,6 +128,22 @@ inline cudaError_t launch_gemv(Fmt fmt, const GemvProblem *probs, int count, con
     return launch_gemv_q8_0_m11_16(probs, count, x, m, k, stream, ctx);
 }
 
+// Fused GeGLU decode: h[m][i] = gelu(x[m] . wg[i]) * (x[m] . wu[i]) with
+// gate_up[0] = {wg, h, n} and gate_up[1] = {wu, unused, n}.
+cudaError_t launch_geglu_q4_0_m1_4(const GemvProblem *gate_up, const float *x, int m, int64_t k,
+                                   cudaStream_t stream, const LaunchCtx &ctx);
+cudaError_t launch_geglu_q4_0_m5_10(const GemvProblem *gate_up, const float *x, int m, int64_t k,
+                                    cudaStream_t stream, const LaunchCtx &ctx);
+cudaError_t launch_geglu_q4_0_m11_16(const GemvProblem *gate_up, const float *x, int m,
+                                     int64_t k, cudaStream_t stream, const LaunchCtx &ctx);
+
+inline cudaError_t launch_geglu_q4_0(const GemvProblem *gate_up, const float *x, int m,
+                                     int64_t k, cudaStream_t stream, const LaunchCtx &ctx) {
+    if (m <= 4) return launch_geglu_q4_0_m1_4(gate_up, x, m, k, stream, ctx);
+    if (m <= 10) return launch_geglu_q4_0_m5_10(gate_up, x, m, k, stream, ctx);
+    return launch_geglu_q4_0_m11_16(gate_up, x, m, k, stream, ctx);
+}
+
 cudaError_t launch_gemm_q4_0(const uint8_t *w, const uint16_t *x, float *y, int64_t m,
                              int64_t n, int64_t k, cudaStream_t stream, const LaunchCtx &ctx);
 

@@ -117,6 +117,25 @@ qmm_status qmm_gemv_q4_0_multi(const qmm_gemv_out *outs, int count, const float 
 qmm_status qmm_gemv_q8_0_multi(const qmm_gemv_out *outs, int count, const float *x, int m,
                                int64_t k, qmm_stream_t stream);
 
+/* ---- Fused GeGLU decode (feed-forward input) ---------------------------
+ * h[r][j] = gelu(g[r][j]) * u[r][j] with g[r][j] = sum_k x[r][k] * wg[j][k]
+ * and u[r][j] = sum_k x[r][k] * wu[j][k], for r < m, j < n: the gate and up
+ * projections of a feed-forward block and their gated product in one
+ * launch, the fused FFN path of "Add generated quant-kernel JIT and
+ * accelerate Gemma4, BGE-M3, and GLiNER2" (second revision, "Summary").
+ * The pages do not name the activation; this call takes the GELU in its
+ * tanh form, gelu(z) = z/2 * (1 + tanh(sqrt(2/pi) * (z + 0.044715 z^3))),
+ * applied to the gate product (the GeGLU of Gemma-family feed-forward
+ * blocks).  g and u are computed as by qmm_gemv_q4_0 and never stored.
+ * wg, wu : N*K/32 Q4_0 blocks each.   x : fp32 [m][k].   h : fp32 [m][n].
+ * Requires what qmm_gemv_q4_0 requires of each weight matrix, and h not
+ * overlapping wg, wu or x.  Accuracy, with e_g = 1e-4 * sum_k |wg*x| + 1e-6
+ * and e_u likewise: |h - h_exact| <= 1.13 * |u| * e_g + |gelu(g)| * e_u
+ * + 1e-5 * (1 + g^2) * |h| + 1e-6 (1.13 bounds |gelu'|; the third term is
+ * the fp32 evaluation of the GELU). */
+qmm_status qmm_gemv_q4_0_geglu(const void *wg, const void *wu, const float *x, float *h, int m,
+                               int64_t n, int64_t k, qmm_stream_t stream);
+
 /* ---- Prefill GEMM (tcgen05 tensor cores) ------------------------------
  * Y[i][j] = sum_k X[i][k] * w[j][k] for i < m, j < n.  X is bf16 [m][k]
  * given as raw bf16 bit patterns; each weight is rounded once to bf16

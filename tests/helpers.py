@@ -31,3 +31,31 @@ def to_dev(a, torch, device="cuda"):
 
 def bf16_tensor(bits, torch, device="cuda"):
     return torch.from_numpy(np.ascontiguousarray(bits).astype(np.int16)).view(torch.bfloat16).to(device)
+
+
+# GeGLU h = gelu(g) * u: the GEMV error of g (scaled by max|gelu'| = 1.1290
+# of the tanh form) and of u, plus the fp32 evaluation of the GELU, whose
+# argument a ~ g^3 carries a relative error of a few ulp (relative error of
+# gelu(g) about 4e-7 * |a| <= 1e-5 * (1 + g^2)).
+GELU_SLOPE_MAX = 1.13
+
+
+def geglu_limit(h_ref, g, u, bound_g, bound_u):
+    e_g = GEMV_REL * bound_g + ABS
+    e_u = GEMV_REL * bound_u + ABS
+    gelu_g = np.divide(h_ref, u, out=np.zeros_like(h_ref), where=u != 0)
+    return (GELU_SLOPE_MAX * np.abs(u) * e_g + np.abs(gelu_g) * e_u
+            + 1e-5 * (1.0 + g * g) * np.abs(h_ref) + ABS)
+
+
+def assert_geglu_within(h, h_ref, g, u, bound_g, bound_u, what=""):
+    h = np.asarray(h, dtype=np.float64)
+    err = np.abs(h - h_ref)
+    lim = geglu_limit(h_ref, g, u, bound_g, bound_u)
+    bad = ~(err <= lim)
+    if bad.any():
+        idx = np.argwhere(bad)[:5]
+        raise AssertionError(
+            f"{what}: {int(bad.sum())} of {bad.size} outputs outside tolerance; first "
+            + ", ".join(f"{tuple(i)}: h={h[tuple(i)]!r} ref={h_ref[tuple(i)]!r} "
+                        f"g={g[tuple(i)]!r} u={u[tuple(i)]!r}" for i in idx))
