@@ -66,7 +66,7 @@ def parse_args(argv=None):
     ap.add_argument("--profile", default=None, metavar="CASE",
                     help="no timing: run CASE a few times for a profiler and exit. CASE is "
                          "decode_grouped (the timed decode step), decode (seven separate calls), "
-                         "gemv:FMT:M:N:K, geglu:M:N:K, dequant:FMT:N:K "
+                         "gemv:FMT:M:N:K, geglu:M:N:K, gemm_geglu:M:N:K, dequant:FMT:N:K "
                          "or gemm:M:N:K")
     ap.add_argument("--profile-launches", type=int, default=3)
     return ap.parse_args(argv)
@@ -100,6 +100,14 @@ def run_profile(args):
         x = torch.from_numpy(synth.activations_f32(m, k, seed=0, stream=16)).to(dev)
         for _ in range(reps):
             qmm.geglu_q4_0(wg, wu, x, n, k)
+    elif parts[0] == "gemm_geglu":
+        m, n, k = int(parts[1]), int(parts[2]), int(parts[3])
+        wg, xb = synth.gemm_case(m, n, k, seed=0, stream=80)
+        wu = synth.q4_0_weights(n, k, seed=0, stream=81)
+        WG, WU = torch.from_numpy(wg).to(dev), torch.from_numpy(wu).to(dev)
+        X = torch.from_numpy(xb.astype(np.int16)).to(dev)
+        for _ in range(reps):
+            qmm.gemm_geglu_q4_0(WG, WU, X, n, k)
     elif parts[0] == "decode":
         cases = [synth.gemv_case("q4_0", 1, p.n, p.k, seed=0, stream=10 + i)
                  for i, p in enumerate(synth.DECODE_LAYER)]
@@ -529,6 +537,29 @@ def measure_gemm(torch, qmm, l2, stream, timer, peaks):
             "us": round(tcm * 1e6, 2),
             "what": "torch.matmul bf16 x bf16 -> bf16 of dense weights: a practical ceiling, not this library"}
         del Wd, Xd, gc
+    # prefill GeGLU: the 8192 x 2048 gate/up pair over the same prompt, h bf16
+    gate = next(p for p in synth.DECODE_LAYER if p.name == "gate")
+    m, n, k = synth.PREFILL_M, gate.n, gate.k
+    wg, xb = synth.gemm_case(m, n, k, seed=0, stream=80)
+    wu = synth.q4_0_weights(n, k, seed=0, stream=81)
+    WG, WU = torch.from_numpy(wg.reshape(-1)).to(dev), torch.from_numpy(wu.reshape(-1)).to(dev)
+    X = torch.from_numpy(xb.astype(np.int16)).to(dev)
+    H = torch.empty((m, n), dtype=torch.int16, device=dev)
+    s = stream.cuda_stream
+    g = capture(torch, stream, lambda: qmm.qmm_gemm_q4_0_geglu(WG, WU, X, H, m, n, k, s))
+    times = []
+    for _ in range(20):
+        gf.replay()
+        times.append(timer.run(g.replay))
+    t = statistics.median(times)
+    flops = 2.0 * m * (2 * n) * k
+    res[f"q4_0_gemm_geglu_{m}x{n}x{k}"] = {
+        "tflops": round(flops / t / 1e12, 1),
+        "frac_bf16_peak": round(flops / t / 1e12 / peaks["bf16_tflops"], 4),
+        "us": round(t * 1e6, 2),
+        "what": "h = bf16(gelu_tanh(X.Wg^T) * (X.Wu^T)), gate and up %dx%d Q4_0, one launch; "
+                "flops count both products" % (n, k),
+        "l2": "flushed (2x L2 write) before each timed launch"}
     return res
 
 

@@ -243,6 +243,29 @@ qmm_status qmm_gemm_q4_0(const void *w, const uint16_t *x_bf16, float *y, int64_
                                       reinterpret_cast<cudaStream_t>(stream), ctx));
 }
 
+qmm_status qmm_gemm_q4_0_geglu(const void *wg, const void *wu, const uint16_t *x_bf16,
+                               uint16_t *h_bf16, int64_t m, int64_t n, int64_t k,
+                               qmm_stream_t stream) {
+    qmm_status s = check_wk(wg, n, k);
+    if (s == QMM_OK) s = check_wk(wu, n, k);
+    if (s != QMM_OK) return s;
+    if (!x_bf16 || !h_bf16) return QMM_ERR_NULL;
+    if (m < 1 || m > (int64_t(1) << 31)) return QMM_ERR_SHAPE;
+    if (k % 256 != 0) return QMM_ERR_UNSUPPORTED;
+    if (!aligned(wg, 16) || !aligned(wu, 16) || !aligned(x_bf16, 16) || !aligned(h_bf16, 2))
+        return QMM_ERR_ALIGN;
+    const size_t hbytes = sizeof(uint16_t) * static_cast<size_t>(m) * n;
+    const size_t wbytes = static_cast<size_t>(n) * (k / kQK) * kQ4_0Bytes;
+    if (overlaps(h_bf16, hbytes, x_bf16, sizeof(uint16_t) * static_cast<size_t>(m) * k) ||
+        overlaps(h_bf16, hbytes, wg, wbytes) || overlaps(h_bf16, hbytes, wu, wbytes))
+        return QMM_ERR_UNSUPPORTED;
+    LaunchCtx ctx;
+    if (!make_ctx(&ctx)) return QMM_ERR_CUDA;
+    return from_cuda(launch_gemm_q4_0_geglu(static_cast<const uint8_t *>(wg),
+                                            static_cast<const uint8_t *>(wu), x_bf16, h_bf16, m, n,
+                                            k, reinterpret_cast<cudaStream_t>(stream), ctx));
+}
+
 const char *qmm_status_string(qmm_status status) {
     switch (status) {
         case QMM_OK: return "ok";

@@ -127,7 +127,8 @@ constexpr size_t kSmemBytes = SmemLayout::total + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 struct GemmParams {
-    float *y;
+    float *y;     // plain GEMM: fp32 [m][n]
+    uint16_t *h;  // GeGLU form: bf16 [m][n] (n = rows of each of the two weights)
     int m, n, k;
     int num_t_blocks;  // token blocks of BT
     int num_tiles;     // pair tiles
@@ -367,6 +368,21 @@ __device__ __forceinline__ float mag(uint32_t v, uint32_t mask, uint32_t magic) 
     return __uint_as_float((v & mask) | magic);
 }
 
+// GELU, tanh form, as z * sigmoid(2a) with a = sqrt(2/pi) * (z + 0.044715 z^3)
+// (equal to z/2 * (1 + tanh(a))).  The result is rounded to bf16, so the
+// fast exponential and division are accurate enough; the exponent is
+// clamped so that the divisor stays finite and in the fast division's range.
+__device__ __forceinline__ float gelu_tanh_fast(float z) {
+    const float a = 0.7978845608028654f * fmaf(0.044715f * z, z * z, z);
+    return __fdividef(z, 1.0f + __expf(fminf(-2.0f * a, 80.0f)));
+}
+
+__device__ __forceinline__ uint16_t to_bf16(float v) {
+    uint16_t r;
+    asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(v));
+    return r;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
@@ -436,9 +452,17 @@ __device__ __forceinline__ void dequant_words_bf16(const uint32_t (&wd)[36], int
 #define MMA_WAIT wait_or_abort
 #endif
 
+// G (GeGLU): tmap_w holds the gate weights and tmap_w2 the up weights (64-row
+// boxes).  A CTA's 128 accumulator rows are 64 features: in lane quarter q,
+// lanes 0-15 hold the gate rows of features 16q..16q+15 and lanes 16-31 the
+// up rows of the same features, so lane l and lane l ^ 16 of an epilogue warp
+// meet with one shuffle and write h = gelu(g) * u as bf16.  A pair tile is
+// 128 features x 256 tokens.
+template <bool G>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_q4_0_kernel(const __grid_constant__ CUtensorMap tmap_x,
-                     const __grid_constant__ CUtensorMap tmap_w, GemmParams p) {
+                     const __grid_constant__ CUtensorMap tmap_w,
+                     const __grid_constant__ CUtensorMap tmap_w2, GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_base = smem_addr(smem_raw);
     const uint32_t sbase = (raw_base + 1023u) & ~1023u;  // 1024-byte aligned (swizzle atoms)
@@ -525,11 +549,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         } else if (lane == 1) {
             // raw weight tiles: this CTA's 128 weight rows
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_w)) : "memory");
+            if constexpr (G)
+                asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_w2))
+                             : "memory");
             uint32_t rit = 0;
             bool ok = true;
             for (int t = pair; ok && t < p.num_tiles; t += num_pairs) {
                 const int wb = t / p.num_t_blocks;
-                const int wrow = wb * 2 * BW + static_cast<int>(rank) * BW;
+                // G: this CTA's 64 features, gate rows then up rows
+                const int wrow = G ? wb * BW + static_cast<int>(rank) * (BW / 2)
+                                   : wb * 2 * BW + static_cast<int>(rank) * BW;
                 for (int kr = 0; kr < KR; ++kr) {
                     const int r = rit % RAW_STAGES;
                     const uint32_t ph = (rit / RAW_STAGES) & 1u;
@@ -537,6 +566,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     mbar_expect_tx_addr(raw_full(r), RAW_STAGE_BYTES);
                     tma_load_2d(sbase + SmemLayout::raw + r * RAW_STAGE_BYTES, &tmap_w, kr * RAW_ROW_BYTES,
                                 wrow, raw_full(r));
+                    if constexpr (G)
+                        tma_load_2d(sbase + SmemLayout::raw + r * RAW_STAGE_BYTES +
+                                        (BW / 2) * RAW_ROW_BYTES,
+                                    &tmap_w2, kr * RAW_ROW_BYTES, wrow, raw_full(r));
                     ++rit;
                 }
             }
@@ -593,7 +626,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // and block `half` (K 32*half..+31) of every 64-wide K stage
         const int q = warp & 3;
         const int half = (warp - WARP_DEQ0) >> 2;  // warp-uniform
-        const int row = q * 32 + lane;             // weight row within the CTA's 128
+        // weight row of the raw stage written to TMEM lane 32q + lane; G: gate
+        // rows of features 16q.. in lanes 0-15, their up rows (stage rows
+        // 64..) in lanes 16-31 (each 8-lane phase of the 16-byte reads still
+        // covers 8 consecutive 144-byte rows: no bank conflicts)
+        const int row = G ? (lane >> 4) * (BW / 2) + q * 16 + (lane & 15) : q * 32 + lane;
         const uint32_t full_leader0 = map_to_rank(bar(0), 0);
         const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + a_col0 +
                                    static_cast<uint32_t>(half * 16);
@@ -655,19 +692,47 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int tb = t % p.num_t_blocks, wb = t / p.num_t_blocks;
             if (!warp_wait_or_abort(d_full, tiles_done & 1u, abort_flag, ctx)) break;
             tc_fence_after();
-            const int n = wb * 2 * BW + static_cast<int>(rank) * BW + q * 32 + lane;
-            const bool n_ok = n < p.n;
+            if constexpr (G) {
+                const bool upper = lane >= 16;  // holds the up row; takes columns 16..31
+                const int f = wb * BW + static_cast<int>(rank) * (BW / 2) + q * 16 + (lane & 15);
+                const bool f_ok = f < p.n;
 #pragma unroll 1
-            for (int c = c0; c < c0 + CPW; ++c) {
-                uint32_t v[32];
-                tmem_ld_32cols(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + c * 32, v);
-                // column j of the accumulator is token tb*BT + j: the leader's 128 tokens
-                // then the peer's 128
-                const int m0 = tb * BT + c * 32;
-                if (n_ok) {
+                for (int c = c0; c < c0 + CPW; ++c) {
+                    uint32_t v[32];
+                    tmem_ld_32cols(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + c * 32, v);
+                    const int m0 = tb * BT + c * 32 + (upper ? 16 : 0);
+                    uint16_t hv[16];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        if (m0 + j < p.m) p.y[static_cast<size_t>(m0 + j) * p.n + n] = __uint_as_float(v[j]);
+                    for (int j = 0; j < 16; ++j) {
+                        // the lower lane passes g of column 16+j, the upper lane u of column j
+                        const float other =
+                            __shfl_xor_sync(0xFFFFFFFFu, __uint_as_float(upper ? v[j] : v[16 + j]), 16);
+                        const float g = upper ? other : __uint_as_float(v[j]);
+                        const float u = upper ? __uint_as_float(v[16 + j]) : other;
+                        hv[j] = to_bf16(gelu_tanh_fast(g) * u);
+                    }
+                    if (f_ok) {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            if (m0 + j < p.m) p.h[static_cast<size_t>(m0 + j) * p.n + f] = hv[j];
+                    }
+                }
+            } else {
+                const int n = wb * 2 * BW + static_cast<int>(rank) * BW + q * 32 + lane;
+                const bool n_ok = n < p.n;
+#pragma unroll 1
+                for (int c = c0; c < c0 + CPW; ++c) {
+                    uint32_t v[32];
+                    tmem_ld_32cols(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + c * 32, v);
+                    // column j of the accumulator is token tb*BT + j: the leader's 128 tokens
+                    // then the peer's 128
+                    const int m0 = tb * BT + c * 32;
+                    if (n_ok) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (m0 + j < p.m)
+                                p.y[static_cast<size_t>(m0 + j) * p.n + n] = __uint_as_float(v[j]);
+                    }
                 }
             }
             tc_fence_before();
@@ -685,35 +750,60 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == WARP_MMA) tmem_dealloc_pair(tmem_base, TMEM_COLS);
 }
 
-}  // namespace
-
-cudaError_t launch_gemm_q4_0(const uint8_t *w, const uint16_t *x, float *y, int64_t m, int64_t n,
-                             int64_t k, cudaStream_t stream, const LaunchCtx &ctx) {
+// One launch: plain GEMM (w2 == nullptr: y fp32) or the GeGLU form (w gate,
+// w2 up: h bf16).
+template <bool G>
+cudaError_t launch(const uint8_t *w, const uint8_t *w2, const uint16_t *x, float *y, uint16_t *h,
+                   int64_t m, int64_t n, int64_t k, cudaStream_t stream, const LaunchCtx &ctx) {
     if (m > (1 << 30) || n > (1 << 30) || k > (1 << 24)) return cudaErrorInvalidValue;
-    CUtensorMap tx, tw;
+    CUtensorMap tx, tw, tw2;
     if (!encode_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, k, m, k * 2, BK, BT_CTA,
                         CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     const uint64_t rowbytes = static_cast<uint64_t>(k / kQK) * kQ4_0Bytes;
+    constexpr uint32_t box_rows = G ? BW / 2 : BW;
     if (!encode_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, rowbytes, n, rowbytes,
-                        RAW_ROW_BYTES, BW))
+                        RAW_ROW_BYTES, box_rows))
         return cudaErrorInvalidValue;
+    if (G) {
+        if (!encode_tmap_2d(&tw2, CU_TENSOR_MAP_DATA_TYPE_UINT8, w2, rowbytes, n, rowbytes,
+                            RAW_ROW_BYTES, box_rows))
+            return cudaErrorInvalidValue;
+    } else {
+        tw2 = tw;
+    }
     GemmParams p;
     p.y = y;
+    p.h = h;
     p.m = static_cast<int>(m);
     p.n = static_cast<int>(n);
     p.k = static_cast<int>(k);
     p.num_t_blocks = static_cast<int>((m + BT - 1) / BT);
-    const int nwb = static_cast<int>((n + 2 * BW - 1) / (2 * BW));
+    // weight rows of a pair tile: 256 rows, or 128 features (gate + up rows)
+    const int64_t tile_rows = G ? BW : 2 * BW;
+    const int nwb = static_cast<int>((n + tile_rows - 1) / tile_rows);
     p.num_tiles = p.num_t_blocks * nwb;
     p.magic = 0x4B000000u;
     p.ctx = ctx;
     static int smem_limits[kMaxDevices] = {0};
-    cudaError_t e = ensure_smem(gemm_q4_0_kernel, kSmemBytes, true, smem_limits);
+    cudaError_t e = ensure_smem(gemm_q4_0_kernel<G>, kSmemBytes, true, smem_limits);
     if (e != cudaSuccess) return e;
     const int pairs = std::max(1, std::min(p.num_tiles, device_sm_count() / 2));
-    return launch_kernel(gemm_q4_0_kernel, dim3(2 * pairs), dim3(NUM_THREADS), kSmemBytes, stream,
-                         2, tx, tw, p);
+    return launch_kernel(gemm_q4_0_kernel<G>, dim3(2 * pairs), dim3(NUM_THREADS), kSmemBytes,
+                         stream, 2, tx, tw, tw2, p);
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_q4_0(const uint8_t *w, const uint16_t *x, float *y, int64_t m, int64_t n,
+                             int64_t k, cudaStream_t stream, const LaunchCtx &ctx) {
+    return launch<false>(w, nullptr, x, y, nullptr, m, n, k, stream, ctx);
+}
+
+cudaError_t launch_gemm_q4_0_geglu(const uint8_t *wg, const uint8_t *wu, const uint16_t *x,
+                                   uint16_t *h, int64_t m, int64_t n, int64_t k,
+                                   cudaStream_t stream, const LaunchCtx &ctx) {
+    return launch<true>(wg, wu, x, nullptr, h, m, n, k, stream, ctx);
 }
 
 }  // namespace qmm

@@ -148,6 +148,24 @@ qmm_status qmm_gemv_q4_0_geglu(const void *wg, const void *wu, const float *x, f
 qmm_status qmm_gemm_q4_0(const void *w, const uint16_t *x_bf16, float *y, int64_t m,
                          int64_t n, int64_t k, qmm_stream_t stream);
 
+/* ---- Prefill GeGLU (tcgen05 tensor cores) -----------------------------
+ * h[i][j] = bf16(gelu(g[i][j]) * u[i][j]) with g[i][j] = sum_k X[i][k] *
+ * wg[j][k] and u[i][j] = sum_k X[i][k] * wu[j][k], for i < m, j < n: the
+ * prefill side of the fused FFN path (same page and section as
+ * qmm_gemv_q4_0_geglu, same GELU), written as bf16 because it is the
+ * activation operand of the down-projection GEMM.  g and u are formed as by
+ * qmm_gemm_q4_0 (weights rounded once to bf16, fp32 sums in tensor memory)
+ * and never stored; h is rounded once to bf16 (nearest even).
+ * wg, wu : N*K/32 Q4_0 blocks each, 16-byte aligned.  x : bf16 [m][k],
+ * 16-byte aligned.  h : bf16 [m][n], 2-byte aligned, not overlapping wg, wu
+ * or x.  Requires m >= 1, n >= 1, k % 256 == 0 (else QMM_ERR_UNSUPPORTED).
+ * Accuracy, with e_g = 2e-3 * sum_k |wg*x| + 1e-6 and e_u likewise:
+ * |h - h_exact| <= 1.13 * |u| * e_g + |gelu(g)| * e_u
+ * + (2^-8 + 1e-5 * (1 + g^2)) * |h| + 1e-6. */
+qmm_status qmm_gemm_q4_0_geglu(const void *wg, const void *wu, const uint16_t *x_bf16,
+                               uint16_t *h_bf16, int64_t m, int64_t n, int64_t k,
+                               qmm_stream_t stream);
+
 /* ---- Utilities --------------------------------------------------------- */
 
 /* Static English text for a status code (never NULL). */
