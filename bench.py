@@ -67,7 +67,7 @@ def parse_args(argv=None):
                     help="no timing: run CASE a few times for a profiler and exit. CASE is "
                          "decode_grouped (the timed decode step), decode (seven separate calls), "
                          "gemv:FMT:M:N:K, geglu:M:N:K, gemm_geglu:M:N:K, dequant:FMT:N:K "
-                         "or gemm:M:N:K")
+                         "gemm:M:N:K or gemm_q8_0:M:N:K")
     ap.add_argument("--profile-launches", type=int, default=3)
     return ap.parse_args(argv)
 
@@ -135,6 +135,12 @@ def run_profile(args):
         X = torch.from_numpy(xb.astype(np.int16)).to(dev)
         for _ in range(reps):
             qmm.gemm_q4_0(W, X, n, k)
+    elif parts[0] == "gemm_q8_0":
+        m, n, k = int(parts[1]), int(parts[2]), int(parts[3])
+        W = torch.from_numpy(synth.q8_0_weights(n, k, seed=0, stream=75)).to(dev)
+        X = torch.from_numpy(synth.activations_bf16(m, k, seed=0, stream=76).astype(np.int16)).to(dev)
+        for _ in range(reps):
+            qmm.gemm("q8_0", W, X, n, k)
     else:
         raise SystemExit(f"unknown profile case {args.profile}")
     torch.cuda.synchronize()
@@ -537,6 +543,25 @@ def measure_gemm(torch, qmm, l2, stream, timer, peaks):
             "us": round(tcm * 1e6, 2),
             "what": "torch.matmul bf16 x bf16 -> bf16 of dense weights: a practical ceiling, not this library"}
         del Wd, Xd, gc
+    # Q8_0 weights through the same kernel (the 8192 x 2048 shape)
+    p = synth.PREFILL_SHAPES[0]
+    m = synth.PREFILL_M
+    W8 = torch.from_numpy(synth.q8_0_weights(p.n, p.k, seed=0, stream=75).reshape(-1)).to(dev)
+    X = torch.from_numpy(synth.activations_bf16(m, p.k, seed=0, stream=76).astype(np.int16)).to(dev)
+    Y = torch.empty((m, p.n), dtype=torch.float32, device=dev)
+    s = stream.cuda_stream
+    g = capture(torch, stream, lambda: qmm.qmm_gemm_q8_0(W8, X, Y, m, p.n, p.k, s))
+    times = []
+    for _ in range(20):
+        gf.replay()
+        times.append(timer.run(g.replay))
+    t = statistics.median(times)
+    flops = 2.0 * m * p.n * p.k
+    res[f"q8_0_gemm_{m}x{p.n}x{p.k}"] = {
+        "tflops": round(flops / t / 1e12, 1),
+        "frac_bf16_peak": round(flops / t / 1e12 / peaks["bf16_tflops"], 4),
+        "us": round(t * 1e6, 2), "l2": "flushed (2x L2 write) before each timed launch"}
+    del W8, Y
     # prefill GeGLU: the 8192 x 2048 gate/up pair over the same prompt, h bf16
     gate = next(p for p in synth.DECODE_LAYER if p.name == "gate")
     m, n, k = synth.PREFILL_M, gate.n, gate.k

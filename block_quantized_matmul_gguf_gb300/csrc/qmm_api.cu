@@ -122,6 +122,22 @@ qmm_status gemv(Fmt fmt, const qmm_gemv_out *outs, int count, const float *x, in
                                  reinterpret_cast<cudaStream_t>(stream), ctx));
 }
 
+qmm_status gemm(Fmt fmt, const void *w, const uint16_t *x_bf16, float *y, int64_t m, int64_t n,
+                int64_t k, qmm_stream_t stream) {
+    qmm_status s = check_wk(w, n, k);
+    if (s != QMM_OK) return s;
+    if (!x_bf16 || !y) return QMM_ERR_NULL;
+    if (m < 1 || m > (int64_t(1) << 31)) return QMM_ERR_SHAPE;
+    if (k % 256 != 0 || n % 4 != 0) return QMM_ERR_UNSUPPORTED;
+    if (!aligned(w, 16) || !aligned(x_bf16, 16) || !aligned(y, 16)) return QMM_ERR_ALIGN;
+    LaunchCtx ctx;
+    if (!make_ctx(&ctx)) return QMM_ERR_CUDA;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const uint8_t *wb = static_cast<const uint8_t *>(w);
+    return from_cuda(fmt == Fmt::Q4_0 ? launch_gemm_q4_0(wb, x_bf16, y, m, n, k, st, ctx)
+                                      : launch_gemm_q8_0(wb, x_bf16, y, m, n, k, st, ctx));
+}
+
 }  // namespace
 
 bool encode_tmap_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *base,
@@ -231,16 +247,12 @@ qmm_status qmm_gemv_q4_0_geglu(const void *wg, const void *wu, const float *x, f
 
 qmm_status qmm_gemm_q4_0(const void *w, const uint16_t *x_bf16, float *y, int64_t m, int64_t n,
                          int64_t k, qmm_stream_t stream) {
-    qmm_status s = check_wk(w, n, k);
-    if (s != QMM_OK) return s;
-    if (!x_bf16 || !y) return QMM_ERR_NULL;
-    if (m < 1 || m > (int64_t(1) << 31)) return QMM_ERR_SHAPE;
-    if (k % 256 != 0 || n % 4 != 0) return QMM_ERR_UNSUPPORTED;
-    if (!aligned(w, 16) || !aligned(x_bf16, 16) || !aligned(y, 16)) return QMM_ERR_ALIGN;
-    LaunchCtx ctx;
-    if (!make_ctx(&ctx)) return QMM_ERR_CUDA;
-    return from_cuda(launch_gemm_q4_0(static_cast<const uint8_t *>(w), x_bf16, y, m, n, k,
-                                      reinterpret_cast<cudaStream_t>(stream), ctx));
+    return gemm(Fmt::Q4_0, w, x_bf16, y, m, n, k, stream);
+}
+
+qmm_status qmm_gemm_q8_0(const void *w, const uint16_t *x_bf16, float *y, int64_t m, int64_t n,
+                         int64_t k, qmm_stream_t stream) {
+    return gemm(Fmt::Q8_0, w, x_bf16, y, m, n, k, stream);
 }
 
 qmm_status qmm_gemm_q4_0_geglu(const void *wg, const void *wu, const uint16_t *x_bf16,

@@ -75,8 +75,7 @@ constexpr int BT = 256;              // tokens per pair tile (MMA N); 128 per CT
 constexpr int BT_CTA = BT / 2;
 constexpr int BK = 64;               // K per stage (one 128-byte swizzle row of X)
 constexpr int UMMA_K = 16;           // K per tcgen05.mma (kind::f16)
-constexpr int RAW_K = 256;           // K per raw stage (8 Q4_0 blocks)
-constexpr int RAW_ROW_BYTES = 144;   // 8 blocks x 18 bytes
+constexpr int RAW_K = 256;           // K per raw stage (8 blocks)
 constexpr int STAGES = QMM_GEMM_STAGES;  // K stages in flight (X in shared memory, A in TMEM)
 constexpr int LOOKAHEAD_KK = QMM_GEMM_LOOKAHEAD_KK;
 // Stages are announced to the MMA thread in groups: one "full" barrier per
@@ -89,9 +88,28 @@ constexpr int GROUP = QMM_GEMM_GROUP;
 constexpr int NGROUPS = STAGES / GROUP;
 static_assert(STAGES % GROUP == 0, "whole groups in the ring");
 static_assert((256 / BK) % GROUP == 0, "k % 256 == 0 makes every tile a whole number of groups");
-constexpr int RAW_STAGES = QMM_GEMM_RAW_STAGES;
 constexpr int X_STAGE_BYTES = BT_CTA * BK * 2;           // 16 KB
-constexpr int RAW_STAGE_BYTES = BW * RAW_ROW_BYTES;      // 18 KB
+
+// Raw weight stages: 128 rows x 256 weights of block bytes, one TMA box.
+// Q4_0: 144-byte rows (18 KB a stage, three stages).  Q8_0: 272-byte rows
+// (34 KB, two stages, so that the CTA's shared memory still fits), loaded as
+// uint16 elements because a box dimension holds at most 256 elements.
+template <Fmt F>
+struct RawFmt;
+template <>
+struct RawFmt<Fmt::Q4_0> {
+    static constexpr int kRowBytes = 8 * kQ4_0Bytes;  // 144
+    static constexpr int kStages = QMM_GEMM_RAW_STAGES;
+    static constexpr int kElemBytes = 1;
+    static constexpr CUtensorMapDataType kType = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+};
+template <>
+struct RawFmt<Fmt::Q8_0> {
+    static constexpr int kRowBytes = 8 * kQ8_0Bytes;  // 272
+    static constexpr int kStages = 2;
+    static constexpr int kElemBytes = 2;
+    static constexpr CUtensorMapDataType kType = CU_TENSOR_MAP_DATA_TYPE_UINT16;
+};
 constexpr uint32_t D_COLS = BT;                          // fp32 accumulator columns
 constexpr uint32_t A_COLS = BK / 2;                      // bf16 pairs per row per stage
 constexpr uint32_t TMEM_COLS = 512;
@@ -112,19 +130,23 @@ constexpr int NUM_THREADS = (WARP_EPI0 + NUM_EPI_WARPS) * 32;  // 448 or 576
 
 static_assert(RAW_K % BK == 0 && BK == 2 * 32, "a K stage is two blocks");
 
+template <Fmt F>
 struct SmemLayout {
+    static constexpr int raw_stages = RawFmt<F>::kStages;
+    static constexpr int raw_stage_bytes = BW * RawFmt<F>::kRowBytes;
     static constexpr int x = 0;
     static constexpr int raw = x + STAGES * X_STAGE_BYTES;
-    static constexpr int bars = raw + RAW_STAGES * RAW_STAGE_BYTES;
+    static constexpr int bars = raw + raw_stages * raw_stage_bytes;
     // barriers: full [NGROUPS], empty [STAGES]; raw_full, raw_empty
-    // [RAW_STAGES]; d_full, d_empty, final
-    static constexpr int nbars = NGROUPS + STAGES + 2 * RAW_STAGES + 3;
+    // [raw_stages]; d_full, d_empty, final
+    static constexpr int nbars = NGROUPS + STAGES + 2 * raw_stages + 3;
     static constexpr int tmem_slot = bars + nbars * 8;
     static constexpr int abort_flag = tmem_slot + 4;
     static constexpr int total = abort_flag + 4;
+    static constexpr size_t smem_bytes = total + 1024;  // + alignment slack
 };
-constexpr size_t kSmemBytes = SmemLayout::total + 1024;  // + alignment slack
-static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+static_assert(SmemLayout<Fmt::Q4_0>::smem_bytes <= 232448, "shared memory per CTA");
+static_assert(SmemLayout<Fmt::Q8_0>::smem_bytes <= 232448, "shared memory per CTA");
 
 struct GemmParams {
     float *y;     // plain GEMM: fp32 [m][n]
@@ -441,7 +463,40 @@ __device__ __forceinline__ void dequant_words_bf16(const uint32_t (&wd)[36], int
     }
 }
 
+// Q8_0 byte with its top bit flipped (q + 128) in the mantissa of 2^23;
+// flip = 2^23's pattern with that byte's top bit set.  One LOP3.
+__device__ __forceinline__ float mag8(uint32_t v, uint32_t mask, uint32_t flip) {
+    return __uint_as_float((mask & (v ^ flip)) | (~mask & flip));
+}
 
+// Dequantise the Q8_0 block that starts `o` bytes into a 144-byte window held
+// in wd[36] (o % 4 is 0 or 2): d, then q[0..31] to 16 bf16 pairs in K order.
+// (2^23 + (q+128)*2^s) - (2^23 + 128*2^s) is q*2^s exactly; times d*2^-s it
+// is q*d exactly (an 8-bit by 11-bit product), rounded once to bf16.
+__device__ __forceinline__ void dequant_q8_block_bf16(const uint32_t (&wd)[36], int o,
+                                                      uint32_t flip0, uint32_t flip1,
+                                                      uint32_t (&out)[16]) {
+    const int base = o >> 2;
+    uint32_t dbits, q[8];
+    if ((o & 3) == 0) {  // d in the low half of word `base`, q from byte o + 2
+        dbits = wd[base] & 0xFFFFu;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) q[i] = __byte_perm(wd[base + i], wd[base + i + 1], 0x5432);
+    } else {  // d in the high half, q word-aligned
+        dbits = wd[base] >> 16;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) q[i] = wd[base + 1 + i];
+    }
+    const float d = half_bits_to_float(dbits);
+    const float2 c = make_float2(-8388736.0f, -8421376.0f);  // -(2^23 + 128*2^s), s = 0, 8
+    const float2 ds = make_float2(d, d * 0.00390625f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t v = q[i], u = v >> 16;
+        out[2 * i + 0] = w_pair(mag8(v, 0x000000FFu, flip0), mag8(v, 0x0000FF00u, flip1), c, ds);
+        out[2 * i + 1] = w_pair(mag8(u, 0x000000FFu, flip0), mag8(u, 0x0000FF00u, flip1), c, ds);
+    }
+}
 
 #ifndef QMM_GEMM_WAIT_CLUSTER
 #define QMM_GEMM_WAIT_CLUSTER 0
@@ -458,11 +513,17 @@ __device__ __forceinline__ void dequant_words_bf16(const uint32_t (&wd)[36], int
 // up rows of the same features, so lane l and lane l ^ 16 of an epilogue warp
 // meet with one shuffle and write h = gelu(g) * u as bf16.  A pair tile is
 // 128 features x 256 tokens.
-template <bool G>
+template <Fmt F, bool G>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-    gemm_q4_0_kernel(const __grid_constant__ CUtensorMap tmap_x,
-                     const __grid_constant__ CUtensorMap tmap_w,
-                     const __grid_constant__ CUtensorMap tmap_w2, GemmParams p) {
+    gemm_kernel(const __grid_constant__ CUtensorMap tmap_x,
+                const __grid_constant__ CUtensorMap tmap_w,
+                const __grid_constant__ CUtensorMap tmap_w2, GemmParams p) {
+    static_assert(!G || F == Fmt::Q4_0, "the GeGLU form is built for Q4_0 weights");
+    using SL = SmemLayout<F>;
+    constexpr int RAW_STAGES = SL::raw_stages;
+    constexpr int RAW_STAGE_BYTES = SL::raw_stage_bytes;
+    constexpr int RAW_ROW_BYTES = RawFmt<F>::kRowBytes;
+    constexpr int RAW_X = RAW_ROW_BYTES / RawFmt<F>::kElemBytes;  // TMA x extent of a raw stage
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_base = smem_addr(smem_raw);
     const uint32_t sbase = (raw_base + 1023u) & ~1023u;  // 1024-byte aligned (swizzle atoms)
@@ -476,7 +537,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int pair = static_cast<int>(blockIdx.x >> 1);
     const int num_pairs = static_cast<int>(gridDim.x >> 1);
 
-    auto bar = [&](int i) -> uint32_t { return sbase + SmemLayout::bars + 8u * i; };
+    auto bar = [&](int i) -> uint32_t { return sbase + SL::bars + 8u * i; };
     // full(g): leader only; for each stage of group g, both X producers
     // (expect_tx + bytes) and the 16 dequantiser warps of the pair.
     // empty(s): both CTAs; multicast commit once the stage's MMAs are done.
@@ -490,8 +551,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t d_full = bar(NGROUPS + STAGES + 2 * RAW_STAGES);       // both
     const uint32_t d_empty = bar(NGROUPS + STAGES + 2 * RAW_STAGES + 1);  // leader: 8
     const uint32_t final_bar = bar(NGROUPS + STAGES + 2 * RAW_STAGES + 2);
-    int *abort_flag = reinterpret_cast<int *>(sgen + SmemLayout::abort_flag);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sgen + SmemLayout::tmem_slot);
+    int *abort_flag = reinterpret_cast<int *>(sgen + SL::abort_flag);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sgen + SL::tmem_slot);
 
     if (threadIdx.x == 0) {
         for (int g = 0; g < NGROUPS; ++g) mbar_init_addr(bar(g), GROUP * (2 + 2 * NUM_DEQ_WARPS));
@@ -506,7 +567,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == WARP_MMA) tmem_alloc_pair(sbase + SmemLayout::tmem_slot, TMEM_COLS);
+    if (warp == WARP_MMA) tmem_alloc_pair(sbase + SL::tmem_slot, TMEM_COLS);
     tc_fence_before();
     __syncthreads();
     cluster_barrier();  // the peer's barriers exist before anyone signals them
@@ -534,7 +595,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (!wait_or_abort(empty(s), ph ^ 1u, abort_flag, ctx)) { ok = false; break; }
                     const uint32_t xf = map_to_rank(full(it), 0);
                     mbar_expect_tx_cluster(xf, X_STAGE_BYTES);
-                    tma_load_2d_pair(sbase + SmemLayout::x + s * X_STAGE_BYTES, &tmap_x, kb * BK, xrow, xf);
+                    tma_load_2d_pair(sbase + SL::x + s * X_STAGE_BYTES, &tmap_x, kb * BK, xrow, xf);
                     ++it;
                 }
             }
@@ -564,12 +625,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const uint32_t ph = (rit / RAW_STAGES) & 1u;
                     if (!wait_or_abort(raw_empty(r), ph ^ 1u, abort_flag, ctx)) { ok = false; break; }
                     mbar_expect_tx_addr(raw_full(r), RAW_STAGE_BYTES);
-                    tma_load_2d(sbase + SmemLayout::raw + r * RAW_STAGE_BYTES, &tmap_w, kr * RAW_ROW_BYTES,
+                    tma_load_2d(sbase + SL::raw + r * RAW_STAGE_BYTES, &tmap_w, kr * RAW_X,
                                 wrow, raw_full(r));
                     if constexpr (G)
-                        tma_load_2d(sbase + SmemLayout::raw + r * RAW_STAGE_BYTES +
+                        tma_load_2d(sbase + SL::raw + r * RAW_STAGE_BYTES +
                                         (BW / 2) * RAW_ROW_BYTES,
-                                    &tmap_w2, kr * RAW_ROW_BYTES, wrow, raw_full(r));
+                                    &tmap_w2, kr * RAW_X, wrow, raw_full(r));
                     ++rit;
                 }
             }
@@ -597,7 +658,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (kb == 0 && !wait_or_abort_cluster(d_empty, (tiles_done & 1u) ^ 1u, abort_flag, ctx))
                     break;
                 tc_fence_after();
-                const uint64_t bdesc = sw128_desc(sbase + SmemLayout::x + s * X_STAGE_BYTES);
+                const uint64_t bdesc = sw128_desc(sbase + SL::x + s * X_STAGE_BYTES);
                 const uint32_t a_tmem = tmem_base + a_col0 + s * A_COLS;
 #pragma unroll
                 for (int kk = 0; kk < BK / UMMA_K; ++kk) {
@@ -634,6 +695,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t full_leader0 = map_to_rank(bar(0), 0);
         const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + a_col0 +
                                    static_cast<uint32_t>(half * 16);
+        const uint32_t flip0 = p.magic | 0x80u, flip1 = p.magic | 0x8000u;  // Q8_0 decode
+        (void)flip0;
+        (void)flip1;
         uint32_t it = 0, rit = 0;
         bool ok = true;
         for (int t = pair; ok && t < p.num_tiles; t += num_pairs) {
@@ -643,41 +707,70 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     ok = false;
                     break;
                 }
-                uint32_t wd[36];
-                const uint8_t *src = sgen + SmemLayout::raw + r * RAW_STAGE_BYTES + row * RAW_ROW_BYTES;
+                // the row's block bytes in windows of 144 bytes (nine 16-byte
+                // reads; rows 144 or 272 bytes apart, so each 8-lane phase
+                // hits 32 distinct banks): Q4_0 one window for the four K
+                // stages, Q8_0 two (bytes 0..143 for K stages 0-1, 128..271
+                // for K stages 2-3)
+                constexpr int WINDOWS = F == Fmt::Q4_0 ? 1 : 2;
+                constexpr int SUBS = (RAW_K / BK) / WINDOWS;  // K stages per window
+                const uint8_t *src = sgen + SL::raw + r * RAW_STAGE_BYTES + row * RAW_ROW_BYTES;
 #pragma unroll
-                for (int qq = 0; qq < 9; ++qq) {
-                    const uint4 v = lds128(src + 16 * qq);
-                    wd[4 * qq + 0] = v.x;
-                    wd[4 * qq + 1] = v.y;
-                    wd[4 * qq + 2] = v.z;
-                    wd[4 * qq + 3] = v.w;
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive_addr(raw_empty(r));
-                ++rit;
+                for (int win = 0; win < WINDOWS; ++win) {
+                    uint32_t wd[36];
 #pragma unroll
-                for (int sub = 0; sub < RAW_K / BK; ++sub) {
-                    const int s = it % STAGES;
-                    if (!warp_wait_or_abort(empty(s), ((it / STAGES) & 1u) ^ 1u, abort_flag, ctx)) {
-                        ok = false;
-                        break;
+                    for (int qq = 0; qq < 9; ++qq) {
+                        const uint4 v = lds128(src + 128 * win + 16 * qq);
+                        wd[4 * qq + 0] = v.x;
+                        wd[4 * qq + 1] = v.y;
+                        wd[4 * qq + 2] = v.z;
+                        wd[4 * qq + 3] = v.w;
                     }
-                    tc_fence_after();
-                    uint4 ch[4];
-                    if (half == 0)
-                        dequant_words_bf16<0, 4>(wd, 2 * sub, p.magic, ch);
-                    else
-                        dequant_words_bf16<0, 4>(wd, 2 * sub + 1, p.magic, ch);
-                    const uint32_t v[16] = {ch[0].x, ch[0].y, ch[0].z, ch[0].w, ch[1].x, ch[1].y,
-                                            ch[1].z, ch[1].w, ch[2].x, ch[2].y, ch[2].z, ch[2].w,
-                                            ch[3].x, ch[3].y, ch[3].z, ch[3].w};
-                    tmem_st_16cols(lane_base + s * A_COLS, v);
-                    tmem_wait_st();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive_remote(full_leader0 + 8u * ((it / GROUP) % NGROUPS));
-                    ++it;
+                    if (win == WINDOWS - 1) {  // the raw stage is in registers
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive_addr(raw_empty(r));
+                        ++rit;
+                    }
+#pragma unroll
+                    for (int sub2 = 0; sub2 < SUBS; ++sub2) {
+                        const int sub = win * SUBS + sub2;
+                        const int s = it % STAGES;
+                        if (!warp_wait_or_abort(empty(s), ((it / STAGES) & 1u) ^ 1u, abort_flag, ctx)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        uint32_t v[16];
+                        if constexpr (F == Fmt::Q4_0) {
+                            uint4 ch[4];
+                            if (half == 0)
+                                dequant_words_bf16<0, 4>(wd, 2 * sub, p.magic, ch);
+                            else
+                                dequant_words_bf16<0, 4>(wd, 2 * sub + 1, p.magic, ch);
+#pragma unroll
+                            for (int c = 0; c < 4; ++c) {
+                                v[4 * c + 0] = ch[c].x;
+                                v[4 * c + 1] = ch[c].y;
+                                v[4 * c + 2] = ch[c].z;
+                                v[4 * c + 3] = ch[c].w;
+                            }
+                        } else {
+                            // block 2*sub + half starts 34*(2*sub + half) - 128*win
+                            // bytes into the window (a constant in each branch)
+                            const int o = 68 * sub - 128 * win;
+                            if (half == 0)
+                                dequant_q8_block_bf16(wd, o, flip0, flip1, v);
+                            else
+                                dequant_q8_block_bf16(wd, o + 34, flip0, flip1, v);
+                        }
+                        tmem_st_16cols(lane_base + s * A_COLS, v);
+                        tmem_wait_st();
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive_remote(full_leader0 + 8u * ((it / GROUP) % NGROUPS));
+                        ++it;
+                    }
+                    if (!ok) break;
                 }
             }
         }
@@ -752,7 +845,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 // One launch: plain GEMM (w2 == nullptr: y fp32) or the GeGLU form (w gate,
 // w2 up: h bf16).
-template <bool G>
+template <Fmt F, bool G>
 cudaError_t launch(const uint8_t *w, const uint8_t *w2, const uint16_t *x, float *y, uint16_t *h,
                    int64_t m, int64_t n, int64_t k, cudaStream_t stream, const LaunchCtx &ctx) {
     if (m > (1 << 30) || n > (1 << 30) || k > (1 << 24)) return cudaErrorInvalidValue;
@@ -760,14 +853,15 @@ cudaError_t launch(const uint8_t *w, const uint8_t *w2, const uint16_t *x, float
     if (!encode_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, k, m, k * 2, BK, BT_CTA,
                         CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-    const uint64_t rowbytes = static_cast<uint64_t>(k / kQK) * kQ4_0Bytes;
+    using RF = RawFmt<F>;
+    const uint64_t rowbytes = static_cast<uint64_t>(k / RAW_K) * RF::kRowBytes;
     constexpr uint32_t box_rows = G ? BW / 2 : BW;
-    if (!encode_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, rowbytes, n, rowbytes,
-                        RAW_ROW_BYTES, box_rows))
+    constexpr uint32_t box_x = RF::kRowBytes / RF::kElemBytes;
+    if (!encode_tmap_2d(&tw, RF::kType, w, rowbytes / RF::kElemBytes, n, rowbytes, box_x, box_rows))
         return cudaErrorInvalidValue;
     if (G) {
-        if (!encode_tmap_2d(&tw2, CU_TENSOR_MAP_DATA_TYPE_UINT8, w2, rowbytes, n, rowbytes,
-                            RAW_ROW_BYTES, box_rows))
+        if (!encode_tmap_2d(&tw2, RF::kType, w2, rowbytes / RF::kElemBytes, n, rowbytes, box_x,
+                            box_rows))
             return cudaErrorInvalidValue;
     } else {
         tw2 = tw;
@@ -785,25 +879,31 @@ cudaError_t launch(const uint8_t *w, const uint8_t *w2, const uint16_t *x, float
     p.num_tiles = p.num_t_blocks * nwb;
     p.magic = 0x4B000000u;
     p.ctx = ctx;
+    constexpr size_t smem = SmemLayout<F>::smem_bytes;
     static int smem_limits[kMaxDevices] = {0};
-    cudaError_t e = ensure_smem(gemm_q4_0_kernel<G>, kSmemBytes, true, smem_limits);
+    cudaError_t e = ensure_smem(gemm_kernel<F, G>, smem, true, smem_limits);
     if (e != cudaSuccess) return e;
     const int pairs = std::max(1, std::min(p.num_tiles, device_sm_count() / 2));
-    return launch_kernel(gemm_q4_0_kernel<G>, dim3(2 * pairs), dim3(NUM_THREADS), kSmemBytes,
-                         stream, 2, tx, tw, tw2, p);
+    return launch_kernel(gemm_kernel<F, G>, dim3(2 * pairs), dim3(NUM_THREADS), smem, stream, 2,
+                         tx, tw, tw2, p);
 }
 
 }  // namespace
 
 cudaError_t launch_gemm_q4_0(const uint8_t *w, const uint16_t *x, float *y, int64_t m, int64_t n,
                              int64_t k, cudaStream_t stream, const LaunchCtx &ctx) {
-    return launch<false>(w, nullptr, x, y, nullptr, m, n, k, stream, ctx);
+    return launch<Fmt::Q4_0, false>(w, nullptr, x, y, nullptr, m, n, k, stream, ctx);
+}
+
+cudaError_t launch_gemm_q8_0(const uint8_t *w, const uint16_t *x, float *y, int64_t m, int64_t n,
+                             int64_t k, cudaStream_t stream, const LaunchCtx &ctx) {
+    return launch<Fmt::Q8_0, false>(w, nullptr, x, y, nullptr, m, n, k, stream, ctx);
 }
 
 cudaError_t launch_gemm_q4_0_geglu(const uint8_t *wg, const uint8_t *wu, const uint16_t *x,
                                    uint16_t *h, int64_t m, int64_t n, int64_t k,
                                    cudaStream_t stream, const LaunchCtx &ctx) {
-    return launch<true>(wg, wu, x, nullptr, h, m, n, k, stream, ctx);
+    return launch<Fmt::Q4_0, true>(wg, wu, x, nullptr, h, m, n, k, stream, ctx);
 }
 
 }  // namespace qmm

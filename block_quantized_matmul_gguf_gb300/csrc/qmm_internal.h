@@ -147,6 +147,9 @@ inline cudaError_t launch_geglu_q4_0(const GemvProblem *gate_up, const float *x,
 cudaError_t launch_gemm_q4_0(const uint8_t *w, const uint16_t *x, float *y, int64_t m,
                              int64_t n, int64_t k, cudaStream_t stream, const LaunchCtx &ctx);
 
+cudaError_t launch_gemm_q8_0(const uint8_t *w, const uint16_t *x, float *y, int64_t m,
+                             int64_t n, int64_t k, cudaStream_t stream, const LaunchCtx &ctx);
+
 // Prefill GeGLU: h[i][j] = bf16(gelu(X[i] . wg[j]) * (X[i] . wu[j])).
 cudaError_t launch_gemm_q4_0_geglu(const uint8_t *wg, const uint8_t *wu, const uint16_t *x,
                                    uint16_t *h, int64_t m, int64_t n, int64_t k,

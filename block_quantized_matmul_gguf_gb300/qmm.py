@@ -29,7 +29,7 @@ QMM_GEMV_MAX_OUTPUTS = 4
 EXPORTED = (
     "qmm_dequant_q4_0", "qmm_dequant_q8_0", "qmm_gemv_q4_0", "qmm_gemv_q8_0",
     "qmm_gemv_q4_0_multi", "qmm_gemv_q8_0_multi", "qmm_gemv_q4_0_geglu",
-    "qmm_gemm_q4_0", "qmm_gemm_q4_0_geglu", "qmm_status_string", "qmm_version", "qmm_get_device_error",
+    "qmm_gemm_q4_0", "qmm_gemm_q8_0", "qmm_gemm_q4_0_geglu", "qmm_status_string", "qmm_version", "qmm_get_device_error",
     "qmm_set_wait_timeout_ns", "qmm_selftest_wait_timeout",
 )
 
@@ -70,6 +70,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         "qmm_gemv_q4_0": [P, P, P, I32, I64, I64, P],
         "qmm_gemv_q8_0": [P, P, P, I32, I64, I64, P],
         "qmm_gemm_q4_0": [P, P, P, I64, I64, I64, P],
+        "qmm_gemm_q8_0": [P, P, P, I64, I64, I64, P],
         "qmm_gemv_q4_0_geglu": [P, P, P, P, I32, I64, I64, P],
         "qmm_gemm_q4_0_geglu": [P, P, P, P, I64, I64, I64, P],
         "qmm_gemv_q4_0_multi": [ctypes.POINTER(GemvOut), I32, P, I32, I64, P],
@@ -176,6 +177,11 @@ def qmm_gemm_q4_0(w, x_bf16, y, m: int, n: int, k: int, stream=None) -> None:
            "qmm_gemm_q4_0")
 
 
+def qmm_gemm_q8_0(w, x_bf16, y, m: int, n: int, k: int, stream=None) -> None:
+    _check(load().qmm_gemm_q8_0(_ptr(w), _ptr(x_bf16), _ptr(y), m, n, k, _stream(stream)),
+           "qmm_gemm_q8_0")
+
+
 def qmm_gemm_q4_0_geglu(wg, wu, x_bf16, h_bf16, m: int, n: int, k: int, stream=None) -> None:
     """h (bf16) = gelu_tanh(X . wg^T) * (X . wu^T) on the tensor cores, one launch."""
     _check(load().qmm_gemm_q4_0_geglu(_ptr(wg), _ptr(wu), _ptr(x_bf16), _ptr(h_bf16), m, n, k,
@@ -219,6 +225,14 @@ def geglu_q4_0(wg, wu, x, n: int, k: int, stream=None):
     h = torch.empty((m, n), dtype=torch.float32, device=x.device)
     qmm_gemv_q4_0_geglu(wg, wu, x, h, m, n, k, stream)
     return h
+
+
+def gemm(fmt: str, w, x_bf16, n: int, k: int, stream=None):
+    import torch
+    m = x_bf16.shape[0]
+    y = torch.empty((m, n), dtype=torch.float32, device=x_bf16.device)
+    (qmm_gemm_q4_0 if fmt == "q4_0" else qmm_gemm_q8_0)(w, x_bf16, y, m, n, k, stream)
+    return y
 
 
 def gemm_geglu_q4_0(wg, wu, x_bf16, n: int, k: int, stream=None):

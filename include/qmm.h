@@ -148,6 +148,13 @@ qmm_status qmm_gemv_q4_0_geglu(const void *wg, const void *wu, const float *x, f
 qmm_status qmm_gemm_q4_0(const void *w, const uint16_t *x_bf16, float *y, int64_t m,
                          int64_t n, int64_t k, qmm_stream_t stream);
 
+/* The same product for Q8_0 weights (each w = q*d, exact in fp32, rounded
+ * once to bf16), with the same requirements, layout and accuracy bound.
+ * Q8_0 at prefill: the weight format of the LM head ("Validation" of the
+ * quant-kernel JIT page) when every prompt position's logits are wanted. */
+qmm_status qmm_gemm_q8_0(const void *w, const uint16_t *x_bf16, float *y, int64_t m,
+                         int64_t n, int64_t k, qmm_stream_t stream);
+
 /* ---- Prefill GeGLU (tcgen05 tensor cores) -----------------------------
  * h[i][j] = bf16(gelu(g[i][j]) * u[i][j]) with g[i][j] = sum_k X[i][k] *
  * wg[j][k] and u[i][j] = sum_k X[i][k] * wu[j][k], for i < m, j < n: the
