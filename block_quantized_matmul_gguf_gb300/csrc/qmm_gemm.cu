@@ -119,14 +119,22 @@ static_assert(LOOKAHEAD_KK >= 0 && LOOKAHEAD_KK < BK / 16, "look-ahead point wit
 constexpr int WARP_PRODUCER = 0;
 constexpr int WARP_MMA = 1;
 constexpr int WARP_DEQ0 = 2;
-constexpr int NUM_DEQ_WARPS = 8;                     // 4 lane quarters x 2 blocks per stage
-constexpr int WARP_EPI0 = WARP_DEQ0 + NUM_DEQ_WARPS;  // 10
+constexpr int DEQ_PER_STAGE = 8;  // warps writing one K stage: 4 lane quarters x 2 blocks
+#ifndef QMM_GEMM_DEQ_PHASES
+#define QMM_GEMM_DEQ_PHASES 1
+#endif
+// 1: one set of dequantiser warps writes every K stage; 2: two sets take
+// alternate K stages, so that one set's latency overlaps the other's work
+constexpr int DEQ_PHASES = QMM_GEMM_DEQ_PHASES;
+static_assert(DEQ_PHASES == 1 || DEQ_PHASES == 2, "dequantiser phases");
+constexpr int NUM_DEQ_WARPS = DEQ_PER_STAGE * DEQ_PHASES;
+constexpr int WARP_EPI0 = WARP_DEQ0 + NUM_DEQ_WARPS;  // 10 or 18
 #ifndef QMM_GEMM_EPI_WARPS
 #define QMM_GEMM_EPI_WARPS 8
 #endif
 constexpr int NUM_EPI_WARPS = QMM_GEMM_EPI_WARPS;  // 4 or 8: one or two per lane quarter
 static_assert(NUM_EPI_WARPS == 4 || NUM_EPI_WARPS == 8, "epilogue warps");
-constexpr int NUM_THREADS = (WARP_EPI0 + NUM_EPI_WARPS) * 32;  // 448 or 576
+constexpr int NUM_THREADS = (WARP_EPI0 + NUM_EPI_WARPS) * 32;  // 448 .. 832
 
 static_assert(RAW_K % BK == 0 && BK == 2 * 32, "a K stage is two blocks");
 
@@ -306,13 +314,38 @@ __device__ __forceinline__ bool abort_set(const int *flag) {
     return *reinterpret_cast<const volatile int *>(flag) != 0;
 }
 
+// try_wait with a suspend-time hint: the thread may sleep up to `ns`
+// nanoseconds (instead of the system's default limit) unless the phase
+// completes first, so that a waiting warp takes fewer issue slots.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar_addr, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; "
+        "selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(bar_addr), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
+#ifndef QMM_GEMM_SUSPEND_NS
+#define QMM_GEMM_SUSPEND_NS 0      // suspend hint of the pipeline waits (0: default limit)
+#endif
+#ifndef QMM_GEMM_EPI_SUSPEND_NS
+#define QMM_GEMM_EPI_SUSPEND_NS 0  // suspend hint of the epilogue's accumulator wait
+#endif
+
 // Bounded wait that also gives up as soon as another role has aborted.
+template <uint32_t HINT = QMM_GEMM_SUSPEND_NS>
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, int *flag,
                                               const LaunchCtx &ctx) {
-    if (mbar_try_wait(bar, parity)) return true;
+    auto try_once = [&]() {
+        return HINT ? mbar_try_wait_hint(bar, parity, HINT) : mbar_try_wait(bar, parity);
+    };
+    if (try_once()) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 0; it < (1u << 30); ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (try_once()) return true;
         if ((it & 15u) == 15u) {
             if (abort_set(flag)) return false;
             if (global_timer_ns() - t0 > ctx.timeout_ns) break;
@@ -353,9 +386,10 @@ __device__ __forceinline__ bool wait_or_abort_cluster(uint32_t bar, uint32_t par
 
 // Warp-wide form: every lane polls, and the warp agrees on the outcome so
 // that the following __syncwarp / .sync.aligned instructions stay uniform.
+template <uint32_t HINT = QMM_GEMM_SUSPEND_NS>
 __device__ __forceinline__ bool warp_wait_or_abort(uint32_t bar, uint32_t parity, int *flag,
                                                    const LaunchCtx &ctx) {
-    const bool ok = wait_or_abort(bar, parity, flag, ctx);
+    const bool ok = wait_or_abort<HINT>(bar, parity, flag, ctx);
     return __all_sync(0xFFFFFFFFu, ok);
 }
 
@@ -555,7 +589,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sgen + SL::tmem_slot);
 
     if (threadIdx.x == 0) {
-        for (int g = 0; g < NGROUPS; ++g) mbar_init_addr(bar(g), GROUP * (2 + 2 * NUM_DEQ_WARPS));
+        for (int g = 0; g < NGROUPS; ++g) mbar_init_addr(bar(g), GROUP * (2 + 2 * DEQ_PER_STAGE));
         for (int s = 0; s < STAGES; ++s) mbar_init_addr(empty(s), 1);
         for (int r = 0; r < RAW_STAGES; ++r) {
             mbar_init_addr(raw_full(r), 1);
@@ -645,36 +679,52 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (leader && lane == 0) {
             // one flat sequence of K stages over this pair's tiles; the wait
             // for stage g+1 is placed after MMA LOOKAHEAD_KK of stage g, so
-            // that its latency overlaps the MMAs still queued in the pipe
+            // that its latency overlaps the MMAs still queued in the pipe.
+            // This thread shares its scheduler with two dequantiser warps, so
+            // its path between MMAs is kept short: the K stage, ring slot,
+            // descriptors and barrier addresses are advanced incrementally
+            // (no run-time division), which measured as the pipeline's pace.
             const uint32_t my_tiles =
                 pair < p.num_tiles ? static_cast<uint32_t>((p.num_tiles - pair + num_pairs - 1) / num_pairs) : 0u;
             const uint32_t total = my_tiles * static_cast<uint32_t>(KB);
+            const uint64_t bdesc0 = sw128_desc(sbase + SL::x);
+            const uint32_t a0 = tmem_base + a_col0;
+            const uint32_t empty0 = empty(0);
             uint32_t tiles_done = 0;
             bool issued = false;
             bool ok = total == 0 || MMA_WAIT(full(0u), 0u, abort_flag, ctx);
+            uint32_t kb = 0, s = 0;   // K stage within the tile, ring slot
+            uint64_t bdesc = bdesc0;  // B (X) descriptor of slot s
+            uint32_t a_tmem = a0;     // A columns of slot s
             for (uint32_t g = 0; ok && g < total; ++g) {
-                const uint32_t kb = g % static_cast<uint32_t>(KB);
-                const int s = static_cast<int>(g % STAGES);
                 if (kb == 0 && !wait_or_abort_cluster(d_empty, (tiles_done & 1u) ^ 1u, abort_flag, ctx))
                     break;
                 tc_fence_after();
-                const uint64_t bdesc = sw128_desc(sbase + SL::x + s * X_STAGE_BYTES);
-                const uint32_t a_tmem = tmem_base + a_col0 + s * A_COLS;
+                const bool group_end = (g & (GROUP - 1)) == GROUP - 1 && g + 1 < total;
 #pragma unroll
                 for (int kk = 0; kk < BK / UMMA_K; ++kk) {
                     // K step kk: 8 TMEM columns of A, 32 bytes along the swizzle row of B
                     umma_bf16_pair_ta(tmem_base, a_tmem + (UMMA_K / 2) * kk, bdesc + 2 * kk, kIdesc,
-                                      (kb | static_cast<uint32_t>(kk)) != 0 ? 1u : 0u);
-                    if (kk == LOOKAHEAD_KK && (g + 1) % GROUP == 0 && g + 1 < total) {
+                                      (kk != 0 || kb != 0) ? 1u : 0u);
+                    if (kk == LOOKAHEAD_KK && group_end) {
                         const uint32_t g1 = g + 1;  // first stage of the next group
                         ok = MMA_WAIT(full(g1), (g1 / STAGES) & 1u, abort_flag, ctx);
                     }
                 }
                 issued = true;
-                umma_commit_pair(empty(s));
-                if (kb + 1 == static_cast<uint32_t>(KB)) {
+                umma_commit_pair(empty0 + 8u * s);
+                if (++kb == static_cast<uint32_t>(KB)) {
                     umma_commit_pair(d_full);
                     ++tiles_done;
+                    kb = 0;
+                }
+                if (++s == STAGES) {
+                    s = 0;
+                    bdesc = bdesc0;
+                    a_tmem = a0;
+                } else {
+                    bdesc += X_STAGE_BYTES >> 4;  // descriptor start address in 16-byte units
+                    a_tmem += A_COLS;
                 }
             }
             if (issued) {  // all MMAs of the pair complete before TMEM is freed
@@ -684,9 +734,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
     } else if (warp < WARP_EPI0) {
         // dequantisers: warp w writes TMEM lanes 32*(w%4)..+31 (its weight rows)
-        // and block `half` (K 32*half..+31) of every 64-wide K stage
+        // and block `half` (K 32*half..+31) of every 64-wide K stage of its
+        // phase (every stage, or every other with two sets of warps); `it`
+        // counts all K stages, so that slots and parities match the MMA's
         const int q = warp & 3;
-        const int half = (warp - WARP_DEQ0) >> 2;  // warp-uniform
+        const int half = ((warp - WARP_DEQ0) >> 2) & 1;            // warp-uniform
+        const int phase = (warp - WARP_DEQ0) / DEQ_PER_STAGE;        // K stages it % DEQ_PHASES
         // weight row of the raw stage written to TMEM lane 32q + lane; G: gate
         // rows of features 16q.. in lanes 0-15, their up rows (stage rows
         // 64..) in lanes 16-31 (each 8-lane phase of the 16-byte reads still
@@ -734,6 +787,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                     for (int sub2 = 0; sub2 < SUBS; ++sub2) {
                         const int sub = win * SUBS + sub2;
+                        if (DEQ_PHASES > 1 && (sub & (DEQ_PHASES - 1)) != phase) {
+                            ++it;  // K stage written by the other set of warps
+                            continue;
+                        }
                         const int s = it % STAGES;
                         if (!warp_wait_or_abort(empty(s), ((it / STAGES) & 1u) ^ 1u, abort_flag, ctx)) {
                             ok = false;
@@ -783,7 +840,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint32_t tiles_done = 0;
         for (int t = pair; t < p.num_tiles; t += num_pairs) {
             const int tb = t % p.num_t_blocks, wb = t / p.num_t_blocks;
-            if (!warp_wait_or_abort(d_full, tiles_done & 1u, abort_flag, ctx)) break;
+            if (!warp_wait_or_abort<QMM_GEMM_EPI_SUSPEND_NS>(d_full, tiles_done & 1u, abort_flag, ctx)) break;
             tc_fence_after();
             if constexpr (G) {
                 const bool upper = lane >= 16;  // holds the up row; takes columns 16..31
