@@ -67,7 +67,7 @@ def parse_args(argv=None):
                     help="no timing: run CASE a few times for a profiler and exit. CASE is "
                          "decode_grouped (the timed decode step), decode (seven separate calls), "
                          "gemv:FMT:M:N:K, geglu:M:N:K, gemm_geglu:M:N:K, dequant:FMT:N:K "
-                         "gemm:M:N:K or gemm_q8_0:M:N:K")
+                         "gemm:M:N:K, gemm_ws:M:N:K (two-phase) or gemm_q8_0:M:N:K")
     ap.add_argument("--profile-launches", type=int, default=3)
     return ap.parse_args(argv)
 
@@ -135,6 +135,14 @@ def run_profile(args):
         X = torch.from_numpy(xb.astype(np.int16)).to(dev)
         for _ in range(reps):
             qmm.gemm_q4_0(W, X, n, k)
+    elif parts[0] == "gemm_ws":
+        m, n, k = int(parts[1]), int(parts[2]), int(parts[3])
+        w, xb = synth.gemm_case(m, n, k, seed=0, stream=1)
+        W = torch.from_numpy(w).to(dev)
+        X = torch.from_numpy(xb.astype(np.int16)).to(dev)
+        WS = torch.empty(qmm.qmm_gemm_workspace_bytes(n, k), dtype=torch.uint8, device=dev)
+        for _ in range(reps):
+            qmm.gemm("q4_0", W, X, n, k, workspace=WS)
     elif parts[0] == "gemm_q8_0":
         m, n, k = int(parts[1]), int(parts[2]), int(parts[3])
         W = torch.from_numpy(synth.q8_0_weights(n, k, seed=0, stream=75)).to(dev)
@@ -499,92 +507,85 @@ def measure_geglu(torch, qmm, l2, stream, timer, hbm, ffn, m):
 
 
 def measure_gemm(torch, qmm, l2, stream, timer, peaks):
+    """Prefill GEMMs: median of 20 launches, L2 flushed before each.  Each
+    product is timed fused (one kernel, no workspace) and two-phase (weights
+    dequantised once into a bf16 workspace, then the shared-memory-operand
+    GEMM; both kernels inside the timed region)."""
     res = {}
     dev = torch.device("cuda")
-    for i, p in enumerate(synth.PREFILL_SHAPES):
-        m = synth.PREFILL_M
-        w, xb = synth.gemm_case(m, p.n, p.k, seed=0, stream=70 + i)
-        W = torch.from_numpy(w.reshape(-1)).to(dev)
-        X = torch.from_numpy(xb.astype(np.int16)).to(dev)
-        Y = torch.empty((m, p.n), dtype=torch.float32, device=dev)
-        flush = torch.empty(2 * l2 // 4, dtype=torch.float32, device=dev)
-        s = stream.cuda_stream
+    flush = torch.empty(2 * l2 // 4, dtype=torch.float32, device=dev)
+    gf = capture(torch, stream, lambda: flush.add_(1.0))
+    s = stream.cuda_stream
+    peak = peaks["bf16_tflops"]
 
-        def call():
-            qmm.qmm_gemm_q4_0(W, X, Y, m, p.n, p.k, s)
-
+    def timed(call):
         g = capture(torch, stream, call)
-        gf = capture(torch, stream, lambda: flush.add_(1.0))
         times = []
         for _ in range(20):
             gf.replay()
             times.append(timer.run(g.replay))
-        t = statistics.median(times)
-        q = statistics.quantiles(times, n=10)
+        return statistics.median(times), statistics.quantiles(times, n=10)
+
+    def entry(name, flops, t, q=None, **extra):
+        e = {"tflops": round(flops / t / 1e12, 1), "frac_bf16_peak": round(flops / t / 1e12 / peak, 4),
+             "us": round(t * 1e6, 2)}
+        if q is not None:
+            e.update(us_p10=round(q[0] * 1e6, 2), us_p90=round(q[-1] * 1e6, 2))
+        e.update(extra)
+        e.setdefault("l2", "flushed (2x L2 write) before each timed launch")
+        res[name] = e
+
+    m = synth.PREFILL_M
+    for i, p in enumerate(synth.PREFILL_SHAPES):
+        w, xb = synth.gemm_case(m, p.n, p.k, seed=0, stream=70 + i)
+        W = torch.from_numpy(w.reshape(-1)).to(dev)
+        X = torch.from_numpy(xb.astype(np.int16)).to(dev)
+        Y = torch.empty((m, p.n), dtype=torch.float32, device=dev)
+        WS = torch.empty(qmm.qmm_gemm_workspace_bytes(p.n, p.k), dtype=torch.uint8, device=dev)
         flops = 2.0 * m * p.n * p.k
-        tfl = flops / t / 1e12
-        res[f"q4_0_gemm_{m}x{p.n}x{p.k}"] = {
-            "tflops": round(tfl, 1), "frac_bf16_peak": round(tfl / peaks["bf16_tflops"], 4),
-            "us": round(t * 1e6, 2), "us_p10": round(q[0] * 1e6, 2), "us_p90": round(q[-1] * 1e6, 2),
-            "l2": "flushed (2x L2 write) before each timed launch"}
+        t, q = timed(lambda: qmm.qmm_gemm_q4_0(W, X, Y, m, p.n, p.k, s))
+        entry(f"q4_0_gemm_{m}x{p.n}x{p.k}", flops, t, q, path="fused")
+        t, q = timed(lambda: qmm.qmm_gemm_q4_0_ws(W, X, Y, m, p.n, p.k, WS, WS.numel(), s))
+        entry(f"q4_0_gemm_two_phase_{m}x{p.n}x{p.k}", flops, t, q,
+              path="dequant to bf16 workspace + shared-memory-operand GEMM")
         # practical ceiling of the same contraction: cuBLAS bf16 with the
         # weights already dense bf16 (no dequantization), same flush and timing
         Wd = torch.randn((p.n, p.k), device=dev).to(torch.bfloat16)
         Xd = torch.randn((m, p.k), device=dev).to(torch.bfloat16)
-        gc = capture(torch, stream, lambda: torch.matmul(Xd, Wd.t()))
-        tc = []
-        for _ in range(20):
-            gf.replay()
-            tc.append(timer.run(gc.replay))
-        tcm = statistics.median(tc)
-        res[f"cublas_bf16_dense_{m}x{p.n}x{p.k}"] = {
-            "tflops": round(flops / tcm / 1e12, 1),
-            "frac_bf16_peak": round(flops / tcm / 1e12 / peaks["bf16_tflops"], 4),
-            "us": round(tcm * 1e6, 2),
-            "what": "torch.matmul bf16 x bf16 -> bf16 of dense weights: a practical ceiling, not this library"}
-        del Wd, Xd, gc
-    # Q8_0 weights through the same kernel (the 8192 x 2048 shape)
+        t, _ = timed(lambda: torch.matmul(Xd, Wd.t()))
+        entry(f"cublas_bf16_dense_{m}x{p.n}x{p.k}", flops, t,
+              what="torch.matmul bf16 x bf16 -> bf16 of dense weights: a practical ceiling, not this library")
+        del Wd, Xd, W, Y, WS
+    # Q8_0 weights (the 8192 x 2048 shape)
     p = synth.PREFILL_SHAPES[0]
-    m = synth.PREFILL_M
     W8 = torch.from_numpy(synth.q8_0_weights(p.n, p.k, seed=0, stream=75).reshape(-1)).to(dev)
     X = torch.from_numpy(synth.activations_bf16(m, p.k, seed=0, stream=76).astype(np.int16)).to(dev)
     Y = torch.empty((m, p.n), dtype=torch.float32, device=dev)
-    s = stream.cuda_stream
-    g = capture(torch, stream, lambda: qmm.qmm_gemm_q8_0(W8, X, Y, m, p.n, p.k, s))
-    times = []
-    for _ in range(20):
-        gf.replay()
-        times.append(timer.run(g.replay))
-    t = statistics.median(times)
+    WS = torch.empty(qmm.qmm_gemm_workspace_bytes(p.n, p.k), dtype=torch.uint8, device=dev)
     flops = 2.0 * m * p.n * p.k
-    res[f"q8_0_gemm_{m}x{p.n}x{p.k}"] = {
-        "tflops": round(flops / t / 1e12, 1),
-        "frac_bf16_peak": round(flops / t / 1e12 / peaks["bf16_tflops"], 4),
-        "us": round(t * 1e6, 2), "l2": "flushed (2x L2 write) before each timed launch"}
-    del W8, Y
+    t, _ = timed(lambda: qmm.qmm_gemm_q8_0(W8, X, Y, m, p.n, p.k, s))
+    entry(f"q8_0_gemm_{m}x{p.n}x{p.k}", flops, t, path="fused")
+    t, _ = timed(lambda: qmm.qmm_gemm_q8_0_ws(W8, X, Y, m, p.n, p.k, WS, WS.numel(), s))
+    entry(f"q8_0_gemm_two_phase_{m}x{p.n}x{p.k}", flops, t,
+          path="dequant to bf16 workspace + shared-memory-operand GEMM")
+    del W8, Y, WS
     # prefill GeGLU: the 8192 x 2048 gate/up pair over the same prompt, h bf16
     gate = next(p for p in synth.DECODE_LAYER if p.name == "gate")
-    m, n, k = synth.PREFILL_M, gate.n, gate.k
+    n, k = gate.n, gate.k
     wg, xb = synth.gemm_case(m, n, k, seed=0, stream=80)
     wu = synth.q4_0_weights(n, k, seed=0, stream=81)
     WG, WU = torch.from_numpy(wg.reshape(-1)).to(dev), torch.from_numpy(wu.reshape(-1)).to(dev)
     X = torch.from_numpy(xb.astype(np.int16)).to(dev)
     H = torch.empty((m, n), dtype=torch.int16, device=dev)
-    s = stream.cuda_stream
-    g = capture(torch, stream, lambda: qmm.qmm_gemm_q4_0_geglu(WG, WU, X, H, m, n, k, s))
-    times = []
-    for _ in range(20):
-        gf.replay()
-        times.append(timer.run(g.replay))
-    t = statistics.median(times)
+    WS = torch.empty(qmm.qmm_gemm_workspace_bytes(n, k, geglu=True), dtype=torch.uint8, device=dev)
     flops = 2.0 * m * (2 * n) * k
-    res[f"q4_0_gemm_geglu_{m}x{n}x{k}"] = {
-        "tflops": round(flops / t / 1e12, 1),
-        "frac_bf16_peak": round(flops / t / 1e12 / peaks["bf16_tflops"], 4),
-        "us": round(t * 1e6, 2),
-        "what": "h = bf16(gelu_tanh(X.Wg^T) * (X.Wu^T)), gate and up %dx%d Q4_0, one launch; "
-                "flops count both products" % (n, k),
-        "l2": "flushed (2x L2 write) before each timed launch"}
+    what = ("h = bf16(gelu_tanh(X.Wg^T) * (X.Wu^T)), gate and up %dx%d Q4_0; flops count both "
+            "products" % (n, k))
+    t, _ = timed(lambda: qmm.qmm_gemm_q4_0_geglu(WG, WU, X, H, m, n, k, s))
+    entry(f"q4_0_gemm_geglu_{m}x{n}x{k}", flops, t, what=what, path="fused")
+    t, _ = timed(lambda: qmm.qmm_gemm_q4_0_geglu_ws(WG, WU, X, H, m, n, k, WS, WS.numel(), s))
+    entry(f"q4_0_gemm_geglu_two_phase_{m}x{n}x{k}", flops, t, what=what,
+          path="dequant to bf16 workspace + shared-memory-operand GEMM")
     return res
 
 

@@ -122,18 +122,41 @@ qmm_status gemv(Fmt fmt, const qmm_gemv_out *outs, int count, const float *x, in
                                  reinterpret_cast<cudaStream_t>(stream), ctx));
 }
 
+// Prompts longer than this take the two-phase path when a workspace is given.
+constexpr int64_t kTwoPhaseMinM = QMM_GEMM_TWO_PHASE_MIN_M;
+
+qmm_status check_workspace(const void *ws, size_t ws_bytes, size_t need) {
+    if (!aligned(ws, 16)) return QMM_ERR_ALIGN;
+    if (ws_bytes < need) return QMM_ERR_SHAPE;
+    return QMM_OK;
+}
+
 qmm_status gemm(Fmt fmt, const void *w, const uint16_t *x_bf16, float *y, int64_t m, int64_t n,
-                int64_t k, qmm_stream_t stream) {
+                int64_t k, qmm_stream_t stream, void *ws = nullptr, size_t ws_bytes = 0) {
     qmm_status s = check_wk(w, n, k);
     if (s != QMM_OK) return s;
     if (!x_bf16 || !y) return QMM_ERR_NULL;
     if (m < 1 || m > (int64_t(1) << 31)) return QMM_ERR_SHAPE;
     if (k % 256 != 0 || n % 4 != 0) return QMM_ERR_UNSUPPORTED;
     if (!aligned(w, 16) || !aligned(x_bf16, 16) || !aligned(y, 16)) return QMM_ERR_ALIGN;
+    const bool two_phase = ws != nullptr && m > kTwoPhaseMinM;
+    if (two_phase) {
+        const size_t need = gemm_workspace_bytes(n, k, false);
+        s = check_workspace(ws, ws_bytes, need);
+        if (s != QMM_OK) return s;
+        const size_t wbytes = static_cast<size_t>(n) * (k / kQK) * block_bytes(fmt);
+        const size_t ybytes = sizeof(float) * static_cast<size_t>(m) * n;
+        if (overlaps(ws, need, w, wbytes) || overlaps(ws, need, x_bf16, 2 * static_cast<size_t>(m) * k) ||
+            overlaps(ws, need, y, ybytes))
+            return QMM_ERR_UNSUPPORTED;
+    }
     LaunchCtx ctx;
     if (!make_ctx(&ctx)) return QMM_ERR_CUDA;
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const uint8_t *wb = static_cast<const uint8_t *>(w);
+    if (two_phase)
+        return from_cuda(launch_gemm_two_phase(fmt, wb, x_bf16, y, m, n, k,
+                                               static_cast<uint16_t *>(ws), st, ctx));
     return from_cuda(fmt == Fmt::Q4_0 ? launch_gemm_q4_0(wb, x_bf16, y, m, n, k, st, ctx)
                                       : launch_gemm_q8_0(wb, x_bf16, y, m, n, k, st, ctx));
 }
@@ -255,9 +278,37 @@ qmm_status qmm_gemm_q8_0(const void *w, const uint16_t *x_bf16, float *y, int64_
     return gemm(Fmt::Q8_0, w, x_bf16, y, m, n, k, stream);
 }
 
+size_t qmm_gemm_workspace_bytes(int64_t n, int64_t k) {
+    if (n < 1 || k < 1) return 0;
+    return gemm_workspace_bytes(n, k, false);
+}
+
+size_t qmm_gemm_geglu_workspace_bytes(int64_t n, int64_t k) {
+    if (n < 1 || k < 1) return 0;
+    return gemm_workspace_bytes(n, k, true);
+}
+
+qmm_status qmm_gemm_q4_0_ws(const void *w, const uint16_t *x_bf16, float *y, int64_t m, int64_t n,
+                            int64_t k, void *workspace, size_t workspace_bytes,
+                            qmm_stream_t stream) {
+    return gemm(Fmt::Q4_0, w, x_bf16, y, m, n, k, stream, workspace, workspace_bytes);
+}
+
+qmm_status qmm_gemm_q8_0_ws(const void *w, const uint16_t *x_bf16, float *y, int64_t m, int64_t n,
+                            int64_t k, void *workspace, size_t workspace_bytes,
+                            qmm_stream_t stream) {
+    return gemm(Fmt::Q8_0, w, x_bf16, y, m, n, k, stream, workspace, workspace_bytes);
+}
+
 qmm_status qmm_gemm_q4_0_geglu(const void *wg, const void *wu, const uint16_t *x_bf16,
                                uint16_t *h_bf16, int64_t m, int64_t n, int64_t k,
                                qmm_stream_t stream) {
+    return qmm_gemm_q4_0_geglu_ws(wg, wu, x_bf16, h_bf16, m, n, k, nullptr, 0, stream);
+}
+
+qmm_status qmm_gemm_q4_0_geglu_ws(const void *wg, const void *wu, const uint16_t *x_bf16,
+                                  uint16_t *h_bf16, int64_t m, int64_t n, int64_t k,
+                                  void *workspace, size_t workspace_bytes, qmm_stream_t stream) {
     qmm_status s = check_wk(wg, n, k);
     if (s == QMM_OK) s = check_wk(wu, n, k);
     if (s != QMM_OK) return s;
@@ -271,11 +322,27 @@ qmm_status qmm_gemm_q4_0_geglu(const void *wg, const void *wu, const uint16_t *x
     if (overlaps(h_bf16, hbytes, x_bf16, sizeof(uint16_t) * static_cast<size_t>(m) * k) ||
         overlaps(h_bf16, hbytes, wg, wbytes) || overlaps(h_bf16, hbytes, wu, wbytes))
         return QMM_ERR_UNSUPPORTED;
+    const bool two_phase = workspace != nullptr && m > kTwoPhaseMinM;
+    if (two_phase) {
+        const size_t need = gemm_workspace_bytes(n, k, true);
+        s = check_workspace(workspace, workspace_bytes, need);
+        if (s != QMM_OK) return s;
+        if (overlaps(workspace, need, wg, wbytes) || overlaps(workspace, need, wu, wbytes) ||
+            overlaps(workspace, need, x_bf16, sizeof(uint16_t) * static_cast<size_t>(m) * k) ||
+            overlaps(workspace, need, h_bf16, hbytes))
+            return QMM_ERR_UNSUPPORTED;
+    }
     LaunchCtx ctx;
     if (!make_ctx(&ctx)) return QMM_ERR_CUDA;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (two_phase)
+        return from_cuda(launch_gemm_geglu_two_phase(static_cast<const uint8_t *>(wg),
+                                                     static_cast<const uint8_t *>(wu), x_bf16,
+                                                     h_bf16, m, n, k,
+                                                     static_cast<uint16_t *>(workspace), st, ctx));
     return from_cuda(launch_gemm_q4_0_geglu(static_cast<const uint8_t *>(wg),
                                             static_cast<const uint8_t *>(wu), x_bf16, h_bf16, m, n,
-                                            k, reinterpret_cast<cudaStream_t>(stream), ctx));
+                                            k, st, ctx));
 }
 
 const char *qmm_status_string(qmm_status status) {

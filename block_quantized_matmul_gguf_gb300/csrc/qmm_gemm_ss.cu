@@ -1,0 +1,434 @@
+// qmm_gemm_ss.cu -- prefill GEMM in two phases for long prompts: the weights
+// are dequantised once into a caller-provided bf16 workspace, then a
+// tensor-core GEMM reads both operands from shared memory.
+//
+// Why: the fused kernel (qmm_gemm.cu) dequantises a weight tile again for
+// every 256-token block, so at M = 2048 each weight is decoded eight times
+// and that integer/fp32 load on the MMA's SMs sets the pipeline's pace (a
+// per-role clock trace showed the MMA-issuing thread slowed by it).  Here the
+// decode runs once per call (an HBM-bound pass: 0.5625 bytes read and 2
+// bytes written per weight, the written copy mostly staying in L2), and the
+// GEMM SMs only move tiles and issue MMAs.
+//
+// Phase 1, dequant_bf16_kernel: one thread per 32-weight block writes
+// bf16((nibble-8)*d) (Q4_0) or bf16(q*d) (Q8_0), each the exact fp32 product
+// rounded once to nearest even -- the same weights the fused kernel forms.
+// GeGLU form: workspace rows are ordered so that each 128-row CTA tile holds,
+// per 32-row lane quarter, 16 gate rows then the 16 up rows of the same
+// features (the order the epilogue pairs them in).
+//
+// Phase 2, gemm_ss_kernel: persistent CTA pairs (cluster of 2), 320 threads:
+//   warp 0      producer: lane 0 loads the stage's A tile (128 weight rows x
+//               64 bf16) and X tile (128 tokens x 64 bf16), 128-byte swizzle,
+//               both completing on the leader CTA's barrier.
+//   warp 1      MMA issuer (leader): tcgen05.mma.cta_group::2.kind::f16 with
+//               A and B from shared-memory descriptors, M = 256 weight rows,
+//               N = 256 tokens, K = 16; two 256-column accumulators in TMEM,
+//               so that a tile's epilogue overlaps the next tile's MMAs.
+//   warps 2-9   epilogue: tcgen05.ld of the finished accumulator, fp32 Y
+//               stores (or the GeGLU pairing and bf16 h stores), then a
+//               cluster arrive that frees the accumulator.
+// Every wait is bounded; a timeout sets the CTA's abort flag, records the
+// error, drains the CTA's own copies and MMAs and frees TMEM.
+#include "qmm_internal.h"
+#include "qmm_tc.cuh"
+
+#include <algorithm>
+
+namespace qmm {
+namespace {
+
+constexpr int SW = 128;                // weight rows per CTA (MMA M = 256 per pair)
+constexpr int ST = 256;                // tokens per pair tile (MMA N)
+constexpr int ST_CTA = ST / 2;
+constexpr int SK = 64;                 // K per stage (one 128-byte swizzle row)
+constexpr int SUMMA_K = 16;
+#ifndef QMM_SS_STAGES
+#define QMM_SS_STAGES 6
+#endif
+constexpr int SSTAGES = QMM_SS_STAGES;
+constexpr int A_TILE_BYTES = SW * SK * 2;      // 16 KB
+constexpr int B_TILE_BYTES = ST_CTA * SK * 2;  // 16 KB
+constexpr int SSTAGE_BYTES = A_TILE_BYTES + B_TILE_BYTES;
+constexpr uint32_t SS_D_COLS = ST;             // one fp32 accumulator
+constexpr uint32_t SS_TMEM_COLS = 512;         // two accumulators
+static_assert(2 * SS_D_COLS <= SS_TMEM_COLS, "tensor memory budget");
+
+constexpr int S_WARP_PROD = 0;
+constexpr int S_WARP_MMA = 1;
+constexpr int S_WARP_EPI0 = 2;
+#ifndef QMM_SS_EPI_WARPS
+#define QMM_SS_EPI_WARPS 8
+#endif
+constexpr int S_EPI = QMM_SS_EPI_WARPS;  // 4 or 8: one or two per lane quarter
+static_assert(S_EPI == 4 || S_EPI == 8, "epilogue warps");
+constexpr int S_THREADS = (S_WARP_EPI0 + S_EPI) * 32;
+
+struct SsLayout {
+    static constexpr int bars = SSTAGES * SSTAGE_BYTES;
+    // full [SSTAGES] (leader), empty [SSTAGES] (both), d_full [2] (both),
+    // d_empty [2] (leader), final
+    static constexpr int nbars = 2 * SSTAGES + 5;
+    static constexpr int tmem_slot = bars + nbars * 8;
+    static constexpr int abort_flag = tmem_slot + 4;
+    static constexpr int total = abort_flag + 4;
+    static constexpr size_t smem_bytes = total + 1024;  // + alignment slack
+};
+static_assert(SsLayout::smem_bytes <= 232448, "shared memory per CTA");
+
+// kind::f16: D fp32, A and B bf16, both K-major, N = 256, M = 256 (the pair).
+constexpr uint32_t kSsIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
+                              (static_cast<uint32_t>(ST >> 3) << 17) |
+                              (static_cast<uint32_t>((2 * SW) >> 4) << 24);
+
+struct SsParams {
+    float *y;     // plain: fp32 [m][n]
+    uint16_t *h;  // GeGLU: bf16 [m][n]
+    int m, n, k;
+    int num_t_blocks;  // token blocks of ST
+    int num_tiles;     // pair tiles
+    LaunchCtx ctx;
+};
+
+// D (TMEM) += A (shared-memory descriptor) x B (shared-memory descriptor),
+// both CTAs' halves.
+__device__ __forceinline__ void umma_bf16_pair_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                                  uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// ---- phase 1: block-format weights -> bf16 rows ------------------------------
+
+// Workspace row `orow` of the GeGLU form: CTA tile fb = orow / 128 holds
+// features fb*64 .. fb*64+63; in lane quarter q (32 rows) the first 16 rows
+// are gate rows of features fb*64 + 16q .. +15, the next 16 the up rows of
+// the same features.
+__device__ __forceinline__ int64_t geglu_source_row(int64_t orow, bool *up) {
+    const int64_t fb = orow >> 7;
+    const int r = static_cast<int>(orow & 127);
+    *up = (r & 16) != 0;
+    return fb * 64 + (r >> 5) * 16 + (r & 15);
+}
+
+template <Fmt F, bool G>
+__global__ void __launch_bounds__(256) dequant_bf16_kernel(const uint8_t *__restrict__ w,
+                                                           const uint8_t *__restrict__ w2,
+                                                           uint16_t *__restrict__ out, int64_t n,
+                                                           int64_t k, int64_t out_rows) {
+    constexpr int kBB = F == Fmt::Q4_0 ? kQ4_0Bytes : kQ8_0Bytes;
+    // the workspace may still be read by the preceding GEMM of this stream
+    pdl_wait();
+    const int64_t nb = k / kQK;
+    const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (idx < out_rows * nb) {
+        const int64_t orow = idx / nb, b = idx - orow * nb;
+        int64_t srow = orow;
+        const uint8_t *src = w;
+        if constexpr (G) {
+            bool up;
+            srow = geglu_source_row(orow, &up);
+            src = up ? w2 : w;
+        }
+        uint32_t packed[16];
+        if (srow < n) {
+            const uint8_t *blk = src + (srow * nb + b) * kBB;
+            const float d = half_bits_to_float(__ldg(blk) | (static_cast<uint32_t>(__ldg(blk + 1)) << 8));
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                float a, c;
+                if constexpr (F == Fmt::Q4_0) {
+                    // weights 2j, 2j+1: nibbles of qs[(2j) % 16] / qs[(2j+1) % 16],
+                    // low nibble for j < 8, high nibble for j >= 8
+                    const int i0 = (2 * j) & 15;
+                    const uint32_t b0 = __ldg(blk + 2 + i0), b1 = __ldg(blk + 3 + i0);
+                    const uint32_t v0 = j < 8 ? (b0 & 15u) : (b0 >> 4);
+                    const uint32_t v1 = j < 8 ? (b1 & 15u) : (b1 >> 4);
+                    a = static_cast<float>(static_cast<int>(v0) - 8) * d;
+                    c = static_cast<float>(static_cast<int>(v1) - 8) * d;
+                } else {
+                    a = static_cast<float>(static_cast<int8_t>(__ldg(blk + 2 + 2 * j))) * d;
+                    c = static_cast<float>(static_cast<int8_t>(__ldg(blk + 3 + 2 * j))) * d;
+                }
+                packed[j] = pack_bf16x2(a, c);
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) packed[j] = 0u;  // rows past N: zero weights
+        }
+        uint4 *dst = reinterpret_cast<uint4 *>(out + orow * k + b * kQK);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            dst[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+    }
+    pdl_launch_dependents();
+}
+
+// ---- phase 2: shared-memory-operand GEMM ------------------------------------
+
+template <bool G>
+__global__ void __launch_bounds__(S_THREADS, 1)
+    gemm_ss_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                   const __grid_constant__ CUtensorMap tmap_x, SsParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_base = smem_addr(smem_raw);
+    const uint32_t sbase = (raw_base + 1023u) & ~1023u;  // 1024-byte aligned (swizzle atoms)
+    uint8_t *sgen = smem_raw + (sbase - raw_base);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const LaunchCtx ctx = p.ctx;
+    const uint32_t rank = cluster_rank();  // 0 = leader of the pair
+    const bool leader = rank == 0;
+    const int pair = static_cast<int>(blockIdx.x >> 1);
+    const int num_pairs = static_cast<int>(gridDim.x >> 1);
+
+    auto bar = [&](int i) -> uint32_t { return sbase + SsLayout::bars + 8u * i; };
+    auto full = [&](int s) { return bar(s); };
+    auto empty = [&](int s) { return bar(SSTAGES + s); };
+    auto d_full = [&](int b) { return bar(2 * SSTAGES + b); };
+    auto d_empty = [&](int b) { return bar(2 * SSTAGES + 2 + b); };
+    const uint32_t final_bar = bar(2 * SSTAGES + 4);
+    int *abort_flag = reinterpret_cast<int *>(sgen + SsLayout::abort_flag);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sgen + SsLayout::tmem_slot);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < SSTAGES; ++s) {
+            mbar_init_addr(full(s), 2);  // one expect-tx arrive per CTA's producer
+            mbar_init_addr(empty(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init_addr(d_full(b), 1);
+            mbar_init_addr(d_empty(b), 2 * S_EPI);
+        }
+        mbar_init_addr(final_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == S_WARP_MMA) tmem_alloc_pair(sbase + SsLayout::tmem_slot, SS_TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    cluster_barrier();  // the peer's barriers exist before anyone signals them
+    tc_fence_after();
+    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
+
+    pdl_wait();  // the workspace and X are written by preceding kernels
+
+    const int KB = p.k / SK;
+    const uint32_t my_tiles =
+        pair < p.num_tiles ? static_cast<uint32_t>((p.num_tiles - pair + num_pairs - 1) / num_pairs) : 0u;
+
+    if (warp == S_WARP_PROD) {
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_a)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_x)) : "memory");
+            uint32_t it = 0;
+            int s = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            for (int t = pair; ok && t < p.num_tiles; t += num_pairs) {
+                const int tb = t % p.num_t_blocks, wb = t / p.num_t_blocks;
+                const int arow = wb * 2 * SW + static_cast<int>(rank) * SW;
+                const int xrow = tb * ST + static_cast<int>(rank) * ST_CTA;
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!wait_or_abort(empty(s), ph ^ 1u, abort_flag, ctx)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t xf = map_to_rank(full(s), 0);
+                    mbar_expect_tx_cluster(xf, SSTAGE_BYTES);
+                    const uint32_t dst = sbase + s * SSTAGE_BYTES;
+                    tma_load_2d_pair(dst, &tmap_a, kb * SK, arow, xf);
+                    tma_load_2d_pair(dst + A_TILE_BYTES, &tmap_x, kb * SK, xrow, xf);
+                    ++it;
+                    if (++s == SSTAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            if (leader) {  // both CTAs' copies complete on the leader's barriers
+                for (int q = 0; q < SSTAGES; ++q) {
+                    if (it > static_cast<uint32_t>(q)) {
+                        const uint32_t last = it - 1 - ((it - 1 - q) % SSTAGES);
+                        wait_drain(full(q), (last / SSTAGES) & 1u, ctx);
+                    }
+                }
+            }
+        }
+    } else if (warp == S_WARP_MMA) {
+        if (leader && lane == 0) {
+            const uint32_t total = my_tiles * static_cast<uint32_t>(KB);
+            const uint64_t desc0 = sw128_desc(sbase);
+            constexpr uint64_t kStageStep = SSTAGE_BYTES >> 4;  // descriptor address units
+            constexpr uint64_t kBOffset = A_TILE_BYTES >> 4;
+            uint32_t kb = 0, tile = 0, buf = 0;
+            int s = 0;
+            uint32_t ph = 0;
+            uint64_t adesc = desc0;
+            bool issued = false, ok = true;
+            for (uint32_t g = 0; ok && g < total; ++g) {
+                if (kb == 0 &&
+                    !wait_or_abort_cluster(d_empty(static_cast<int>(buf)), ((tile >> 1) & 1u) ^ 1u,
+                                           abort_flag, ctx))
+                    break;
+                if (!wait_or_abort(full(s), ph, abort_flag, ctx)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + buf * SS_D_COLS;
+#pragma unroll
+                for (int kk = 0; kk < SK / SUMMA_K; ++kk)  // 32 bytes along the swizzle row
+                    umma_bf16_pair_ss(d_tmem, adesc + 2 * kk, adesc + kBOffset + 2 * kk, kSsIdesc,
+                                      (kk != 0 || kb != 0) ? 1u : 0u);
+                issued = true;
+                umma_commit_pair(empty(s));
+                if (++kb == static_cast<uint32_t>(KB)) {
+                    umma_commit_pair(d_full(static_cast<int>(buf)));
+                    kb = 0;
+                    ++tile;
+                    buf ^= 1u;
+                }
+                if (++s == SSTAGES) {
+                    s = 0;
+                    ph ^= 1u;
+                    adesc = desc0;
+                } else {
+                    adesc += kStageStep;
+                }
+            }
+            if (issued) {  // all MMAs of the pair complete before TMEM is freed
+                umma_commit_pair(final_bar);
+                wait_drain(final_bar, 0, ctx);
+            }
+        }
+    } else {
+        // epilogue: lane i of lane quarter q holds accumulator row 32q+i;
+        // columns are tokens (the leader's 128, then the peer's)
+        const int q = warp & 3;
+        constexpr int CPW = (ST / 32) / (S_EPI / 4);  // 32-column chunks per warp
+        const int c0 = ((warp - S_WARP_EPI0) >> 2) * CPW;
+        uint32_t tile = 0;
+        for (int t = pair; t < p.num_tiles; t += num_pairs, ++tile) {
+            const int tb = t % p.num_t_blocks, wb = t / p.num_t_blocks;
+            const int buf = static_cast<int>(tile & 1u);
+            if (!warp_wait_or_abort(d_full(buf), (tile >> 1) & 1u, abort_flag, ctx)) break;
+            tc_fence_after();
+            const uint32_t d_lane = tmem_base + buf * SS_D_COLS + (static_cast<uint32_t>(q * 32) << 16);
+            if constexpr (G) {
+                const bool upper = lane >= 16;  // holds the up row; takes columns 16..31
+                const int f = wb * SW + static_cast<int>(rank) * (SW / 2) + q * 16 + (lane & 15);
+                const bool f_ok = f < p.n;
+#pragma unroll 1
+                for (int c = c0; c < c0 + CPW; ++c) {
+                    uint32_t v[32];
+                    tmem_ld_32cols(d_lane + c * 32, v);
+                    const int m0 = tb * ST + c * 32 + (upper ? 16 : 0);
+                    uint16_t hv[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float other =
+                            __shfl_xor_sync(0xFFFFFFFFu, __uint_as_float(upper ? v[j] : v[16 + j]), 16);
+                        const float g = upper ? other : __uint_as_float(v[j]);
+                        const float u = upper ? __uint_as_float(v[16 + j]) : other;
+                        hv[j] = to_bf16(gelu_tanh_fast(g) * u);
+                    }
+                    if (f_ok) {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            if (m0 + j < p.m) p.h[static_cast<size_t>(m0 + j) * p.n + f] = hv[j];
+                    }
+                }
+            } else {
+                const int n = wb * 2 * SW + static_cast<int>(rank) * SW + q * 32 + lane;
+                const bool n_ok = n < p.n;
+#pragma unroll 1
+                for (int c = c0; c < c0 + CPW; ++c) {
+                    uint32_t v[32];
+                    tmem_ld_32cols(d_lane + c * 32, v);
+                    const int m0 = tb * ST + c * 32;
+                    if (n_ok) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (m0 + j < p.m)
+                                p.y[static_cast<size_t>(m0 + j) * p.n + n] = __uint_as_float(v[j]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(map_to_rank(d_empty(buf), 0));
+        }
+    }
+
+    pdl_launch_dependents();
+    tc_fence_before();
+    __syncthreads();
+    cluster_barrier();  // the leader has drained; the peer's shared memory may go
+    tc_fence_after();
+    if (warp == S_WARP_MMA) tmem_dealloc_pair(tmem_base, SS_TMEM_COLS);
+}
+
+// Workspace rows: N (plain) or 128 rows per 64 features (GeGLU).
+int64_t workspace_rows(int64_t n, bool geglu) { return geglu ? (n + 63) / 64 * 128 : n; }
+
+template <Fmt F, bool G>
+cudaError_t launch_two_phase(const uint8_t *w, const uint8_t *w2, const uint16_t *x, float *y,
+                             uint16_t *h, int64_t m, int64_t n, int64_t k, uint16_t *ws,
+                             cudaStream_t stream, const LaunchCtx &ctx) {
+    if (m > (1 << 30) || n > (1 << 30) || k > (1 << 24)) return cudaErrorInvalidValue;
+    const int64_t rows = workspace_rows(n, G);
+    // phase 1
+    const int64_t blocks = rows * (k / kQK);
+    const unsigned grid1 = static_cast<unsigned>((blocks + 255) / 256);
+    cudaError_t e = launch_kernel(dequant_bf16_kernel<F, G>, dim3(grid1), dim3(256), 0, stream, 1,
+                                  w, w2, ws, n, k, rows);
+    if (e != cudaSuccess) return e;
+    // phase 2
+    CUtensorMap ta, tx;
+    if (!encode_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ws, k, rows, k * 2, SK, SW,
+                        CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, k, m, k * 2, SK, ST_CTA,
+                        CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    SsParams p;
+    p.y = y;
+    p.h = h;
+    p.m = static_cast<int>(m);
+    p.n = static_cast<int>(n);
+    p.k = static_cast<int>(k);
+    p.num_t_blocks = static_cast<int>((m + ST - 1) / ST);
+    // a pair tile covers 256 workspace rows: 256 outputs, or 128 GeGLU features
+    const int64_t per_tile = G ? SW : 2 * SW;
+    p.num_tiles = p.num_t_blocks * static_cast<int>((n + per_tile - 1) / per_tile);
+    p.ctx = ctx;
+    static int smem_limits[kMaxDevices] = {0};
+    e = ensure_smem(gemm_ss_kernel<G>, SsLayout::smem_bytes, true, smem_limits);
+    if (e != cudaSuccess) return e;
+    const int pairs = std::max(1, std::min(p.num_tiles, device_sm_count() / 2));
+    return launch_kernel(gemm_ss_kernel<G>, dim3(2 * pairs), dim3(S_THREADS), SsLayout::smem_bytes,
+                         stream, 2, ta, tx, p);
+}
+
+}  // namespace
+
+size_t gemm_workspace_bytes(int64_t n, int64_t k, bool geglu) {
+    return static_cast<size_t>(workspace_rows(n, geglu)) * static_cast<size_t>(k) * 2;
+}
+
+cudaError_t launch_gemm_two_phase(Fmt fmt, const uint8_t *w, const uint16_t *x, float *y,
+                                  int64_t m, int64_t n, int64_t k, uint16_t *ws,
+                                  cudaStream_t stream, const LaunchCtx &ctx) {
+    return fmt == Fmt::Q4_0
+               ? launch_two_phase<Fmt::Q4_0, false>(w, nullptr, x, y, nullptr, m, n, k, ws, stream, ctx)
+               : launch_two_phase<Fmt::Q8_0, false>(w, nullptr, x, y, nullptr, m, n, k, ws, stream, ctx);
+}
+
+cudaError_t launch_gemm_geglu_two_phase(const uint8_t *wg, const uint8_t *wu, const uint16_t *x,
+                                        uint16_t *h, int64_t m, int64_t n, int64_t k, uint16_t *ws,
+                                        cudaStream_t stream, const LaunchCtx &ctx) {
+    return launch_two_phase<Fmt::Q4_0, true>(wg, wu, x, nullptr, h, m, n, k, ws, stream, ctx);
+}
+
+}  // namespace qmm

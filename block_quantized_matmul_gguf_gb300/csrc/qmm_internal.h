@@ -155,6 +155,21 @@ cudaError_t launch_gemm_q4_0_geglu(const uint8_t *wg, const uint8_t *wu, const u
                                    uint16_t *h, int64_t m, int64_t n, int64_t k,
                                    cudaStream_t stream, const LaunchCtx &ctx);
 
+#ifndef QMM_GEMM_TWO_PHASE_MIN_M
+#define QMM_GEMM_TWO_PHASE_MIN_M 256  // longer prompts take the two-phase path given a workspace
+#endif
+
+// Two-phase prefill GEMM (weights dequantised once into a bf16 workspace,
+// then a shared-memory-operand tensor-core GEMM).  gemm_workspace_bytes is
+// the workspace it needs.
+size_t gemm_workspace_bytes(int64_t n, int64_t k, bool geglu);
+cudaError_t launch_gemm_two_phase(Fmt fmt, const uint8_t *w, const uint16_t *x, float *y,
+                                  int64_t m, int64_t n, int64_t k, uint16_t *ws,
+                                  cudaStream_t stream, const LaunchCtx &ctx);
+cudaError_t launch_gemm_geglu_two_phase(const uint8_t *wg, const uint8_t *wu, const uint16_t *x,
+                                        uint16_t *h, int64_t m, int64_t n, int64_t k, uint16_t *ws,
+                                        cudaStream_t stream, const LaunchCtx &ctx);
+
 cudaError_t launch_selftest_wait(cudaStream_t stream, const LaunchCtx &ctx);
 
 }  // namespace qmm

@@ -29,7 +29,9 @@ QMM_GEMV_MAX_OUTPUTS = 4
 EXPORTED = (
     "qmm_dequant_q4_0", "qmm_dequant_q8_0", "qmm_gemv_q4_0", "qmm_gemv_q8_0",
     "qmm_gemv_q4_0_multi", "qmm_gemv_q8_0_multi", "qmm_gemv_q4_0_geglu",
-    "qmm_gemm_q4_0", "qmm_gemm_q8_0", "qmm_gemm_q4_0_geglu", "qmm_status_string", "qmm_version", "qmm_get_device_error",
+    "qmm_gemm_q4_0", "qmm_gemm_q8_0", "qmm_gemm_q4_0_geglu",
+    "qmm_gemm_q4_0_ws", "qmm_gemm_q8_0_ws", "qmm_gemm_q4_0_geglu_ws",
+    "qmm_gemm_workspace_bytes", "qmm_gemm_geglu_workspace_bytes", "qmm_status_string", "qmm_version", "qmm_get_device_error",
     "qmm_set_wait_timeout_ns", "qmm_selftest_wait_timeout",
 )
 
@@ -64,6 +66,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         _build.build_library()
     lib = ctypes.CDLL(path)
     P, I64, I32, U64 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint64
+    SZ = ctypes.c_size_t
     sig = {
         "qmm_dequant_q4_0": [P, P, I64, I64, P],
         "qmm_dequant_q8_0": [P, P, I64, I64, P],
@@ -73,6 +76,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         "qmm_gemm_q8_0": [P, P, P, I64, I64, I64, P],
         "qmm_gemv_q4_0_geglu": [P, P, P, P, I32, I64, I64, P],
         "qmm_gemm_q4_0_geglu": [P, P, P, P, I64, I64, I64, P],
+        "qmm_gemm_q4_0_ws": [P, P, P, I64, I64, I64, P, SZ, P],
+        "qmm_gemm_q8_0_ws": [P, P, P, I64, I64, I64, P, SZ, P],
+        "qmm_gemm_q4_0_geglu_ws": [P, P, P, P, I64, I64, I64, P, SZ, P],
         "qmm_gemv_q4_0_multi": [ctypes.POINTER(GemvOut), I32, P, I32, I64, P],
         "qmm_gemv_q8_0_multi": [ctypes.POINTER(GemvOut), I32, P, I32, I64, P],
         "qmm_get_device_error": [P],
@@ -86,6 +92,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.qmm_status_string.restype = ctypes.c_char_p
     lib.qmm_version.argtypes = []
     lib.qmm_version.restype = ctypes.c_int
+    for name in ("qmm_gemm_workspace_bytes", "qmm_gemm_geglu_workspace_bytes"):
+        getattr(lib, name).argtypes = [I64, I64]
+        getattr(lib, name).restype = SZ
     lib.qmm_set_wait_timeout_ns.argtypes = [U64]
     lib.qmm_set_wait_timeout_ns.restype = None
     _lib = lib
@@ -188,6 +197,27 @@ def qmm_gemm_q4_0_geglu(wg, wu, x_bf16, h_bf16, m: int, n: int, k: int, stream=N
                                       _stream(stream)), "qmm_gemm_q4_0_geglu")
 
 
+def qmm_gemm_workspace_bytes(n: int, k: int, geglu: bool = False) -> int:
+    lib = load()
+    return int((lib.qmm_gemm_geglu_workspace_bytes if geglu else lib.qmm_gemm_workspace_bytes)(n, k))
+
+
+def qmm_gemm_q4_0_ws(w, x_bf16, y, m, n, k, ws, ws_bytes, stream=None) -> None:
+    _check(load().qmm_gemm_q4_0_ws(_ptr(w), _ptr(x_bf16), _ptr(y), m, n, k, _ptr(ws), int(ws_bytes),
+                                   _stream(stream)), "qmm_gemm_q4_0_ws")
+
+
+def qmm_gemm_q8_0_ws(w, x_bf16, y, m, n, k, ws, ws_bytes, stream=None) -> None:
+    _check(load().qmm_gemm_q8_0_ws(_ptr(w), _ptr(x_bf16), _ptr(y), m, n, k, _ptr(ws), int(ws_bytes),
+                                   _stream(stream)), "qmm_gemm_q8_0_ws")
+
+
+def qmm_gemm_q4_0_geglu_ws(wg, wu, x_bf16, h_bf16, m, n, k, ws, ws_bytes, stream=None) -> None:
+    _check(load().qmm_gemm_q4_0_geglu_ws(_ptr(wg), _ptr(wu), _ptr(x_bf16), _ptr(h_bf16), m, n, k,
+                                         _ptr(ws), int(ws_bytes), _stream(stream)),
+           "qmm_gemm_q4_0_geglu_ws")
+
+
 def qmm_get_device_error(stream=None) -> int:
     """Synchronise `stream`; return (and clear) the device error word."""
     return int(load().qmm_get_device_error(_stream(stream)))
@@ -227,20 +257,30 @@ def geglu_q4_0(wg, wu, x, n: int, k: int, stream=None):
     return h
 
 
-def gemm(fmt: str, w, x_bf16, n: int, k: int, stream=None):
+def gemm(fmt: str, w, x_bf16, n: int, k: int, stream=None, workspace=None):
+    """workspace: a device tensor of at least qmm_gemm_workspace_bytes(n, k) bytes
+    (the two-phase path for m > 256), or None (the fused call)."""
     import torch
     m = x_bf16.shape[0]
     y = torch.empty((m, n), dtype=torch.float32, device=x_bf16.device)
-    (qmm_gemm_q4_0 if fmt == "q4_0" else qmm_gemm_q8_0)(w, x_bf16, y, m, n, k, stream)
+    if workspace is None:
+        (qmm_gemm_q4_0 if fmt == "q4_0" else qmm_gemm_q8_0)(w, x_bf16, y, m, n, k, stream)
+    else:
+        (qmm_gemm_q4_0_ws if fmt == "q4_0" else qmm_gemm_q8_0_ws)(
+            w, x_bf16, y, m, n, k, workspace, workspace.numel() * workspace.element_size(), stream)
     return y
 
 
-def gemm_geglu_q4_0(wg, wu, x_bf16, n: int, k: int, stream=None):
+def gemm_geglu_q4_0(wg, wu, x_bf16, n: int, k: int, stream=None, workspace=None):
     """Returns h as an int16 tensor of bf16 bit patterns [m][n]."""
     import torch
     m = x_bf16.shape[0]
     h = torch.empty((m, n), dtype=torch.int16, device=x_bf16.device)
-    qmm_gemm_q4_0_geglu(wg, wu, x_bf16, h, m, n, k, stream)
+    if workspace is None:
+        qmm_gemm_q4_0_geglu(wg, wu, x_bf16, h, m, n, k, stream)
+    else:
+        qmm_gemm_q4_0_geglu_ws(wg, wu, x_bf16, h, m, n, k, workspace,
+                               workspace.numel() * workspace.element_size(), stream)
     return h
 
 

@@ -155,6 +155,31 @@ qmm_status qmm_gemm_q4_0(const void *w, const uint16_t *x_bf16, float *y, int64_
 qmm_status qmm_gemm_q8_0(const void *w, const uint16_t *x_bf16, float *y, int64_t m,
                          int64_t n, int64_t k, qmm_stream_t stream);
 
+/* ---- Prefill GEMM with a workspace (long prompts) -----------------------
+ * The same products as qmm_gemm_q4_0 / qmm_gemm_q8_0 / qmm_gemm_q4_0_geglu,
+ * with the same arithmetic (each weight rounded once to bf16, fp32 sums in
+ * tensor memory) and accuracy bound.  For m > 256 with a workspace, the
+ * weights are first dequantised once into the workspace as bf16 (so that
+ * they are not decoded again for every 256-token block) and a second kernel
+ * runs the tensor-core GEMM from it; otherwise the call is the fused one and
+ * the workspace is not touched.
+ * workspace : caller-owned device memory, 16-byte aligned, at least
+ *             qmm_gemm_workspace_bytes(n, k) bytes (qmm_gemm_geglu_
+ *             workspace_bytes for the GeGLU form), not overlapping any
+ *             argument; NULL selects the fused call.  Its contents are
+ *             scratch: overwritten by the call, meaningless after it.  Calls
+ *             that may run concurrently need separate workspaces.
+ * Returns QMM_ERR_SHAPE if workspace_bytes is too small, QMM_ERR_ALIGN if
+ * the workspace is misaligned; other checks as for the calls without it. */
+size_t qmm_gemm_workspace_bytes(int64_t n, int64_t k);
+size_t qmm_gemm_geglu_workspace_bytes(int64_t n, int64_t k);
+qmm_status qmm_gemm_q4_0_ws(const void *w, const uint16_t *x_bf16, float *y, int64_t m,
+                            int64_t n, int64_t k, void *workspace, size_t workspace_bytes,
+                            qmm_stream_t stream);
+qmm_status qmm_gemm_q8_0_ws(const void *w, const uint16_t *x_bf16, float *y, int64_t m,
+                            int64_t n, int64_t k, void *workspace, size_t workspace_bytes,
+                            qmm_stream_t stream);
+
 /* ---- Prefill GeGLU (tcgen05 tensor cores) -----------------------------
  * h[i][j] = bf16(gelu(g[i][j]) * u[i][j]) with g[i][j] = sum_k X[i][k] *
  * wg[j][k] and u[i][j] = sum_k X[i][k] * wu[j][k], for i < m, j < n: the
@@ -172,6 +197,9 @@ qmm_status qmm_gemm_q8_0(const void *w, const uint16_t *x_bf16, float *y, int64_
 qmm_status qmm_gemm_q4_0_geglu(const void *wg, const void *wu, const uint16_t *x_bf16,
                                uint16_t *h_bf16, int64_t m, int64_t n, int64_t k,
                                qmm_stream_t stream);
+qmm_status qmm_gemm_q4_0_geglu_ws(const void *wg, const void *wu, const uint16_t *x_bf16,
+                                  uint16_t *h_bf16, int64_t m, int64_t n, int64_t k,
+                                  void *workspace, size_t workspace_bytes, qmm_stream_t stream);
 
 /* ---- Utilities --------------------------------------------------------- */
 

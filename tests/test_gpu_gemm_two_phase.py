@@ -1,0 +1,112 @@
+"""GPU parity of the two-phase prefill GEMM (weights dequantised once into a
+bf16 workspace, then a shared-memory-operand tensor-core GEMM) against the
+CPU oracle, and bit-for-bit against the fused kernel (same weights, same MMA
+sequence)."""
+import numpy as np
+import pytest
+
+from block_quantized_matmul_gguf_gb300 import synth
+from helpers import GEMM_REL, assert_geglu_within, assert_within, bf16_tensor, to_dev
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def qmm():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from block_quantized_matmul_gguf_gb300 import build, qmm as q
+    build.build_library()
+    q.load()
+    return q
+
+
+def _bf16_to_f32(bits):
+    return (np.asarray(bits).astype(np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def _ws(qmm, n, k, geglu=False):
+    return torch.empty(qmm.qmm_gemm_workspace_bytes(n, k, geglu), dtype=torch.uint8, device="cuda")
+
+
+def _weights(fmt, n, k, seed, stream=0):
+    return (synth.q4_0_weights if fmt == "q4_0" else synth.q8_0_weights)(n, k, seed=seed, stream=stream)
+
+
+@pytest.mark.parametrize("fmt", ["q4_0", "q8_0"])
+@pytest.mark.parametrize("m,n,k", [(257, 4, 256), (300, 260, 512), (513, 768, 1024),
+                                   (700, 1000, 256), (1024, 384, 2048)])
+def test_two_phase_matches_oracle_and_fused(qmm, oracle_mod, fmt, m, n, k):
+    w = _weights(fmt, n, k, seed=m + n)
+    xb = synth.activations_bf16(m, k, seed=m + n, stream=5)
+    wd, xd = to_dev(w, torch), bf16_tensor(xb, torch)
+    y2 = qmm.gemm(fmt, wd, xd, n, k, workspace=_ws(qmm, n, k))
+    y1 = qmm.gemm(fmt, wd, xd, n, k)
+    torch.cuda.synchronize()
+    assert qmm.qmm_get_device_error() == 0
+    f = oracle_mod.gemv_q4_0 if fmt == "q4_0" else oracle_mod.gemv_q8_0
+    y_ref, bound = f(w, _bf16_to_f32(xb), m, n, k)
+    assert_within(y2.cpu().numpy(), y_ref, bound, GEMM_REL, f"two-phase {fmt} {m}x{n}x{k}")
+    assert torch.equal(y2, y1), "two-phase and fused results differ"
+
+
+def test_two_phase_full_size_sampled(qmm, oracle_mod):
+    p = synth.PREFILL_SHAPES[0]
+    m = synth.PREFILL_M
+    w, xb = synth.gemm_case(m, p.n, p.k, seed=0, stream=70)
+    wd, xd = to_dev(w, torch), bf16_tensor(xb, torch)
+    y2 = qmm.gemm("q4_0", wd, xd, p.n, p.k, workspace=_ws(qmm, p.n, p.k))
+    y1 = qmm.gemm("q4_0", wd, xd, p.n, p.k)
+    torch.cuda.synchronize()
+    assert torch.equal(y2, y1)
+    rng = np.random.default_rng(3)
+    mi = rng.integers(0, m, 2000)
+    ni = rng.integers(0, p.n, 2000)
+    y_ref, bound = oracle_mod.gemm_q4_0_at(w, xb, m, p.n, p.k, mi, ni)
+    assert_within(y2[torch.from_numpy(mi).cuda(), torch.from_numpy(ni).cuda()].cpu().numpy(),
+                  y_ref, bound, GEMM_REL, "two-phase full size")
+
+
+@pytest.mark.parametrize("m,n,k", [(300, 200, 512), (512, 384, 2048), (700, 1000, 256)])
+def test_two_phase_geglu(qmm, oracle_mod, m, n, k):
+    wg = synth.q4_0_weights(n, k, seed=m, stream=0)
+    wu = synth.q4_0_weights(n, k, seed=m, stream=1)
+    xb = synth.activations_bf16(m, k, seed=m, stream=2)
+    a, b, xd = to_dev(wg, torch), to_dev(wu, torch), bf16_tensor(xb, torch)
+    h2 = qmm.gemm_geglu_q4_0(a, b, xd, n, k, workspace=_ws(qmm, n, k, geglu=True))
+    h1 = qmm.gemm_geglu_q4_0(a, b, xd, n, k)
+    torch.cuda.synchronize()
+    assert qmm.qmm_get_device_error() == 0
+    assert torch.equal(h2, h1), "two-phase and fused GeGLU differ"
+    h_ref, g, u, bg, bu = oracle_mod.geglu_q4_0(wg, wu, _bf16_to_f32(xb), m, n, k)
+    assert_geglu_within(_bf16_to_f32(h2.cpu().numpy()), h_ref, g, u, bg, bu, f"{m}x{n}x{k}",
+                        rel=GEMM_REL, out_rel=2.0 ** -8)
+
+
+def test_short_prompt_ignores_the_workspace(qmm):
+    m, n, k = 256, 512, 512
+    w, xb = synth.gemm_case(m, n, k, seed=9)
+    ws = _ws(qmm, n, k)
+    ws.fill_(0xA5)
+    y = qmm.gemm("q4_0", to_dev(w, torch), bf16_tensor(xb, torch), n, k, workspace=ws)
+    torch.cuda.synchronize()
+    assert bool((ws == 0xA5).all())
+    assert torch.isfinite(y).all()
+
+
+def test_workspace_argument_checks(qmm):
+    m, n, k = 300, 64, 256
+    w = torch.zeros(n * (k // 32) * 18, dtype=torch.uint8, device="cuda")
+    x = torch.zeros((m, k), dtype=torch.int16, device="cuda")
+    y = torch.empty((m, n), dtype=torch.float32, device="cuda")
+    need = qmm.qmm_gemm_workspace_bytes(n, k)
+    assert need == n * k * 2
+    assert qmm.qmm_gemm_workspace_bytes(n, k, geglu=True) == (n + 63) // 64 * 128 * k * 2
+    ws = torch.empty(need + 64, dtype=torch.uint8, device="cuda")
+    for args, status in [((w, x, y, m, n, k, ws, need - 1), qmm.QMM_ERR_SHAPE),
+                         ((w, x, y, m, n, k, ws[8:].data_ptr(), need), qmm.QMM_ERR_ALIGN),
+                         ((w, x, y, m, n, k, y, need), qmm.QMM_ERR_UNSUPPORTED)]:
+        with pytest.raises(qmm.QmmError) as e:
+            qmm.qmm_gemm_q4_0_ws(*args)
+        assert e.value.status == status, args
