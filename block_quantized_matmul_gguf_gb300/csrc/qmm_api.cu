@@ -278,6 +278,20 @@ qmm_status qmm_gemm_q8_0(const void *w, const uint16_t *x_bf16, float *y, int64_
     return gemm(Fmt::Q8_0, w, x_bf16, y, m, n, k, stream);
 }
 
+qmm_status qmm_gemm_q4_0_prefill(const void *w, const uint16_t *x_bf16, float *y, int64_t m,
+                                 int64_t n, int64_t k, qmm_stream_t stream) {
+    qmm_status s = check_wk(w, n, k);
+    if (s != QMM_OK) return s;
+    if (!x_bf16 || !y) return QMM_ERR_NULL;
+    if (m < 1 || m > (int64_t(1) << 31)) return QMM_ERR_SHAPE;
+    if (k % 256 != 0 || n % 4 != 0) return QMM_ERR_UNSUPPORTED;
+    if (!aligned(w, 16) || !aligned(x_bf16, 16) || !aligned(y, 16)) return QMM_ERR_ALIGN;
+    LaunchCtx ctx;
+    if (!make_ctx(&ctx)) return QMM_ERR_CUDA;
+    return from_cuda(launch_gemm_q4_0_prefill(static_cast<const uint8_t *>(w), x_bf16, y, m, n, k,
+                                              reinterpret_cast<cudaStream_t>(stream), ctx));
+}
+
 size_t qmm_gemm_workspace_bytes(int64_t n, int64_t k) {
     if (n < 1 || k < 1) return 0;
     return gemm_workspace_bytes(n, k, false);

@@ -82,9 +82,10 @@ constexpr uint32_t kSsIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
                               (static_cast<uint32_t>((2 * SW) >> 4) << 24);
 
 struct SsParams {
-    float *y;     // plain: fp32 [m][n]
+    float *y;     // plain: fp32 [m][ldy]
     uint16_t *h;  // GeGLU: bf16 [m][n]
     int m, n, k;
+    int ldy;      // row stride of y (n, or wider when a call covers a column range)
     int num_t_blocks;  // token blocks of ST
     int num_tiles;     // pair tiles
     LaunchCtx ctx;
@@ -352,7 +353,7 @@ __global__ void __launch_bounds__(S_THREADS, 1)
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
                             if (m0 + j < p.m)
-                                p.y[static_cast<size_t>(m0 + j) * p.n + n] = __uint_as_float(v[j]);
+                                p.y[static_cast<size_t>(m0 + j) * p.ldy + n] = __uint_as_float(v[j]);
                     }
                 }
             }
@@ -376,7 +377,7 @@ int64_t workspace_rows(int64_t n, bool geglu) { return geglu ? (n + 63) / 64 * 1
 template <Fmt F, bool G>
 cudaError_t launch_two_phase(const uint8_t *w, const uint8_t *w2, const uint16_t *x, float *y,
                              uint16_t *h, int64_t m, int64_t n, int64_t k, uint16_t *ws,
-                             cudaStream_t stream, const LaunchCtx &ctx) {
+                             cudaStream_t stream, const LaunchCtx &ctx, int64_t ldy = 0) {
     if (m > (1 << 30) || n > (1 << 30) || k > (1 << 24)) return cudaErrorInvalidValue;
     const int64_t rows = workspace_rows(n, G);
     // phase 1
@@ -398,6 +399,7 @@ cudaError_t launch_two_phase(const uint8_t *w, const uint8_t *w2, const uint16_t
     p.m = static_cast<int>(m);
     p.n = static_cast<int>(n);
     p.k = static_cast<int>(k);
+    p.ldy = static_cast<int>(ldy > 0 ? ldy : n);
     p.num_t_blocks = static_cast<int>((m + ST - 1) / ST);
     // a pair tile covers 256 workspace rows: 256 outputs, or 128 GeGLU features
     const int64_t per_tile = G ? SW : 2 * SW;
@@ -411,7 +413,34 @@ cudaError_t launch_two_phase(const uint8_t *w, const uint8_t *w2, const uint16_t
                          stream, 2, ta, tx, p);
 }
 
+// The library's own scratch for qmm_gemm_q4_0_prefill: bf16 weight rows of
+// one column chunk at a time (64 MB: 16384 rows at K = 2048).
+constexpr size_t kScratchBytes = size_t(64) << 20;
+static __device__ __align__(256) uint16_t g_prefill_scratch[kScratchBytes / sizeof(uint16_t)];
+
 }  // namespace
+
+cudaError_t launch_gemm_q4_0_prefill(const uint8_t *w, const uint16_t *x, float *y, int64_t m,
+                                     int64_t n, int64_t k, cudaStream_t stream,
+                                     const LaunchCtx &ctx) {
+    // weight rows per chunk: whole pair tiles that fit the scratch
+    const int64_t chunk = static_cast<int64_t>(kScratchBytes / (static_cast<size_t>(k) * 2)) / (2 * SW) * (2 * SW);
+    if (m <= QMM_GEMM_TWO_PHASE_MIN_M || chunk < 2 * SW)
+        return launch_gemm_q4_0(w, x, y, m, n, k, stream, ctx);
+    void *scratch = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&scratch, g_prefill_scratch);
+    if (e != cudaSuccess) return e;
+    const int64_t row_bytes = (k / kQK) * kQ4_0Bytes;
+    for (int64_t n0 = 0; n0 < n; n0 += chunk) {
+        const int64_t nc = std::min(chunk, n - n0);
+        // columns n0 .. n0+nc of y: the chunk's outputs, row stride n
+        e = launch_two_phase<Fmt::Q4_0, false>(w + n0 * row_bytes, nullptr, x, y + n0, nullptr, m,
+                                               nc, k, static_cast<uint16_t *>(scratch), stream,
+                                               ctx, n);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
 
 size_t gemm_workspace_bytes(int64_t n, int64_t k, bool geglu) {
     return static_cast<size_t>(workspace_rows(n, geglu)) * static_cast<size_t>(k) * 2;

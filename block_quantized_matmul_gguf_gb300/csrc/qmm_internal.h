@@ -170,6 +170,12 @@ cudaError_t launch_gemm_geglu_two_phase(const uint8_t *wg, const uint8_t *wu, co
                                         uint16_t *h, int64_t m, int64_t n, int64_t k, uint16_t *ws,
                                         cudaStream_t stream, const LaunchCtx &ctx);
 
+// Two-phase Q4_0 prefill GEMM on the library's own static scratch (column
+// chunks that fit it; fused kernel for m <= 256 or chunks under one tile).
+cudaError_t launch_gemm_q4_0_prefill(const uint8_t *w, const uint16_t *x, float *y, int64_t m,
+                                     int64_t n, int64_t k, cudaStream_t stream,
+                                     const LaunchCtx &ctx);
+
 cudaError_t launch_selftest_wait(cudaStream_t stream, const LaunchCtx &ctx);
 
 }  // namespace qmm

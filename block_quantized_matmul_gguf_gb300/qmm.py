@@ -30,7 +30,7 @@ EXPORTED = (
     "qmm_dequant_q4_0", "qmm_dequant_q8_0", "qmm_gemv_q4_0", "qmm_gemv_q8_0",
     "qmm_gemv_q4_0_multi", "qmm_gemv_q8_0_multi", "qmm_gemv_q4_0_geglu",
     "qmm_gemm_q4_0", "qmm_gemm_q8_0", "qmm_gemm_q4_0_geglu",
-    "qmm_gemm_q4_0_ws", "qmm_gemm_q8_0_ws", "qmm_gemm_q4_0_geglu_ws",
+    "qmm_gemm_q4_0_ws", "qmm_gemm_q8_0_ws", "qmm_gemm_q4_0_geglu_ws", "qmm_gemm_q4_0_prefill",
     "qmm_gemm_workspace_bytes", "qmm_gemm_geglu_workspace_bytes", "qmm_status_string", "qmm_version", "qmm_get_device_error",
     "qmm_set_wait_timeout_ns", "qmm_selftest_wait_timeout",
 )
@@ -77,6 +77,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         "qmm_gemv_q4_0_geglu": [P, P, P, P, I32, I64, I64, P],
         "qmm_gemm_q4_0_geglu": [P, P, P, P, I64, I64, I64, P],
         "qmm_gemm_q4_0_ws": [P, P, P, I64, I64, I64, P, SZ, P],
+        "qmm_gemm_q4_0_prefill": [P, P, P, I64, I64, I64, P],
         "qmm_gemm_q8_0_ws": [P, P, P, I64, I64, I64, P, SZ, P],
         "qmm_gemm_q4_0_geglu_ws": [P, P, P, P, I64, I64, I64, P, SZ, P],
         "qmm_gemv_q4_0_multi": [ctypes.POINTER(GemvOut), I32, P, I32, I64, P],
@@ -216,6 +217,12 @@ def qmm_gemm_q4_0_geglu_ws(wg, wu, x_bf16, h_bf16, m, n, k, ws, ws_bytes, stream
     _check(load().qmm_gemm_q4_0_geglu_ws(_ptr(wg), _ptr(wu), _ptr(x_bf16), _ptr(h_bf16), m, n, k,
                                          _ptr(ws), int(ws_bytes), _stream(stream)),
            "qmm_gemm_q4_0_geglu_ws")
+
+
+def qmm_gemm_q4_0_prefill(w, x_bf16, y, m: int, n: int, k: int, stream=None) -> None:
+    """Two-phase Q4_0 GEMM on the library's own scratch (no workspace argument)."""
+    _check(load().qmm_gemm_q4_0_prefill(_ptr(w), _ptr(x_bf16), _ptr(y), m, n, k, _stream(stream)),
+           "qmm_gemm_q4_0_prefill")
 
 
 def qmm_get_device_error(stream=None) -> int:

@@ -180,6 +180,17 @@ qmm_status qmm_gemm_q8_0_ws(const void *w, const uint16_t *x_bf16, float *y, int
                             int64_t n, int64_t k, void *workspace, size_t workspace_bytes,
                             qmm_stream_t stream);
 
+/* The Q4_0 product of qmm_gemm_q4_0_ws without a caller workspace: for
+ * m > 256 the weights are dequantised into a 64 MB scratch array that is
+ * part of the library (a module-scope device variable, one per GPU), in
+ * column chunks of whole 256-row tiles that fit it, each chunk followed by
+ * its GEMM; otherwise the fused call.  Allocates nothing.  Same requirements,
+ * arithmetic and accuracy as qmm_gemm_q4_0.  The scratch is shared by every
+ * call of this entry point on the device, so calls on different streams must
+ * not run concurrently (the caller orders them, e.g. with events). */
+qmm_status qmm_gemm_q4_0_prefill(const void *w, const uint16_t *x_bf16, float *y, int64_t m,
+                                 int64_t n, int64_t k, qmm_stream_t stream);
+
 /* ---- Prefill GeGLU (tcgen05 tensor cores) -----------------------------
  * h[i][j] = bf16(gelu(g[i][j]) * u[i][j]) with g[i][j] = sum_k X[i][k] *
  * wg[j][k] and u[i][j] = sum_k X[i][k] * wu[j][k], for i < m, j < n: the

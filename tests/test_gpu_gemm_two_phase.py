@@ -110,3 +110,39 @@ def test_workspace_argument_checks(qmm):
         with pytest.raises(qmm.QmmError) as e:
             qmm.qmm_gemm_q4_0_ws(*args)
         assert e.value.status == status, args
+
+
+# ---- the same product on the library's own scratch (no workspace argument) ----
+
+def _prefill(qmm, w, x, m, n, k):
+    y = torch.empty((m, n), dtype=torch.float32, device="cuda")
+    qmm.qmm_gemm_q4_0_prefill(w, x, y, m, n, k)
+    torch.cuda.synchronize()
+    assert qmm.qmm_get_device_error() == 0
+    return y
+
+
+@pytest.mark.parametrize("m,n,k", [(300, 260, 512), (1024, 384, 2048), (200, 512, 512)])
+def test_prefill_static_scratch_equals_fused(qmm, oracle_mod, m, n, k):
+    w, xb = synth.gemm_case(m, n, k, seed=m + 1)
+    wd, xd = to_dev(w, torch), bf16_tensor(xb, torch)
+    y = _prefill(qmm, wd, xd, m, n, k)
+    assert torch.equal(y, qmm.gemm("q4_0", wd, xd, n, k))
+    y_ref, bound = oracle_mod.gemm_q4_0(w, xb, m, n, k)
+    assert_within(y.cpu().numpy(), y_ref, bound, GEMM_REL, f"prefill {m}x{n}x{k}")
+
+
+def test_prefill_static_scratch_column_chunks(qmm, oracle_mod):
+    """K = 16384: the 64 MB scratch holds 2048 weight rows, so N = 5000 runs
+    as three column chunks (2048, 2048, 904) written with the full row stride."""
+    m, n, k = 300, 5000, 16384
+    w, xb = synth.gemm_case(m, n, k, seed=77)
+    wd, xd = to_dev(w, torch), bf16_tensor(xb, torch)
+    y = _prefill(qmm, wd, xd, m, n, k)
+    assert torch.equal(y, qmm.gemm("q4_0", wd, xd, n, k))
+    rng = np.random.default_rng(4)
+    mi = rng.integers(0, m, 1500)
+    ni = np.concatenate([rng.integers(0, n, 1496), [2047, 2048, 4095, 4999]])
+    mi = np.concatenate([mi[:1496], [0, 1, m - 1, m - 1]])
+    y_ref, bound = oracle_mod.gemm_q4_0_at(w, xb, m, n, k, mi, ni)
+    assert_within(y.cpu().numpy()[mi, ni], y_ref, bound, GEMM_REL, "prefill chunks")
