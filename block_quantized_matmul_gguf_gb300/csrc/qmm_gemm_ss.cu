@@ -115,55 +115,77 @@ __device__ __forceinline__ int64_t geglu_source_row(int64_t orow, bool *up) {
     return fb * 64 + (r >> 5) * 16 + (r & 15);
 }
 
+// One thread per 32-weight block.  The block's bytes (2-byte aligned) are
+// read as 16-bit words into the word layout the exact decode helpers take
+// (d in the low half of word 0, quants from byte 2); its 64 bytes of bf16 go
+// through shared memory so that each warp store writes 512 contiguous bytes
+// (a 256-thread CTA covers 256 consecutive blocks = 16 KB of output, because
+// workspace rows are exactly K weights long).  Grid-stride over CTA groups.
+constexpr int kDeqThreads = 256;
+constexpr int kDeqStageRow = kDeqThreads + 2;  // 16-byte pieces per row: 258 keeps reads conflict-free
+
 template <Fmt F, bool G>
-__global__ void __launch_bounds__(256) dequant_bf16_kernel(const uint8_t *__restrict__ w,
-                                                           const uint8_t *__restrict__ w2,
-                                                           uint16_t *__restrict__ out, int64_t n,
-                                                           int64_t k, int64_t out_rows) {
+__global__ void __launch_bounds__(kDeqThreads) dequant_bf16_kernel(const uint8_t *__restrict__ w,
+                                                                   const uint8_t *__restrict__ w2,
+                                                                   uint16_t *__restrict__ out,
+                                                                   int64_t n, int64_t k,
+                                                                   int64_t out_rows, uint32_t magic) {
     constexpr int kBB = F == Fmt::Q4_0 ? kQ4_0Bytes : kQ8_0Bytes;
+    constexpr int NH = kBB / 2;            // 16-bit words of a block: 9 or 17
+    constexpr int NW = (NH + 1) / 2;       // 32-bit words: 5 or 9
+    __shared__ uint4 stage[4 * kDeqStageRow];  // piece q of thread t at [q][t]
     // the workspace may still be read by the preceding GEMM of this stream
     pdl_wait();
     const int64_t nb = k / kQK;
-    const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (idx < out_rows * nb) {
-        const int64_t orow = idx / nb, b = idx - orow * nb;
-        int64_t srow = orow;
-        const uint8_t *src = w;
-        if constexpr (G) {
-            bool up;
-            srow = geglu_source_row(orow, &up);
-            src = up ? w2 : w;
-        }
-        uint32_t packed[16];
-        if (srow < n) {
-            const uint8_t *blk = src + (srow * nb + b) * kBB;
-            const float d = half_bits_to_float(__ldg(blk) | (static_cast<uint32_t>(__ldg(blk + 1)) << 8));
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                float a, c;
-                if constexpr (F == Fmt::Q4_0) {
-                    // weights 2j, 2j+1: nibbles of qs[(2j) % 16] / qs[(2j+1) % 16],
-                    // low nibble for j < 8, high nibble for j >= 8
-                    const int i0 = (2 * j) & 15;
-                    const uint32_t b0 = __ldg(blk + 2 + i0), b1 = __ldg(blk + 3 + i0);
-                    const uint32_t v0 = j < 8 ? (b0 & 15u) : (b0 >> 4);
-                    const uint32_t v1 = j < 8 ? (b1 & 15u) : (b1 >> 4);
-                    a = static_cast<float>(static_cast<int>(v0) - 8) * d;
-                    c = static_cast<float>(static_cast<int>(v1) - 8) * d;
-                } else {
-                    a = static_cast<float>(static_cast<int8_t>(__ldg(blk + 2 + 2 * j))) * d;
-                    c = static_cast<float>(static_cast<int8_t>(__ldg(blk + 3 + 2 * j))) * d;
-                }
-                packed[j] = pack_bf16x2(a, c);
+    const int64_t total = out_rows * nb;
+    const int t = threadIdx.x;
+    for (int64_t base = static_cast<int64_t>(blockIdx.x) * kDeqThreads; base < total;
+         base += static_cast<int64_t>(gridDim.x) * kDeqThreads) {
+        const int64_t idx = base + t;
+        uint4 o[4] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u),
+                      make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
+        if (idx < total) {
+            const int64_t orow = idx / nb, b = idx - orow * nb;
+            int64_t srow = orow;
+            const uint8_t *src = w;
+            if constexpr (G) {
+                bool up;
+                srow = geglu_source_row(orow, &up);
+                src = up ? w2 : w;
             }
-        } else {
+            if (srow < n) {  // rows past N stay zero weights
+                const uint16_t *h = reinterpret_cast<const uint16_t *>(src + (srow * nb + b) * kBB);
+                uint32_t wd[NW];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) packed[j] = 0u;  // rows past N: zero weights
+                for (int i = 0; i < NW; ++i) {
+                    const uint32_t lo = __ldg(h + 2 * i);
+                    const uint32_t hi = 2 * i + 1 < NH ? static_cast<uint32_t>(__ldg(h + 2 * i + 1)) : 0u;
+                    wd[i] = lo | (hi << 16);
+                }
+                if constexpr (F == Fmt::Q4_0) {
+                    uint32_t w36[36];  // block 0 of a chunk window: only words 0..4 are read
+#pragma unroll
+                    for (int i = 0; i < 36; ++i) w36[i] = i < NW ? wd[i] : 0u;
+                    dequant_words_bf16<0, 4>(w36, 0, magic, o);
+                } else {
+                    uint32_t v[16];
+                    dequant_q8_block_bf16(wd, 0, magic | 0x80u, magic | 0x8000u, v);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) o[q] = make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                }
+            }
         }
-        uint4 *dst = reinterpret_cast<uint4 *>(out + orow * k + b * kQK);
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-            dst[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+        for (int q = 0; q < 4; ++q) stage[q * kDeqStageRow + t] = o[q];
+        __syncthreads();
+        // output piece p (16 bytes) of this group: piece p % 4 of block p / 4
+        uint4 *dst = reinterpret_cast<uint4 *>(out + base * kQK);
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int pc = t + kDeqThreads * r;
+            if (base + pc / 4 < total) dst[pc] = stage[(pc & 3) * kDeqStageRow + (pc >> 2)];
+        }
+        __syncthreads();
     }
     pdl_launch_dependents();
 }
@@ -381,10 +403,10 @@ cudaError_t launch_two_phase(const uint8_t *w, const uint8_t *w2, const uint16_t
     if (m > (1 << 30) || n > (1 << 30) || k > (1 << 24)) return cudaErrorInvalidValue;
     const int64_t rows = workspace_rows(n, G);
     // phase 1
-    const int64_t blocks = rows * (k / kQK);
-    const unsigned grid1 = static_cast<unsigned>((blocks + 255) / 256);
-    cudaError_t e = launch_kernel(dequant_bf16_kernel<F, G>, dim3(grid1), dim3(256), 0, stream, 1,
-                                  w, w2, ws, n, k, rows);
+    const int64_t groups = (rows * (k / kQK) + kDeqThreads - 1) / kDeqThreads;
+    const unsigned grid1 = static_cast<unsigned>(std::min<int64_t>(groups, 8LL * device_sm_count()));
+    cudaError_t e = launch_kernel(dequant_bf16_kernel<F, G>, dim3(grid1), dim3(kDeqThreads), 0, stream,
+                                  1, w, w2, ws, n, k, rows, 0x4B000000u);
     if (e != cudaSuccess) return e;
     // phase 2
     CUtensorMap ta, tx;

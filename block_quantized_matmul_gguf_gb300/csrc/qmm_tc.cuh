@@ -274,4 +274,101 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return r;
 }
 
+// ---- weight decode to bf16 (exact fp32 product, one rounding) ---------------
+
+// 2^23 + (v & mask) as a float.  `magic` (0x4B000000) comes from the kernel
+// parameters so that it sits in a register: with the mask and the magic both
+// immediates the compiler splits the extraction into two LOP3.
+__device__ __forceinline__ float mag(uint32_t v, uint32_t mask, uint32_t magic) {
+    return __uint_as_float((v & mask) | magic);
+}
+
+// bf16 pair (k, k+1) from two 2^23-magic nibble floats: exact (nibble-8)*2^s
+// by one packed add, exact (nibble-8)*d by one packed multiply with d*2^-s,
+// one rounding to bf16.
+__device__ __forceinline__ uint32_t w_pair(float ma, float mb, float2 c, float2 ds) {
+    const float2 f = __fadd2_rn(make_float2(ma, mb), c);
+    const float2 w = __fmul2_rn(f, ds);
+    return pack_bf16x2(w.x, w.y);
+}
+
+// Dequantise qs words [I0, I0 + NI) of Q4_0 block `b` (0..7) of a 144-byte
+// row chunk held in wd[36].  Word i holds weights 4i..4i+3 (low nibbles) and
+// 16+4i..19+4i (high nibbles); out[0..NI/2) are the low 16-byte chunks
+// (K 8*I0/2 ..), out[NI/2..NI) the high ones (K 16 + ...).
+template <int I0, int NI>
+__device__ __forceinline__ void dequant_words_bf16(const uint32_t (&wd)[36], int b, uint32_t magic,
+                                                   uint4 (&out)[NI]) {
+    const int base = (18 * b) >> 2;
+    uint32_t dbits, q[4];
+    if ((b & 1) == 0) {
+        dbits = wd[base] & 0xFFFFu;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) q[i] = __byte_perm(wd[base + i], wd[base + i + 1], 0x5432);
+    } else {
+        dbits = wd[base] >> 16;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) q[i] = wd[base + 1 + i];
+    }
+    const float d = half_bits_to_float(dbits);
+    const float d4 = d * 0.0625f, d8 = d * 0.00390625f, d12 = d * 0.000244140625f,
+                d16 = d * 1.52587890625e-05f;
+    const float2 c08 = make_float2(-8388616.0f, -8390656.0f);  // s = 0, 8
+    const float2 c168 = make_float2(-8912896.0f, -8390656.0f); // s = 16, 8
+    const float2 c412 = make_float2(-8388736.0f, -8421376.0f); // s = 4, 12
+    const float2 d08 = make_float2(d, d8), d168 = make_float2(d16, d8), d412 = make_float2(d4, d12);
+    uint32_t lo[2 * NI], hi[2 * NI];
+#pragma unroll
+    for (int j = 0; j < NI; ++j) {
+        const uint32_t v = q[I0 + j], u = v >> 16;
+        // low nibbles: weights 4i .. 4i+3
+        lo[2 * j + 0] = w_pair(mag(v, 0x0000000Fu, magic), mag(v, 0x00000F00u, magic), c08, d08);
+        lo[2 * j + 1] = w_pair(mag(v, 0x000F0000u, magic), mag(u, 0x00000F00u, magic), c168, d168);
+        // high nibbles: weights 16+4i .. 19+4i
+        hi[2 * j + 0] = w_pair(mag(v, 0x000000F0u, magic), mag(v, 0x0000F000u, magic), c412, d412);
+        hi[2 * j + 1] = w_pair(mag(u, 0x000000F0u, magic), mag(u, 0x0000F000u, magic), c412, d412);
+    }
+#pragma unroll
+    for (int c = 0; c < NI / 2; ++c) {
+        out[c] = make_uint4(lo[4 * c], lo[4 * c + 1], lo[4 * c + 2], lo[4 * c + 3]);
+        out[NI / 2 + c] = make_uint4(hi[4 * c], hi[4 * c + 1], hi[4 * c + 2], hi[4 * c + 3]);
+    }
+}
+
+// Q8_0 byte with its top bit flipped (q + 128) in the mantissa of 2^23;
+// flip = 2^23's pattern with that byte's top bit set.  One LOP3.
+__device__ __forceinline__ float mag8(uint32_t v, uint32_t mask, uint32_t flip) {
+    return __uint_as_float((mask & (v ^ flip)) | (~mask & flip));
+}
+
+// Dequantise the Q8_0 block that starts `o` bytes into a window of row bytes
+// held in wd[NW] (o % 4 is 0 or 2): d, then q[0..31] to 16 bf16 pairs in K order.
+// (2^23 + (q+128)*2^s) - (2^23 + 128*2^s) is q*2^s exactly; times d*2^-s it
+// is q*d exactly (an 8-bit by 11-bit product), rounded once to bf16.
+template <int NW>
+__device__ __forceinline__ void dequant_q8_block_bf16(const uint32_t (&wd)[NW], int o,
+                                                      uint32_t flip0, uint32_t flip1,
+                                                      uint32_t (&out)[16]) {
+    const int base = o >> 2;
+    uint32_t dbits, q[8];
+    if ((o & 3) == 0) {  // d in the low half of word `base`, q from byte o + 2
+        dbits = wd[base] & 0xFFFFu;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) q[i] = __byte_perm(wd[base + i], wd[base + i + 1], 0x5432);
+    } else {  // d in the high half, q word-aligned
+        dbits = wd[base] >> 16;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) q[i] = wd[base + 1 + i];
+    }
+    const float d = half_bits_to_float(dbits);
+    const float2 c = make_float2(-8388736.0f, -8421376.0f);  // -(2^23 + 128*2^s), s = 0, 8
+    const float2 ds = make_float2(d, d * 0.00390625f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t v = q[i], u = v >> 16;
+        out[2 * i + 0] = w_pair(mag8(v, 0x000000FFu, flip0), mag8(v, 0x0000FF00u, flip1), c, ds);
+        out[2 * i + 1] = w_pair(mag8(u, 0x000000FFu, flip0), mag8(u, 0x0000FF00u, flip1), c, ds);
+    }
+}
+
 }  // namespace qmm
