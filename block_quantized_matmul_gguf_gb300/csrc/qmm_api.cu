@@ -122,9 +122,6 @@ qmm_status gemv(Fmt fmt, const qmm_gemv_out *outs, int count, const float *x, in
                                  reinterpret_cast<cudaStream_t>(stream), ctx));
 }
 
-// Prompts longer than this take the two-phase path when a workspace is given.
-constexpr int64_t kTwoPhaseMinM = QMM_GEMM_TWO_PHASE_MIN_M;
-
 qmm_status check_workspace(const void *ws, size_t ws_bytes, size_t need) {
     if (!aligned(ws, 16)) return QMM_ERR_ALIGN;
     if (ws_bytes < need) return QMM_ERR_SHAPE;
@@ -139,7 +136,7 @@ qmm_status gemm(Fmt fmt, const void *w, const uint16_t *x_bf16, float *y, int64_
     if (m < 1 || m > (int64_t(1) << 31)) return QMM_ERR_SHAPE;
     if (k % 256 != 0 || n % 4 != 0) return QMM_ERR_UNSUPPORTED;
     if (!aligned(w, 16) || !aligned(x_bf16, 16) || !aligned(y, 16)) return QMM_ERR_ALIGN;
-    const bool two_phase = ws != nullptr && m > kTwoPhaseMinM;
+    const bool two_phase = ws != nullptr && use_two_phase(m, k);
     if (two_phase) {
         const size_t need = gemm_workspace_bytes(n, k, false);
         s = check_workspace(ws, ws_bytes, need);
@@ -336,7 +333,7 @@ qmm_status qmm_gemm_q4_0_geglu_ws(const void *wg, const void *wu, const uint16_t
     if (overlaps(h_bf16, hbytes, x_bf16, sizeof(uint16_t) * static_cast<size_t>(m) * k) ||
         overlaps(h_bf16, hbytes, wg, wbytes) || overlaps(h_bf16, hbytes, wu, wbytes))
         return QMM_ERR_UNSUPPORTED;
-    const bool two_phase = workspace != nullptr && m > kTwoPhaseMinM;
+    const bool two_phase = workspace != nullptr && use_two_phase(m, k);
     if (two_phase) {
         const size_t need = gemm_workspace_bytes(n, k, true);
         s = check_workspace(workspace, workspace_bytes, need);

@@ -447,7 +447,7 @@ cudaError_t launch_gemm_q4_0_prefill(const uint8_t *w, const uint16_t *x, float 
                                      const LaunchCtx &ctx) {
     // weight rows per chunk: whole pair tiles that fit the scratch
     const int64_t chunk = static_cast<int64_t>(kScratchBytes / (static_cast<size_t>(k) * 2)) / (2 * SW) * (2 * SW);
-    if (m <= QMM_GEMM_TWO_PHASE_MIN_M || chunk < 2 * SW)
+    if (!use_two_phase(m, k) || chunk < 2 * SW)
         return launch_gemm_q4_0(w, x, y, m, n, k, stream, ctx);
     void *scratch = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&scratch, g_prefill_scratch);

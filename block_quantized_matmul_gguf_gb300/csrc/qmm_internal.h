@@ -155,9 +155,12 @@ cudaError_t launch_gemm_q4_0_geglu(const uint8_t *wg, const uint8_t *wu, const u
                                    uint16_t *h, int64_t m, int64_t n, int64_t k,
                                    cudaStream_t stream, const LaunchCtx &ctx);
 
-#ifndef QMM_GEMM_TWO_PHASE_MIN_M
-#define QMM_GEMM_TWO_PHASE_MIN_M 256  // longer prompts take the two-phase path given a workspace
-#endif
+// When the two-phase GEMM pays: the dequant pass costs about 0.65 us per
+// million weights, the fused kernel's redundant decode grows with the
+// number of 256-token blocks.  Measured crossovers at 2048 tokens' scale:
+// N x K = 8192 x 2048 from m = 768, 16384 x 2048 from m = 1024; at
+// K = 8192 the two-phase GEMM wins from the second token block on.
+inline bool use_two_phase(int64_t m, int64_t k) { return m > 512 || (m > 256 && k >= 4096); }
 
 // Two-phase prefill GEMM (weights dequantised once into a bf16 workspace,
 // then a shared-memory-operand tensor-core GEMM).  gemm_workspace_bytes is

@@ -158,11 +158,11 @@ qmm_status qmm_gemm_q8_0(const void *w, const uint16_t *x_bf16, float *y, int64_
 /* ---- Prefill GEMM with a workspace (long prompts) -----------------------
  * The same products as qmm_gemm_q4_0 / qmm_gemm_q8_0 / qmm_gemm_q4_0_geglu,
  * with the same arithmetic (each weight rounded once to bf16, fp32 sums in
- * tensor memory) and accuracy bound.  For m > 256 with a workspace, the
- * weights are first dequantised once into the workspace as bf16 (so that
- * they are not decoded again for every 256-token block) and a second kernel
- * runs the tensor-core GEMM from it; otherwise the call is the fused one and
- * the workspace is not touched.
+ * tensor memory) and accuracy bound.  With a workspace, when m > 512 or
+ * (m > 256 and k >= 4096), the weights are first dequantised once into the
+ * workspace as bf16 (so that they are not decoded again for every 256-token
+ * block) and a second kernel runs the tensor-core GEMM from it; otherwise
+ * the call is the fused one and the workspace is not touched.
  * workspace : caller-owned device memory, 16-byte aligned, at least
  *             qmm_gemm_workspace_bytes(n, k) bytes (qmm_gemm_geglu_
  *             workspace_bytes for the GeGLU form), not overlapping any
@@ -181,10 +181,11 @@ qmm_status qmm_gemm_q8_0_ws(const void *w, const uint16_t *x_bf16, float *y, int
                             qmm_stream_t stream);
 
 /* The Q4_0 product of qmm_gemm_q4_0_ws without a caller workspace: for
- * m > 256 the weights are dequantised into a 64 MB scratch array that is
+ * long prompts the weights are dequantised into a 64 MB scratch array that is
  * part of the library (a module-scope device variable, one per GPU), in
  * column chunks of whole 256-row tiles that fit it, each chunk followed by
- * its GEMM; otherwise the fused call.  Allocates nothing.  Same requirements,
+ * its GEMM, under the same length rule as the _ws calls; otherwise the
+ * fused call.  Allocates nothing.  Same requirements,
  * arithmetic and accuracy as qmm_gemm_q4_0.  The scratch is shared by every
  * call of this entry point on the device, so calls on different streams must
  * not run concurrently (the caller orders them, e.g. with events). */

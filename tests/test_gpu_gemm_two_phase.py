@@ -35,8 +35,9 @@ def _weights(fmt, n, k, seed, stream=0):
 
 
 @pytest.mark.parametrize("fmt", ["q4_0", "q8_0"])
-@pytest.mark.parametrize("m,n,k", [(257, 4, 256), (300, 260, 512), (513, 768, 1024),
-                                   (700, 1000, 256), (1024, 384, 2048)])
+# two phases when m > 512, or m > 256 with k >= 4096
+@pytest.mark.parametrize("m,n,k", [(520, 4, 256), (600, 260, 512), (513, 768, 1024),
+                                   (700, 1000, 256), (1024, 384, 2048), (300, 136, 4096)])
 def test_two_phase_matches_oracle_and_fused(qmm, oracle_mod, fmt, m, n, k):
     w = _weights(fmt, n, k, seed=m + n)
     xb = synth.activations_bf16(m, k, seed=m + n, stream=5)
@@ -68,7 +69,7 @@ def test_two_phase_full_size_sampled(qmm, oracle_mod):
                   y_ref, bound, GEMM_REL, "two-phase full size")
 
 
-@pytest.mark.parametrize("m,n,k", [(300, 200, 512), (512, 384, 2048), (700, 1000, 256)])
+@pytest.mark.parametrize("m,n,k", [(600, 200, 512), (520, 384, 2048), (700, 1000, 256), (300, 72, 4096)])
 def test_two_phase_geglu(qmm, oracle_mod, m, n, k):
     wg = synth.q4_0_weights(n, k, seed=m, stream=0)
     wu = synth.q4_0_weights(n, k, seed=m, stream=1)
@@ -84,8 +85,9 @@ def test_two_phase_geglu(qmm, oracle_mod, m, n, k):
                         rel=GEMM_REL, out_rel=2.0 ** -8)
 
 
-def test_short_prompt_ignores_the_workspace(qmm):
-    m, n, k = 256, 512, 512
+@pytest.mark.parametrize("m,k", [(256, 512), (512, 2048), (256, 4096)])
+def test_short_prompt_ignores_the_workspace(qmm, m, k):
+    n = 512
     w, xb = synth.gemm_case(m, n, k, seed=9)
     ws = _ws(qmm, n, k)
     ws.fill_(0xA5)
@@ -96,11 +98,11 @@ def test_short_prompt_ignores_the_workspace(qmm):
 
 
 def test_workspace_argument_checks(qmm):
-    m, n, k = 300, 64, 256
+    m, n, k = 600, 64, 256
     w = torch.zeros(n * (k // 32) * 18, dtype=torch.uint8, device="cuda")
     x = torch.zeros((m, k), dtype=torch.int16, device="cuda")
     y = torch.empty((m, n), dtype=torch.float32, device="cuda")
-    need = qmm.qmm_gemm_workspace_bytes(n, k)
+    need = qmm.qmm_gemm_workspace_bytes(n, k)  # 32 KB: y (153.6 KB) covers it
     assert need == n * k * 2
     assert qmm.qmm_gemm_workspace_bytes(n, k, geglu=True) == (n + 63) // 64 * 128 * k * 2
     ws = torch.empty(need + 64, dtype=torch.uint8, device="cuda")
@@ -122,7 +124,7 @@ def _prefill(qmm, w, x, m, n, k):
     return y
 
 
-@pytest.mark.parametrize("m,n,k", [(300, 260, 512), (1024, 384, 2048), (200, 512, 512)])
+@pytest.mark.parametrize("m,n,k", [(600, 260, 512), (1024, 384, 2048), (200, 512, 512), (300, 256, 4096)])
 def test_prefill_static_scratch_equals_fused(qmm, oracle_mod, m, n, k):
     w, xb = synth.gemm_case(m, n, k, seed=m + 1)
     wd, xd = to_dev(w, torch), bf16_tensor(xb, torch)
