@@ -50,6 +50,14 @@ from block_quantized_matmul_gguf_gb300 import synth  # noqa: E402
 
 METRIC = "quant GEMV weight GB/s (% of HBM peak); Q4_0 prefill GEMM TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# Non-tensor FP32 FMA peak from unit counts and clock (no measured figure is
+# available): 152 SMs x 128 FMA lanes x 2 flop per cycle at the maximum SM clock.
+GB300_SMS = 152
+FP32_LANES_PER_SM = 128
+
+
+def fp32_peak_tflops(peaks) -> float:
+    return GB300_SMS * FP32_LANES_PER_SM * 2 * float(peaks.get("sm_max_mhz", 2070.0)) * 1e6 / 1e12
 
 
 def parse_args(argv=None):
@@ -438,7 +446,13 @@ def run_secondary(torch, qmm, l2, stream, timer, peaks):
         el = timer.run(lambda: layer.run_steps(steps))
         gbs = layer.step_bytes * steps / el / 1e9
         resident = layer.R * layer.step_bytes
+        # at M rows each weight takes M FMAs (2M flop) per 18/32 (Q4_0) or
+        # 34/32 (Q8_0) bytes: the FP32-issue ceiling in weight bytes per second
+        bpw = (18 if fmt == "q4_0" else 34) / 32.0
+        fp32_ceiling = fp32_peak_tflops(peaks) * 1e12 * bpw / (2 * m) / 1e9
         out[name] = {"gbs": round(gbs, 1), "frac_hbm": round(gbs / hbm, 4),
+                     "fp32_ceiling_gbs": round(fp32_ceiling, 1),
+                     "frac_of_min_ceiling": round(gbs / min(hbm, fp32_ceiling), 4),
                      "us_per_call": round(el / steps / layer.launches_per_step * 1e6, 3),
                      "replicas": layer.R,
                      "l2": ("weights rotate through %d replicas (%.0f MB, %s)"
@@ -620,12 +634,28 @@ def cpu_baseline(seconds: float):
         if el1 >= seconds / 4:
             break
     oracle.set_threads(cores)
+    # the prefill GEMM oracle on a slice of its workload: 16 of the 2048 tokens
+    # of the 2048 x 8192 x 2048 product
+    gp = synth.PREFILL_SHAPES[0]
+    gw, gx = synth.gemm_case(16, gp.n, gp.k, seed=0, stream=70)
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        oracle.gemm_q4_0(gw, gx, 16, gp.n, gp.k)
+        reps += 1
+        elg = time.perf_counter() - t0
+        if elg >= min(3.0, seconds / 4):
+            break
+    gemm_gflops = 2.0 * 16 * gp.n * gp.k * reps / elg / 1e9
     return {"value": round(value, 4), "unit": "GB/s", "cores": cores,
             "kind": "oracle",
             "sample": f"{passes} full passes of the decode-layer set (M=1, 7 Q4_0 projections) "
                       f"in {el:.1f} s, binary64 C oracle, {cores} OpenMP threads",
             "single_thread": {"value": round(step_bytes * passes1 / el1 / 1e9, 4), "unit": "GB/s",
-                              "sample": f"{passes1} passes in {el1:.1f} s on 1 thread"}}
+                              "sample": f"{passes1} passes in {el1:.1f} s on 1 thread"},
+            "gemm": {"value": round(gemm_gflops, 3), "unit": "GFLOP/s",
+                     "sample": f"{reps} passes of 16 tokens x {gp.n} x {gp.k} (Q4_0, bf16 X) in "
+                               f"{elg:.1f} s, binary64 C oracle, {cores} OpenMP threads"}}
 
 
 # ----------------------------------------------------------------- arms
