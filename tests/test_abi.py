@@ -86,3 +86,70 @@ def test_multi_argument_checks(lib):
     arr[1].y = 8192
     assert lib.qmm_gemv_q4_0_multi(arr, 2, 16, 1, 48, 0) == qmm.QMM_ERR_SHAPE     # k % 32
     assert lib.qmm_gemv_q4_0_multi(arr, 2, 16, 17, 64, 0) == qmm.QMM_ERR_SHAPE    # m
+
+
+# ---- the entry points added for the fused FFN, Q8_0 prefill and workspaces ----
+# (fake, never dereferenced pointer values: every case fails a check before any
+# CUDA call; 1 << 24 apart so that ranges do not overlap unless meant to)
+
+A, B, C, D, WS = 1 << 24, 2 << 24, 3 << 24, 4 << 24, 5 << 24
+
+
+def test_geglu_gemv_argument_checks(lib):
+    L = lib
+    assert L.qmm_gemv_q4_0_geglu(0, B, C, D, 1, 64, 256, 0) == qmm.QMM_ERR_NULL
+    assert L.qmm_gemv_q4_0_geglu(A, 0, C, D, 1, 64, 256, 0) == qmm.QMM_ERR_NULL
+    assert L.qmm_gemv_q4_0_geglu(A, B, 0, D, 1, 64, 256, 0) == qmm.QMM_ERR_NULL
+    assert L.qmm_gemv_q4_0_geglu(A, B, C, 0, 1, 64, 256, 0) == qmm.QMM_ERR_NULL
+    assert L.qmm_gemv_q4_0_geglu(A, B, C, D, 0, 64, 256, 0) == qmm.QMM_ERR_SHAPE
+    assert L.qmm_gemv_q4_0_geglu(A, B, C, D, 17, 64, 256, 0) == qmm.QMM_ERR_SHAPE
+    assert L.qmm_gemv_q4_0_geglu(A, B, C, D, 1, 64, 100, 0) == qmm.QMM_ERR_SHAPE
+    assert L.qmm_gemv_q4_0_geglu(A, B, C + 2, D, 1, 64, 256, 0) == qmm.QMM_ERR_ALIGN
+    assert L.qmm_gemv_q4_0_geglu(A, B, C, C + 64, 1, 64, 256, 0) == qmm.QMM_ERR_UNSUPPORTED  # h over x
+    assert L.qmm_gemv_q4_0_geglu(A, B, C, B + 16, 1, 64, 256, 0) == qmm.QMM_ERR_UNSUPPORTED  # h over wu
+
+
+def test_q8_0_gemm_and_prefill_argument_checks(lib):
+    L = lib
+    for f in (L.qmm_gemm_q8_0, L.qmm_gemm_q4_0_prefill):
+        assert f(0, B, C, 256, 256, 256, 0) == qmm.QMM_ERR_NULL
+        assert f(A, 0, C, 256, 256, 256, 0) == qmm.QMM_ERR_NULL
+        assert f(A, B, 0, 256, 256, 256, 0) == qmm.QMM_ERR_NULL
+        assert f(A, B, C, 0, 256, 256, 0) == qmm.QMM_ERR_SHAPE
+        assert f(A, B, C, 256, 256, 100, 0) == qmm.QMM_ERR_SHAPE
+        assert f(A, B, C, 256, 256, 288, 0) == qmm.QMM_ERR_UNSUPPORTED   # k % 256
+        assert f(A, B, C, 256, 254, 256, 0) == qmm.QMM_ERR_UNSUPPORTED   # n % 4
+        assert f(A + 8, B, C, 256, 256, 256, 0) == qmm.QMM_ERR_ALIGN
+        assert f(A, B + 8, C, 256, 256, 256, 0) == qmm.QMM_ERR_ALIGN
+
+
+def test_geglu_gemm_argument_checks(lib):
+    L = lib
+    assert L.qmm_gemm_q4_0_geglu(0, B, C, D, 256, 64, 256, 0) == qmm.QMM_ERR_NULL
+    assert L.qmm_gemm_q4_0_geglu(A, B, C, D, 0, 64, 256, 0) == qmm.QMM_ERR_SHAPE
+    assert L.qmm_gemm_q4_0_geglu(A, B, C, D, 256, 64, 288, 0) == qmm.QMM_ERR_UNSUPPORTED
+    assert L.qmm_gemm_q4_0_geglu(A, B + 8, C, D, 256, 64, 256, 0) == qmm.QMM_ERR_ALIGN
+    assert L.qmm_gemm_q4_0_geglu(A, B, C, D + 1, 256, 64, 256, 0) == qmm.QMM_ERR_ALIGN
+    assert L.qmm_gemm_q4_0_geglu(A, B, C, C + 256, 256, 64, 256, 0) == qmm.QMM_ERR_UNSUPPORTED
+
+
+def test_workspace_sizes_and_checks(lib):
+    assert qmm.qmm_gemm_workspace_bytes(8192, 2048) == 8192 * 2048 * 2
+    assert qmm.qmm_gemm_workspace_bytes(100, 256) == 100 * 256 * 2
+    assert qmm.qmm_gemm_workspace_bytes(0, 256) == 0
+    # GeGLU: 128 rows (64 gate + 64 up) per 64 features
+    assert qmm.qmm_gemm_workspace_bytes(100, 256, geglu=True) == 2 * 128 * 256 * 2
+    assert qmm.qmm_gemm_workspace_bytes(8192, 2048, geglu=True) == 8192 * 2 * 2048 * 2
+    L = lib
+    m, n, k = 600, 256, 256  # m > 512: the two-phase path, so the workspace is checked
+    need = n * k * 2
+    for f in (L.qmm_gemm_q4_0_ws, L.qmm_gemm_q8_0_ws):
+        assert f(A, B, C, m, n, k, WS, need - 1, 0) == qmm.QMM_ERR_SHAPE
+        assert f(A, B, C, m, n, k, WS + 8, need, 0) == qmm.QMM_ERR_ALIGN
+        assert f(A, B, C, m, n, k, C + 1024, need, 0) == qmm.QMM_ERR_UNSUPPORTED  # over y
+        assert f(A, B, C, m, n, k, A, need, 0) == qmm.QMM_ERR_UNSUPPORTED         # over w
+    gneed = qmm.qmm_gemm_workspace_bytes(n, k, geglu=True)
+    g = L.qmm_gemm_q4_0_geglu_ws
+    assert g(A, B, C, D, m, n, k, WS, gneed - 1, 0) == qmm.QMM_ERR_SHAPE
+    assert g(A, B, C, D, m, n, k, WS + 8, gneed, 0) == qmm.QMM_ERR_ALIGN
+    assert g(A, B, C, D, m, n, k, B, gneed, 0) == qmm.QMM_ERR_UNSUPPORTED           # over wu
