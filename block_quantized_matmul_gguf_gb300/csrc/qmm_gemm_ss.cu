@@ -46,6 +46,9 @@ constexpr int SUMMA_K = 16;
 #ifndef QMM_SS_STAGES
 #define QMM_SS_STAGES 6
 #endif
+#ifndef QMM_SS_SPLIT_TAIL
+#define QMM_SS_SPLIT_TAIL 1  // 1: a sparse last round runs as 128-token half tiles
+#endif
 constexpr int SSTAGES = QMM_SS_STAGES;
 constexpr int A_TILE_BYTES = SW * SK * 2;      // 16 KB
 constexpr int B_TILE_BYTES = ST_CTA * SK * 2;  // 16 KB
@@ -76,10 +79,14 @@ struct SsLayout {
 };
 static_assert(SsLayout::smem_bytes <= 232448, "shared memory per CTA");
 
-// kind::f16: D fp32, A and B bf16, both K-major, N = 256, M = 256 (the pair).
-constexpr uint32_t kSsIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
-                              (static_cast<uint32_t>(ST >> 3) << 17) |
-                              (static_cast<uint32_t>((2 * SW) >> 4) << 24);
+// kind::f16: D fp32, A and B bf16, both K-major, M = 256 (the pair), N = 256
+// tokens (a full tile) or 128 (a half tile of the last round).
+constexpr uint32_t ss_idesc(int n_tokens) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n_tokens >> 3) << 17) |
+           (static_cast<uint32_t>((2 * SW) >> 4) << 24);
+}
+constexpr uint32_t kSsIdesc = ss_idesc(ST);
+constexpr uint32_t kSsIdescHalf = ss_idesc(ST / 2);
 
 struct SsParams {
     float *y;     // plain: fp32 [m][ldy]
@@ -88,8 +95,31 @@ struct SsParams {
     int ldy;      // row stride of y (n, or wider when a call covers a column range)
     int num_t_blocks;  // token blocks of ST
     int num_tiles;     // pair tiles
+    int full_items;    // work items 0 .. full_items-1 are whole tiles ...
+    int num_items;     // ... the rest are half tiles (128 tokens) of the last round
     LaunchCtx ctx;
 };
+
+// Work item w of the persistent schedule: a whole tile, or -- when the last
+// round would leave most pairs idle -- one 128-token half of a tile.
+struct SsItem {
+    int tb, wb;   // token block, weight block
+    int tok0;     // first token
+    bool half;    // 128 tokens instead of 256
+};
+__device__ __forceinline__ SsItem ss_item(const SsParams &p, int w) {
+    SsItem it;
+    int t = w, hh = 0;
+    it.half = w >= p.full_items;
+    if (it.half) {
+        t = p.full_items + ((w - p.full_items) >> 1);
+        hh = (w - p.full_items) & 1;
+    }
+    it.tb = t % p.num_t_blocks;
+    it.wb = t / p.num_t_blocks;
+    it.tok0 = it.tb * ST + hh * (ST / 2);
+    return it;
+}
 
 // D (TMEM) += A (shared-memory descriptor) x B (shared-memory descriptor),
 // both CTAs' halves.
@@ -195,7 +225,8 @@ __global__ void __launch_bounds__(kDeqThreads) dequant_bf16_kernel(const uint8_t
 template <bool G>
 __global__ void __launch_bounds__(S_THREADS, 1)
     gemm_ss_kernel(const __grid_constant__ CUtensorMap tmap_a,
-                   const __grid_constant__ CUtensorMap tmap_x, SsParams p) {
+                   const __grid_constant__ CUtensorMap tmap_x,
+                   const __grid_constant__ CUtensorMap tmap_x_half, SsParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_base = smem_addr(smem_raw);
     const uint32_t sbase = (raw_base + 1023u) & ~1023u;  // 1024-byte aligned (swizzle atoms)
@@ -241,31 +272,35 @@ __global__ void __launch_bounds__(S_THREADS, 1)
     pdl_wait();  // the workspace and X are written by preceding kernels
 
     const int KB = p.k / SK;
-    const uint32_t my_tiles =
-        pair < p.num_tiles ? static_cast<uint32_t>((p.num_tiles - pair + num_pairs - 1) / num_pairs) : 0u;
+    const uint32_t my_items =
+        pair < p.num_items ? static_cast<uint32_t>((p.num_items - pair + num_pairs - 1) / num_pairs) : 0u;
 
     if (warp == S_WARP_PROD) {
         if (lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_a)) : "memory");
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_x)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_x_half)) : "memory");
             uint32_t it = 0;
             int s = 0;
             uint32_t ph = 0;
             bool ok = true;
-            for (int t = pair; ok && t < p.num_tiles; t += num_pairs) {
-                const int tb = t % p.num_t_blocks, wb = t / p.num_t_blocks;
-                const int arow = wb * 2 * SW + static_cast<int>(rank) * SW;
-                const int xrow = tb * ST + static_cast<int>(rank) * ST_CTA;
+            for (int w = pair; ok && w < p.num_items; w += num_pairs) {
+                const SsItem item = ss_item(p, w);
+                const int arow = item.wb * 2 * SW + static_cast<int>(rank) * SW;
+                // this CTA's share of the item's tokens: 128 (whole tile) or 64 (half)
+                const int xrow = item.tok0 + static_cast<int>(rank) * (item.half ? ST_CTA / 2 : ST_CTA);
+                const uint32_t bytes = item.half ? A_TILE_BYTES + B_TILE_BYTES / 2 : SSTAGE_BYTES;
+                const CUtensorMap *xmap = item.half ? &tmap_x_half : &tmap_x;
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!wait_or_abort(empty(s), ph ^ 1u, abort_flag, ctx)) {
                         ok = false;
                         break;
                     }
                     const uint32_t xf = map_to_rank(full(s), 0);
-                    mbar_expect_tx_cluster(xf, SSTAGE_BYTES);
+                    mbar_expect_tx_cluster(xf, bytes);
                     const uint32_t dst = sbase + s * SSTAGE_BYTES;
                     tma_load_2d_pair(dst, &tmap_a, kb * SK, arow, xf);
-                    tma_load_2d_pair(dst + A_TILE_BYTES, &tmap_x, kb * SK, xrow, xf);
+                    tma_load_2d_pair(dst + A_TILE_BYTES, xmap, kb * SK, xrow, xf);
                     ++it;
                     if (++s == SSTAGES) {
                         s = 0;
@@ -284,7 +319,9 @@ __global__ void __launch_bounds__(S_THREADS, 1)
         }
     } else if (warp == S_WARP_MMA) {
         if (leader && lane == 0) {
-            const uint32_t total = my_tiles * static_cast<uint32_t>(KB);
+            const uint32_t total = my_items * static_cast<uint32_t>(KB);
+            int w = pair;  // the current work item
+            uint32_t idesc = ss_item(p, w).half ? kSsIdescHalf : kSsIdesc;
             const uint64_t desc0 = sw128_desc(sbase);
             constexpr uint64_t kStageStep = SSTAGE_BYTES >> 4;  // descriptor address units
             constexpr uint64_t kBOffset = A_TILE_BYTES >> 4;
@@ -303,7 +340,7 @@ __global__ void __launch_bounds__(S_THREADS, 1)
                 const uint32_t d_tmem = tmem_base + buf * SS_D_COLS;
 #pragma unroll
                 for (int kk = 0; kk < SK / SUMMA_K; ++kk)  // 32 bytes along the swizzle row
-                    umma_bf16_pair_ss(d_tmem, adesc + 2 * kk, adesc + kBOffset + 2 * kk, kSsIdesc,
+                    umma_bf16_pair_ss(d_tmem, adesc + 2 * kk, adesc + kBOffset + 2 * kk, idesc,
                                       (kk != 0 || kb != 0) ? 1u : 0u);
                 issued = true;
                 umma_commit_pair(empty(s));
@@ -312,6 +349,8 @@ __global__ void __launch_bounds__(S_THREADS, 1)
                     kb = 0;
                     ++tile;
                     buf ^= 1u;
+                    w += num_pairs;
+                    if (w < p.num_items) idesc = ss_item(p, w).half ? kSsIdescHalf : kSsIdesc;
                 }
                 if (++s == SSTAGES) {
                     s = 0;
@@ -330,11 +369,15 @@ __global__ void __launch_bounds__(S_THREADS, 1)
         // epilogue: lane i of lane quarter q holds accumulator row 32q+i;
         // columns are tokens (the leader's 128, then the peer's)
         const int q = warp & 3;
-        constexpr int CPW = (ST / 32) / (S_EPI / 4);  // 32-column chunks per warp
-        const int c0 = ((warp - S_WARP_EPI0) >> 2) * CPW;
+        constexpr int CPW = (ST / 32) / (S_EPI / 4);  // 32-column chunks per warp (whole tile)
+        const int part = (warp - S_WARP_EPI0) >> 2;   // which share of the columns
         uint32_t tile = 0;
-        for (int t = pair; t < p.num_tiles; t += num_pairs, ++tile) {
-            const int tb = t % p.num_t_blocks, wb = t / p.num_t_blocks;
+        for (int w = pair; w < p.num_items; w += num_pairs, ++tile) {
+            const SsItem item = ss_item(p, w);
+            const int wb = item.wb;
+            // accumulator column j is token tok0 + j (the leader's tokens, then the peer's)
+            const int cpw = item.half ? CPW / 2 : CPW;
+            const int c0 = part * cpw;
             const int buf = static_cast<int>(tile & 1u);
             if (!warp_wait_or_abort(d_full(buf), (tile >> 1) & 1u, abort_flag, ctx)) break;
             tc_fence_after();
@@ -344,10 +387,10 @@ __global__ void __launch_bounds__(S_THREADS, 1)
                 const int f = wb * SW + static_cast<int>(rank) * (SW / 2) + q * 16 + (lane & 15);
                 const bool f_ok = f < p.n;
 #pragma unroll 1
-                for (int c = c0; c < c0 + CPW; ++c) {
+                for (int c = c0; c < c0 + cpw; ++c) {
                     uint32_t v[32];
                     tmem_ld_32cols(d_lane + c * 32, v);
-                    const int m0 = tb * ST + c * 32 + (upper ? 16 : 0);
+                    const int m0 = item.tok0 + c * 32 + (upper ? 16 : 0);
                     uint16_t hv[16];
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
@@ -367,10 +410,10 @@ __global__ void __launch_bounds__(S_THREADS, 1)
                 const int n = wb * 2 * SW + static_cast<int>(rank) * SW + q * 32 + lane;
                 const bool n_ok = n < p.n;
 #pragma unroll 1
-                for (int c = c0; c < c0 + CPW; ++c) {
+                for (int c = c0; c < c0 + cpw; ++c) {
                     uint32_t v[32];
                     tmem_ld_32cols(d_lane + c * 32, v);
-                    const int m0 = tb * ST + c * 32;
+                    const int m0 = item.tok0 + c * 32;
                     if (n_ok) {
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
@@ -409,10 +452,12 @@ cudaError_t launch_two_phase(const uint8_t *w, const uint8_t *w2, const uint16_t
                                   1, w, w2, ws, n, k, rows, 0x4B000000u);
     if (e != cudaSuccess) return e;
     // phase 2
-    CUtensorMap ta, tx;
+    CUtensorMap ta, tx, tx_half;
     if (!encode_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ws, k, rows, k * 2, SK, SW,
                         CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, k, m, k * 2, SK, ST_CTA,
+                        CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tmap_2d(&tx_half, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, k, m, k * 2, SK, ST_CTA / 2,
                         CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     SsParams p;
@@ -427,12 +472,19 @@ cudaError_t launch_two_phase(const uint8_t *w, const uint8_t *w2, const uint16_t
     const int64_t per_tile = G ? SW : 2 * SW;
     p.num_tiles = p.num_t_blocks * static_cast<int>((n + per_tile - 1) / per_tile);
     p.ctx = ctx;
+    const int pair_count = std::max(1, device_sm_count() / 2);
+    // a last round that would leave more than half the pairs idle runs as
+    // 128-token halves of its tiles
+    const int rem = p.num_tiles % pair_count;
+    const bool split = QMM_SS_SPLIT_TAIL && p.num_tiles > pair_count && rem > 0 && 2 * rem <= pair_count;
+    p.full_items = split ? p.num_tiles - rem : p.num_tiles;
+    p.num_items = split ? p.num_tiles + rem : p.num_tiles;
     static int smem_limits[kMaxDevices] = {0};
     e = ensure_smem(gemm_ss_kernel<G>, SsLayout::smem_bytes, true, smem_limits);
     if (e != cudaSuccess) return e;
-    const int pairs = std::max(1, std::min(p.num_tiles, device_sm_count() / 2));
+    const int pairs = std::min(p.num_items, pair_count);
     return launch_kernel(gemm_ss_kernel<G>, dim3(2 * pairs), dim3(S_THREADS), SsLayout::smem_bytes,
-                         stream, 2, ta, tx, p);
+                         stream, 2, ta, tx, tx_half, p);
 }
 
 // The library's own scratch for qmm_gemm_q4_0_prefill: bf16 weight rows of

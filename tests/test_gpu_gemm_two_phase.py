@@ -148,3 +148,40 @@ def test_prefill_static_scratch_column_chunks(qmm, oracle_mod):
     mi = np.concatenate([mi[:1496], [0, 1, m - 1, m - 1]])
     y_ref, bound = oracle_mod.gemm_q4_0_at(w, xb, m, n, k, mi, ni)
     assert_within(y.cpu().numpy()[mi, ni], y_ref, bound, GEMM_REL, "prefill chunks")
+
+
+# ---- sparse last rounds run as 128-token half tiles ----
+
+@pytest.mark.parametrize("m,n,k", [(1900, 2560, 512), (2048, 2560, 256)])
+def test_two_phase_half_tile_tail(qmm, oracle_mod, m, n, k):
+    """80 pair tiles over 76 pairs: the last 4 tiles run as 8 half tiles (ragged
+    tokens in the first shape)."""
+    w, xb = synth.gemm_case(m, n, k, seed=n + m)
+    wd, xd = to_dev(w, torch), bf16_tensor(xb, torch)
+    y2 = qmm.gemm("q4_0", wd, xd, n, k, workspace=_ws(qmm, n, k))
+    y1 = qmm.gemm("q4_0", wd, xd, n, k)
+    torch.cuda.synchronize()
+    assert qmm.qmm_get_device_error() == 0
+    assert torch.equal(y2, y1)
+    rng = np.random.default_rng(m)
+    mi = np.concatenate([rng.integers(0, m, 3000), [m - 1, m - 1, 1792, 1920 % m]])
+    ni = np.concatenate([rng.integers(0, n, 3000), [n - 1, 0, 2559, 2304]])
+    y_ref, bound = oracle_mod.gemm_q4_0_at(w, xb, m, n, k, mi, ni)
+    assert_within(y2.cpu().numpy()[mi, ni], y_ref, bound, GEMM_REL, f"half tail {m}x{n}x{k}")
+
+
+def test_two_phase_geglu_half_tile_tail(qmm, oracle_mod):
+    """GeGLU with 1280 features: 8 token blocks x 10 feature blocks = 80 tiles."""
+    m, n, k = 2048, 1280, 512
+    wg = synth.q4_0_weights(n, k, seed=8, stream=0)
+    wu = synth.q4_0_weights(n, k, seed=8, stream=1)
+    xb = synth.activations_bf16(m, k, seed=8, stream=2)
+    a, b, xd = to_dev(wg, torch), to_dev(wu, torch), bf16_tensor(xb, torch)
+    h2 = qmm.gemm_geglu_q4_0(a, b, xd, n, k, workspace=_ws(qmm, n, k, geglu=True))
+    h1 = qmm.gemm_geglu_q4_0(a, b, xd, n, k)
+    torch.cuda.synchronize()
+    assert qmm.qmm_get_device_error() == 0
+    assert torch.equal(h2, h1)
+    h_ref, g, u, bg, bu = oracle_mod.geglu_q4_0(wg, wu, _bf16_to_f32(xb)[1792:], m - 1792, n, k)
+    assert_geglu_within(_bf16_to_f32(h2[1792:].cpu().numpy()), h_ref, g, u, bg, bu, "geglu tail",
+                        rel=GEMM_REL, out_rel=2.0 ** -8)
