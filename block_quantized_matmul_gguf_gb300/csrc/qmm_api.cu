@@ -369,7 +369,7 @@ const char *qmm_status_string(qmm_status status) {
     return "unknown status";
 }
 
-int qmm_version(void) { return 100; }
+int qmm_version(void) { return 200; }
 
 qmm_status qmm_get_device_error(qmm_stream_t stream) {
     cudaError_t e;

@@ -11,7 +11,11 @@
  *
  *   dequant : W (blocks) -> dense fp32 W[N][K], bit-exact
  *   gemv    : y[m][n] = sum_k x[m][k] * w[n][k], fp32 x, M = 1..16 rows
- *   gemm    : Y[m][n] = sum_k X[m][k] * w[n][k], bf16 X, M >= 1 (prefill)
+ *             (one weight matrix, or up to four sharing x in one launch)
+ *   gemm    : Y[m][n] = sum_k X[m][k] * w[n][k], bf16 X, M >= 1 (prefill),
+ *             fused, or in two phases through a bf16 workspace
+ *   geglu   : h = gelu(x.Wg^T) * (x.Wu^T), the feed-forward input, for
+ *             decode (gemv) and prefill (gemm)
  *
  * Block formats (GGUF; 32 weights per block, K a multiple of 32):
  *   Q4_0, 18 bytes: binary16 scale d (little endian) then qs[16]; qs[j] holds
@@ -26,9 +30,11 @@
  * Ownership and execution.  Every pointer is a caller-owned DEVICE pointer on
  * the current CUDA device.  Outputs are overwritten, never accumulated into.
  * Calls are asynchronous on `stream` (NULL = legacy default stream) and never
- * synchronise.  The library allocates no device memory; its only device
- * state is one error word per GPU (a module-scope variable).  Calls
- * on different streams may run concurrently.  Kernels are launched with
+ * synchronise.  The library allocates no device memory; its device state is
+ * one error word per GPU and the 64 MB scratch array of
+ * qmm_gemm_q4_0_prefill (module-scope variables).  Calls on different
+ * streams may run concurrently, except qmm_gemm_q4_0_prefill (shared
+ * scratch) and _ws calls sharing a workspace.  Kernels are launched with
  * programmatic dependent launch: a call may start while the preceding
  * kernel of this library in the same stream is finishing, and waits for it
  * before reading activations or writing outputs.  A GEMV may read its weight
