@@ -53,3 +53,23 @@ def test_single_process_defaults(monkeypatch):
     assert bench.aggregate(10.0, 2.0, 1) == 5.0
     args = bench.parse_args([])
     assert args.steps >= 1 and args.warmup >= 3 and args.impl == "ours"
+
+
+def test_reference_arm_json_contract(monkeypatch):
+    """The reference arm (the oracle on the host cores) prints the same line
+    as ours, marked impl=reference, with its own CPU baseline and zero e2e copies."""
+    for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+    import bench
+    args = bench.parse_args(["--impl", "reference", "--steps", "1", "--warmup", "3"])
+    line = bench.run_reference(args, bench.Dist())
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "dtype", "config", "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC
+    assert line["value"] > 0 and line["unit"] == "GB/s" and line["warmup"] >= 3
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"]
+    e2e = line["e2e"]
+    assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+    assert e2e["value"] == line["value"] and e2e["unit"] == line["unit"]
