@@ -44,7 +44,7 @@ constexpr int ST_CTA = ST / 2;
 constexpr int SK = 64;                 // K per stage (one 128-byte swizzle row)
 constexpr int SUMMA_K = 16;
 #ifndef QMM_SS_STAGES
-#define QMM_SS_STAGES 6
+#define QMM_SS_STAGES 7
 #endif
 #ifndef QMM_SS_SPLIT_TAIL
 #define QMM_SS_SPLIT_TAIL 1  // 1: a sparse last round runs as 128-token half tiles
