@@ -128,14 +128,28 @@ qmm_status check_workspace(const void *ws, size_t ws_bytes, size_t need) {
     return QMM_OK;
 }
 
-qmm_status gemm(Fmt fmt, const void *w, const uint16_t *x_bf16, float *y, int64_t m, int64_t n,
-                int64_t k, qmm_stream_t stream, void *ws = nullptr, size_t ws_bytes = 0) {
+// Checks shared by the tensor-core GEMM entry points (plain product): y is
+// fp32 [m][n], written with 4-byte stores; y may overlap neither input.
+qmm_status check_gemm(Fmt fmt, const void *w, const uint16_t *x_bf16, const float *y, int64_t m,
+                      int64_t n, int64_t k) {
     qmm_status s = check_wk(w, n, k);
     if (s != QMM_OK) return s;
     if (!x_bf16 || !y) return QMM_ERR_NULL;
-    if (m < 1 || m > (int64_t(1) << 31)) return QMM_ERR_SHAPE;
-    if (k % 256 != 0 || n % 4 != 0) return QMM_ERR_UNSUPPORTED;
-    if (!aligned(w, 16) || !aligned(x_bf16, 16) || !aligned(y, 16)) return QMM_ERR_ALIGN;
+    if (m < 1) return QMM_ERR_SHAPE;
+    if (k % 256 != 0 || m > kGemmMaxM || n > kGemmMaxN || k > kGemmMaxK)
+        return QMM_ERR_UNSUPPORTED;
+    if (!aligned(w, 16) || !aligned(x_bf16, 16) || !aligned(y, 4)) return QMM_ERR_ALIGN;
+    const size_t ybytes = sizeof(float) * static_cast<size_t>(m) * n;
+    const size_t wbytes = static_cast<size_t>(n) * (k / kQK) * block_bytes(fmt);
+    if (overlaps(y, ybytes, w, wbytes) || overlaps(y, ybytes, x_bf16, 2 * static_cast<size_t>(m) * k))
+        return QMM_ERR_UNSUPPORTED;
+    return QMM_OK;
+}
+
+qmm_status gemm(Fmt fmt, const void *w, const uint16_t *x_bf16, float *y, int64_t m, int64_t n,
+                int64_t k, qmm_stream_t stream, void *ws = nullptr, size_t ws_bytes = 0) {
+    qmm_status s = check_gemm(fmt, w, x_bf16, y, m, n, k);
+    if (s != QMM_OK) return s;
     const bool two_phase = ws != nullptr && use_two_phase(m, k);
     if (two_phase) {
         const size_t need = gemm_workspace_bytes(n, k, false);
@@ -277,12 +291,8 @@ qmm_status qmm_gemm_q8_0(const void *w, const uint16_t *x_bf16, float *y, int64_
 
 qmm_status qmm_gemm_q4_0_prefill(const void *w, const uint16_t *x_bf16, float *y, int64_t m,
                                  int64_t n, int64_t k, qmm_stream_t stream) {
-    qmm_status s = check_wk(w, n, k);
+    qmm_status s = check_gemm(Fmt::Q4_0, w, x_bf16, y, m, n, k);
     if (s != QMM_OK) return s;
-    if (!x_bf16 || !y) return QMM_ERR_NULL;
-    if (m < 1 || m > (int64_t(1) << 31)) return QMM_ERR_SHAPE;
-    if (k % 256 != 0 || n % 4 != 0) return QMM_ERR_UNSUPPORTED;
-    if (!aligned(w, 16) || !aligned(x_bf16, 16) || !aligned(y, 16)) return QMM_ERR_ALIGN;
     LaunchCtx ctx;
     if (!make_ctx(&ctx)) return QMM_ERR_CUDA;
     return from_cuda(launch_gemm_q4_0_prefill(static_cast<const uint8_t *>(w), x_bf16, y, m, n, k,
@@ -324,8 +334,8 @@ qmm_status qmm_gemm_q4_0_geglu_ws(const void *wg, const void *wu, const uint16_t
     if (s == QMM_OK) s = check_wk(wu, n, k);
     if (s != QMM_OK) return s;
     if (!x_bf16 || !h_bf16) return QMM_ERR_NULL;
-    if (m < 1 || m > (int64_t(1) << 31)) return QMM_ERR_SHAPE;
-    if (k % 256 != 0) return QMM_ERR_UNSUPPORTED;
+    if (m < 1) return QMM_ERR_SHAPE;
+    if (k % 256 != 0 || m > kGemmMaxM || n > kGemmMaxN || k > kGemmMaxK) return QMM_ERR_UNSUPPORTED;
     if (!aligned(wg, 16) || !aligned(wu, 16) || !aligned(x_bf16, 16) || !aligned(h_bf16, 2))
         return QMM_ERR_ALIGN;
     const size_t hbytes = sizeof(uint16_t) * static_cast<size_t>(m) * n;
@@ -369,7 +379,7 @@ const char *qmm_status_string(qmm_status status) {
     return "unknown status";
 }
 
-int qmm_version(void) { return 200; }
+int qmm_version(void) { return 201; }
 
 qmm_status qmm_get_device_error(qmm_stream_t stream) {
     cudaError_t e;

@@ -439,52 +439,79 @@ __global__ void __launch_bounds__(S_THREADS, 1)
 // Workspace rows: N (plain) or 128 rows per 64 features (GeGLU).
 int64_t workspace_rows(int64_t n, bool geglu) { return geglu ? (n + 63) / 64 * 128 : n; }
 
+// One two-phase product, split into the host work that can fail (tensor-map
+// encoding, kernel attributes) and the two launches, so that a caller
+// issuing several products can finish every check before launching any.
+template <Fmt F, bool G>
+struct TwoPhase {
+    const uint8_t *w = nullptr, *w2 = nullptr;
+    uint16_t *ws = nullptr;
+    int64_t n = 0, k = 0, rows = 0;
+    unsigned grid1 = 0;
+    int pairs = 0;
+    CUtensorMap ta, tx, tx_half;
+    SsParams p;
+
+    // ldy: row stride of y (0: n).  Launches nothing.
+    cudaError_t prepare(const uint8_t *w_, const uint8_t *w2_, const uint16_t *x, float *y,
+                        uint16_t *h, int64_t m, int64_t n_, int64_t k_, uint16_t *ws_,
+                        const LaunchCtx &ctx, int64_t ldy = 0) {
+        if (m > (1 << 30) || n_ > (1 << 30) || k_ > (1 << 24)) return cudaErrorInvalidValue;
+        w = w_;
+        w2 = w2_;
+        ws = ws_;
+        n = n_;
+        k = k_;
+        rows = workspace_rows(n, G);
+        const int64_t groups = (rows * (k / kQK) + kDeqThreads - 1) / kDeqThreads;
+        grid1 = static_cast<unsigned>(std::min<int64_t>(groups, 8LL * device_sm_count()));
+        if (!encode_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ws, k, rows, k * 2, SK, SW,
+                            CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, k, m, k * 2, SK, ST_CTA,
+                            CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_tmap_2d(&tx_half, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, k, m, k * 2, SK,
+                            ST_CTA / 2, CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+        p.y = y;
+        p.h = h;
+        p.m = static_cast<int>(m);
+        p.n = static_cast<int>(n);
+        p.k = static_cast<int>(k);
+        p.ldy = static_cast<int>(ldy > 0 ? ldy : n);
+        p.num_t_blocks = static_cast<int>((m + ST - 1) / ST);
+        // a pair tile covers 256 workspace rows: 256 outputs, or 128 GeGLU features
+        const int64_t per_tile = G ? SW : 2 * SW;
+        p.num_tiles = p.num_t_blocks * static_cast<int>((n + per_tile - 1) / per_tile);
+        p.ctx = ctx;
+        const int pair_count = std::max(1, device_sm_count() / 2);
+        // a last round that would leave more than half the pairs idle runs as
+        // 128-token halves of its tiles
+        const int rem = p.num_tiles % pair_count;
+        const bool split =
+            QMM_SS_SPLIT_TAIL && p.num_tiles > pair_count && rem > 0 && 2 * rem <= pair_count;
+        p.full_items = split ? p.num_tiles - rem : p.num_tiles;
+        p.num_items = split ? p.num_tiles + rem : p.num_tiles;
+        pairs = std::min(p.num_items, pair_count);
+        static int smem_limits[kMaxDevices] = {0};
+        return ensure_smem(gemm_ss_kernel<G>, SsLayout::smem_bytes, true, smem_limits);
+    }
+
+    cudaError_t launch(cudaStream_t stream) const {
+        cudaError_t e = launch_kernel(dequant_bf16_kernel<F, G>, dim3(grid1), dim3(kDeqThreads), 0,
+                                      stream, 1, w, w2, ws, n, k, rows, 0x4B000000u);
+        if (e != cudaSuccess) return e;
+        return launch_kernel(gemm_ss_kernel<G>, dim3(2 * pairs), dim3(S_THREADS),
+                             SsLayout::smem_bytes, stream, 2, ta, tx, tx_half, p);
+    }
+};
+
 template <Fmt F, bool G>
 cudaError_t launch_two_phase(const uint8_t *w, const uint8_t *w2, const uint16_t *x, float *y,
                              uint16_t *h, int64_t m, int64_t n, int64_t k, uint16_t *ws,
-                             cudaStream_t stream, const LaunchCtx &ctx, int64_t ldy = 0) {
-    if (m > (1 << 30) || n > (1 << 30) || k > (1 << 24)) return cudaErrorInvalidValue;
-    const int64_t rows = workspace_rows(n, G);
-    // phase 1
-    const int64_t groups = (rows * (k / kQK) + kDeqThreads - 1) / kDeqThreads;
-    const unsigned grid1 = static_cast<unsigned>(std::min<int64_t>(groups, 8LL * device_sm_count()));
-    cudaError_t e = launch_kernel(dequant_bf16_kernel<F, G>, dim3(grid1), dim3(kDeqThreads), 0, stream,
-                                  1, w, w2, ws, n, k, rows, 0x4B000000u);
-    if (e != cudaSuccess) return e;
-    // phase 2
-    CUtensorMap ta, tx, tx_half;
-    if (!encode_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ws, k, rows, k * 2, SK, SW,
-                        CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, k, m, k * 2, SK, ST_CTA,
-                        CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_tmap_2d(&tx_half, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, k, m, k * 2, SK, ST_CTA / 2,
-                        CU_TENSOR_MAP_SWIZZLE_128B))
-        return cudaErrorInvalidValue;
-    SsParams p;
-    p.y = y;
-    p.h = h;
-    p.m = static_cast<int>(m);
-    p.n = static_cast<int>(n);
-    p.k = static_cast<int>(k);
-    p.ldy = static_cast<int>(ldy > 0 ? ldy : n);
-    p.num_t_blocks = static_cast<int>((m + ST - 1) / ST);
-    // a pair tile covers 256 workspace rows: 256 outputs, or 128 GeGLU features
-    const int64_t per_tile = G ? SW : 2 * SW;
-    p.num_tiles = p.num_t_blocks * static_cast<int>((n + per_tile - 1) / per_tile);
-    p.ctx = ctx;
-    const int pair_count = std::max(1, device_sm_count() / 2);
-    // a last round that would leave more than half the pairs idle runs as
-    // 128-token halves of its tiles
-    const int rem = p.num_tiles % pair_count;
-    const bool split = QMM_SS_SPLIT_TAIL && p.num_tiles > pair_count && rem > 0 && 2 * rem <= pair_count;
-    p.full_items = split ? p.num_tiles - rem : p.num_tiles;
-    p.num_items = split ? p.num_tiles + rem : p.num_tiles;
-    static int smem_limits[kMaxDevices] = {0};
-    e = ensure_smem(gemm_ss_kernel<G>, SsLayout::smem_bytes, true, smem_limits);
-    if (e != cudaSuccess) return e;
-    const int pairs = std::min(p.num_items, pair_count);
-    return launch_kernel(gemm_ss_kernel<G>, dim3(2 * pairs), dim3(S_THREADS), SsLayout::smem_bytes,
-                         stream, 2, ta, tx, tx_half, p);
+                             cudaStream_t stream, const LaunchCtx &ctx) {
+    TwoPhase<F, G> tp;
+    const cudaError_t e = tp.prepare(w, w2, x, y, h, m, n, k, ws, ctx);
+    return e != cudaSuccess ? e : tp.launch(stream);
 }
 
 // The library's own scratch for qmm_gemm_q4_0_prefill: bf16 weight rows of
@@ -498,19 +525,28 @@ cudaError_t launch_gemm_q4_0_prefill(const uint8_t *w, const uint16_t *x, float 
                                      int64_t n, int64_t k, cudaStream_t stream,
                                      const LaunchCtx &ctx) {
     // weight rows per chunk: whole pair tiles that fit the scratch
-    const int64_t chunk = static_cast<int64_t>(kScratchBytes / (static_cast<size_t>(k) * 2)) / (2 * SW) * (2 * SW);
+    const int64_t chunk =
+        static_cast<int64_t>(kScratchBytes / (static_cast<size_t>(k) * 2)) / (2 * SW) * (2 * SW);
     if (!use_two_phase(m, k) || chunk < 2 * SW)
         return launch_gemm_q4_0(w, x, y, m, n, k, stream, ctx);
     void *scratch = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&scratch, g_prefill_scratch);
     if (e != cudaSuccess) return e;
+    uint16_t *ws = static_cast<uint16_t *>(scratch);
     const int64_t row_bytes = (k / kQK) * kQ4_0Bytes;
+    // every host step that can fail runs before the first launch: here for
+    // the last chunk, and in the loop for the first one (every other chunk
+    // has the first chunk's shape)
+    const int64_t last0 = (n - 1) / chunk * chunk;
+    TwoPhase<Fmt::Q4_0, false> tp;
+    e = tp.prepare(w + last0 * row_bytes, nullptr, x, y + last0, nullptr, m, n - last0, k, ws,
+                   ctx, n);
+    if (e != cudaSuccess) return e;
     for (int64_t n0 = 0; n0 < n; n0 += chunk) {
         const int64_t nc = std::min(chunk, n - n0);
         // columns n0 .. n0+nc of y: the chunk's outputs, row stride n
-        e = launch_two_phase<Fmt::Q4_0, false>(w + n0 * row_bytes, nullptr, x, y + n0, nullptr, m,
-                                               nc, k, static_cast<uint16_t *>(scratch), stream,
-                                               ctx, n);
+        e = tp.prepare(w + n0 * row_bytes, nullptr, x, y + n0, nullptr, m, nc, k, ws, ctx, n);
+        if (e == cudaSuccess) e = tp.launch(stream);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;

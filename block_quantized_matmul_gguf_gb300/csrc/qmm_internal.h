@@ -173,8 +173,17 @@ cudaError_t launch_gemm_geglu_two_phase(const uint8_t *wg, const uint8_t *wu, co
                                         uint16_t *h, int64_t m, int64_t n, int64_t k, uint16_t *ws,
                                         cudaStream_t stream, const LaunchCtx &ctx);
 
+// Largest sizes the tensor-core GEMM launchers take (tile indices and tensor
+// map extents stay in 32-bit range); the API returns QMM_ERR_UNSUPPORTED
+// beyond them before launching anything.
+constexpr int64_t kGemmMaxM = int64_t(1) << 30;
+constexpr int64_t kGemmMaxN = int64_t(1) << 30;
+constexpr int64_t kGemmMaxK = int64_t(1) << 24;
+
 // Two-phase Q4_0 prefill GEMM on the library's own static scratch (column
-// chunks that fit it; fused kernel for m <= 256 or chunks under one tile).
+// chunks that fit it; the fused kernel below the two-phase length rule).
+// Every host step that can fail for the call's chunk shapes runs before the
+// first launch.
 cudaError_t launch_gemm_q4_0_prefill(const uint8_t *w, const uint16_t *x, float *y, int64_t m,
                                      int64_t n, int64_t k, cudaStream_t stream,
                                      const LaunchCtx &ctx);

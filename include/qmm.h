@@ -45,7 +45,9 @@
  *
  * Errors.  Arguments are checked before anything is launched; a failed check
  * returns its status and launches nothing.  A launch failure returns
- * QMM_ERR_CUDA.  Device-side waits are bounded: a kernel that gives up
+ * QMM_ERR_CUDA; a call that launches several kernels may have launched some
+ * of them by then, so after QMM_ERR_CUDA the contents of its outputs (and of
+ * any workspace) are undefined.  Device-side waits are bounded: a kernel that gives up
  * records QMM_ERR_TIMEOUT in the device error word, which
  * qmm_get_device_error() reports.  No entry point aborts the process.
  */
@@ -148,9 +150,10 @@ qmm_status qmm_gemv_q4_0_geglu(const void *wg, const void *wu, const float *x, f
  * ((nibble-8)*d, round to nearest even) and products are summed in fp32
  * in tensor memory.  Y : fp32 [m][n].
  * Requires m >= 1, n >= 1, k % 256 == 0, k >= 256, w and x 16-byte aligned,
- * y 16-byte aligned and n % 4 == 0.  Other valid shapes return
- * QMM_ERR_UNSUPPORTED.  Accuracy: |Y - Y_exact| <= 2e-3 * sum_k |w*x| + 1e-6
- * per output. */
+ * y 4-byte aligned, y not overlapping w or x, and m <= 2^30, n <= 2^30,
+ * k <= 2^24.  Valid shapes outside these (k % 256 != 0, the size limits, an
+ * overlapping y) return QMM_ERR_UNSUPPORTED.  Accuracy: |Y - Y_exact| <=
+ * 2e-3 * sum_k |w*x| + 1e-6 per output. */
 qmm_status qmm_gemm_q4_0(const void *w, const uint16_t *x_bf16, float *y, int64_t m,
                          int64_t n, int64_t k, qmm_stream_t stream);
 
@@ -191,10 +194,11 @@ qmm_status qmm_gemm_q8_0_ws(const void *w, const uint16_t *x_bf16, float *y, int
  * part of the library (a module-scope device variable, one per GPU), in
  * column chunks of whole 256-row tiles that fit it, each chunk followed by
  * its GEMM, under the same length rule as the _ws calls; otherwise the
- * fused call.  Allocates nothing.  Same requirements,
- * arithmetic and accuracy as qmm_gemm_q4_0.  The scratch is shared by every
- * call of this entry point on the device, so calls on different streams must
- * not run concurrently (the caller orders them, e.g. with events). */
+ * fused call.  Allocates nothing.  Same requirements (y not overlapping w
+ * or x included), arithmetic and accuracy as qmm_gemm_q4_0.  The scratch is
+ * shared by every call of this entry point on the device, so calls on
+ * different streams must not run concurrently (the caller orders them, e.g.
+ * with events). */
 qmm_status qmm_gemm_q4_0_prefill(const void *w, const uint16_t *x_bf16, float *y, int64_t m,
                                  int64_t n, int64_t k, qmm_stream_t stream);
 

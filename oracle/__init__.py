@@ -68,6 +68,8 @@ def _load():
         getattr(lib, name).restype = None
     lib.qmm_oracle_geglu_q4_0.argtypes = [P, P, P, I64, I64, I64, P, P, P, P, P]
     lib.qmm_oracle_geglu_q4_0.restype = None
+    lib.qmm_oracle_geglu_q4_0_at.argtypes = [P, P, P, I64, P, P, I64, P, P, P, P, P]
+    lib.qmm_oracle_geglu_q4_0_at.restype = None
     lib.qmm_oracle_set_threads.argtypes = [ctypes.c_int]
     lib.qmm_oracle_set_threads.restype = None
     lib.qmm_oracle_get_threads.argtypes = []
@@ -193,4 +195,24 @@ def geglu_q4_0(wg, wu, x, m, n, k):
         raise ValueError(f"activation buffer has {x.size} values, expected {m * k}")
     outs = [np.empty((m, n), dtype=np.float64) for _ in range(5)]
     _load().qmm_oracle_geglu_q4_0(_ptr(wg), _ptr(wu), _ptr(x), m, n, k, *[_ptr(o) for o in outs])
+    return tuple(outs)
+
+
+def geglu_q4_0_at(wg, wu, x, m, n, k, mi, ni):
+    """Outputs (mi[i], ni[i]) of geglu_q4_0: (h, g, u, bound_g, bound_u), each
+    binary64 of the sample's length."""
+    wg = _blocks(wg, n, k, Q4_0_BYTES)
+    wu = _blocks(wu, n, k, Q4_0_BYTES)
+    x = np.ascontiguousarray(x, dtype=np.float32).reshape(-1)
+    if x.size != m * k:
+        raise ValueError(f"activation buffer has {x.size} values, expected {m * k}")
+    mi = np.ascontiguousarray(mi, dtype=np.int64).reshape(-1)
+    ni = np.ascontiguousarray(ni, dtype=np.int64).reshape(-1)
+    if mi.shape != ni.shape:
+        raise ValueError("index arrays differ in length")
+    if mi.size and (mi.min() < 0 or mi.max() >= m or ni.min() < 0 or ni.max() >= n):
+        raise ValueError("sample index out of range")
+    outs = [np.empty(mi.size, dtype=np.float64) for _ in range(5)]
+    _load().qmm_oracle_geglu_q4_0_at(_ptr(wg), _ptr(wu), _ptr(x), k, _ptr(mi), _ptr(ni), mi.size,
+                                     *[_ptr(o) for o in outs])
     return tuple(outs)

@@ -208,3 +208,19 @@ void qmm_oracle_geglu_q4_0(const uint8_t *wg, const uint8_t *wu, const float *x,
         if (bound_u) bound_u[i] = bu;
     }
 }
+
+void qmm_oracle_geglu_q4_0_at(const uint8_t *wg, const uint8_t *wu, const float *x, int64_t k,
+                              const int64_t *mi, const int64_t *ni, int64_t count, double *h,
+                              double *g, double *u, double *bound_g, double *bound_u) {
+#pragma omp parallel for schedule(dynamic, 4) num_threads(qmm_oracle_get_threads())
+    for (int64_t i = 0; i < count; i++) {
+        double gv, uv, bg, bu;
+        dot(wg, x, k, mi[i], ni[i], q4_0_weight, Q4_0_BYTES, act_f32, &gv, &bg);
+        dot(wu, x, k, mi[i], ni[i], q4_0_weight, Q4_0_BYTES, act_f32, &uv, &bu);
+        h[i] = gelu_tanh(gv) * uv;
+        if (g) g[i] = gv;
+        if (u) u[i] = uv;
+        if (bound_g) bound_g[i] = bg;
+        if (bound_u) bound_u[i] = bu;
+    }
+}

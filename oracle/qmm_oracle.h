@@ -90,6 +90,12 @@ void qmm_oracle_geglu_q4_0(const uint8_t *wg, const uint8_t *wu, const float *x,
                            int64_t n, int64_t k, double *h, double *g, double *u,
                            double *bound_g, double *bound_u);
 
+/* Sampled outputs of qmm_oracle_geglu_q4_0: for i < count, element i of
+ * each output array is that function's output (mi[i], ni[i]). */
+void qmm_oracle_geglu_q4_0_at(const uint8_t *wg, const uint8_t *wu, const float *x, int64_t k,
+                              const int64_t *mi, const int64_t *ni, int64_t count, double *h,
+                              double *g, double *u, double *bound_g, double *bound_u);
+
 /* Host threads used by the loops over outputs (OpenMP); <=0 means all. */
 void qmm_oracle_set_threads(int nthreads);
 int qmm_oracle_get_threads(void);

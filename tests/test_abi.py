@@ -64,7 +64,6 @@ def test_null_and_shape_errors_return_before_any_launch(lib):
     assert L.qmm_gemm_q4_0(0, 16, 16, 256, 256, 256, 0) == qmm.QMM_ERR_NULL
     assert L.qmm_gemm_q4_0(16, 16, 16, 0, 256, 256, 0) == qmm.QMM_ERR_SHAPE
     assert L.qmm_gemm_q4_0(16, 16, 16, 256, 256, 288, 0) == qmm.QMM_ERR_UNSUPPORTED
-    assert L.qmm_gemm_q4_0(16, 16, 16, 256, 254, 256, 0) == qmm.QMM_ERR_UNSUPPORTED
     assert L.qmm_gemm_q4_0(18, 16, 16, 256, 256, 256, 0) == qmm.QMM_ERR_ALIGN
 
 
@@ -118,9 +117,23 @@ def test_q8_0_gemm_and_prefill_argument_checks(lib):
         assert f(A, B, C, 0, 256, 256, 0) == qmm.QMM_ERR_SHAPE
         assert f(A, B, C, 256, 256, 100, 0) == qmm.QMM_ERR_SHAPE
         assert f(A, B, C, 256, 256, 288, 0) == qmm.QMM_ERR_UNSUPPORTED   # k % 256
-        assert f(A, B, C, 256, 254, 256, 0) == qmm.QMM_ERR_UNSUPPORTED   # n % 4
         assert f(A + 8, B, C, 256, 256, 256, 0) == qmm.QMM_ERR_ALIGN
         assert f(A, B + 8, C, 256, 256, 256, 0) == qmm.QMM_ERR_ALIGN
+        assert f(A, B, C + 2, 256, 256, 256, 0) == qmm.QMM_ERR_ALIGN      # y % 4
+
+
+@pytest.mark.parametrize("name", ["qmm_gemm_q4_0", "qmm_gemm_q8_0", "qmm_gemm_q4_0_prefill"])
+def test_gemm_output_overlap_and_size_limits(lib, name):
+    """y may overlap neither w nor x; m, n above 2^30 and k above 2^24 are
+    valid shapes this build does not take.  All rejected before any launch."""
+    f = getattr(lib, name)
+    m, n, k = 256, 256, 256
+    wbytes = n * (k // 32) * (18 if "q4_0" in name else 34)
+    assert f(A, B, A + wbytes - 4, m, n, k, 0) == qmm.QMM_ERR_UNSUPPORTED   # y over w's tail
+    assert f(A, B, B + 64, m, n, k, 0) == qmm.QMM_ERR_UNSUPPORTED           # y over x
+    assert f(A, B, C, (1 << 30) + 1, 1, k, 0) == qmm.QMM_ERR_UNSUPPORTED
+    assert f(A, B, C, 1, (1 << 30) + 1, k, 0) == qmm.QMM_ERR_UNSUPPORTED
+    assert f(A, B, C, 1, 1, (1 << 24) + 256, 0) == qmm.QMM_ERR_UNSUPPORTED
 
 
 def test_geglu_gemm_argument_checks(lib):

@@ -64,9 +64,7 @@ def test_gemm_geglu_prefill_ffn_full_size_sampled(qmm, oracle_mod):
     rng = np.random.default_rng(9)
     mi = rng.integers(0, m, 4000)
     ni = rng.integers(0, n, 4000)
-    g, bg = oracle_mod.gemv_q4_0_at(wg, x, m, n, k, mi, ni)
-    u, bu = oracle_mod.gemv_q4_0_at(wu, x, m, n, k, mi, ni)
-    h_ref = torch.nn.functional.gelu(torch.from_numpy(g), approximate="tanh").numpy() * u
+    h_ref, g, u, bg, bu = oracle_mod.geglu_q4_0_at(wg, wu, x, m, n, k, mi, ni)
     assert_geglu_within(h[mi, ni], h_ref, g, u, bg, bu, "prefill ffn", rel=GEMM_REL,
                         out_rel=BF16_OUT)
     assert np.all(np.isfinite(h))

@@ -111,7 +111,7 @@ def test_gemm_q8_0_argument_checks(qmm):
     for args, status in [((0, x, y, m, n, k), qmm.QMM_ERR_NULL),
                          ((w, x, y, m, n, 100), qmm.QMM_ERR_SHAPE),
                          ((w, x, y, m, n, 96), qmm.QMM_ERR_UNSUPPORTED),
-                         ((w, x, y, m, 6, k), qmm.QMM_ERR_UNSUPPORTED),
+                         ((w, x, x, m, n, k), qmm.QMM_ERR_UNSUPPORTED),   # y over x
                          ((w[1:].data_ptr(), x, y, m, n, k), qmm.QMM_ERR_ALIGN)]:
         with pytest.raises(qmm.QmmError) as e:
             qmm.qmm_gemm_q8_0(*args)

@@ -52,19 +52,26 @@ def test_two_phase_matches_oracle_and_fused(qmm, oracle_mod, fmt, m, n, k):
     assert torch.equal(y2, y1), "two-phase and fused results differ"
 
 
-def test_two_phase_full_size_sampled(qmm, oracle_mod):
-    p = synth.PREFILL_SHAPES[0]
+@pytest.mark.parametrize("shape", synth.PREFILL_SHAPES, ids=lambda p: f"{p.n}x{p.k}")
+def test_two_phase_full_size_equals_fused(qmm, oracle_mod, shape):
+    """The 2048-token prefill at both weight shapes, on the inputs whose every
+    output the fused kernel's full-size test checks against the oracle: the
+    workspace and static-scratch calls give the fused kernel's exact bits."""
     m = synth.PREFILL_M
-    w, xb = synth.gemm_case(m, p.n, p.k, seed=0, stream=70)
+    w, xb = synth.gemm_case(m, shape.n, shape.k, seed=0,
+                            stream=70 + synth.PREFILL_SHAPES.index(shape))
     wd, xd = to_dev(w, torch), bf16_tensor(xb, torch)
-    y2 = qmm.gemm("q4_0", wd, xd, p.n, p.k, workspace=_ws(qmm, p.n, p.k))
-    y1 = qmm.gemm("q4_0", wd, xd, p.n, p.k)
+    y2 = qmm.gemm("q4_0", wd, xd, shape.n, shape.k, workspace=_ws(qmm, shape.n, shape.k))
+    y1 = qmm.gemm("q4_0", wd, xd, shape.n, shape.k)
+    y3 = torch.empty_like(y1)
+    qmm.qmm_gemm_q4_0_prefill(wd, xd, y3, m, shape.n, shape.k)
     torch.cuda.synchronize()
-    assert torch.equal(y2, y1)
+    assert qmm.qmm_get_device_error() == 0
+    assert torch.equal(y2, y1) and torch.equal(y3, y1)
     rng = np.random.default_rng(3)
     mi = rng.integers(0, m, 2000)
-    ni = rng.integers(0, p.n, 2000)
-    y_ref, bound = oracle_mod.gemm_q4_0_at(w, xb, m, p.n, p.k, mi, ni)
+    ni = rng.integers(0, shape.n, 2000)
+    y_ref, bound = oracle_mod.gemm_q4_0_at(w, xb, m, shape.n, shape.k, mi, ni)
     assert_within(y2[torch.from_numpy(mi).cuda(), torch.from_numpy(ni).cuda()].cpu().numpy(),
                   y_ref, bound, GEMM_REL, "two-phase full size")
 

@@ -345,6 +345,11 @@ def test_sampled_outputs_match_full(oracle_mod):
     yg, bg = oracle_mod.gemm_q4_0(w, xb, m, n, k)
     ysg, bsg = oracle_mod.gemm_q4_0_at(w, xb, m, n, k, mi, ni)
     assert np.array_equal(ysg, yg[mi, ni]) and np.array_equal(bsg, bg[mi, ni])
+    wu = synth.q4_0_weights(n, k, seed=5)
+    full = oracle_mod.geglu_q4_0(case.w, wu, case.x, m, n, k)
+    at = oracle_mod.geglu_q4_0_at(case.w, wu, case.x, m, n, k, mi, ni)
+    for a, f in zip(at, full):
+        assert np.array_equal(a, f[mi, ni])
 
 
 # ---------------------------------------------------------------- tolerance sanity
