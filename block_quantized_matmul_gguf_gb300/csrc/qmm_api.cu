@@ -293,6 +293,7 @@ qmm_status qmm_gemm_q4_0_prefill(const void *w, const uint16_t *x_bf16, float *y
                                  int64_t n, int64_t k, qmm_stream_t stream) {
     qmm_status s = check_gemm(Fmt::Q4_0, w, x_bf16, y, m, n, k);
     if (s != QMM_OK) return s;
+    if (k > kPrefillMaxK) return QMM_ERR_SCRATCH;
     LaunchCtx ctx;
     if (!make_ctx(&ctx)) return QMM_ERR_CUDA;
     return from_cuda(launch_gemm_q4_0_prefill(static_cast<const uint8_t *>(w), x_bf16, y, m, n, k,
@@ -375,11 +376,13 @@ const char *qmm_status_string(qmm_status status) {
         case QMM_ERR_UNSUPPORTED: return "valid arguments not supported by this build";
         case QMM_ERR_CUDA: return "CUDA runtime error";
         case QMM_ERR_TIMEOUT: return "a device-side wait timed out";
+        case QMM_ERR_SCRATCH:
+            return "problem larger than the entry point's fixed scratch (qmm_gemm_q4_0_prefill: k > 131072)";
     }
     return "unknown status";
 }
 
-int qmm_version(void) { return 201; }
+int qmm_version(void) { return 202; }
 
 qmm_status qmm_get_device_error(qmm_stream_t stream) {
     cudaError_t e;

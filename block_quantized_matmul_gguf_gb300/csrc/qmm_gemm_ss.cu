@@ -34,6 +34,7 @@
 #include "qmm_tc.cuh"
 
 #include <algorithm>
+#include <mutex>
 
 namespace qmm {
 namespace {
@@ -515,22 +516,46 @@ cudaError_t launch_two_phase(const uint8_t *w, const uint8_t *w2, const uint16_t
 }
 
 // The library's own scratch for qmm_gemm_q4_0_prefill: bf16 weight rows of
-// one column chunk at a time (64 MB: 16384 rows at K = 2048).
+// one column chunk at a time (64 MiB: 16384 rows at K = 2048, 256 rows at
+// the largest K the entry point accepts).  Every GPU that loads the library
+// holds it until the process exits.
 constexpr size_t kScratchBytes = size_t(64) << 20;
 static __device__ __align__(256) uint16_t g_prefill_scratch[kScratchBytes / sizeof(uint16_t)];
+static_assert(kScratchBytes == static_cast<size_t>(kPrefillMaxK) * 2 * (2 * SW),
+              "one 256-row chunk at the largest accepted K fills the scratch");
+
+// Device address of the scratch, resolved once per device (with that device
+// current) on the first call of the entry point there.  In host code the
+// array's name is only a stand-in for the symbol, never a device address.
+std::mutex g_scratch_mu;
+void *g_scratch_ptr[kMaxDevices] = {};
+
+cudaError_t prefill_scratch(void **out) {
+    const int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_ptr[dev]) {
+        void *p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_prefill_scratch);
+        if (e != cudaSuccess) return e;
+        g_scratch_ptr[dev] = p;
+    }
+    *out = g_scratch_ptr[dev];
+    return cudaSuccess;
+}
 
 }  // namespace
 
 cudaError_t launch_gemm_q4_0_prefill(const uint8_t *w, const uint16_t *x, float *y, int64_t m,
                                      int64_t n, int64_t k, cudaStream_t stream,
                                      const LaunchCtx &ctx) {
+    if (k > kPrefillMaxK) return cudaErrorInvalidValue;  // the API rejects it first
+    if (!use_two_phase(m, k)) return launch_gemm_q4_0(w, x, y, m, n, k, stream, ctx);
     // weight rows per chunk: whole pair tiles that fit the scratch
     const int64_t chunk =
         static_cast<int64_t>(kScratchBytes / (static_cast<size_t>(k) * 2)) / (2 * SW) * (2 * SW);
-    if (!use_two_phase(m, k) || chunk < 2 * SW)
-        return launch_gemm_q4_0(w, x, y, m, n, k, stream, ctx);
     void *scratch = nullptr;
-    cudaError_t e = cudaGetSymbolAddress(&scratch, g_prefill_scratch);
+    cudaError_t e = prefill_scratch(&scratch);
     if (e != cudaSuccess) return e;
     uint16_t *ws = static_cast<uint16_t *>(scratch);
     const int64_t row_bytes = (k / kQK) * kQ4_0Bytes;

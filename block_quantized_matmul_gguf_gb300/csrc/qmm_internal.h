@@ -173,6 +173,10 @@ cudaError_t launch_gemm_geglu_two_phase(const uint8_t *wg, const uint8_t *wu, co
                                         uint16_t *h, int64_t m, int64_t n, int64_t k, uint16_t *ws,
                                         cudaStream_t stream, const LaunchCtx &ctx);
 
+// Largest K of qmm_gemm_q4_0_prefill: one 256-row chunk of bf16 weights
+// (256 * K * 2 bytes) must fit its 64 MiB static scratch.
+constexpr int64_t kPrefillMaxK = 131072;
+
 // Largest sizes the tensor-core GEMM launchers take (tile indices and tensor
 // map extents stay in 32-bit range); the API returns QMM_ERR_UNSUPPORTED
 // beyond them before launching anything.

@@ -22,6 +22,7 @@ QMM_ERR_ALIGN = 3
 QMM_ERR_UNSUPPORTED = 4
 QMM_ERR_CUDA = 5
 QMM_ERR_TIMEOUT = 6
+QMM_ERR_SCRATCH = 7
 QMM_GEMV_MAX_M = 16
 
 QMM_GEMV_MAX_OUTPUTS = 4
@@ -220,7 +221,10 @@ def qmm_gemm_q4_0_geglu_ws(wg, wu, x_bf16, h_bf16, m, n, k, ws, ws_bytes, stream
 
 
 def qmm_gemm_q4_0_prefill(w, x_bf16, y, m: int, n: int, k: int, stream=None) -> None:
-    """Two-phase Q4_0 GEMM on the library's own scratch (no workspace argument)."""
+    """The Q4_0 prefill product without a workspace argument, for callers
+    that cannot allocate device memory: long prompts run in two phases on a
+    64 MiB scratch array owned by the library (k <= 131072, else status
+    QMM_ERR_SCRATCH).  Calls that overlap on the GPU race on that scratch."""
     _check(load().qmm_gemm_q4_0_prefill(_ptr(w), _ptr(x_bf16), _ptr(y), m, n, k, _stream(stream)),
            "qmm_gemm_q4_0_prefill")
 

@@ -67,7 +67,9 @@ typedef enum qmm_status {
     QMM_ERR_ALIGN = 3,       /* a pointer lacks the alignment the call needs    */
     QMM_ERR_UNSUPPORTED = 4, /* valid arguments this build does not handle     */
     QMM_ERR_CUDA = 5,        /* a CUDA runtime call or launch failed           */
-    QMM_ERR_TIMEOUT = 6      /* a device-side wait hit its limit               */
+    QMM_ERR_TIMEOUT = 6,     /* a device-side wait hit its limit               */
+    QMM_ERR_SCRATCH = 7      /* the problem exceeds an entry point's fixed
+                                scratch (qmm_gemm_q4_0_prefill only)          */
 } qmm_status;
 
 /* Same type as cudaStream_t; NULL is the legacy default stream. */
@@ -189,16 +191,35 @@ qmm_status qmm_gemm_q8_0_ws(const void *w, const uint16_t *x_bf16, float *y, int
                             int64_t n, int64_t k, void *workspace, size_t workspace_bytes,
                             qmm_stream_t stream);
 
-/* The Q4_0 product of qmm_gemm_q4_0_ws without a caller workspace: for
- * long prompts the weights are dequantised into a 64 MB scratch array that is
- * part of the library (a module-scope device variable, one per GPU), in
- * column chunks of whole 256-row tiles that fit it, each chunk followed by
- * its GEMM, under the same length rule as the _ws calls; otherwise the
- * fused call.  Allocates nothing.  Same requirements (y not overlapping w
- * or x included), arithmetic and accuracy as qmm_gemm_q4_0.  The scratch is
- * shared by every call of this entry point on the device, so calls on
- * different streams must not run concurrently (the caller orders them, e.g.
- * with events). */
+/* The Q4_0 product of qmm_gemm_q4_0_ws for callers that cannot allocate
+ * device memory.  The pages have no counterpart of this entry point: it
+ * exists for hosts whose device memory is all owned by their own allocator
+ * (a serving engine's arena or a framework's caching allocator with a fixed
+ * budget), which forbid a library from calling cudaMalloc, and for plugin
+ * interfaces that hand an operator only its inputs and outputs, with no
+ * workspace slot and no allocator to ask.
+ *
+ * Instead of a caller workspace it uses a 64 MiB scratch array that is part
+ * of the library (a module-scope __device__ array: every GPU that loads the
+ * library holds it until the process exits).  For long prompts (m > 512, or
+ * m > 256 with k >= 4096) the weights are dequantised into it in column
+ * chunks of whole 256-row tiles, each chunk followed by its GEMM; shorter
+ * prompts take the fused kernel and leave the scratch alone.  The call makes
+ * no cudaMalloc, cudaFree or other allocating call.  Same arithmetic, result
+ * and accuracy as qmm_gemm_q4_0 (bit-identical to it and to
+ * qmm_gemm_q4_0_ws), and the same requirements, plus:
+ *   k <= 131072: one 256-row chunk (256 * k bf16 values) must fit the
+ *     scratch; a larger k returns QMM_ERR_SCRATCH and launches nothing.
+ * Set-up: the first call on a device (with that device current) resolves
+ * the scratch's device address once; make that first call before any
+ * stream capture begins on the device.
+ * Sharing: every call of this entry point on a device uses the same
+ * scratch, which keeps the last call's contents (nothing in it needs to
+ * start at zero: each chunk's rows are written before they are read).
+ * Calls that overlap on the GPU -- on different streams, or from different
+ * threads without ordering -- race on the scratch and give wrong results;
+ * the caller orders them (one stream, or events).  Calls on one stream are
+ * ordered by the stream. */
 qmm_status qmm_gemm_q4_0_prefill(const void *w, const uint16_t *x_bf16, float *y, int64_t m,
                                  int64_t n, int64_t k, qmm_stream_t stream);
 

@@ -41,8 +41,9 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings_and_version(lib):
-    for s in range(7):
+    for s in range(8):
         assert qmm.status_string(s)
+    assert "scratch" in qmm.status_string(qmm.QMM_ERR_SCRATCH)
     assert qmm.status_string(99) == "unknown status"
     assert qmm.qmm_version() >= 100
 
@@ -134,6 +135,19 @@ def test_gemm_output_overlap_and_size_limits(lib, name):
     assert f(A, B, C, (1 << 30) + 1, 1, k, 0) == qmm.QMM_ERR_UNSUPPORTED
     assert f(A, B, C, 1, (1 << 30) + 1, k, 0) == qmm.QMM_ERR_UNSUPPORTED
     assert f(A, B, C, 1, 1, (1 << 24) + 256, 0) == qmm.QMM_ERR_UNSUPPORTED
+
+
+def test_prefill_rejects_k_beyond_its_scratch(lib):
+    """qmm_gemm_q4_0_prefill keeps one 256-row chunk of bf16 weights in its
+    64 MiB scratch: k <= 131072.  Beyond that it returns QMM_ERR_SCRATCH
+    before any CUDA call, whatever m is (the other GEMMs take such k)."""
+    L = lib
+    w, x, y = 1 << 24, 1 << 36, 1 << 40  # far apart: the large x does not reach y
+    for m in (1, 300, 2048):
+        assert L.qmm_gemm_q4_0_prefill(w, x, y, m, 4, 131072 + 256, 0) == qmm.QMM_ERR_SCRATCH
+    assert L.qmm_gemm_q4_0_prefill(w, x, y, 1, 4, 1 << 24, 0) == qmm.QMM_ERR_SCRATCH
+    # argument errors are still reported first
+    assert L.qmm_gemm_q4_0_prefill(0, x, y, 1, 4, 131072 + 256, 0) == qmm.QMM_ERR_NULL
 
 
 def test_geglu_gemm_argument_checks(lib):
