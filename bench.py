@@ -74,7 +74,7 @@ def parse_args(argv=None):
     ap.add_argument("--profile", default=None, metavar="CASE",
                     help="no timing: run CASE a few times for a profiler and exit. CASE is "
                          "decode_grouped (the timed decode step), decode (seven separate calls), "
-                         "gemv:FMT:M:N:K, geglu:M:N:K, gemm_geglu:M:N:K, dequant:FMT:N:K "
+                         "gemv:FMT:M:N:K, gemv_tc:M:N:K, geglu:M:N:K, gemm_geglu:M:N:K, dequant:FMT:N:K "
                          "gemm:M:N:K, gemm_ws:M:N:K (two-phase) or gemm_q8_0:M:N:K")
     ap.add_argument("--profile-launches", type=int, default=3)
     return ap.parse_args(argv)
@@ -130,6 +130,12 @@ def run_profile(args):
         w, x = torch.from_numpy(c.w).to(dev), torch.from_numpy(c.x).to(dev)
         for _ in range(reps):
             qmm.gemv(fmt, w, x, n, k)
+    elif parts[0] == "gemv_tc":
+        m, n, k = int(parts[1]), int(parts[2]), int(parts[3])
+        c = synth.gemv_case("q4_0", m, n, k, seed=0, stream=1)
+        w, x = torch.from_numpy(c.w).to(dev), torch.from_numpy(c.x).to(dev)
+        for _ in range(reps):
+            qmm.gemv_tc_q4_0(w, x, n, k)
     elif parts[0] == "dequant":
         fmt, n, k = parts[1], int(parts[2]), int(parts[3])
         c = synth.gemv_case(fmt, 1, n, k, seed=0, stream=1)
@@ -352,7 +358,7 @@ class DecodeLayer:
     share one activation matrix and run as one call."""
 
     def __init__(self, torch, qmm, l2_bytes, stream, m=1, projections=synth.DECODE_LAYER,
-                 stream_base=10, fmt="q4_0", weights=None, groups=None):
+                 stream_base=10, fmt="q4_0", weights=None, groups=None, tensor_cores=False):
         self.torch, self.qmm, self.m, self.fmt = torch, qmm, m, fmt
         self.projs = projections
         self.cases = [synth.gemv_case(fmt, m, p.n, p.k, seed=0, stream=stream_base + i,
@@ -387,6 +393,8 @@ class DecodeLayer:
             off += m * p.n
         self.stream = stream
         self.fn = qmm.qmm_gemv_q4_0 if fmt == "q4_0" else qmm.qmm_gemv_q8_0
+        if tensor_cores:  # the tensor-core GEMV (single projections only)
+            self.fn = qmm.qmm_gemv_q4_0_tc
         self.fn_multi = qmm.qmm_gemv_q4_0_multi if fmt == "q4_0" else qmm.qmm_gemv_q8_0_multi
         # one graph for a whole rotation and one per single step, all captured
         # (and replayed once, which uploads them) before anything is timed
@@ -523,7 +531,7 @@ def run_secondary(torch, qmm, l2, stream, timer, peaks, sms):
 
     weight_cache = {}
 
-    def gemv_entry(name, fmt, m, projs, base, grouped=False):
+    def gemv_entry(name, fmt, m, projs, base, grouped=False, tensor_cores=False):
         key = (fmt, base, tuple((p.n, p.k) for p in projs))
         if key not in weight_cache:
             weight_cache.clear()
@@ -531,7 +539,8 @@ def run_secondary(torch, qmm, l2, stream, timer, peaks, sms):
                                  for i, p in enumerate(projs)]
         layer = DecodeLayer(torch, qmm, l2, stream, m=m, projections=projs, stream_base=base,
                             fmt=fmt, weights=weight_cache[key],
-                            groups=(tuple(p.name for p in projs),) if grouped else None)
+                            groups=(tuple(p.name for p in projs),) if grouped else None,
+                            tensor_cores=tensor_cores)
         steps = max(layer.R, (2000 // layer.R) * layer.R)
         layer.warm_graphs()
         layer.prepare_timed(steps)
@@ -560,6 +569,10 @@ def run_secondary(torch, qmm, l2, stream, timer, peaks, sms):
     for m in synth.BATCHED_M:
         for i, p in enumerate(synth.BATCHED_SHAPES):
             gemv_entry(f"q4_0_gemv_{p.n}x{p.k}_m{m}", "q4_0", m, (p,), 30 + i)
+    # the same batched products on the tensor cores (qmm_gemv_q4_0_tc)
+    for m in (1,) + tuple(synth.BATCHED_M):
+        for i, p in enumerate(synth.BATCHED_SHAPES):
+            gemv_entry(f"q4_0_gemv_tc_{p.n}x{p.k}_m{m}", "q4_0", m, (p,), 30 + i, tensor_cores=True)
     for m in synth.LM_HEAD_M:
         gemv_entry(f"q8_0_lm_head_262144x2048_m{m}", "q8_0", m, (synth.LM_HEAD,), 50)
     # the feed-forward input: gate and up as one grouped call (two outputs

@@ -279,6 +279,24 @@ qmm_status qmm_gemv_q4_0_geglu(const void *wg, const void *wu, const float *x, f
     return from_cuda(launch_geglu_q4_0(gate_up, x, m, k, reinterpret_cast<cudaStream_t>(stream), ctx));
 }
 
+qmm_status qmm_gemv_q4_0_tc(const void *w, const float *x, float *y, int m, int64_t n, int64_t k,
+                            qmm_stream_t stream) {
+    qmm_status s = check_wk(w, n, k);
+    if (s != QMM_OK) return s;
+    if (!x || !y) return QMM_ERR_NULL;
+    if (m < 1 || m > QMM_GEMV_MAX_M) return QMM_ERR_SHAPE;
+    if (!gemv_tc_shape_ok(m, n, k)) return QMM_ERR_UNSUPPORTED;
+    if (!aligned(w, 16) || !aligned(x, 16) || !aligned(y, 4)) return QMM_ERR_ALIGN;
+    const size_t ybytes = sizeof(float) * static_cast<size_t>(m) * n;
+    const size_t wbytes = static_cast<size_t>(n) * (k / kQK) * kQ4_0Bytes;
+    if (overlaps(y, ybytes, w, wbytes) || overlaps(y, ybytes, x, sizeof(float) * static_cast<size_t>(m) * k))
+        return QMM_ERR_UNSUPPORTED;
+    LaunchCtx ctx;
+    if (!make_ctx(&ctx)) return QMM_ERR_CUDA;
+    return from_cuda(launch_gemv_tc_q4_0(static_cast<const uint8_t *>(w), x, y, m, n, k,
+                                         reinterpret_cast<cudaStream_t>(stream), ctx));
+}
+
 qmm_status qmm_gemm_q4_0(const void *w, const uint16_t *x_bf16, float *y, int64_t m, int64_t n,
                          int64_t k, qmm_stream_t stream) {
     return gemm(Fmt::Q4_0, w, x_bf16, y, m, n, k, stream);
@@ -382,7 +400,7 @@ const char *qmm_status_string(qmm_status status) {
     return "unknown status";
 }
 
-int qmm_version(void) { return 202; }
+int qmm_version(void) { return 300; }
 
 qmm_status qmm_get_device_error(qmm_stream_t stream) {
     cudaError_t e;

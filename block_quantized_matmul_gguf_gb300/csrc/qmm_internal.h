@@ -192,6 +192,13 @@ cudaError_t launch_gemm_q4_0_prefill(const uint8_t *w, const uint16_t *x, float 
                                      int64_t n, int64_t k, cudaStream_t stream,
                                      const LaunchCtx &ctx);
 
+// Batched decode GEMV on the tensor cores (Q4_0, 1 <= m <= 16, k % 256 == 0,
+// w and x 16-byte aligned).  gemv_tc_shape_ok: the launcher has a launch
+// shape for (m, n, k) (the CTA's activation slice fits shared memory).
+bool gemv_tc_shape_ok(int m, int64_t n, int64_t k);
+cudaError_t launch_gemv_tc_q4_0(const uint8_t *w, const float *x, float *y, int m, int64_t n,
+                                int64_t k, cudaStream_t stream, const LaunchCtx &ctx);
+
 cudaError_t launch_selftest_wait(cudaStream_t stream, const LaunchCtx &ctx);
 
 }  // namespace qmm

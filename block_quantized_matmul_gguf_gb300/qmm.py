@@ -29,7 +29,7 @@ QMM_GEMV_MAX_OUTPUTS = 4
 
 EXPORTED = (
     "qmm_dequant_q4_0", "qmm_dequant_q8_0", "qmm_gemv_q4_0", "qmm_gemv_q8_0",
-    "qmm_gemv_q4_0_multi", "qmm_gemv_q8_0_multi", "qmm_gemv_q4_0_geglu",
+    "qmm_gemv_q4_0_multi", "qmm_gemv_q8_0_multi", "qmm_gemv_q4_0_geglu", "qmm_gemv_q4_0_tc",
     "qmm_gemm_q4_0", "qmm_gemm_q8_0", "qmm_gemm_q4_0_geglu",
     "qmm_gemm_q4_0_ws", "qmm_gemm_q8_0_ws", "qmm_gemm_q4_0_geglu_ws", "qmm_gemm_q4_0_prefill",
     "qmm_gemm_workspace_bytes", "qmm_gemm_geglu_workspace_bytes", "qmm_status_string", "qmm_version", "qmm_get_device_error",
@@ -73,6 +73,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         "qmm_dequant_q8_0": [P, P, I64, I64, P],
         "qmm_gemv_q4_0": [P, P, P, I32, I64, I64, P],
         "qmm_gemv_q8_0": [P, P, P, I32, I64, I64, P],
+        "qmm_gemv_q4_0_tc": [P, P, P, I32, I64, I64, P],
         "qmm_gemm_q4_0": [P, P, P, I64, I64, I64, P],
         "qmm_gemm_q8_0": [P, P, P, I64, I64, I64, P],
         "qmm_gemv_q4_0_geglu": [P, P, P, P, I32, I64, I64, P],
@@ -155,6 +156,12 @@ def qmm_gemv_q4_0(w, x, y, m: int, n: int, k: int, stream=None) -> None:
 def qmm_gemv_q8_0(w, x, y, m: int, n: int, k: int, stream=None) -> None:
     _check(load().qmm_gemv_q8_0(_ptr(w), _ptr(x), _ptr(y), m, n, k, _stream(stream)),
            "qmm_gemv_q8_0")
+
+
+def qmm_gemv_q4_0_tc(w, x, y, m: int, n: int, k: int, stream=None) -> None:
+    """The Q4_0 GEMV on the tensor cores (batched decode, same accuracy bound)."""
+    _check(load().qmm_gemv_q4_0_tc(_ptr(w), _ptr(x), _ptr(y), m, n, k, _stream(stream)),
+           "qmm_gemv_q4_0_tc")
 
 
 def _outs(outs):
@@ -257,6 +264,14 @@ def gemv(fmt: str, w, x, n: int, k: int, stream=None):
     m = x.shape[0]
     y = torch.empty((m, n), dtype=torch.float32, device=x.device)
     (qmm_gemv_q4_0 if fmt == "q4_0" else qmm_gemv_q8_0)(w, x, y, m, n, k, stream)
+    return y
+
+
+def gemv_tc_q4_0(w, x, n: int, k: int, stream=None):
+    import torch
+    m = x.shape[0]
+    y = torch.empty((m, n), dtype=torch.float32, device=x.device)
+    qmm_gemv_q4_0_tc(w, x, y, m, n, k, stream)
     return y
 
 

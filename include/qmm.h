@@ -146,6 +146,27 @@ qmm_status qmm_gemv_q8_0_multi(const qmm_gemv_out *outs, int count, const float 
 qmm_status qmm_gemv_q4_0_geglu(const void *wg, const void *wu, const float *x, float *h, int m,
                                int64_t n, int64_t k, qmm_stream_t stream);
 
+/* ---- Batched decode GEMV on the tensor cores ----------------------------
+ * The product of qmm_gemv_q4_0 (same layouts, same accuracy bound
+ * |y - y_exact| <= 1e-4 * sum_k |w*x| + 1e-6), computed on the tcgen05
+ * tensor cores, for the small batches of tokens that decode batching and
+ * MTP verification produce ("Add generated quant-kernel JIT and accelerate
+ * Gemma4, BGE-M3, and GLiNER2", first revision, "Summary" and "Benchmarks":
+ * Gemma4 QAT batching, E4B MTP k=1).  Arithmetic: per 32-weight block the
+ * exact integers (nibble - 8) (bf16) multiply x split into two bf16 parts,
+ * x_hi = bf16(x) and x_lo = bf16(x - x_hi) (|x - x_hi - x_lo| <= 2^-16 |x|),
+ * summed in fp32 in tensor memory; each block's sum is then scaled by its d
+ * and accumulated in fp32.  qmm_gemv_q4_0 remains the fp32 CUDA-core call.
+ * Requires 1 <= m <= QMM_GEMV_MAX_M, n >= 1, k % 256 == 0, k >= 256, w and x
+ * 16-byte aligned, y 4-byte aligned and not overlapping w or x.  Valid
+ * shapes it does not take return QMM_ERR_UNSUPPORTED: k % 256 != 0, n > 2^30,
+ * and shapes whose share of the activations per CTA does not fit shared
+ * memory with the K range split at most 8 ways (a power of two dividing
+ * k / 256).  Every k up to 5632 (m <= 8) or 2560 (m > 8) is taken; larger k
+ * needs such a split, up to k = 36864 (m <= 8) or 14336 (m > 8). */
+qmm_status qmm_gemv_q4_0_tc(const void *w, const float *x, float *y, int m, int64_t n,
+                            int64_t k, qmm_stream_t stream);
+
 /* ---- Prefill GEMM (tcgen05 tensor cores) ------------------------------
  * Y[i][j] = sum_k X[i][k] * w[j][k] for i < m, j < n.  X is bf16 [m][k]
  * given as raw bf16 bit patterns; each weight is rounded once to bf16
