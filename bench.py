@@ -69,6 +69,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-secondary", action="store_true",
                     help="skip the secondary workloads (headline only)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", default=None, metavar="REGEX",
+                    help="secondary workloads: run only those whose name matches REGEX")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--profile", default=None, metavar="CASE",
@@ -524,14 +526,19 @@ def measure_e2e(torch, qmm, layer: DecodeLayer, steps: int, dist, graphs: bool):
     return el, h2d, d2h
 
 
-def run_secondary(torch, qmm, l2, stream, timer, peaks, sms):
-    """Other workloads, each as GB/s or TFLOP/s per GPU (rank 0)."""
+def run_secondary(torch, qmm, l2, stream, timer, peaks, sms, only=None):
+    """Other workloads, each as GB/s or TFLOP/s per GPU (rank 0).  only: a
+    regular expression; workloads whose names do not match are skipped."""
+    import re
     out = {}
     hbm = peaks["hbm_gbs"]
+    wanted = (lambda name: re.search(only, name) is not None) if only else (lambda name: True)
 
     weight_cache = {}
 
     def gemv_entry(name, fmt, m, projs, base, grouped=False, tensor_cores=False):
+        if not wanted(name):
+            return
         key = (fmt, base, tuple((p.n, p.k) for p in projs))
         if key not in weight_cache:
             weight_cache.clear()
@@ -580,14 +587,17 @@ def run_secondary(torch, qmm, l2, stream, timer, peaks, sms):
     ffn = tuple(p for p in synth.DECODE_LAYER if p.name in ("gate", "up"))
     for m in (1, 8):
         gemv_entry(f"q4_0_decode_gate_up_grouped_m{m}", "q4_0", m, ffn, 14, grouped=True)
+        if not wanted(f"q4_0_decode_ffn_geglu_m{m}"):
+            continue
         try:
             out.update(measure_geglu(torch, qmm, l2, stream, timer, hbm, ffn, m))
         except Exception as e:  # noqa: BLE001 - reported, not hidden
             out[f"q4_0_decode_ffn_geglu_m{m}"] = {"error": str(e)[:200]}
-    try:
-        out.update(measure_gemm(torch, qmm, l2, stream, timer, peaks))
-    except Exception as e:  # noqa: BLE001 - reported, not hidden
-        out["q4_0_gemm"] = {"error": str(e)[:200]}
+    if wanted("q4_0_gemm_2048x8192x2048"):
+        try:
+            out.update(measure_gemm(torch, qmm, l2, stream, timer, peaks))
+        except Exception as e:  # noqa: BLE001 - reported, not hidden
+            out["q4_0_gemm"] = {"error": str(e)[:200]}
     return out
 
 
@@ -956,7 +966,7 @@ def run_ours(args, dist):
         "gpu_launches": args.steps * launches_per_step,
     }
     if not args.no_secondary and dist.rank == 0:
-        secondary = run_secondary(torch, qmm, l2, stream, timer, peaks, sms)
+        secondary = run_secondary(torch, qmm, l2, stream, timer, peaks, sms, args.only)
         result["kernels"] = kernel_summary(secondary)
         result["secondary"] = secondary
     if dist.rank == 0 and not args.no_cpu_baseline:

@@ -28,21 +28,26 @@
 // (L0, L2), (L1, L3), (H0, H2), (H1, H3): the block's K order is permuted,
 // and the B operand is written with the same permutation.
 //
-// Structure: one CTA per SM (512 TMEM columns), 320 threads, persistent over
+// Structure: one CTA per SM (512 TMEM columns), 448 threads, persistent over
 // 128-row tiles; the K range is split over a thread-block cluster of ks CTAs
 // (partial sums pushed to rank 0's shared memory and added in rank order).
 //   warp 0      producer: TMA of raw Q4_0 stages (128 rows x 144 bytes = 256
-//               weights per row); issued before the programmatic-launch wait
-//               (weights are read-only model data).
-//   warp 1      TMEM allocation and the MMA thread: per block, two
-//               tcgen05.mma.cta_group::1.kind::f16 (M = 128, N = 2 Mp, K = 16)
-//               into one of 8 D slots, committed to the epilogue.
-//   warps 2-5   dequantisers: lane quarter q = warp % 4, one weight row per
-//               lane; write the stage's A (128 columns) with tcgen05.st and
-//               the blocks' d (fp32) to shared memory.
-//   warps 6-9   epilogue: tcgen05.ld of a block's D slot, y[t] += d*(hi+lo);
-//               at the end of a tile the K parts are added and y stored.
-//   warps 2-9 first convert the CTA's activation slice to B (bf16 hi/lo,
+//               weights per row), from the first instruction after barrier
+//               set-up and before the programmatic-launch wait (weights are
+//               read-only model data).
+//   warp 1      TMEM allocation and the MMA thread: per group of 64 D columns
+//               (2 blocks at N = 32, 4 at N = 16), two tcgen05.mma.cta_group::1
+//               .kind::f16 (M = 128, N = 2 Mp, K = 16) per block into its own
+//               D slot, then one commit for the group (a commit costs about
+//               as much issue time as an MMA of these shapes).
+//   warps 2-9   dequantisers: lane quarter q = warp % 4, one weight row per
+//               lane, half of a stage's 8 blocks per warp; write A with
+//               tcgen05.st and the blocks' d (fp32) to shared memory.
+//   warps 10-13 epilogue: one tcgen05.ld of a group's D slots, y[t] +=
+//               d*(hi+lo); at the end of a tile the K parts are added and y
+//               stored (with one tile per cluster, after the final cluster
+//               barrier, so that no per-tile cluster handshake is needed).
+//   warps 2-13 first convert the CTA's activation slice to B (bf16 hi/lo,
 //   128-byte swizzle, K-major) in shared memory.
 // Every wait is bounded; a timeout sets the CTA's abort flag and records the
 // error; the kernel drains its own copies and MMAs and frees TMEM.
@@ -63,11 +68,13 @@ constexpr int TC_DS = 8;              // D slots in TMEM (one block each)
 constexpr uint32_t TC_A_COLS = TCK / 2;          // 128 columns per A slot
 constexpr uint32_t TC_D_COL0 = TC_AS * TC_A_COLS;  // 256
 constexpr uint32_t TC_TMEM_COLS = 512;
-constexpr int TC_THREADS = 320;
-constexpr int TC_WARP_PROD = 0, TC_WARP_MMA = 1, TC_WARP_DEQ0 = 2, TC_WARP_EPI0 = 6;
-constexpr int TC_CONVERTERS = 256;    // warps 2-9
-static_assert(TC_WARP_EPI0 - TC_WARP_DEQ0 == 4 && TC_THREADS == (TC_WARP_EPI0 + 4) * 32,
-              "four dequantiser and four epilogue warps, one per TMEM lane quarter");
+constexpr int TC_WARP_PROD = 0, TC_WARP_MMA = 1, TC_WARP_DEQ0 = 2;
+constexpr int TC_DEQ_WARPS = 8;       // two per TMEM lane quarter, four blocks of a stage each
+constexpr int TC_WARP_EPI0 = TC_WARP_DEQ0 + TC_DEQ_WARPS;  // 10
+constexpr int TC_WARP_MMA2 = TC_WARP_EPI0 + 4;             // 14: the second MMA thread
+constexpr int TC_THREADS = (TC_WARP_MMA2 + 1) * 32;        // 480
+constexpr int TC_CONVERTERS = 4 * 32 * 3;                  // warps 2-13
+static_assert(TC_DEQ_WARPS == 8, "dequantiser warp w takes lane quarter w % 4, half (w - 2) / 4");
 constexpr int TC_MAX_KS = 8;
 // one CTA per SM: every CTA takes more than half of the SM's shared memory,
 // so that a second CTA (which would wait for the TMEM this one holds) never
@@ -123,40 +130,100 @@ template <int MP>
 __device__ __forceinline__ void convert_activations(const float *__restrict__ x, int m, int k,
                                                     int k0, int cta_k, uint8_t *b_smem, int tid) {
     constexpr int N = 2 * MP;
-    const int units = MP * (cta_k >> 3);  // (token, 16-byte chunk of 8 K slots)
-    for (int u = tid; u < units; u += TC_CONVERTERS) {
-        const int t = u / (cta_k >> 3);
-        const int ch = u - t * (cta_k >> 3);  // chunk along K: slots 8ch .. 8ch+7
-        float v[8];
-        if (t < m) {
-            // slots 8i..8i+7 of block ch/4 (i = ch % 4): weights 4i + {0,2,1,3}
-            // and 16 + 4i + {0,2,1,3}
-            const int blk = ch >> 2, i = ch & 3;
-            const float *src = x + static_cast<size_t>(t) * k + k0 + 32 * blk + 4 * i;
-            const float4 a = *reinterpret_cast<const float4 *>(src);
-            const float4 c = *reinterpret_cast<const float4 *>(src + 16);
-            v[0] = a.x; v[1] = a.z; v[2] = a.y; v[3] = a.w;
-            v[4] = c.x; v[5] = c.z; v[6] = c.y; v[7] = c.w;
+    constexpr int U = 4;  // units per thread whose loads are in flight together
+    const int cpt = cta_k >> 3;    // 16-byte chunks (8 K slots) per token
+    const int units = MP * cpt;    // (token, chunk)
+    for (int u0 = tid; u0 < units; u0 += U * TC_CONVERTERS) {
+        float4 ld[U][2];
+#pragma unroll
+        for (int j = 0; j < U; ++j) {
+            const int u = u0 + j * TC_CONVERTERS;
+            const int t = u / cpt;
+            ld[j][0] = ld[j][1] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            if (u < units && t < m) {
+                // slots 8i..8i+7 of block ch/4 (i = ch % 4): weights 4i + {0,2,1,3}
+                // and 16 + 4i + {0,2,1,3}
+                const int ch = u - t * cpt;
+                const float *src = x + static_cast<size_t>(t) * k + k0 + 32 * (ch >> 2) + 4 * (ch & 3);
+                ld[j][0] = *reinterpret_cast<const float4 *>(src);
+                ld[j][1] = *reinterpret_cast<const float4 *>(src + 16);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < U; ++j) {
+            const int u = u0 + j * TC_CONVERTERS;
+            if (u >= units) break;
+            const int t = u / cpt;
+            const int ch = u - t * cpt;
+            const float4 a = ld[j][0], c = ld[j][1];
+            const float v[8] = {a.x, a.z, a.y, a.w, c.x, c.z, c.y, c.w};
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                hi[q] = pack_bf16x2(v[2 * q], v[2 * q + 1]);
+                const float h0 = __uint_as_float(hi[q] << 16), h1 = __uint_as_float(hi[q] & 0xFFFF0000u);
+                lo[q] = pack_bf16x2(v[2 * q] - h0, v[2 * q + 1] - h1);
+            }
+            const int sl = ch >> 3, c16 = ch & 7;
+#pragma unroll
+            for (int part = 0; part < 2; ++part) {
+                const int row = t + part * MP;
+                const uint32_t off = static_cast<uint32_t>(sl) * (N * 128) + (row >> 3) * 1024 +
+                                     (row & 7) * 128 + ((c16 ^ (row & 7)) << 4);
+                *reinterpret_cast<uint4 *>(b_smem + off) =
+                    part == 0 ? make_uint4(hi[0], hi[1], hi[2], hi[3]) : make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            }
+        }
+    }
+}
+
+// Split cluster barrier: arrive early, wait only where it matters.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+// Named barrier over the warps after the producer (TMEM address handed out).
+__device__ __forceinline__ void sync_after_producer() {
+    asm volatile("bar.sync 1, %0;" ::"r"(TC_THREADS - 32) : "memory");
+}
+
+// Dequantiser half H (blocks 4H .. 4H+3) of one row's 256-weight stage, held
+// in wd[36]: (nibble - 8) as bf16 pairs into TMEM columns a_col + 16 b, and
+// the blocks' d (fp32) into dsm_row[b * TW].
+template <int H>
+__device__ __forceinline__ void dequant_half(const uint32_t (&wd)[36], uint32_t taddr_slot,
+                                             float *dsm_row) {
+    const uint32_t M128 = 0x43004300u;                       // bf16 128.0, 128.0
+    const uint32_t ONE = 0x3F803F80u, NEG136 = 0xC308C308u;  // 1, -136
+#pragma unroll
+    for (int bb = 0; bb < 4; ++bb) {
+        const int b = 4 * H + bb;
+        const int base = (18 * b) >> 2;
+        uint32_t dbits, qw[4];
+        if ((b & 1) == 0) {
+            dbits = wd[base] & 0xFFFFu;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) qw[i] = __byte_perm(wd[base + i], wd[base + i + 1], 0x5432);
         } else {
+            dbits = wd[base] >> 16;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) v[j] = 0.0f;
+            for (int i = 0; i < 4; ++i) qw[i] = wd[base + 1 + i];
         }
-        uint32_t hi[4], lo[4];
+        dsm_row[b * TW] = half_bits_to_float(dbits);
+        uint32_t cols[16];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            hi[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
-            const float h0 = __uint_as_float(hi[j] << 16), h1 = __uint_as_float(hi[j] & 0xFFFF0000u);
-            lo[j] = pack_bf16x2(v[2 * j] - h0, v[2 * j + 1] - h1);
+        for (int i = 0; i < 4; ++i) {
+            // every nibble is moved to bits 0-3 of its 16-bit half first: bf16
+            // has 7 mantissa bits, so bits 4-7 would reach the exponent
+            const uint32_t v = qw[i];
+            cols[4 * i + 0] = bf16x2_fma((v & 0x000F000Fu) | M128, ONE, NEG136);
+            cols[4 * i + 1] = bf16x2_fma(((v >> 8) & 0x000F000Fu) | M128, ONE, NEG136);
+            cols[4 * i + 2] = bf16x2_fma(((v >> 4) & 0x000F000Fu) | M128, ONE, NEG136);
+            cols[4 * i + 3] = bf16x2_fma(((v >> 12) & 0x000F000Fu) | M128, ONE, NEG136);
         }
-        const int sl = ch >> 3, c16 = ch & 7;
-#pragma unroll
-        for (int part = 0; part < 2; ++part) {
-            const int row = t + part * MP;
-            const uint32_t off = static_cast<uint32_t>(sl) * (N * 128) + (row >> 3) * 1024 +
-                                 (row & 7) * 128 + ((c16 ^ (row & 7)) << 4);
-            *reinterpret_cast<uint4 *>(b_smem + off) =
-                part == 0 ? make_uint4(hi[0], hi[1], hi[2], hi[3]) : make_uint4(lo[0], lo[1], lo[2], lo[3]);
-        }
+        tmem_st_16cols(taddr_slot + b * 16, cols);
     }
 }
 
@@ -166,6 +233,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                    TcParams p) {
     constexpr int N = 2 * MP;
     constexpr uint32_t kIdesc = tc_idesc(N);
+    constexpr int BPW = 64 / N;  // blocks per D group: 64 TMEM columns, one commit, one load
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_base = smem_addr(smem_raw);
     const uint32_t sbase = (raw_base + 1023u) & ~1023u;  // 1024-byte aligned (swizzle atoms)
@@ -179,9 +247,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int cluster = static_cast<int>(blockIdx.x / ks);
     const int RS = p.raw_stages;
     const int C = p.cta_chunks;
+    // every cluster handles at most one tile: the K parts are then added after
+    // the final cluster barrier instead of through per-tile handshakes
+    const bool single_tile = p.tiles <= p.clusters;
 
     // barriers: raw_full[RS], raw_empty[RS], a_full[AS], a_empty[AS],
-    // d_full[DS], d_empty[DS], red_full[4], red_empty[4], b_ready, final
+    // d_full[DS], d_empty[DS] (the first slot of each D group is used),
+    // red_full[4], red_empty[4], b_ready, final[2] (one per MMA thread)
     const uint32_t bars = sbase + p.off_bars;
     auto raw_full = [&](int r) { return bars + 8u * r; };
     auto raw_empty = [&](int r) { return bars + 8u * (RS + r); };
@@ -192,48 +264,58 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const uint32_t red_full0 = d_empty0 + 8u * TC_DS;
     const uint32_t red_empty0 = red_full0 + 8u * 4;
     const uint32_t b_ready = red_empty0 + 8u * 4;
-    const uint32_t final_bar = b_ready + 8u;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sgen + p.off_bars + 8 * (2 * RS + 2 * TC_AS + 2 * TC_DS + 10));
+    const uint32_t final_bar0 = b_ready + 8u;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sgen + p.off_bars + 8 * (2 * RS + 2 * TC_AS + 2 * TC_DS + 11));
     int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
     float *dsm = reinterpret_cast<float *>(sgen + p.off_dsm);    // [AS][8 blocks][128 rows]
     float *part = reinterpret_cast<float *>(sgen + p.off_part);  // [ks-1][128 rows][MP+1]
 
     if (threadIdx.x == 0) {
+        // the weight tensor map's first fetch overlaps the barrier set-up
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_w)) : "memory");
         for (int r = 0; r < RS; ++r) {
             mbar_init_addr(raw_full(r), 1);
-            mbar_init_addr(raw_empty(r), 4);
+            mbar_init_addr(raw_empty(r), TC_DEQ_WARPS);
         }
         for (int a = 0; a < TC_AS; ++a) {
-            mbar_init_addr(a_full0 + 8u * a, 4);
-            mbar_init_addr(a_empty0 + 8u * a, 1 + 4);  // MMA commit + 4 epilogue warps
+            mbar_init_addr(a_full0 + 8u * a, TC_DEQ_WARPS);
+            mbar_init_addr(a_empty0 + 8u * a, 2 + 4);  // 2 MMA-thread commits + 4 epilogue warps
         }
         for (int d = 0; d < TC_DS; ++d) {
             mbar_init_addr(d_full0 + 8u * d, 1);
             mbar_init_addr(d_empty0 + 8u * d, 4);
         }
         for (int q = 0; q < 4; ++q) {
-            mbar_init_addr(red_full0 + 8u * q, 32u * (ks > 1 ? ks - 1 : 1));
-            mbar_init_addr(red_empty0 + 8u * q, 32);
+            // one tile per cluster: rank 0's warp q expects the peers' partial
+            // sums as bulk-copy bytes (one arrival), and each peer waits for
+            // one acknowledgement; otherwise per-lane handshakes per tile
+            mbar_init_addr(red_full0 + 8u * q, single_tile ? 1u : 32u * (ks > 1 ? ks - 1 : 1));
+            mbar_init_addr(red_empty0 + 8u * q, single_tile ? 1u : 32u);
         }
         mbar_init_addr(b_ready, TC_CONVERTERS);
-        mbar_init_addr(final_bar, 1);
+        mbar_init_addr(final_bar0, 1);
+        mbar_init_addr(final_bar0 + 8u, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == TC_WARP_MMA) tmem_alloc_cta(smem_addr(tmem_slot), TC_TMEM_COLS);
-    tc_fence_before();
     __syncthreads();
-    if (ks > 1) cluster_barrier();  // the peers' barriers exist before anyone signals them
-    tc_fence_after();
-    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
+    // this CTA's barriers exist: announce it to the cluster now, wait for the
+    // peers only before the first access to their shared memory
+    if (ks > 1) cluster_arrive_relaxed();
+    bool cluster_waited = false;
 
     const int my_tiles = cluster < p.tiles ? (p.tiles - cluster + p.clusters - 1) / p.clusters : 0;
     const uint32_t total_stages = static_cast<uint32_t>(my_tiles) * static_cast<uint32_t>(C);
     const int chunk0 = static_cast<int>(rank) * C;  // first raw stage of this CTA's K range
 
+    uint32_t tmem_base = 0;
+    float y[MP];
+#pragma unroll
+    for (int t = 0; t < MP; ++t) y[t] = 0.0f;
+
     if (warp == TC_WARP_PROD) {
+        // weight stages from the start: they need neither TMEM nor the activations
         if (lane == 0) {
-            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_w)) : "memory");
             uint32_t it = 0;
             int r = 0;
             uint32_t ph = 0;
@@ -263,12 +345,25 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 }
             }
         }
-    } else if (warp == TC_WARP_MMA) {
+        __syncwarp();
+    } else {
+        if (warp == TC_WARP_MMA) tmem_alloc_cta(smem_addr(tmem_slot), TC_TMEM_COLS);
+        tc_fence_before();
+        sync_after_producer();
+        tc_fence_after();
+        tmem_base = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
+    }
+
+    if (warp == TC_WARP_MMA || warp == TC_WARP_MMA2) {
+        // two MMA threads on different schedulers take alternate D groups:
+        // one thread issuing every MMA was slowed by the busy warps sharing its
+        // scheduler; each commits (and drains) only its own MMAs
+        const uint32_t mine = warp == TC_WARP_MMA ? 0u : 1u;
         if (lane == 0) {
             bool ok = total_stages == 0 || wait_or_abort(b_ready, 0, abort_flag, ctx);
             const uint64_t bdesc0 = sw128_desc(sbase);
             bool issued = false;
-            uint32_t g = 0;  // blocks issued
+            uint32_t g = 0;  // blocks of all groups so far
             int a = 0;
             uint32_t aph = 0;
             int c = 0;
@@ -276,22 +371,27 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 if (!wait_or_abort(a_full0 + 8u * a, aph, abort_flag, ctx)) break;
                 tc_fence_after();
 #pragma unroll 1
-                for (int b = 0; b < 8; ++b, ++g) {
-                    const uint32_t ds = g % TC_DS;
-                    if (!wait_or_abort(d_empty0 + 8u * ds, ((g / TC_DS) & 1u) ^ 1u, abort_flag, ctx)) {
+                for (int b0 = 0; b0 < 8; b0 += BPW, g += BPW) {
+                    if (((g / BPW) & 1u) != mine) continue;
+                    const uint32_t ds0 = g % TC_DS;
+                    if (!wait_or_abort(d_empty0 + 8u * ds0, ((g / TC_DS) & 1u) ^ 1u, abort_flag, ctx)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    // K slots of block b of chunk c: slice (4c + b/2), 64 bytes in for odd b
-                    const uint64_t bdesc = bdesc0 + ((static_cast<uint64_t>(4 * c + (b >> 1)) * (N * 128) +
-                                                      (b & 1) * 64) >> 4);
-                    const uint32_t a_tmem = tmem_base + a * TC_A_COLS + b * 16;
-                    const uint32_t d_tmem = tmem_base + TC_D_COL0 + ds * N;
-                    umma_bf16_cta_ta(d_tmem, a_tmem, bdesc, kIdesc, 0u);
-                    umma_bf16_cta_ta(d_tmem, a_tmem + 8, bdesc + 2, kIdesc, 1u);  // +16 K: 32 bytes
+#pragma unroll
+                    for (int j = 0; j < BPW; ++j) {
+                        const int b = b0 + j;
+                        // K slots of block b of chunk c: slice (4c + b/2), 64 bytes in for odd b
+                        const uint64_t bdesc =
+                            bdesc0 + ((static_cast<uint64_t>(4 * c + (b >> 1)) * (N * 128) + (b & 1) * 64) >> 4);
+                        const uint32_t a_tmem = tmem_base + a * TC_A_COLS + b * 16;
+                        const uint32_t d_tmem = tmem_base + TC_D_COL0 + (ds0 + j) * N;
+                        umma_bf16_cta_ta(d_tmem, a_tmem, bdesc, kIdesc, 0u);
+                        umma_bf16_cta_ta(d_tmem, a_tmem + 8, bdesc + 2, kIdesc, 1u);  // +16 K: 32 bytes
+                    }
                     issued = true;
-                    umma_commit_cta(d_full0 + 8u * ds);
+                    umma_commit_cta(d_full0 + 8u * ds0);
                 }
                 if (!ok) break;
                 umma_commit_cta(a_empty0 + 8u * a);
@@ -301,13 +401,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 }
                 if (++c == C) c = 0;
             }
-            if (issued) {  // every MMA completes before TMEM is freed
-                umma_commit_cta(final_bar);
-                wait_drain(final_bar, 0, ctx);
+            if (issued) {  // this thread's MMAs complete before TMEM is freed
+                umma_commit_cta(final_bar0 + 8u * mine);
+                wait_drain(final_bar0 + 8u * mine, 0, ctx);
             }
         }
-    } else {
-        // warps 2-9: the activation slice -> B (after the programmatic-launch
+        __syncwarp();
+    } else if (warp >= TC_WARP_DEQ0) {
+        // warps 2-13: the activation slice -> B (after the programmatic-launch
         // wait: x is written by the preceding kernel)
         pdl_wait();
         convert_activations<MP>(x, p.m, k, chunk0 * TCK, C * TCK, sgen, threadIdx.x - 64);
@@ -319,9 +420,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const int row = 32 * q + lane;    // weight row within the tile (TMEM lane)
         const uint32_t lane_off = static_cast<uint32_t>(32 * q) << 16;
         if (warp < TC_WARP_EPI0) {
-            // ---- dequantisers ----
-            const uint32_t M128 = 0x43004300u;                       // bf16 128.0, 128.0
-            const uint32_t ONE = 0x3F803F80u, NEG136 = 0xC308C308u;  // 1, -136
+            // ---- dequantisers: two warps per lane quarter, four blocks each ----
+            const int half = (warp - TC_WARP_DEQ0) >> 2;
             int r = 0, a = 0;
             uint32_t rph = 0, aph = 0;
             for (uint32_t it = 0; it < total_stages; ++it) {
@@ -344,34 +444,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 }
                 if (!warp_wait_or_abort(a_empty0 + 8u * a, aph ^ 1u, abort_flag, ctx)) break;
                 tc_fence_after();
-#pragma unroll
-                for (int b = 0; b < 8; ++b) {
-                    const int base = (18 * b) >> 2;
-                    uint32_t dbits, qw[4];
-                    if ((b & 1) == 0) {
-                        dbits = wd[base] & 0xFFFFu;
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) qw[i] = __byte_perm(wd[base + i], wd[base + i + 1], 0x5432);
-                    } else {
-                        dbits = wd[base] >> 16;
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) qw[i] = wd[base + 1 + i];
-                    }
-                    dsm[(a * 8 + b) * TW + row] = half_bits_to_float(dbits);
-                    uint32_t cols[16];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        // every nibble is moved to bits 0-3 of its 16-bit half
-                        // first: bf16 has 7 mantissa bits, so bits 4-7 would
-                        // reach the exponent
-                        const uint32_t v = qw[i];
-                        cols[4 * i + 0] = bf16x2_fma((v & 0x000F000Fu) | M128, ONE, NEG136);
-                        cols[4 * i + 1] = bf16x2_fma(((v >> 8) & 0x000F000Fu) | M128, ONE, NEG136);
-                        cols[4 * i + 2] = bf16x2_fma(((v >> 4) & 0x000F000Fu) | M128, ONE, NEG136);
-                        cols[4 * i + 3] = bf16x2_fma(((v >> 12) & 0x000F000Fu) | M128, ONE, NEG136);
-                    }
-                    tmem_st_16cols(tmem_base + lane_off + a * TC_A_COLS + b * 16, cols);
-                }
+                const uint32_t taddr = tmem_base + lane_off + a * TC_A_COLS;
+                float *dsm_row = dsm + a * 8 * TW + row;
+                if (half == 0)
+                    dequant_half<0>(wd, taddr, dsm_row);
+                else
+                    dequant_half<1>(wd, taddr, dsm_row);
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
@@ -383,9 +461,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             }
         } else {
             // ---- epilogue ----
-            float y[MP];
-#pragma unroll
-            for (int t = 0; t < MP; ++t) y[t] = 0.0f;
             uint32_t g = 0;
             int a = 0, c = 0, tile_i = 0;
             uint32_t aph = 0;
@@ -393,26 +468,27 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             for (uint32_t it = 0; ok && it < total_stages; ++it) {
                 if (!warp_wait_or_abort(a_full0 + 8u * a, aph, abort_flag, ctx)) break;
 #pragma unroll 1
-                for (int b = 0; b < 8; ++b, ++g) {
-                    const uint32_t ds = g % TC_DS;
-                    if (!warp_wait_or_abort(d_full0 + 8u * ds, (g / TC_DS) & 1u, abort_flag, ctx)) {
+                for (int b0 = 0; b0 < 8; b0 += BPW, g += BPW) {
+                    const uint32_t ds0 = g % TC_DS;
+                    if (!warp_wait_or_abort(d_full0 + 8u * ds0, (g / TC_DS) & 1u, abort_flag, ctx)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    uint32_t v[N];
-                    if constexpr (N == 16) {
-                        tmem_ld_16cols(tmem_base + lane_off + TC_D_COL0 + ds * N, v);
-                    } else {
-                        tmem_ld_32cols(tmem_base + lane_off + TC_D_COL0 + ds * N, v);
-                    }
+                    // the group's D slots are 64 consecutive TMEM columns
+                    uint32_t v[64];
+                    tmem_ld_64cols(tmem_base + lane_off + TC_D_COL0 + ds0 * N, v);
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive_addr(d_empty0 + 8u * ds);
-                    const float d = dsm[(a * 8 + b) * TW + row];
+                    if (lane == 0) mbar_arrive_addr(d_empty0 + 8u * ds0);
 #pragma unroll
-                    for (int t = 0; t < MP; ++t)
-                        y[t] = fmaf(d, __uint_as_float(v[t]) + __uint_as_float(v[MP + t]), y[t]);
+                    for (int j = 0; j < BPW; ++j) {
+                        const float d = dsm[(a * 8 + b0 + j) * TW + row];
+#pragma unroll
+                        for (int t = 0; t < MP; ++t)
+                            y[t] = fmaf(d, __uint_as_float(v[j * N + t]) + __uint_as_float(v[j * N + MP + t]),
+                                        y[t]);
+                    }
                 }
                 if (!ok) break;
                 __syncwarp();
@@ -426,6 +502,51 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 c = 0;
                 const int n_row = (cluster + tile_i * p.clusters) * TW + row;
                 const uint32_t tpar = static_cast<uint32_t>(tile_i) & 1u;
+                if (ks > 1 && !cluster_waited) {  // the peers are running: their shared memory exists
+                    cluster_wait();
+                    cluster_waited = true;
+                }
+                if (ks > 1 && single_tile) {
+                    if (rank != 0) {
+                        // partial sums staged in this CTA's own buffer, then one
+                        // bulk copy into rank 0's, completing as bytes on rank
+                        // 0's barrier (no cluster-scope release needed)
+                        float *stage = part + (q * 32 + lane) * MP;
+#pragma unroll
+                        for (int t = 0; t < MP; ++t) stage[t] = y[t];
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            const uint32_t dst = map_to_rank(
+                                smem_addr(part + ((rank - 1) * 4 + q) * 32 * MP), 0);
+                            bulk_s2cluster(dst, smem_addr(part + q * 32 * MP), 32 * MP * 4,
+                                           map_to_rank(red_full0 + 8u * q, 0));
+                        }
+                        // rank 0 acknowledges once it has the bytes: this CTA's
+                        // buffer (the copy's source) stays until then
+                        if (!warp_wait_or_abort(red_empty0 + 8u * q, 0, abort_flag, ctx)) break;
+                    } else {
+                        if (lane == 0)
+                            mbar_expect_tx_addr(red_full0 + 8u * q, (ks - 1) * 32 * MP * 4);
+                        if (!warp_wait_or_abort(red_full0 + 8u * q, 0, abort_flag, ctx)) break;
+                        for (uint32_t rr = 1; rr < ks; ++rr) {
+                            const float *pp = part + (((rr - 1) * 4 + q) * 32 + lane) * MP;
+#pragma unroll
+                            for (int t = 0; t < MP; ++t) y[t] += pp[t];
+                        }
+                        __syncwarp();
+                        if (lane == 0)
+                            for (uint32_t rr = 1; rr < ks; ++rr)
+                                mbar_arrive_remote_relaxed(map_to_rank(red_empty0 + 8u * q, rr));
+                        if (n_row < p.n) {
+#pragma unroll
+                            for (int t = 0; t < MP; ++t)
+                                if (t < p.m) p.y[static_cast<size_t>(t) * p.n + n_row] = y[t];
+                        }
+                    }
+                    ++tile_i;
+                    continue;  // the only tile
+                }
                 if (ks > 1 && rank != 0) {
                     if (!warp_wait_or_abort(red_empty0 + 8u * q, tpar ^ 1u, abort_flag, ctx)) break;
                     const uint32_t dst = map_to_rank(
@@ -476,7 +597,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
     tc_fence_before();
     __syncthreads();
-    if (ks > 1) cluster_barrier();  // no peer still writes into this CTA's shared memory
+    if (ks > 1) {
+        if (!cluster_waited) cluster_wait();  // the start-up phase of the cluster barrier
+        // several tiles per cluster: no peer may still write this CTA's shared
+        // memory (with one tile, every transfer was waited for above)
+        if (!single_tile) cluster_barrier();
+    }
     tc_fence_after();
     if (warp == TC_WARP_MMA) tmem_dealloc_cta(tmem_base, TC_TMEM_COLS);
 }
@@ -499,7 +625,7 @@ TcShape tc_layout(int64_t k, int ks, int rs) {
     const size_t b_bytes = static_cast<size_t>(C_cta) * TCK * N * 2;
     const size_t dsm_bytes = static_cast<size_t>(TC_AS) * 8 * TW * 4;
     const size_t part_bytes = static_cast<size_t>(std::max(ks - 1, 1)) * TW * (MP + 1) * 4;
-    const int nbars = 2 * rs + 2 * TC_AS + 2 * TC_DS + 10;
+    const int nbars = 2 * rs + 2 * TC_AS + 2 * TC_DS + 11;
     sh.ks = ks;
     sh.raw_stages = rs;
     sh.off_raw = b_bytes;
@@ -513,16 +639,18 @@ TcShape tc_layout(int64_t k, int ks, int rs) {
 // K parts ks (cluster size): among the splits whose layout fits with at
 // least two raw stages, the one that keeps the most SMs busy over whole
 // rounds of tiles (ties: fewer parts); then the deepest ring (up to 8) that
-// fits.  ks == 0: no split fits.
-template <int MP>
-TcShape tc_shape(int64_t n, int64_t k, int sms) {
+// fits.  max_clusters(ks) is how many clusters of ks CTAs (one per SM) can
+// be resident at once: with 8-CTA clusters that is fewer than SMs / 8, and
+// launching more would run them in a second wave.  ks == 0: no split fits.
+template <int MP, typename MaxClusters>
+TcShape tc_shape(int64_t n, int64_t k, int sms, MaxClusters max_clusters) {
     TcShape best{};
     const int tiles = static_cast<int>((n + TW - 1) / TW);
     const int C = static_cast<int>(k / TCK);
     double best_eff = -1.0;
     for (int ks = 1; ks <= TC_MAX_KS && C % ks == 0; ks *= 2) {
         if (tc_layout<MP>(k, ks, 2).smem > kTcSmemCap) continue;
-        const int clusters = std::max(1, std::min(tiles, sms / ks));
+        const int clusters = std::max(1, std::min(tiles, std::min(sms / ks, max_clusters(ks))));
         const int rounds = (tiles + clusters - 1) / clusters;
         const double eff = static_cast<double>(tiles) * ks / (static_cast<double>(rounds) * sms);
         if (eff > best_eff + 1e-9) {
@@ -540,7 +668,34 @@ TcShape tc_shape(int64_t n, int64_t k, int sms) {
 template <int MP>
 cudaError_t launch_tc(const uint8_t *w, const float *x, float *y, int m, int64_t n, int64_t k,
                       cudaStream_t stream, const LaunchCtx &ctx) {
-    const TcShape sh = tc_shape<MP>(n, k, device_sm_count());
+    // resident clusters per cluster size, queried once per device and size
+    static int max_active[kMaxDevices][TC_MAX_KS + 1] = {};
+    const int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    static int smem_limits[kMaxDevices] = {0};
+    cudaError_t e = ensure_smem(gemv_tc_kernel<MP>, kTcSmemCap, true, smem_limits);
+    if (e != cudaSuccess) return e;
+    auto max_clusters = [&](int ks) {
+        int &cached = max_active[dev][ks];
+        if (__atomic_load_n(&cached, __ATOMIC_ACQUIRE) > 0) return cached;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(ks));
+        cfg.blockDim = dim3(TC_THREADS);
+        cfg.dynamicSmemBytes = TC_MIN_SMEM;  // every layout is at least this (one CTA per SM)
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = static_cast<unsigned>(ks);
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int num = 0;
+        if (cudaOccupancyMaxActiveClusters(&num, gemv_tc_kernel<MP>, &cfg) != cudaSuccess || num < 1)
+            num = std::max(1, device_sm_count() / (2 * ks));  // conservative if the query fails
+        __atomic_store_n(&cached, num, __ATOMIC_RELEASE);
+        return num;
+    };
+    const TcShape sh = tc_shape<MP>(n, k, device_sm_count(), max_clusters);
     if (sh.ks == 0 || sh.smem > kTcSmemCap) return cudaErrorInvalidValue;
     CUtensorMap tw;
     const uint64_t rowbytes = static_cast<uint64_t>(k / TCK) * TC_ROW_BYTES;
@@ -559,9 +714,6 @@ cudaError_t launch_tc(const uint8_t *w, const float *x, float *y, int m, int64_t
     p.off_part = static_cast<uint32_t>(sh.off_part);
     p.off_bars = static_cast<uint32_t>(sh.off_bars);
     p.ctx = ctx;
-    static int smem_limits[kMaxDevices] = {0};
-    cudaError_t e = ensure_smem(gemv_tc_kernel<MP>, sh.smem, true, smem_limits);
-    if (e != cudaSuccess) return e;
     return launch_kernel(gemv_tc_kernel<MP>, dim3(static_cast<unsigned>(sh.clusters * sh.ks)),
                          dim3(TC_THREADS), sh.smem, stream, static_cast<unsigned>(sh.ks), tw, x,
                          static_cast<int>(k), p);
@@ -574,7 +726,8 @@ bool gemv_tc_shape_ok(int m, int64_t n, int64_t k) {
         k > (int64_t(1) << 24))
         return false;
     // whether some cluster split fits does not depend on the SM count
-    return (m <= 8 ? tc_shape<8>(n, k, 152).ks : tc_shape<16>(n, k, 152).ks) > 0;
+    auto any = [](int) { return 1; };
+    return (m <= 8 ? tc_shape<8>(n, k, 152, any).ks : tc_shape<16>(n, k, 152, any).ks) > 0;
 }
 
 cudaError_t launch_gemv_tc_q4_0(const uint8_t *w, const float *x, float *y, int m, int64_t n,
