@@ -76,6 +76,7 @@ def parse_args(argv=None):
     ap.add_argument("--profile", default=None, metavar="CASE",
                     help="no timing: run CASE a few times for a profiler and exit. CASE is "
                          "decode_grouped (the timed decode step), decode (seven separate calls), "
+                         "gate_up:M (the step's gate+up launch), "
                          "gemv:FMT:M:N:K, gemv_tc:M:N:K, geglu:M:N:K, gemm_geglu:M:N:K, dequant:FMT:N:K "
                          "gemm:M:N:K, gemm_ws:M:N:K (two-phase) or gemm_q8_0:M:N:K")
     ap.add_argument("--profile-launches", type=int, default=3)
@@ -103,6 +104,16 @@ def run_profile(args):
             for g, x in zip(groups, X):
                 qmm.qmm_gemv_q4_0_multi([(W[i], Y[i], cases[i].n) for i in g], x, 1,
                                         cases[g[0]].k)
+    elif parts[0] == "gate_up":
+        # the decode step's gate+up launch: two 8192 x 2048 Q4_0 matrices sharing x
+        m = int(parts[1]) if len(parts) > 1 else 1
+        projs = [p for p in synth.DECODE_LAYER if p.name in ("gate", "up")]
+        W = [torch.from_numpy(synth.q4_0_weights(p.n, p.k, seed=0, stream=14 + i)).to(dev)
+             for i, p in enumerate(projs)]
+        Y = [torch.empty((m, p.n), dtype=torch.float32, device=dev) for p in projs]
+        x = torch.from_numpy(synth.activations_f32(m, projs[0].k, seed=0, stream=16)).to(dev)
+        for _ in range(reps):
+            qmm.qmm_gemv_q4_0_multi([(w, y, p.n) for w, y, p in zip(W, Y, projs)], x, m, projs[0].k)
     elif parts[0] == "geglu":
         m, n, k = int(parts[1]), int(parts[2]), int(parts[3])
         wg = torch.from_numpy(synth.q4_0_weights(n, k, seed=0, stream=14)).to(dev)
