@@ -15,8 +15,12 @@
 //    every row chunk 16-byte aligned.  A tile's K range is split over kw
 //    warps of a CTA (partial sums added through shared memory) and, for
 //    small N, over a thread-block cluster of ksplit CTAs (partials pushed
-//    into rank 0's shared memory with remote stores, one cluster barrier,
-//    added in rank order).  No global scratch; the summation order is fixed.
+//    into rank 0's activation slice with remote stores once every rank is
+//    done reading activations, then added in rank order by all of rank 0's
+//    threads).  No global scratch; the summation order is fixed.
+//  * Q4_0 at M >= 10 (the FMA pipe, not the loads, bounds it): the row-pair
+//    form, four rows per lane, two lanes per row, two rows per packed FMA and
+//    the block scale folded into the weights (q4_0_chunk_rp).
 //  * A warp streams its chunks through its own ring of shared-memory stages.
 //  * One 2-D TMA load moves a warp's 32 rows x one chunk (4.6 KB Q4_0,
 //    8.7 KB Q8_0) and an mbarrier with a byte count tracks the stage (many
@@ -71,6 +75,15 @@
 #ifndef QMM_GEMV_R_SMALL
 #define QMM_GEMV_R_SMALL 1        // rows per lane for the small (two lanes per row) case
 #endif
+#ifndef QMM_GEMV_RP_MIN_M
+#define QMM_GEMV_RP_MIN_M 10      // Q4_0: smallest M that takes the row-pair form
+#endif
+#ifndef QMM_GEMV_RP_L
+#define QMM_GEMV_RP_L 2           // row-pair form: lanes per row (each half of the qs words)
+#endif
+#ifndef QMM_GEMV_RP_R
+#define QMM_GEMV_RP_R 4           // row-pair form: rows per lane (two pairs)
+#endif
 #ifndef QMM_GEMV_PROXY_FENCE
 #define QMM_GEMV_PROXY_FENCE 0    // 1: fence.proxy.async before refilling a stage (not needed)
 #endif
@@ -94,6 +107,7 @@ static_assert((QMM_GEMV_MAX_KW & (QMM_GEMV_MAX_KW - 1)) == 0 &&
               "K parts per CTA and per cluster are powers of two (the kernel shifts by them)");
 
 constexpr int kChunkK = 256;
+constexpr int kRpMaxProducts = 1024;  // row-pair form: products summed in one fp32 accumulator
 constexpr uint32_t kMagic = 0x4B000000u;  // 2^23
 
 // TMA view of the weight bytes: Q4_0 as uint8 (box 144 x 32), Q8_0 as
@@ -461,6 +475,94 @@ __device__ __forceinline__ void q8_0_chunk_wide(const uint8_t *src, int rstride,
     }
 }
 
+// Row-pair form for wide M (Q4_0; the FMA pipe, not the loads, bounds it).
+// A packed FMA carries two weight rows of one activation value,
+//   acc[p][m] += (w[2p][k], w[2p+1][k]) * (x[m][k], x[m][k]),
+// so each activation read from shared memory feeds R rows and the
+// accumulators take R*M registers (the k-pair form above needs 2*R*M for the
+// same reuse).  The block scale is folded into the weights: (nibble-8)*d is
+// exact in fp32 (a 4-bit integer times an 11-bit significand), so acc is a
+// plain fp32 sum of the products w*x over the lane's share of K.
+//
+// Lane h of the L lanes of a row decodes qs words i = h, h+L, ... of every
+// block of the chunk.  The L lanes then read activations 4i..4i+3 and
+// 16+4i..19+4i: distinct banks, so one shared-memory pass serves all of them.
+// `row` is the row's chunk in shared memory (rows rstride bytes apart).
+template <int M, int L, int R>
+__device__ __forceinline__ void q4_0_chunk_rp(const uint8_t *row, int rstride, const float *xk,
+                                              int XS, int h, uint32_t magic,
+                                              float2 (&acc)[R / 2][M]) {
+    static_assert(R % 2 == 0 && 4 % L == 0, "rows come in pairs; L divides the 4 qs words");
+    constexpr int NW = 4 / L;
+    // m * 2^-s - (2^(23-s) + 8) turns 2^23's float with nibble v at bit s
+    // into v - 8, exactly
+    const float2 S0 = f2(1.0f, 1.0f), B0 = f2(-8388616.0f, -8388616.0f);
+    const float2 S4 = f2(0.0625f, 0.0625f), B4 = f2(-524296.0f, -524296.0f);
+    const float2 S8 = f2(0.00390625f, 0.00390625f), B8 = f2(-32776.0f, -32776.0f);
+    const float2 S12 = f2(0.000244140625f, 0.000244140625f), B12 = f2(-2056.0f, -2056.0f);
+    const float2 S16 = f2(1.52587890625e-05f, 1.52587890625e-05f), B16 = f2(-136.0f, -136.0f);
+#pragma unroll 1
+    for (int bp = 0; bp < 4; ++bp) {  // block pairs: 36 bytes, 4-byte aligned
+        const uint8_t *pb = row + 36 * bp;
+        float2 dd[2][R / 2];  // (d of row 2p, d of row 2p+1) for the pair's two blocks
+#pragma unroll
+        for (int p = 0; p < R / 2; ++p) {
+            const uint8_t *r0 = pb + 2 * p * rstride, *r1 = r0 + rstride;
+            const uint32_t a0 = *reinterpret_cast<const uint32_t *>(r0);
+            const uint32_t a1 = *reinterpret_cast<const uint32_t *>(r1);
+            const uint32_t c0 = *reinterpret_cast<const uint32_t *>(r0 + 16);
+            const uint32_t c1 = *reinterpret_cast<const uint32_t *>(r1 + 16);
+            dd[0][p] = f2(half_bits_to_float(a0 & 0xFFFFu), half_bits_to_float(a1 & 0xFFFFu));
+            dd[1][p] = f2(half_bits_to_float(c0 >> 16), half_bits_to_float(c1 >> 16));
+        }
+#pragma unroll 1
+        for (int wi = 0; wi < NW; ++wi) {
+            const int i = h + L * wi;  // qs word of each block
+            const uint8_t *pw = pb + 4 * i;
+#pragma unroll
+            for (int hb = 0; hb < 2; ++hb) {
+                const int b = 2 * bp + hb;
+                float2 w[R / 2][8];  // weights 4i..4i+3 and 16+4i..19+4i of both rows
+#pragma unroll
+                for (int p = 0; p < R / 2; ++p) {
+                    const uint8_t *q0 = pw + 2 * p * rstride, *q1 = q0 + rstride;
+                    uint32_t v0, v1;
+                    if (hb == 0) {  // even block: qs starts 2 bytes into a word
+                        v0 = __byte_perm(*reinterpret_cast<const uint32_t *>(q0),
+                                         *reinterpret_cast<const uint32_t *>(q0 + 4), 0x5432);
+                        v1 = __byte_perm(*reinterpret_cast<const uint32_t *>(q1),
+                                         *reinterpret_cast<const uint32_t *>(q1 + 4), 0x5432);
+                    } else {
+                        v0 = *reinterpret_cast<const uint32_t *>(q0 + 20);
+                        v1 = *reinterpret_cast<const uint32_t *>(q1 + 20);
+                    }
+                    const uint32_t u0 = v0 >> 16, u1 = v1 >> 16;
+                    const float2 d = dd[hb][p];
+                    w[p][0] = __fmul2_rn(__ffma2_rn(f2(mag(v0, 0x0000000Fu, magic), mag(v1, 0x0000000Fu, magic)), S0, B0), d);
+                    w[p][1] = __fmul2_rn(__ffma2_rn(f2(mag(v0, 0x00000F00u, magic), mag(v1, 0x00000F00u, magic)), S8, B8), d);
+                    w[p][2] = __fmul2_rn(__ffma2_rn(f2(mag(v0, 0x000F0000u, magic), mag(v1, 0x000F0000u, magic)), S16, B16), d);
+                    w[p][3] = __fmul2_rn(__ffma2_rn(f2(mag(u0, 0x00000F00u, magic), mag(u1, 0x00000F00u, magic)), S8, B8), d);
+                    w[p][4] = __fmul2_rn(__ffma2_rn(f2(mag(v0, 0x000000F0u, magic), mag(v1, 0x000000F0u, magic)), S4, B4), d);
+                    w[p][5] = __fmul2_rn(__ffma2_rn(f2(mag(v0, 0x0000F000u, magic), mag(v1, 0x0000F000u, magic)), S12, B12), d);
+                    w[p][6] = __fmul2_rn(__ffma2_rn(f2(mag(u0, 0x000000F0u, magic), mag(u1, 0x000000F0u, magic)), S4, B4), d);
+                    w[p][7] = __fmul2_rn(__ffma2_rn(f2(mag(u0, 0x0000F000u, magic), mag(u1, 0x0000F000u, magic)), S12, B12), d);
+                }
+#pragma unroll
+                for (int m = 0; m < M; ++m) {
+                    const float4 xa = lds128f(xk + m * XS + 32 * b + 4 * i);
+                    const float4 xb = lds128f(xk + m * XS + 32 * b + 16 + 4 * i);
+                    const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+#pragma unroll
+                    for (int p = 0; p < R / 2; ++p)
+#pragma unroll
+                        for (int t = 0; t < 8; ++t)
+                            acc[p][m] = __ffma2_rn(w[p][t], f2(xv[t], xv[t]), acc[p][m]);
+                }
+            }
+        }
+    }
+}
+
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -474,6 +576,13 @@ __device__ __forceinline__ uint32_t cluster_nctarank() {
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
                  ::: "memory");
+}
+// The two halves of cluster_sync, for work in between.
+__device__ __forceinline__ void gemv_cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void gemv_cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void st_dsmem_f32(const float *local, uint32_t rank, float v) {
@@ -525,10 +634,11 @@ __device__ __forceinline__ float gelu_tanh(float z) {
 #ifndef QMM_GEMV_MAX_THREADS
 #define QMM_GEMV_MAX_THREADS 256
 #endif
-template <Fmt F, int M, int L, int R, bool G = false>
+template <Fmt F, int M, int L, int R, bool G = false, bool RP = false>
 __global__ void __launch_bounds__(QMM_GEMV_MAX_THREADS)
     gemv_stream_kernel(const __grid_constant__ StreamMaps maps, StreamParams p) {
     static_assert(!G || R == 2, "GeGLU pairs the gate and up rows of one output in a lane");
+    static_assert(!RP || (F == Fmt::Q4_0 && !G && R % 2 == 0), "row-pair form: Q4_0 row pairs");
     constexpr int CB = StreamFmt<F>::kChunkBytes;
     constexpr int kLaneRows = 32 / L;                 // rows covered by one pass of the lanes
     constexpr int kRowsPerWarp = kLaneRows * R;       // L lanes share a row; a lane owns R rows
@@ -571,13 +681,21 @@ __global__ void __launch_bounds__(QMM_GEMV_MAX_THREADS)
     const int w_c0 = kpart * cpw;                            // first chunk of the warp, CTA-relative
     const int XS = cta_chunks * kChunkK;  // activation floats per row in shared memory
 
-    // shared memory: ring [nw][S][32 rows][CB] | xs [M][XS] | red [nw][M][32] |
-    //                part [ksplit][rw][M][32] (rank 0 only) | bars [nw][S] | xbar
-    uint8_t *my_ring = smem + static_cast<size_t>(warp) * S * kRowsPerWarp * CB;
-    float *xs = reinterpret_cast<float *>(smem + static_cast<size_t>(nw) * S * kRowsPerWarp * CB);
-    float *red = xs + M * XS;
-    float *part = red + nw * M * kRowsPerWarp;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(part + ksplit * p.rw * M * kRowsPerWarp);
+    // shared memory: ring [nw][S][rows][CB] | xs [M][XS] | (part) | bars [nw][S] | xbar
+    // A warp's K-part sums for the in-CTA reduction ([M][rows] floats) go to
+    // the start of its own ring once its last stage has been read.  The
+    // cluster's K-part sums, part [ksplit][rw][M][rows] (rank 0 only), reuse
+    // the activation slice when they fit in it (all ranks are done reading
+    // activations by then), else follow it.
+    static_assert(4 * M <= CB, "a warp's partial sums fit one ring stage");
+    const size_t ring_bytes = static_cast<size_t>(S) * kRowsPerWarp * CB;  // per warp
+    uint8_t *my_ring = smem + warp * ring_bytes;
+    auto red_of = [&](int w_) { return reinterpret_cast<float *>(smem + w_ * ring_bytes); };
+    float *xs = reinterpret_cast<float *>(smem + nw * ring_bytes);
+    const int part_floats = static_cast<int>(ksplit) * p.rw * M * kRowsPerWarp;
+    const bool part_in_xs = part_floats <= M * XS;
+    float *part = part_in_xs ? xs : xs + M * XS;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(xs + M * XS + (part_in_xs ? 0 : part_floats));
     uint64_t *my_bars = bars + warp * S;
     uint64_t *xbar = bars + nw * S;
 
@@ -627,6 +745,11 @@ __global__ void __launch_bounds__(QMM_GEMV_MAX_THREADS)
     for (int j = 0; j < R; ++j)
 #pragma unroll
         for (int m = 0; m < M; ++m) tot[j][m] = 0.0f;
+    float2 acc[RP ? R / 2 : 1][RP ? M : 1];  // row-pair sums (RP)
+#pragma unroll
+    for (int j = 0; j < (RP ? R / 2 : 1); ++j)
+#pragma unroll
+        for (int m = 0; m < (RP ? M : 1); ++m) acc[j][m] = f2(0.0f, 0.0f);
 
     int consumed = 0;
     // every warp waits for the activations (so none exits with the copy in flight)
@@ -643,7 +766,10 @@ __global__ void __launch_bounds__(QMM_GEMV_MAX_THREADS)
             ++consumed;
             const uint8_t *src = my_ring + (st * kRowsPerWarp + r) * CB + h * (CB / L);
             const float *xk = xs + (w_c0 + i) * kChunkK + h * (kChunkK / L);
-            if constexpr (M > QMM_GEMV_R2_MAX_M && L == 1) {
+            if constexpr (RP) {  // the lane picks its qs words itself: row and chunk starts
+                q4_0_chunk_rp<M, L, R>(my_ring + (st * kRowsPerWarp + r) * CB, kLaneRows * CB,
+                                       xs + (w_c0 + i) * kChunkK, XS, h, p.magic, acc);
+            } else if constexpr (M > QMM_GEMV_R2_MAX_M && L == 1) {
                 if constexpr (F == Fmt::Q4_0)
                     q4_0_chunk_wide<M, R>(src, kLaneRows * CB, xk, XS, p.magic, tot);
                 else
@@ -679,6 +805,17 @@ __global__ void __launch_bounds__(QMM_GEMV_MAX_THREADS)
             mbar_wait(&my_bars[j % S], static_cast<uint32_t>(j / S) & 1u, p.ctx);
     }
 
+    // this CTA reads no more activations: its slice may take the cluster's sums
+    if (ksplit > 1) gemv_cluster_arrive();
+    if constexpr (RP) {  // pair p holds rows 2p and 2p+1 of the lane
+#pragma unroll
+        for (int j = 0; j < R / 2; ++j)
+#pragma unroll
+            for (int m = 0; m < M; ++m) {
+                tot[2 * j][m] = acc[j][m].x;
+                tot[2 * j + 1][m] = acc[j][m].y;
+            }
+    }
     // 0) the L lanes of a row add their shares (every lane ends with the sum)
 #pragma unroll
     for (int off = 1; off < L; off <<= 1) {
@@ -695,16 +832,19 @@ __global__ void __launch_bounds__(QMM_GEMV_MAX_THREADS)
             for (int j = 0; j < R; ++j)
 #pragma unroll
                 for (int m = 0; m < M; ++m)
-                    red[(warp * M + m) * kRowsPerWarp + j * kLaneRows + r] = tot[j][m];
+                    red_of(warp)[m * kRowsPerWarp + j * kLaneRows + r] = tot[j][m];
         }
         __syncthreads();
         if (kpart == 0) {
-            for (int q = 1; q < kw; ++q) {
 #pragma unroll
-                for (int j = 0; j < R; ++j)
+            for (int q = 1; q < QMM_GEMV_MAX_KW; ++q) {
+                if (q < kw) {
 #pragma unroll
-                    for (int m = 0; m < M; ++m)
-                        tot[j][m] += red[((warp + q) * M + m) * kRowsPerWarp + j * kLaneRows + r];
+                    for (int j = 0; j < R; ++j)
+#pragma unroll
+                        for (int m = 0; m < M; ++m)
+                            tot[j][m] += red_of(warp + q)[m * kRowsPerWarp + j * kLaneRows + r];
+                }
             }
         }
     }
@@ -732,6 +872,7 @@ __global__ void __launch_bounds__(QMM_GEMV_MAX_THREADS)
         }
         return;
     }
+    gemv_cluster_wait();  // every CTA of the cluster is done with its activations
     if (kpart == 0 && writer) {
         float *slot = part + ((rank * p.rw + tile_in_cta) * M) * kRowsPerWarp;
 #pragma unroll
@@ -741,33 +882,33 @@ __global__ void __launch_bounds__(QMM_GEMV_MAX_THREADS)
                 st_dsmem_f32(slot + m * kRowsPerWarp + j * kLaneRows + r, 0, tot[j][m]);
     }
     cluster_sync();
-    if (rank == 0 && kpart == 0 && writer && G) {
-        const int row = row0 + r;
-        if (row < n_rows) {
-#pragma unroll
-            for (int m = 0; m < M; ++m) {
-                float s[R];
-#pragma unroll
-                for (int j = 0; j < R; ++j) {
-                    s[j] = 0.0f;
-                    for (uint32_t q = 0; q < ksplit; ++q)
-                        s[j] += part[((q * p.rw + tile_in_cta) * M + m) * kRowsPerWarp + j * kLaneRows + r];
-                }
-                y[static_cast<size_t>(m) * n_rows + row] = gelu_tanh(s[0]) * s[1];
-            }
-        }
-    } else if (rank == 0 && kpart == 0 && writer) {
-#pragma unroll
-        for (int j = 0; j < R; ++j) {
-            const int row = row0 + j * kLaneRows + r;
+    if (rank == 0) {
+        // every thread of rank 0 adds the ranks' sums of some outputs, in rank
+        // order (the same order for every output); consecutive threads take
+        // consecutive rows.  The rank loop is unrolled to the largest cluster
+        // with a guard: a run-time loop measured about 100 ns per partial.
+        const int total = p.rw * M * kTileRows;
+        const int qstride = p.rw * M * kRowsPerWarp;
+        for (int o = threadIdx.x; o < total; o += blockDim.x) {
+            const int rt = o % kTileRows;  // row within the tile
+            const int mt = o / kTileRows;
+            const int m = mt % M;
+            const int tile = mt / M;
+            const int row = (group * p.rw + tile) * kTileRows + rt;
             if (row >= n_rows) continue;
+            const float *pp = part + (tile * M + m) * kRowsPerWarp + rt;
+            float s0 = 0.0f, s1 = 0.0f;
 #pragma unroll
-            for (int m = 0; m < M; ++m) {
-                float s = 0.0f;
-                for (uint32_t q = 0; q < ksplit; ++q)
-                    s += part[((q * p.rw + tile_in_cta) * M + m) * kRowsPerWarp + j * kLaneRows + r];
-                y[static_cast<size_t>(m) * n_rows + row] = s;
+            for (uint32_t q = 0; q < QMM_GEMV_MAX_KSPLIT; ++q) {
+                if (q < ksplit) {
+                    s0 += pp[q * qstride];
+                    if constexpr (G) s1 += pp[q * qstride + kLaneRows];  // the up row
+                }
             }
+            if constexpr (G)
+                y[static_cast<size_t>(m) * n_rows + row] = gelu_tanh(s0) * s1;
+            else
+                y[static_cast<size_t>(m) * n_rows + row] = s0;
         }
     }
 }
@@ -873,8 +1014,10 @@ StreamShape stream_shape(int64_t tiles, int64_t k, int sms) {
         const int cta_chunks = t.kw * t.cpw;
         return static_cast<size_t>(nw) * t.stages * kRowsPerWarp * CB +
                sizeof(float) * (static_cast<size_t>(M) * cta_chunks * kChunkK +
-                                static_cast<size_t>(nw) * M * kRowsPerWarp +
-                                static_cast<size_t>(t.ksplit) * t.rw * M * kRowsPerWarp) +
+                                (static_cast<size_t>(t.ksplit) * t.rw * kRowsPerWarp <=
+                                         static_cast<size_t>(cta_chunks) * kChunkK
+                                     ? 0
+                                     : static_cast<size_t>(t.ksplit) * t.rw * M * kRowsPerWarp)) +
                sizeof(uint64_t) * (nw * t.stages + 1) + 128;
     };
     // fit the shared-memory budget: shallower rings, then fewer tiles per CTA,
@@ -901,7 +1044,7 @@ StreamShape stream_shape(int64_t tiles, int64_t k, int sms) {
 // probs[i].w (probs[i].n rows) and output probs[i].y.  G (GeGLU): count == 2,
 // probs[0] the gate weights and the output h, probs[1] the up weights (same
 // n); one problem of n outputs whose tiles read both.
-template <Fmt F, int M, int L, int R, bool G = false>
+template <Fmt F, int M, int L, int R, bool G = false, bool RP = false>
 cudaError_t launch_stream(const GemvProblem *probs, int count, const float *x, int64_t k,
                           cudaStream_t stream, const LaunchCtx &ctx) {
     constexpr int kRowsPerWarp = 32 / L * R;
@@ -911,6 +1054,9 @@ cudaError_t launch_stream(const GemvProblem *probs, int count, const float *x, i
     for (int i = 0; i < (G ? 1 : count); ++i) tiles += (probs[i].n + kTileRows - 1) / kTileRows;
     const StreamShape sh = stream_shape<F, M, L, R>(tiles, k, device_sm_count());
     if (sh.smem > kGemvSmemCap) return kShapeTooLarge;  // nothing launched
+    // the row-pair form sums at most 1024 products per fp32 accumulator (a
+    // lane's share of each of its chunks is 256 / L weights)
+    if (RP && sh.cpw * (kChunkK / L) > kRpMaxProducts) return kShapeTooLarge;
     StreamMaps maps;
     StreamParams p;
     p.x = x;
@@ -946,7 +1092,7 @@ cudaError_t launch_stream(const GemvProblem *probs, int count, const float *x, i
         }
     }
     p.group_begin[kMaxGemvProblems] = static_cast<int>(groups);
-    auto kern = gemv_stream_kernel<F, M, L, R, G>;
+    auto kern = gemv_stream_kernel<F, M, L, R, G, RP>;
     static int smem_limits[kMaxDevices] = {0};  // this instantiation's own cache
     const cudaError_t e = ensure_smem(kern, sh.smem, true, smem_limits);
     if (e != cudaSuccess) return e;
@@ -982,6 +1128,19 @@ cudaError_t launch_m(const GemvProblem *probs, int count, const float *x, int64_
                     e = launch_stream<F, M, 1, 2, true>(probs, count, x, k, stream, ctx);
             } else {
                 e = launch_stream<F, M, 1, 2, true>(probs, count, x, k, stream, ctx);
+            }
+        } else if constexpr (F == Fmt::Q4_0 && M >= QMM_GEMV_RP_MIN_M) {
+            // wide M: row pairs (the FMA pipe bounds it); a K share too long
+            // for one accumulator takes the per-block form below
+            e = launch_stream<F, M, QMM_GEMV_RP_L, QMM_GEMV_RP_R, false, true>(probs, count, x, k,
+                                                                              stream, ctx);
+            if (e == kShapeTooLarge) {
+                if constexpr (M <= QMM_GEMV_R_WIDE_MAX_M) {
+                    e = launch_stream<F, M, 1, 2>(probs, count, x, k, stream, ctx);
+                    if (e == kShapeTooLarge) e = launch_stream<F, M, 1, 1>(probs, count, x, k, stream, ctx);
+                } else {
+                    e = launch_stream<F, M, 1, 1>(probs, count, x, k, stream, ctx);
+                }
             }
         } else if constexpr (M <= QMM_GEMV_R2_MAX_M) {
             if (units <= QMM_GEMV_L2_UNITS)

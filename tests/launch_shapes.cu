@@ -21,7 +21,7 @@ void fail(const char *what, const char *fmt, int M, int L, int R, long long k, l
     ++violations;
 }
 
-template <Fmt F, int M, int L, int R>
+template <Fmt F, int M, int L, int R, bool RP = false>
 void check(const char *fmt) {
     constexpr int kRowsPerWarp = 32 / L * R;
     for (long long k : {256LL, 512LL, 768LL, 1024LL, 1280LL, 2048LL, 4096LL, 8192LL, 16384LL,
@@ -36,7 +36,9 @@ void check(const char *fmt) {
             if (static_cast<long long>(sh.kw) * sh.ksplit * sh.cpw != chunks) fail("K cover", fmt, M, L, R, k, n);
             if (sh.stages < 1 || sh.stages > sh.cpw) fail("stages", fmt, M, L, R, k, n);
             if (sh.rw < 1 || sh.rw * sh.kw * 32 > QMM_GEMV_MAX_THREADS) fail("threads", fmt, M, L, R, k, n);
-            if (sh.smem > kGemvSmemCap)
+            if (RP && (sh.smem > kGemvSmemCap || sh.cpw * (kChunkK / L) > kRpMaxProducts))  // another form runs
+                std::printf("ROWPAIR_REFUSED %s M=%d L=%d R=%d k=%lld n=%lld\n", fmt, M, L, R, k, n);
+            else if (sh.smem > kGemvSmemCap)
                 std::printf("REFUSED %s M=%d L=%d R=%d k=%lld n=%lld\n", fmt, M, L, R, k, n);
         }
     }
@@ -56,6 +58,8 @@ void check_m(const char *fmt) {
         check<F, M, 1, 1>(fmt);
         check<F, M, 1, 2>(fmt);  // GeGLU
     }
+    if constexpr (F == Fmt::Q4_0 && M >= QMM_GEMV_RP_MIN_M)  // the row-pair form
+        check<F, M, QMM_GEMV_RP_L, QMM_GEMV_RP_R, true>(fmt);
 }
 
 template <Fmt F, int... Ms>

@@ -151,8 +151,9 @@ def test_gemv_degenerate_inputs(qmm):
     assert torch.count_nonzero(y).item() == 0
 
 
-def test_gemv_deterministic(qmm):
-    case = synth.gemv_case("q4_0", 4, 2048, 2048, seed=5)
+@pytest.mark.parametrize("m", [4, 16])
+def test_gemv_deterministic(qmm, m):
+    case = synth.gemv_case("q4_0", m, 2048, 2048, seed=5)
     w, x = to_dev(case.w, torch), to_dev(case.x, torch)
     a = qmm.gemv("q4_0", w, x, case.n, case.k)
     s = torch.cuda.Stream()
@@ -163,12 +164,14 @@ def test_gemv_deterministic(qmm):
     assert torch.equal(a.view(torch.int32), b.view(torch.int32))
 
 
-def test_gemv_one_hot_equals_dequant(qmm):
+@pytest.mark.parametrize("cols", [[0, 17, 255, 256, 1023],
+                                  # 12 rows of x: the row-pair form (M >= 10)
+                                  [0, 1, 2, 3, 4, 15, 16, 19, 31, 511, 512, 1023]])
+def test_gemv_one_hot_equals_dequant(qmm, cols):
     """x = e_c gives the dequantized column exactly (both on the GPU)."""
     n, k = 300, 1024
     case = synth.gemv_case("q4_0", 1, n, k, seed=6)
     w = to_dev(case.w, torch)
-    cols = [0, 17, 255, 256, 1023]
     x = torch.zeros((len(cols), k), device="cuda")
     for i, c in enumerate(cols):
         x[i, c] = 1.0
@@ -339,3 +342,19 @@ def test_gemv_wide_m_two_rows_per_lane_and_its_fallback(qmm, oracle_mod, fmt, m,
     case = synth.gemv_case(fmt, m, n, k, seed=m * 13 + n)
     y_ref, bound = _oracle_gemv(oracle_mod, fmt, case)
     assert_within(_run_gemv(qmm, fmt, case), y_ref, bound, GEMV_REL, f"{fmt} {m}x{n}x{k}")
+
+
+@pytest.mark.parametrize("m,n,k", [(10, 200, 2048), (13, 1000, 4096), (16, 70, 8192), (11, 3000, 256),
+                                   (16, 130, 16384), (10, 16384, 16384), (16, 130, 32768),
+                                   (11, 256, 18432)])
+def test_gemv_row_pairs_and_their_fallback(qmm, oracle_mod, m, n, k):
+    """Q4_0 at M >= 10 packs two weight rows into each FMA with the block scale
+    folded into the weights: ragged 64-row tiles, cluster splits (up to 8 x 8
+    K parts at 130 x 16384), several tiles per launch, and 16384 x 16384, where
+    each accumulator sums the most products the form allows (8 chunks, 1024
+    per lane).  The last two shapes leave the row-pair form: at 130 x 32768 its
+    activation slice does not fit shared memory; at 256 x 18432 (72 chunks, at
+    most 8 K parts) a lane's share would be 1152 products."""
+    case = synth.gemv_case("q4_0", m, n, k, seed=m * 7 + n)
+    y_ref, bound = _oracle_gemv(oracle_mod, "q4_0", case)
+    assert_within(_run_gemv(qmm, "q4_0", case), y_ref, bound, GEMV_REL, f"q4_0 {m}x{n}x{k}")

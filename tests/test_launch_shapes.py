@@ -42,7 +42,7 @@ def test_every_shape_is_well_formed(report):
 
 def test_byte_wise_fallback_only_for_very_large_k(report):
     _, out = report
-    refused = re.findall(r"REFUSED (\w+) M=(\d+) L=(\d) R=(\d) k=(\d+) n=(\d+)", out)
+    refused = re.findall(r"^REFUSED (\w+) M=(\d+) L=(\d) R=(\d) k=(\d+) n=(\d+)", out, re.M)
     assert refused, "the enumeration reaches shapes that cannot fit (K up to 2^20)"
     for fmt, m, l, r, k, n in refused:
         k, m = int(k), int(m)
@@ -51,3 +51,18 @@ def test_byte_wise_fallback_only_for_very_large_k(report):
             assert m >= 8, (fmt, m, l, r, k, n)
             if fmt == "q4_0":
                 assert m >= 13 and r == "2", (fmt, m, l, r, k, n)
+
+
+def test_row_pair_form_refused_only_for_large_k(report):
+    """Q4_0 at M >= 10 leaves the row-pair form (for the per-block forms) only
+    where a lane's K share would pass 1024 products (4 chunks per lane at two
+    lanes a row: 8 chunks) or shared memory does not fit: K >= 16384, or a
+    chunk count with an odd factor of 9 or more (K parts are powers of two).
+    Never at the batched and decode workloads' sizes (K <= 8192)."""
+    _, out = report
+    refused = re.findall(r"ROWPAIR_REFUSED (\w+) M=(\d+) L=(\d) R=(\d) k=(\d+) n=(\d+)", out)
+    for fmt, m, l, r, k, n in refused:
+        chunks = int(k) // 256
+        odd = chunks // (chunks & -chunks)
+        assert fmt == "q4_0" and int(m) >= 10 and (int(k) >= 16384 or odd >= 9), (fmt, m, l, r, k, n)
+    assert "ROWPAIR_REFUSED q4_0 M=16" in out  # K = 2^20 cannot fit
