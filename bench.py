@@ -593,6 +593,8 @@ def run_secondary(torch, qmm, l2, stream, timer, peaks, sms, only=None):
             gemv_entry(f"q4_0_gemv_tc_{p.n}x{p.k}_m{m}", "q4_0", m, (p,), 30 + i, tensor_cores=True)
     for m in synth.LM_HEAD_M:
         gemv_entry(f"q8_0_lm_head_262144x2048_m{m}", "q8_0", m, (synth.LM_HEAD,), 50)
+    # the same 262144 x 2048 matrix in Q4_0 (302 MB), one token
+    gemv_entry("q4_0_gemv_262144x2048_m1", "q4_0", 1, (synth.LM_HEAD,), 52)
     # the feed-forward input: gate and up as one grouped call (two outputs
     # written) against the fused GeGLU call (h = gelu(g) * u written)
     ffn = tuple(p for p in synth.DECODE_LAYER if p.name in ("gate", "up"))
@@ -852,6 +854,7 @@ def kernel_summary(secondary):
     pick = {
         "gemv_q8_0_lm_head_262144x2048_m1": ("q8_0_lm_head_262144x2048_m1", "gbs", "frac_hbm"),
         "gemv_q8_0_lm_head_262144x2048_m8": ("q8_0_lm_head_262144x2048_m8", "gbs", "frac_of_min_ceiling"),
+        "gemv_q4_0_262144x2048_m1": ("q4_0_gemv_262144x2048_m1", "gbs", "frac_hbm"),
         "gemv_q4_0_8192x2048_m16": ("q4_0_gemv_8192x2048_m16", "gbs", "frac_of_min_ceiling"),
         "gemm_q4_0_2048x8192x2048": ("q4_0_gemm_2048x8192x2048", "tflops", "frac_bf16_peak"),
         "gemm_q4_0_2048x2048x8192": ("q4_0_gemm_2048x2048x8192", "tflops", "frac_bf16_peak"),

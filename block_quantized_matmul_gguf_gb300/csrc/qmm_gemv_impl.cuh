@@ -84,6 +84,23 @@
 #ifndef QMM_GEMV_RP_R
 #define QMM_GEMV_RP_R 4           // row-pair form: rows per lane (two pairs)
 #endif
+// Ring stages a warp requests before the dependency wait, per format; the
+// rest follow the activation copy, which would otherwise queue behind them
+// (Q4_0 262144 x 2048: the copy's wait went from 4.9 us per CTA, and the
+// launch from 98.5 to 90.4 us).  Q8_0 keeps its whole ring ahead: its LM
+// head measured 10 % slower with one stage.
+#ifndef QMM_GEMV_PREWAIT_Q4_0
+#define QMM_GEMV_PREWAIT_Q4_0 1
+#endif
+#ifndef QMM_GEMV_PREWAIT_Q8_0
+#define QMM_GEMV_PREWAIT_Q8_0 8
+#endif
+#ifndef QMM_GEMV_PERSIST
+#define QMM_GEMV_PERSIST 1         // large single Q4_0 matrices at M <= 4: the persistent form
+#endif
+#ifndef QMM_GEMV_PERSIST_Q8_0
+#define QMM_GEMV_PERSIST_Q8_0 1    // the same for Q8_0
+#endif
 #ifndef QMM_GEMV_PROXY_FENCE
 #define QMM_GEMV_PROXY_FENCE 0    // 1: fence.proxy.async before refilling a stage (not needed)
 #endif
@@ -727,9 +744,10 @@ __global__ void __launch_bounds__(QMM_GEMV_MAX_THREADS)
     // has finished (programmatic dependent launch): weights are read-only
     // model data that no kernel of this library writes.  Activations are read
     // and outputs written only after the wait below.
+    constexpr int kPrewait = F == Fmt::Q4_0 ? QMM_GEMV_PREWAIT_Q4_0 : QMM_GEMV_PREWAIT_Q8_0;
     int issued = 0;
     if (warp_active)
-        for (; issued < min(S, cpw); ++issued) issue(issued, issued);
+        for (; issued < min(min(S, cpw), kPrewait); ++issued) issue(issued, issued);
     pdl_wait();
     if (threadIdx.x == 0) {  // activations: one bulk copy per row m of the CTA's K range
         mbar_arrive_expect_tx(xbar, static_cast<uint32_t>(M * XS * sizeof(float)));
@@ -739,6 +757,11 @@ __global__ void __launch_bounds__(QMM_GEMV_MAX_THREADS)
                      static_cast<uint32_t>(XS * sizeof(float)), xbar);
     }
     pdl_launch_dependents();
+    if (kPrewait < min(S, cpw)) {  // (the same in every warp) the rest of the ring, after the
+        __syncthreads();           // activation copy
+        if (warp_active)
+            for (; issued < min(S, cpw); ++issued) issue(issued, issued);
+    }
 
     float tot[R][M];
 #pragma unroll
@@ -753,13 +776,14 @@ __global__ void __launch_bounds__(QMM_GEMV_MAX_THREADS)
 
     int consumed = 0;
     // every warp waits for the activations (so none exits with the copy in flight)
-    const bool x_ok = mbar_wait(xbar, 0, p.ctx);
+    const bool x_ok = __all_sync(0xFFFFFFFFu, mbar_wait(xbar, 0, p.ctx));
     bool failed = !x_ok;
     if (warp_active) {
         int st = 0;         // i % S, kept incrementally (S is a run-time value)
         uint32_t par = 0;   // (i / S) & 1
         for (int i = 0; i < cpw && !failed; ++i) {
-            if (!mbar_wait(&my_bars[st], par, p.ctx)) {
+            // a lane's wait can give up while another's succeeds: the warp decides together
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&my_bars[st], par, p.ctx))) {
                 failed = true;
                 break;
             }
@@ -909,6 +933,187 @@ __global__ void __launch_bounds__(QMM_GEMV_MAX_THREADS)
                 y[static_cast<size_t>(m) * n_rows + row] = gelu_tanh(s0) * s1;
             else
                 y[static_cast<size_t>(m) * n_rows + row] = s0;
+        }
+    }
+}
+
+// ---- Persistent form: large N at M <= 4 (one launch that spans many waves) ----
+// One CTA per SM.  CTA c owns whole tiles [c*T/G, (c+1)*T/G) of the T row
+// tiles (G CTAs), so every SM gets the same work to within one tile; its nw
+// warps split the CTA's (tile, chunk) units evenly, in order.  A warp streams
+// its units through its ring without a break at tile boundaries and keeps one
+// set of sums per tile: a tile it covers whole it writes out, a tile it shares
+// with the previous or the next warp goes to a shared-memory slot, and after
+// one CTA barrier the two halves are added, earlier chunks first.  The
+// activations are copied once per CTA.  Each warp covers at least one tile's
+// worth of units (the launcher requires T/G >= nw), so a tile is shared by at
+// most two warps.
+struct PersistParams {
+    const float *x;
+    float *y;
+    int n;          // rows
+    int tiles;      // row tiles (32 * R rows each)
+    int chunks;     // K / 256
+    int stages;     // ring depth per warp
+    uint32_t magic;  // 0x4B000000 (2^23), kept in a register by the kernel
+    LaunchCtx ctx;
+};
+
+template <Fmt F, int M, int R>
+__global__ void __launch_bounds__(QMM_GEMV_MAX_THREADS)
+    gemv_persist_kernel(const __grid_constant__ CUtensorMap wmap, PersistParams p) {
+    static_assert(M <= QMM_GEMV_R2_MAX_M, "the per-block chunk forms of small M");
+    constexpr int CB = StreamFmt<F>::kChunkBytes;
+    constexpr int EB = StreamFmt<F>::kElemBytes;
+    constexpr int kRows = 32 * R;  // lane r owns rows r, r + 32, ... of a tile
+    extern __shared__ __align__(128) uint8_t smem_dyn[];
+    uint8_t *smem = smem_dyn + ((128u - (smem_addr(smem_dyn) & 127u)) & 127u);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const int S = p.stages, C = p.chunks, XS = C * kChunkK;
+    const int G = gridDim.x;
+    const int t0 = static_cast<int>(static_cast<int64_t>(blockIdx.x) * p.tiles / G);
+    const int t1 = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * p.tiles / G);
+    const int uc = (t1 - t0) * C;  // the CTA's units, tile-major
+    const int u0 = static_cast<int>(static_cast<int64_t>(warp) * uc / nw);
+    const int nu = static_cast<int>(static_cast<int64_t>(warp + 1) * uc / nw) - u0;
+
+    // shared memory: ring [nw][S][kRows][CB] | xs [M][XS] | slots [nw][2][M][kRows] |
+    //                bars [nw][S] | xbar
+    const size_t ring_bytes = static_cast<size_t>(S) * kRows * CB;  // per warp
+    uint8_t *my_ring = smem + warp * ring_bytes;
+    float *xs = reinterpret_cast<float *>(smem + nw * ring_bytes);
+    float *slots = xs + M * XS;  // [warp][0]: a tile's later chunks, [warp][1]: its earlier ones
+    uint64_t *bars = reinterpret_cast<uint64_t *>(slots + nw * 2 * M * kRows);
+    uint64_t *my_bars = bars + warp * S;
+    uint64_t *xbar = bars + nw * S;
+
+    if (lane == 0) {
+        if (warp == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&wmap)) : "memory");
+            mbar_init(xbar, 1);
+        }
+        for (int s = 0; s < S; ++s) mbar_init(&my_bars[s], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();  // barriers initialised before any thread waits on them
+
+    int it = t0 + u0 / C, ic = u0 % C;  // next unit to request (every lane keeps the count)
+    auto issue = [&](int st) {
+        if (lane == 0) {
+            mbar_arrive_expect_tx(&my_bars[st], kRows * CB);
+            tma_load_2d(my_ring + st * kRows * CB, &wmap, ic * (CB / EB), it * kRows, &my_bars[st]);
+        }
+        if (++ic == C) {
+            ic = 0;
+            ++it;
+        }
+    };
+    // weights before the dependency wait (read-only model data), activations after
+    constexpr int kPrewait = F == Fmt::Q4_0 ? QMM_GEMV_PREWAIT_Q4_0 : QMM_GEMV_PREWAIT_Q8_0;
+    int issued = 0;
+    for (; issued < min(min(S, nu), kPrewait); ++issued) issue(issued);
+    pdl_wait();
+    if (threadIdx.x == 0) {  // activations: one bulk copy per row m
+        mbar_arrive_expect_tx(xbar, static_cast<uint32_t>(M * XS * sizeof(float)));
+#pragma unroll
+        for (int m = 0; m < M; ++m)
+            bulk_g2s(xs + m * XS, p.x + static_cast<size_t>(m) * XS,
+                     static_cast<uint32_t>(XS * sizeof(float)), xbar);
+    }
+    pdl_launch_dependents();
+    if (kPrewait < S) {  // (the same in every warp) the rest of the ring, after the activations
+        __syncthreads();
+        for (; issued < min(S, nu); ++issued) issue(issued);
+    }
+
+    float tot[R][M];
+#pragma unroll
+    for (int j = 0; j < R; ++j)
+#pragma unroll
+        for (int m = 0; m < M; ++m) tot[j][m] = 0.0f;
+    // every warp waits for the activations (so none exits with the copy in flight)
+    const bool x_ok = __all_sync(0xFFFFFFFFu, mbar_wait(xbar, 0, p.ctx));
+    bool failed = !x_ok;
+    int consumed = 0;
+    int tc = t0 + u0 / C, cc = u0 % C;  // the unit being added
+    bool head = cc != 0;                // the first tile began in the previous warp's units
+    int st = 0;
+    uint32_t par = 0;
+    for (int i = 0; i < nu && !failed; ++i) {
+        // a lane's wait can give up while another's succeeds: the warp decides together
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&my_bars[st], par, p.ctx))) {
+            failed = true;
+            break;
+        }
+        ++consumed;
+        const uint8_t *src = my_ring + (st * kRows + lane) * CB;
+        const float *xk = xs + cc * kChunkK;
+        if constexpr (F == Fmt::Q4_0)
+            q4_0_chunk<M, 1, R>(src, 32 * CB, xk, XS, p.magic, tot);
+        else
+            q8_0_chunk<M, 1, R>(src, 32 * CB, xk, XS, p.magic, tot);
+        __syncwarp();  // every lane is done reading the stage before it is refilled
+        if (issued < nu) {
+            issue(st);
+            ++issued;
+        }
+        if (++st == S) {
+            st = 0;
+            par ^= 1u;
+        }
+        if (cc == C - 1 || i == nu - 1) {  // this warp's share of tile tc ends here
+            float *slot = head ? slots + (warp * 2 + 0) * M * kRows
+                               : (cc != C - 1 ? slots + (warp * 2 + 1) * M * kRows : nullptr);
+            if (slot) {
+#pragma unroll
+                for (int j = 0; j < R; ++j)
+#pragma unroll
+                    for (int m = 0; m < M; ++m) slot[m * kRows + j * 32 + lane] = tot[j][m];
+            } else {
+#pragma unroll
+                for (int j = 0; j < R; ++j) {
+                    const int row = tc * kRows + j * 32 + lane;
+                    if (row < p.n) {
+#pragma unroll
+                        for (int m = 0; m < M; ++m)
+                            p.y[static_cast<size_t>(m) * p.n + row] = tot[j][m];
+                    }
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < R; ++j)
+#pragma unroll
+                for (int m = 0; m < M; ++m) tot[j][m] = 0.0f;
+            head = false;
+        }
+        if (++cc == C) {
+            cc = 0;
+            ++tc;
+        }
+    }
+    if (failed) {
+        // Let copies still in flight land before the CTA's shared memory is
+        // released; each wait is again bounded.
+        if (!x_ok) mbar_wait(xbar, 0, p.ctx);
+        for (int j = consumed; j < issued; ++j)
+            mbar_wait(&my_bars[j % S], static_cast<uint32_t>(j / S) & 1u, p.ctx);
+    }
+    __syncthreads();
+    // a tile shared with the previous warp: its earlier chunks (that warp's
+    // last slot) plus the later ones (this warp's first slot)
+    if (warp > 0 && u0 % C != 0) {
+        const int t = t0 + u0 / C;
+        const float *early = slots + ((warp - 1) * 2 + 1) * M * kRows;
+        const float *late = slots + (warp * 2 + 0) * M * kRows;
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+            const int row = t * kRows + j * 32 + lane;
+            if (row < p.n) {
+#pragma unroll
+                for (int m = 0; m < M; ++m)
+                    p.y[static_cast<size_t>(m) * p.n + row] =
+                        early[m * kRows + j * 32 + lane] + late[m * kRows + j * 32 + lane];
+            }
         }
     }
 }
@@ -1101,6 +1306,54 @@ cudaError_t launch_stream(const GemvProblem *probs, int count, const float *x, i
                          static_cast<unsigned>(sh.ksplit), maps, p);
 }
 
+
+// The persistent form (one problem): one CTA per SM, warps and ring depth
+// chosen for the shared-memory budget.  kShapeTooLarge when the matrix has
+// too few tiles for every warp to hold one, or nothing fits.
+template <Fmt F, int M, int R>
+cudaError_t launch_persist(const GemvProblem &pr, const float *x, int64_t k, cudaStream_t stream,
+                           const LaunchCtx &ctx) {
+    constexpr int CB = StreamFmt<F>::kChunkBytes;
+    constexpr int EB = StreamFmt<F>::kElemBytes;
+    constexpr int kRows = 32 * R;
+    const int sms = device_sm_count();
+    const int64_t tiles = (pr.n + kRows - 1) / kRows;
+    const int64_t C = k / kChunkK;
+    auto smem_of = [&](int nw, int S) {
+        return static_cast<size_t>(nw) * S * kRows * CB +
+               sizeof(float) * (static_cast<size_t>(M) * C * kChunkK + static_cast<size_t>(nw) * 2 * M * kRows) +
+               sizeof(uint64_t) * (nw * S + 1) + 128;
+    };
+    // 8 warps with at least two stages each, else 4 warps with the deepest ring that fits
+    int nw = 0, S = 0;
+    for (int w : {8, 4}) {
+        for (int s = QMM_GEMV_STAGES; s >= 2 && nw == 0; --s)
+            if (smem_of(w, s) <= kGemvSmemCap) nw = w, S = s;
+        if (nw != 0) break;
+    }
+    if (nw == 0) return kShapeTooLarge;
+    const size_t smem = smem_of(nw, S);
+    if (smem > kGemvSmemCap || tiles < static_cast<int64_t>(nw) * sms) return kShapeTooLarge;
+    CUtensorMap map;
+    const uint64_t rowbytes = static_cast<uint64_t>(C) * CB;
+    if (!encode_tmap_2d(&map, StreamFmt<F>::kType, pr.w, rowbytes / EB, pr.n, rowbytes, CB / EB, kRows))
+        return cudaErrorInvalidValue;
+    PersistParams p;
+    p.x = x;
+    p.y = pr.y;
+    p.n = static_cast<int>(pr.n);
+    p.tiles = static_cast<int>(tiles);
+    p.chunks = static_cast<int>(C);
+    p.stages = S;
+    p.magic = kMagic;
+    p.ctx = ctx;
+    auto kern = gemv_persist_kernel<F, M, R>;
+    static int smem_limits[kMaxDevices] = {0};
+    const cudaError_t e = ensure_smem(kern, smem, false, smem_limits);
+    if (e != cudaSuccess) return e;
+    return launch_kernel(kern, dim3(static_cast<unsigned>(sms)), dim3(nw * 32), smem, stream, 1, map, p);
+}
+
 template <Fmt F, int M, bool G = false>
 cudaError_t launch_m(const GemvProblem *probs, int count, const float *x, int64_t k,
                      cudaStream_t stream, const LaunchCtx &ctx) {
@@ -1143,10 +1396,15 @@ cudaError_t launch_m(const GemvProblem *probs, int count, const float *x, int64_
                 }
             }
         } else if constexpr (M <= QMM_GEMV_R2_MAX_M) {
-            if (units <= QMM_GEMV_L2_UNITS)
+            if (units <= QMM_GEMV_L2_UNITS) {
                 e = launch_stream<F, M, 2, QMM_GEMV_R_SMALL>(probs, count, x, k, stream, ctx);
-            else
-                e = launch_stream<F, M, 1, 2>(probs, count, x, k, stream, ctx);
+            } else {
+                // one large matrix: the persistent form when every warp gets a tile
+                constexpr bool kPersist = F == Fmt::Q4_0 ? QMM_GEMV_PERSIST : QMM_GEMV_PERSIST_Q8_0;
+                e = count == 1 && kPersist ? launch_persist<F, M, 2>(probs[0], x, k, stream, ctx)
+                                           : kShapeTooLarge;
+                if (e == kShapeTooLarge) e = launch_stream<F, M, 1, 2>(probs, count, x, k, stream, ctx);
+            }
         } else {
             // the activation loads bound wide M; two rows per lane halve them per
             // FMA until the accumulators crowd the registers (M > 10); where
