@@ -96,7 +96,7 @@
 #define QMM_GEMV_PREWAIT_Q8_0 8
 #endif
 #ifndef QMM_GEMV_PERSIST
-#define QMM_GEMV_PERSIST 1         // large single Q4_0 matrices at M <= 4: the persistent form
+#define QMM_GEMV_PERSIST 1         // large single Q4_0 matrices at M <= 10: the persistent form
 #endif
 #ifndef QMM_GEMV_PERSIST_Q8_0
 #define QMM_GEMV_PERSIST_Q8_0 1    // the same for Q8_0
@@ -651,8 +651,24 @@ __device__ __forceinline__ float gelu_tanh(float z) {
 #ifndef QMM_GEMV_MAX_THREADS
 #define QMM_GEMV_MAX_THREADS 256
 #endif
+// Register budget hint (CTAs of QMM_GEMV_MAX_THREADS per SM that it must
+// allow).  Without one, ptxas kept the M <= 4 kernels near 80 registers;
+// allowing two CTAs' worth (up to 128) took the decode step from 19.0 to
+// 18.05 us.  The row-pair form needs more than 128 and gets one CTA's worth;
+// the per-block forms of M 5..9 are left to ptxas.
+#ifndef QMM_GEMV_MB_L1
+#define QMM_GEMV_MB_L1 2
+#endif
+#ifndef QMM_GEMV_MB_L2
+#define QMM_GEMV_MB_L2 2
+#endif
+template <int M, int L, bool RP>
+struct StreamMinBlocks {
+    static constexpr int value =
+        RP ? 1 : (M <= QMM_GEMV_R2_MAX_M ? (L == 1 ? QMM_GEMV_MB_L1 : QMM_GEMV_MB_L2) : 0);
+};
 template <Fmt F, int M, int L, int R, bool G = false, bool RP = false>
-__global__ void __launch_bounds__(QMM_GEMV_MAX_THREADS)
+__global__ void __launch_bounds__(QMM_GEMV_MAX_THREADS, (StreamMinBlocks<M, L, RP>::value))
     gemv_stream_kernel(const __grid_constant__ StreamMaps maps, StreamParams p) {
     static_assert(!G || R == 2, "GeGLU pairs the gate and up rows of one output in a lane");
     static_assert(!RP || (F == Fmt::Q4_0 && !G && R % 2 == 0), "row-pair form: Q4_0 row pairs");
@@ -937,7 +953,7 @@ __global__ void __launch_bounds__(QMM_GEMV_MAX_THREADS)
     }
 }
 
-// ---- Persistent form: large N at M <= 4 (one launch that spans many waves) ----
+// ---- Persistent form: large N at M <= 10 (one launch that spans many waves) ----
 // One CTA per SM.  CTA c owns whole tiles [c*T/G, (c+1)*T/G) of the T row
 // tiles (G CTAs), so every SM gets the same work to within one tile; its nw
 // warps split the CTA's (tile, chunk) units evenly, in order.  A warp streams
@@ -960,9 +976,9 @@ struct PersistParams {
 };
 
 template <Fmt F, int M, int R>
-__global__ void __launch_bounds__(QMM_GEMV_MAX_THREADS)
+__global__ void __launch_bounds__(QMM_GEMV_MAX_THREADS, 1)  // one CTA per SM
     gemv_persist_kernel(const __grid_constant__ CUtensorMap wmap, PersistParams p) {
-    static_assert(M <= QMM_GEMV_R2_MAX_M, "the per-block chunk forms of small M");
+    static_assert(M <= QMM_GEMV_R_WIDE_MAX_M, "the per-block chunk forms");
     constexpr int CB = StreamFmt<F>::kChunkBytes;
     constexpr int EB = StreamFmt<F>::kElemBytes;
     constexpr int kRows = 32 * R;  // lane r owns rows r, r + 32, ... of a tile
@@ -1048,10 +1064,16 @@ __global__ void __launch_bounds__(QMM_GEMV_MAX_THREADS)
         ++consumed;
         const uint8_t *src = my_ring + (st * kRows + lane) * CB;
         const float *xk = xs + cc * kChunkK;
-        if constexpr (F == Fmt::Q4_0)
+        if constexpr (M > QMM_GEMV_R2_MAX_M) {
+            if constexpr (F == Fmt::Q4_0)
+                q4_0_chunk_wide<M, R>(src, 32 * CB, xk, XS, p.magic, tot);
+            else
+                q8_0_chunk_wide<M, R>(src, 32 * CB, xk, XS, p.magic, tot);
+        } else if constexpr (F == Fmt::Q4_0) {
             q4_0_chunk<M, 1, R>(src, 32 * CB, xk, XS, p.magic, tot);
-        else
+        } else {
             q8_0_chunk<M, 1, R>(src, 32 * CB, xk, XS, p.magic, tot);
+        }
         __syncwarp();  // every lane is done reading the stage before it is refilled
         if (issued < nu) {
             issue(st);
@@ -1410,7 +1432,10 @@ cudaError_t launch_m(const GemvProblem *probs, int count, const float *x, int64_
             // FMA until the accumulators crowd the registers (M > 10); where
             // their shared memory does not fit, one row per lane
             if constexpr (M <= QMM_GEMV_R_WIDE_MAX_M) {
-                e = launch_stream<F, M, 1, 2>(probs, count, x, k, stream, ctx);
+                constexpr bool kPersist = F == Fmt::Q4_0 ? QMM_GEMV_PERSIST : QMM_GEMV_PERSIST_Q8_0;
+                e = count == 1 && kPersist ? launch_persist<F, M, 2>(probs[0], x, k, stream, ctx)
+                                           : kShapeTooLarge;
+                if (e == kShapeTooLarge) e = launch_stream<F, M, 1, 2>(probs, count, x, k, stream, ctx);
                 if (e == kShapeTooLarge) e = launch_stream<F, M, 1, 1>(probs, count, x, k, stream, ctx);
             } else {
                 e = launch_stream<F, M, 1, 1>(probs, count, x, k, stream, ctx);

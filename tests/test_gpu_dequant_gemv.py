@@ -363,13 +363,15 @@ def test_gemv_row_pairs_and_their_fallback(qmm, oracle_mod, m, n, k):
 @pytest.mark.parametrize("fmt,m,n,k", [("q4_0", 1, 80000, 256), ("q4_0", 2, 100003, 512),
                                        ("q4_0", 4, 90000, 2048), ("q4_0", 3, 78000, 1280),
                                        ("q8_0", 1, 40000, 2048), ("q8_0", 2, 50001, 768),
-                                       ("q4_0", 1, 77000, 512)])
+                                       ("q4_0", 6, 80000, 1280), ("q4_0", 9, 90001, 512),
+                                       ("q8_0", 8, 40000, 2048), ("q4_0", 1, 77000, 512)])
 def test_gemv_persistent_form(qmm, oracle_mod, fmt, m, n, k):
-    """Large single matrices at M <= 4 run one CTA per SM over an even share of
+    """Large single matrices at M <= 10 run one CTA per SM over an even share of
     whole tiles, their warps splitting the units so that some tiles are shared
     by two warps (K = 512, 1280, 768, 2048: several chunks per tile) and added
-    after a CTA barrier; ragged N (100003, 50001); 77000 x 512 has too few
-    tiles for every warp and takes the streaming form."""
+    after a CTA barrier; ragged N (100003, 50001, 90001); M = 6, 8, 9 use the
+    per-block loop of wide M; 77000 x 512 has too few tiles for every warp and
+    takes the streaming form."""
     case = synth.gemv_case(fmt, m, n, k, seed=n % 1000 + k)
     y_ref, bound = _oracle_gemv(oracle_mod, fmt, case)
     y = _run_gemv(qmm, fmt, case)
