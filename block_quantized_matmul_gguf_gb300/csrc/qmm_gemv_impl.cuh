@@ -105,7 +105,7 @@
 #define QMM_GEMV_PROXY_FENCE 0    // 1: fence.proxy.async before refilling a stage (not needed)
 #endif
 #ifndef QMM_GEMV_X_BYTES
-#define QMM_GEMV_X_BYTES 65536    // activation slice per CTA (shared memory)
+#define QMM_GEMV_X_BYTES 98304    // activation slice per CTA (shared memory)
 #endif
 
 namespace qmm {
@@ -654,18 +654,21 @@ __device__ __forceinline__ float gelu_tanh(float z) {
 // Register budget hint (CTAs of QMM_GEMV_MAX_THREADS per SM that it must
 // allow).  Without one, ptxas kept the M <= 4 kernels near 80 registers;
 // allowing two CTAs' worth (up to 128) took the decode step from 19.0 to
-// 18.05 us.  The row-pair form needs more than 128 and gets one CTA's worth;
-// the per-block forms of M 5..9 are left to ptxas.
+// 18.05 us.  The row-pair form needs more than 128 and the per-block forms of
+// M 5..9 measured 1-2 % faster with more: both get one CTA's worth.
 #ifndef QMM_GEMV_MB_L1
 #define QMM_GEMV_MB_L1 2
 #endif
 #ifndef QMM_GEMV_MB_L2
 #define QMM_GEMV_MB_L2 2
 #endif
+#ifndef QMM_GEMV_MB_WIDE
+#define QMM_GEMV_MB_WIDE 1
+#endif
 template <int M, int L, bool RP>
 struct StreamMinBlocks {
     static constexpr int value =
-        RP ? 1 : (M <= QMM_GEMV_R2_MAX_M ? (L == 1 ? QMM_GEMV_MB_L1 : QMM_GEMV_MB_L2) : 0);
+        RP ? 1 : (M <= QMM_GEMV_R2_MAX_M ? (L == 1 ? QMM_GEMV_MB_L1 : QMM_GEMV_MB_L2) : QMM_GEMV_MB_WIDE);
 };
 template <Fmt F, int M, int L, int R, bool G = false, bool RP = false>
 __global__ void __launch_bounds__(QMM_GEMV_MAX_THREADS, (StreamMinBlocks<M, L, RP>::value))
