@@ -105,7 +105,7 @@
 #define QMM_GEMV_PROXY_FENCE 0    // 1: fence.proxy.async before refilling a stage (not needed)
 #endif
 #ifndef QMM_GEMV_X_BYTES
-#define QMM_GEMV_X_BYTES 98304    // activation slice per CTA (shared memory)
+#define QMM_GEMV_X_BYTES 131072   // activation slice per CTA (shared memory)
 #endif
 
 namespace qmm {
