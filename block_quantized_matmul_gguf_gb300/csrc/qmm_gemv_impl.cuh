@@ -30,13 +30,18 @@
 //  * The CTA's slice of the activations (M rows x its K range) is copied
 //    into shared memory by bulk copies issued by one thread after the
 //    programmatic-launch wait; warps wait on its mbarrier and read x as
-//    warp-wide broadcasts.  No thread waits on another warp.
+//    warp-wide broadcasts.  Q4_0 warps request one weight stage before that
+//    wait and the rest after the copy, so that it does not queue behind them.
 //  * Decode without int->float conversions: OR-ing a nibble (or an offset
 //    byte) at bit s into the mantissa of 2^23 gives m = 2^23 + v*2^s exactly;
 //    one FMA m*2^-s - (2^23 + 8*2^s)*2^-s (Q4_0; +128 for Q8_0) leaves the
 //    exact integer nibble-8 (or q).  Both that FMA and the product with x run
 //    as packed f32x2 instructions, four independent chains at small M.
 //  * Per block: acc = sum_j (nibble_j - 8) * x_j in fp32, then y += d * acc.
+//
+// Persistent kernel (one large matrix, M <= 10): one CTA per SM over an equal
+// run of whole tiles, the CTA's warps splitting its (tile, chunk) units
+// evenly; see gemv_persist_kernel.
 //
 // Byte-wise kernel: any K % 32 == 0 and any alignment, and the shapes whose
 // activation slice does not fit shared memory at any cluster split; a warp
