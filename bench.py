@@ -711,6 +711,29 @@ def measure_gemm(torch, qmm, l2, stream, timer, peaks):
                      for r in range(R)]),
               path="two-phase on the library's own scratch (no workspace argument)", replicas=R)
         del W, X, Y, WS
+        # a short prompt (256 tokens) with the same weights: fused alone, and
+        # with a workspace, where the fused kernel splits K through it
+        ms = synth.SHORT_PROMPT_M
+        w, xb = synth.gemm_case(ms, p.n, p.k, seed=0, stream=74 + i)
+        W0 = torch.from_numpy(w.reshape(-1)).to(dev)
+        X0 = torch.from_numpy(xb.astype(np.int16)).to(dev)
+        R = replicas(W0.numel() + 2 * X0.numel() + 4 * ms * p.n)
+        W = [W0.clone() for _ in range(R)]
+        X = [X0.clone() for _ in range(R)]
+        Y = [torch.empty((ms, p.n), dtype=torch.float32, device=dev) for _ in range(R)]
+        WS = [torch.empty(qmm.qmm_gemm_workspace_bytes(p.n, p.k), dtype=torch.uint8, device=dev)
+              for _ in range(2)]
+        del W0, X0
+        flops_s = 2.0 * ms * p.n * p.k
+        entry(f"q4_0_gemm_{ms}x{p.n}x{p.k}", flops_s,
+              timed([lambda r=r: qmm.qmm_gemm_q4_0(W[r], X[r], Y[r], ms, p.n, p.k, s) for r in range(R)]),
+              path="fused, one pass over K per tile", replicas=R)
+        entry(f"q4_0_gemm_ws_{ms}x{p.n}x{p.k}", flops_s,
+              timed([lambda r=r: qmm.qmm_gemm_q4_0_ws(W[r], X[r], Y[r], ms, p.n, p.k, WS[r % 2],
+                                                      WS[r % 2].numel(), s) for r in range(R)]),
+              path="fused with K split into parts through the workspace, then the parts added",
+              replicas=R)
+        del W, X, Y, WS
         # practical ceiling of the same contraction: cuBLAS bf16 with the
         # weights already dense bf16 (no dequantization), same rotation
         Wd = [torch.randn((p.n, p.k), device=dev).to(torch.bfloat16) for _ in range(2)]

@@ -150,13 +150,15 @@ qmm_status gemm(Fmt fmt, const void *w, const uint16_t *x_bf16, float *y, int64_
                 int64_t k, qmm_stream_t stream, void *ws = nullptr, size_t ws_bytes = 0) {
     qmm_status s = check_gemm(fmt, w, x_bf16, y, m, n, k);
     if (s != QMM_OK) return s;
-    const bool two_phase = ws != nullptr && use_two_phase(m, k);
-    if (two_phase) {
+    const bool two_phase = ws != nullptr && use_two_phase_gemm(m, n, k);
+    const size_t wbytes = static_cast<size_t>(n) * (k / kQK) * block_bytes(fmt);
+    const size_t ybytes = sizeof(float) * static_cast<size_t>(m) * n;
+    if (ws != nullptr) {
+        // two phases: the dequantised weights; one phase (short prompts):
+        // room for K-split partial products
         const size_t need = gemm_workspace_bytes(n, k, false);
         s = check_workspace(ws, ws_bytes, need);
         if (s != QMM_OK) return s;
-        const size_t wbytes = static_cast<size_t>(n) * (k / kQK) * block_bytes(fmt);
-        const size_t ybytes = sizeof(float) * static_cast<size_t>(m) * n;
         if (overlaps(ws, need, w, wbytes) || overlaps(ws, need, x_bf16, 2 * static_cast<size_t>(m) * k) ||
             overlaps(ws, need, y, ybytes))
             return QMM_ERR_UNSUPPORTED;
@@ -168,8 +170,13 @@ qmm_status gemm(Fmt fmt, const void *w, const uint16_t *x_bf16, float *y, int64_
     if (two_phase)
         return from_cuda(launch_gemm_two_phase(fmt, wb, x_bf16, y, m, n, k,
                                                static_cast<uint16_t *>(ws), st, ctx));
-    return from_cuda(fmt == Fmt::Q4_0 ? launch_gemm_q4_0(wb, x_bf16, y, m, n, k, st, ctx)
-                                      : launch_gemm_q8_0(wb, x_bf16, y, m, n, k, st, ctx));
+    // K-split budget: fixed by the shape (not by what this caller happens to
+    // give), so that every workspace and the prefill entry's scratch choose
+    // the same split and give the same bits
+    float *part = static_cast<float *>(ws);
+    const size_t budget = ws != nullptr ? fused_part_budget(n, k) : 0;
+    return from_cuda(fmt == Fmt::Q4_0 ? launch_gemm_q4_0(wb, x_bf16, y, m, n, k, st, ctx, part, budget)
+                                      : launch_gemm_q8_0(wb, x_bf16, y, m, n, k, st, ctx, part, budget));
 }
 
 }  // namespace
@@ -362,7 +369,7 @@ qmm_status qmm_gemm_q4_0_geglu_ws(const void *wg, const void *wu, const uint16_t
     if (overlaps(h_bf16, hbytes, x_bf16, sizeof(uint16_t) * static_cast<size_t>(m) * k) ||
         overlaps(h_bf16, hbytes, wg, wbytes) || overlaps(h_bf16, hbytes, wu, wbytes))
         return QMM_ERR_UNSUPPORTED;
-    const bool two_phase = workspace != nullptr && use_two_phase(m, k);
+    const bool two_phase = workspace != nullptr && use_two_phase_geglu(m, k);
     if (two_phase) {
         const size_t need = gemm_workspace_bytes(n, k, true);
         s = check_workspace(workspace, workspace_bytes, need);

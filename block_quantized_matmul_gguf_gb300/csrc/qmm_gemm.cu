@@ -160,9 +160,11 @@ static_assert(SmemLayout<Fmt::Q8_0>::smem_bytes <= 232448, "shared memory per CT
 struct GemmParams {
     float *y;     // plain GEMM: fp32 [m][n]
     uint16_t *h;  // GeGLU form: bf16 [m][n] (n = rows of each of the two weights)
+    float *part;  // K split (ksplit > 1): fp32 [ksplit][m][n] partial products
     int m, n, k;
     int num_t_blocks;  // token blocks of BT
     int num_tiles;     // pair tiles
+    int ksplit;        // K parts per tile (plain GEMM only); a work item is (tile, part)
     uint32_t magic;    // 0x4B000000 (2^23)
     LaunchCtx ctx;
 };
@@ -252,8 +254,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     pdl_wait();
 
-    const int KB = p.k / BK;     // K stages per tile
-    const int KR = p.k / RAW_K;  // raw stages per tile
+    // Work items: (pair tile t, K part s), item = t * ksplit + s; an item
+    // covers K stages [s * KB, (s + 1) * KB).
+    const int KB = p.k / BK / p.ksplit;     // K stages per item
+    const int KR = p.k / RAW_K / p.ksplit;  // raw stages per item
+    const int num_items = p.num_tiles * p.ksplit;
 
     if (warp == WARP_PRODUCER) {
         if (lane == 0) {
@@ -261,7 +266,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_x)) : "memory");
             uint32_t it = 0;
             bool ok = true;
-            for (int t = pair; ok && t < p.num_tiles; t += num_pairs) {
+            for (int item = pair; ok && item < num_items; item += num_pairs) {
+                const int t = item / p.ksplit;
+                const int kb0 = (item - t * p.ksplit) * KB;
                 const int tb = t % p.num_t_blocks;
                 const int xrow = tb * BT + static_cast<int>(rank) * BT_CTA;
                 for (int kb = 0; kb < KB; ++kb) {
@@ -270,7 +277,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (!wait_or_abort(empty(s), ph ^ 1u, abort_flag, ctx)) { ok = false; break; }
                     const uint32_t xf = map_to_rank(full(it), 0);
                     mbar_expect_tx_cluster(xf, X_STAGE_BYTES);
-                    tma_load_2d_pair(sbase + SL::x + s * X_STAGE_BYTES, &tmap_x, kb * BK, xrow, xf);
+                    tma_load_2d_pair(sbase + SL::x + s * X_STAGE_BYTES, &tmap_x, (kb0 + kb) * BK, xrow, xf);
                     ++it;
                 }
             }
@@ -290,7 +297,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                              : "memory");
             uint32_t rit = 0;
             bool ok = true;
-            for (int t = pair; ok && t < p.num_tiles; t += num_pairs) {
+            for (int item = pair; ok && item < num_items; item += num_pairs) {
+                const int t = item / p.ksplit;
+                const int kr0 = (item - t * p.ksplit) * KR;
                 const int wb = t / p.num_t_blocks;
                 // G: this CTA's 64 features, gate rows then up rows
                 const int wrow = G ? wb * BW + static_cast<int>(rank) * (BW / 2)
@@ -300,12 +309,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const uint32_t ph = (rit / RAW_STAGES) & 1u;
                     if (!wait_or_abort(raw_empty(r), ph ^ 1u, abort_flag, ctx)) { ok = false; break; }
                     mbar_expect_tx_addr(raw_full(r), RAW_STAGE_BYTES);
-                    tma_load_2d(sbase + SL::raw + r * RAW_STAGE_BYTES, &tmap_w, kr * RAW_X,
+                    tma_load_2d(sbase + SL::raw + r * RAW_STAGE_BYTES, &tmap_w, (kr0 + kr) * RAW_X,
                                 wrow, raw_full(r));
                     if constexpr (G)
                         tma_load_2d(sbase + SL::raw + r * RAW_STAGE_BYTES +
                                         (BW / 2) * RAW_ROW_BYTES,
-                                    &tmap_w2, kr * RAW_X, wrow, raw_full(r));
+                                    &tmap_w2, (kr0 + kr) * RAW_X, wrow, raw_full(r));
                     ++rit;
                 }
             }
@@ -325,9 +334,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // its path between MMAs is kept short: the K stage, ring slot,
             // descriptors and barrier addresses are advanced incrementally
             // (no run-time division), which measured as the pipeline's pace.
-            const uint32_t my_tiles =
-                pair < p.num_tiles ? static_cast<uint32_t>((p.num_tiles - pair + num_pairs - 1) / num_pairs) : 0u;
-            const uint32_t total = my_tiles * static_cast<uint32_t>(KB);
+            const uint32_t my_items =
+                pair < num_items ? static_cast<uint32_t>((num_items - pair + num_pairs - 1) / num_pairs) : 0u;
+            const uint32_t total = my_items * static_cast<uint32_t>(KB);
             const uint64_t bdesc0 = sw128_desc(sbase + SL::x);
             const uint32_t a0 = tmem_base + a_col0;
             const uint32_t empty0 = empty(0);
@@ -394,7 +403,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         (void)flip1;
         uint32_t it = 0, rit = 0;
         bool ok = true;
-        for (int t = pair; ok && t < p.num_tiles; t += num_pairs) {
+        for (int item = pair; ok && item < num_items; item += num_pairs) {
             for (int kr = 0; ok && kr < KR; ++kr) {
                 const int r = rit % RAW_STAGES;
                 if (!warp_wait_or_abort(raw_full(r), (rit / RAW_STAGES) & 1u, abort_flag, ctx)) {
@@ -479,7 +488,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int c0 = ((warp - WARP_EPI0) >> 2) * CPW;
         const uint32_t d_empty_leader = map_to_rank(d_empty, 0);
         uint32_t tiles_done = 0;
-        for (int t = pair; t < p.num_tiles; t += num_pairs) {
+        for (int item = pair; item < num_items; item += num_pairs) {
+            const int t = item / p.ksplit;
             const int tb = t % p.num_t_blocks, wb = t / p.num_t_blocks;
             if (!warp_wait_or_abort<QMM_GEMM_EPI_SUSPEND_NS>(d_full, tiles_done & 1u, abort_flag, ctx)) break;
             tc_fence_after();
@@ -509,6 +519,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 }
             } else {
+                // the whole product, or this item's K part of it
+                float *yo = p.ksplit > 1 ? p.part + static_cast<size_t>(item - t * p.ksplit) * p.m * p.n
+                                         : p.y;
                 const int n = wb * 2 * BW + static_cast<int>(rank) * BW + q * 32 + lane;
                 const bool n_ok = n < p.n;
 #pragma unroll 1
@@ -522,7 +535,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
                             if (m0 + j < p.m)
-                                p.y[static_cast<size_t>(m0 + j) * p.n + n] = __uint_as_float(v[j]);
+                                yo[static_cast<size_t>(m0 + j) * p.n + n] = __uint_as_float(v[j]);
                     }
                 }
             }
@@ -541,11 +554,87 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == WARP_MMA) tmem_dealloc_pair(tmem_base, TMEM_COLS);
 }
 
+// y = sum of the K parts, in part order (the same order for every output).
+// V: 16-byte accesses (y 16-byte aligned and mn % 4 == 0; the parts always
+// are), so that each thread has a whole part's float4 of every part in
+// flight; otherwise 4-byte ones.
+template <bool V>
+__global__ void __launch_bounds__(256) splitk_sum_kernel(const float *__restrict__ part,
+                                                         float *__restrict__ y, int64_t mn, int ks) {
+    pdl_wait();
+    pdl_launch_dependents();
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const int64_t start = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if constexpr (V) {
+        const float4 *p4 = reinterpret_cast<const float4 *>(part);
+        float4 *y4 = reinterpret_cast<float4 *>(y);
+        const int64_t n4 = mn / 4;
+        for (int64_t i = start; i < n4; i += stride) {
+            float4 v[8];  // ks <= 8: every part's load issued before the adds
+#pragma unroll
+            for (int s = 0; s < 8; ++s)
+                if (s < ks) v[s] = __ldcg(p4 + static_cast<int64_t>(s) * n4 + i);
+            float4 acc = v[0];
+#pragma unroll
+            for (int s = 1; s < 8; ++s) {
+                if (s < ks) {
+                    acc.x += v[s].x;
+                    acc.y += v[s].y;
+                    acc.z += v[s].z;
+                    acc.w += v[s].w;
+                }
+            }
+            y4[i] = acc;
+        }
+    } else {
+        for (int64_t i = start; i < mn; i += stride) {
+            float v[8];
+#pragma unroll
+            for (int s = 0; s < 8; ++s)
+                if (s < ks) v[s] = __ldcg(part + static_cast<int64_t>(s) * mn + i);
+            float acc = v[0];
+#pragma unroll
+            for (int s = 1; s < 8; ++s)
+                if (s < ks) acc += v[s];
+            y[i] = acc;
+        }
+    }
+}
+
+// K parts for a plain GEMM whose tiles leave most pairs idle: the split (1,
+// 2, 4 or 8, dividing the raw stages) that best fills the pairs, if its
+// partial products fit `part_bytes` and it fills them clearly better than no
+// split.  An item of a split tile is its K part (fewer stages, same work per
+// stage), so the fill is the share of pair rounds that are busy.
+int choose_ksplit(int64_t m, int64_t n, int64_t k, int num_tiles, int pairs, size_t part_bytes) {
+    if (num_tiles >= pairs) return 1;
+    auto fill = [&](int ks) {
+        const int64_t items = static_cast<int64_t>(num_tiles) * ks;
+        const int64_t rounds = (items + pairs - 1) / pairs;
+        return static_cast<double>(items) / static_cast<double>(rounds * pairs);
+    };
+    int best = 1;
+    double best_fill = fill(1);
+    for (int ks = 2; ks <= 8; ks *= 2) {
+        if ((k / RAW_K) % ks != 0) break;
+        if (static_cast<size_t>(ks) * static_cast<size_t>(m) * static_cast<size_t>(n) * sizeof(float) > part_bytes)
+            break;
+        const double f = fill(ks);
+        if (f > best_fill + 0.05) {
+            best = ks;
+            best_fill = f;
+        }
+    }
+    return best;
+}
+
 // One launch: plain GEMM (w2 == nullptr: y fp32) or the GeGLU form (w gate,
-// w2 up: h bf16).
+// w2 up: h bf16).  part (plain GEMM, may be null): room for K-split partial
+// products; with a split, a second kernel adds them into y.
 template <Fmt F, bool G>
 cudaError_t launch(const uint8_t *w, const uint8_t *w2, const uint16_t *x, float *y, uint16_t *h,
-                   int64_t m, int64_t n, int64_t k, cudaStream_t stream, const LaunchCtx &ctx) {
+                   int64_t m, int64_t n, int64_t k, cudaStream_t stream, const LaunchCtx &ctx,
+                   float *part = nullptr, size_t part_bytes = 0) {
     if (m > (1 << 30) || n > (1 << 30) || k > (1 << 24)) return cudaErrorInvalidValue;
     CUtensorMap tx, tw, tw2;
     if (!encode_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, k, m, k * 2, BK, BT_CTA,
@@ -575,27 +664,56 @@ cudaError_t launch(const uint8_t *w, const uint8_t *w2, const uint16_t *x, float
     const int64_t tile_rows = G ? BW : 2 * BW;
     const int nwb = static_cast<int>((n + tile_rows - 1) / tile_rows);
     p.num_tiles = p.num_t_blocks * nwb;
+    const int all_pairs = std::max(1, device_sm_count() / 2);
+    p.ksplit = (!G && part != nullptr) ? gemm_fused_ksplit(m, n, k, part_bytes) : 1;
+    p.part = p.ksplit > 1 ? part : nullptr;
     p.magic = 0x4B000000u;
     p.ctx = ctx;
     constexpr size_t smem = SmemLayout<F>::smem_bytes;
     static int smem_limits[kMaxDevices] = {0};
     cudaError_t e = ensure_smem(gemm_kernel<F, G>, smem, true, smem_limits);
     if (e != cudaSuccess) return e;
-    const int pairs = std::max(1, std::min(p.num_tiles, device_sm_count() / 2));
-    return launch_kernel(gemm_kernel<F, G>, dim3(2 * pairs), dim3(NUM_THREADS), smem, stream, 2,
-                         tx, tw, tw2, p);
+    const int pairs = std::min(p.num_tiles * p.ksplit, all_pairs);
+    e = launch_kernel(gemm_kernel<F, G>, dim3(2 * pairs), dim3(NUM_THREADS), smem, stream, 2,
+                      tx, tw, tw2, p);
+    if (e != cudaSuccess || p.ksplit == 1) return e;
+    const int64_t mn = m * n;
+    const bool vec = mn % 4 == 0 && (reinterpret_cast<uintptr_t>(y) & 15) == 0;
+    const int64_t threads = vec ? mn / 4 : mn;
+    const unsigned blocks = static_cast<unsigned>(
+        std::min<int64_t>((threads + 255) / 256, static_cast<int64_t>(device_sm_count()) * 8));
+    return vec ? launch_kernel(splitk_sum_kernel<true>, dim3(blocks), dim3(256), 0, stream, 1,
+                               static_cast<const float *>(p.part), y, mn, p.ksplit)
+               : launch_kernel(splitk_sum_kernel<false>, dim3(blocks), dim3(256), 0, stream, 1,
+                               static_cast<const float *>(p.part), y, mn, p.ksplit);
 }
 
 }  // namespace
 
+int gemm_fused_ksplit(int64_t m, int64_t n, int64_t k, size_t part_bytes) {
+    if (part_bytes == 0) return 1;
+    const int64_t tiles = (m + BT - 1) / BT * ((n + 2 * BW - 1) / (2 * BW));
+    return choose_ksplit(m, n, k, static_cast<int>(tiles), std::max(1, device_sm_count() / 2),
+                         part_bytes);
+}
+
+bool use_two_phase_gemm(int64_t m, int64_t n, int64_t k) {
+    const int64_t blocks = (m + BT - 1) / BT;
+    if (blocks <= 1) return false;
+    if (blocks <= 4 && gemm_fused_ksplit(m, n, k, fused_part_budget(n, k)) > 1) return false;
+    return blocks >= 3 || k >= 8192;
+}
+
 cudaError_t launch_gemm_q4_0(const uint8_t *w, const uint16_t *x, float *y, int64_t m, int64_t n,
-                             int64_t k, cudaStream_t stream, const LaunchCtx &ctx) {
-    return launch<Fmt::Q4_0, false>(w, nullptr, x, y, nullptr, m, n, k, stream, ctx);
+                             int64_t k, cudaStream_t stream, const LaunchCtx &ctx, float *part,
+                             size_t part_bytes) {
+    return launch<Fmt::Q4_0, false>(w, nullptr, x, y, nullptr, m, n, k, stream, ctx, part, part_bytes);
 }
 
 cudaError_t launch_gemm_q8_0(const uint8_t *w, const uint16_t *x, float *y, int64_t m, int64_t n,
-                             int64_t k, cudaStream_t stream, const LaunchCtx &ctx) {
-    return launch<Fmt::Q8_0, false>(w, nullptr, x, y, nullptr, m, n, k, stream, ctx);
+                             int64_t k, cudaStream_t stream, const LaunchCtx &ctx, float *part,
+                             size_t part_bytes) {
+    return launch<Fmt::Q8_0, false>(w, nullptr, x, y, nullptr, m, n, k, stream, ctx, part, part_bytes);
 }
 
 cudaError_t launch_gemm_q4_0_geglu(const uint8_t *wg, const uint8_t *wu, const uint16_t *x,

@@ -550,7 +550,14 @@ cudaError_t launch_gemm_q4_0_prefill(const uint8_t *w, const uint16_t *x, float 
                                      int64_t n, int64_t k, cudaStream_t stream,
                                      const LaunchCtx &ctx) {
     if (k > kPrefillMaxK) return cudaErrorInvalidValue;  // the API rejects it first
-    if (!use_two_phase(m, k)) return launch_gemm_q4_0(w, x, y, m, n, k, stream, ctx);
+    if (!use_two_phase_gemm(m, n, k)) {  // one phase; the scratch takes K-split partial products
+        void *scratch = nullptr;
+        const cudaError_t e = prefill_scratch(&scratch);
+        if (e != cudaSuccess) return e;
+        // the K-split budget qmm_gemm_q4_0_ws takes too: the same bits
+        return launch_gemm_q4_0(w, x, y, m, n, k, stream, ctx, static_cast<float *>(scratch),
+                                fused_part_budget(n, k));
+    }
     // weight rows per chunk: whole pair tiles that fit the scratch
     const int64_t chunk =
         static_cast<int64_t>(kScratchBytes / (static_cast<size_t>(k) * 2)) / (2 * SW) * (2 * SW);
@@ -579,6 +586,10 @@ cudaError_t launch_gemm_q4_0_prefill(const uint8_t *w, const uint16_t *x, float 
 
 size_t gemm_workspace_bytes(int64_t n, int64_t k, bool geglu) {
     return static_cast<size_t>(workspace_rows(n, geglu)) * static_cast<size_t>(k) * 2;
+}
+
+size_t fused_part_budget(int64_t n, int64_t k) {
+    return std::min(kScratchBytes, gemm_workspace_bytes(n, k, false));
 }
 
 cudaError_t launch_gemm_two_phase(Fmt fmt, const uint8_t *w, const uint16_t *x, float *y,

@@ -144,23 +144,47 @@ inline cudaError_t launch_geglu_q4_0(const GemvProblem *gate_up, const float *x,
     return launch_geglu_q4_0_m11_16(gate_up, x, m, k, stream, ctx);
 }
 
+// Fused prefill GEMM.  part / part_bytes (optional, 16-byte aligned, not
+// overlapping any operand): room for K-split partial products, used when the
+// product has too few tiles to fill the SMs (short prompts); the call then
+// adds the parts into y with a second kernel, in a fixed order.
 cudaError_t launch_gemm_q4_0(const uint8_t *w, const uint16_t *x, float *y, int64_t m,
-                             int64_t n, int64_t k, cudaStream_t stream, const LaunchCtx &ctx);
+                             int64_t n, int64_t k, cudaStream_t stream, const LaunchCtx &ctx,
+                             float *part = nullptr, size_t part_bytes = 0);
 
 cudaError_t launch_gemm_q8_0(const uint8_t *w, const uint16_t *x, float *y, int64_t m,
-                             int64_t n, int64_t k, cudaStream_t stream, const LaunchCtx &ctx);
+                             int64_t n, int64_t k, cudaStream_t stream, const LaunchCtx &ctx,
+                             float *part = nullptr, size_t part_bytes = 0);
 
 // Prefill GeGLU: h[i][j] = bf16(gelu(X[i] . wg[j]) * (X[i] . wu[j])).
 cudaError_t launch_gemm_q4_0_geglu(const uint8_t *wg, const uint8_t *wu, const uint16_t *x,
                                    uint16_t *h, int64_t m, int64_t n, int64_t k,
                                    cudaStream_t stream, const LaunchCtx &ctx);
 
-// When the two-phase GEMM pays: the dequant pass costs about 0.65 us per
-// million weights, the fused kernel's redundant decode grows with the
-// number of 256-token blocks.  Measured crossovers at 2048 tokens' scale:
-// N x K = 8192 x 2048 from m = 768, 16384 x 2048 from m = 1024; at
-// K = 8192 the two-phase GEMM wins from the second token block on.
-inline bool use_two_phase(int64_t m, int64_t k) { return m > 512 || (m > 256 && k >= 4096); }
+// The K split the fused plain GEMM takes for an (m, n, k) product given
+// part_bytes of room for partial products (1: none).
+int gemm_fused_ksplit(int64_t m, int64_t n, int64_t k, size_t part_bytes);
+
+// Room for K-split partial products that the one-phase product takes, out of
+// a caller workspace of gemm_workspace_bytes(n, k, false) or out of the
+// prefill entry's 64 MiB scratch: the same for both, so that both choose the
+// same split and give the same bits.
+size_t fused_part_budget(int64_t n, int64_t k);
+
+// When the two-phase plain GEMM pays, from measurements of both forms at
+// N x K = 2048 x 8192, 8192 x 2048, 16384 x 2048, 4096 x 4096 and
+// 8192 x 8192 for m = 256..2048.  The dequant pass costs about 0.65 us per
+// million weights; the fused kernel decodes the weights again for every
+// 256-token block, and a product whose pair tiles fill under half the pairs
+// runs the fused kernel with a K split instead.  So: never for one token
+// block; not for up to four blocks when the fused kernel splits K (the
+// two-phase GEMM has as few tiles and K times longer ones); otherwise from
+// the third block, or from the second at K >= 8192.
+bool use_two_phase_gemm(int64_t m, int64_t n, int64_t k);
+
+// The GeGLU form has no K split: two phases from the third token block, or
+// from the second at K >= 4096.
+inline bool use_two_phase_geglu(int64_t m, int64_t k) { return m > 512 || (m > 256 && k >= 4096); }
 
 // Two-phase prefill GEMM (weights dequantised once into a bf16 workspace,
 // then a shared-memory-operand tensor-core GEMM).  gemm_workspace_bytes is

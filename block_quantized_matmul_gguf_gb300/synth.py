@@ -186,6 +186,7 @@ LM_HEAD = Projection("lm_head", 262144, 2048)
 LM_HEAD_M = (1, 8)
 PREFILL_M = 2048
 PREFILL_SHAPES = (Projection("wide", 8192, 2048), Projection("tall", 2048, 8192))
+SHORT_PROMPT_M = 256  # the shortest prefill the GEMM path takes (M >= 256)
 
 
 def q4_0_bytes(n: int, k: int) -> int:

@@ -54,6 +54,7 @@
 #ifndef QMM_H
 #define QMM_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -190,11 +191,21 @@ qmm_status qmm_gemm_q8_0(const void *w, const uint16_t *x_bf16, float *y, int64_
 /* ---- Prefill GEMM with a workspace (long prompts) -----------------------
  * The same products as qmm_gemm_q4_0 / qmm_gemm_q8_0 / qmm_gemm_q4_0_geglu,
  * with the same arithmetic (each weight rounded once to bf16, fp32 sums in
- * tensor memory) and accuracy bound.  With a workspace, when m > 512 or
- * (m > 256 and k >= 4096), the weights are first dequantised once into the
- * workspace as bf16 (so that they are not decoded again for every 256-token
- * block) and a second kernel runs the tensor-core GEMM from it; otherwise
- * the call is the fused one and the workspace is not touched.
+ * tensor memory) and accuracy bound.  With a workspace, a call takes one
+ * of two forms, chosen from (m, n, k) and the GPU's SM count:
+ *   two phases: the weights are first dequantised once into the workspace
+ *     as bf16 (so that they are not decoded again for every 256-token
+ *     block) and a second kernel runs the tensor-core GEMM from it;
+ *   one phase: the fused call; when its 256 x 256 tiles are too few to
+ *     occupy the GPU's SM pairs, it splits K into 2, 4 or 8 parts whose
+ *     fp32 partial products go to the workspace, and a second kernel adds
+ *     them in part order.  Split results differ from qmm_gemm_q4_0's by
+ *     rounding only (same bound) and are the same for every workspace of a
+ *     call's shape.
+ * Two phases are taken from the third 256-token block on (m > 512), or
+ * from the second at k >= 8192, except that up to four blocks (m <= 1024)
+ * stay in one phase when the fused call splits K there.  For the GeGLU
+ * form (no K split): two phases when m > 512, or m > 256 with k >= 4096.
  * workspace : caller-owned device memory, 16-byte aligned, at least
  *             qmm_gemm_workspace_bytes(n, k) bytes (qmm_gemm_geglu_
  *             workspace_bytes for the GeGLU form), not overlapping any
@@ -222,13 +233,14 @@ qmm_status qmm_gemm_q8_0_ws(const void *w, const uint16_t *x_bf16, float *y, int
  *
  * Instead of a caller workspace it uses a 64 MiB scratch array that is part
  * of the library (a module-scope __device__ array: every GPU that loads the
- * library holds it until the process exits).  For long prompts (m > 512, or
- * m > 256 with k >= 4096) the weights are dequantised into it in column
- * chunks of whole 256-row tiles, each chunk followed by its GEMM; shorter
- * prompts take the fused kernel and leave the scratch alone.  The call makes
- * no cudaMalloc, cudaFree or other allocating call.  Same arithmetic, result
- * and accuracy as qmm_gemm_q4_0 (bit-identical to it and to
- * qmm_gemm_q4_0_ws), and the same requirements, plus:
+ * library holds it until the process exits).  Where qmm_gemm_q4_0_ws runs
+ * in two phases, the weights are dequantised into it in column chunks of
+ * whole 256-row tiles, each chunk followed by its GEMM; elsewhere it runs
+ * the fused kernel with the K split of qmm_gemm_q4_0_ws through the
+ * scratch.  The call makes no cudaMalloc, cudaFree or other
+ * allocating call.  Same arithmetic, result and accuracy as
+ * qmm_gemm_q4_0_ws (bit-identical to it; to qmm_gemm_q4_0 too except where
+ * short prompts split K), and the same requirements, plus:
  *   k <= 131072: one 256-row chunk (256 * k bf16 values) must fit the
  *     scratch; a larger k returns QMM_ERR_SCRATCH and launches nothing.
  * Set-up: the first call on a device (with that device current) resolves

@@ -32,6 +32,21 @@ def test_header_declares_the_entry_points():
     assert set(syms) <= set(qmm.EXPORTED) | set(syms)
 
 
+@pytest.mark.parametrize("lang,std", [("c", "-std=c99"), ("c++", "-std=c++11")])
+def test_header_compiles_on_its_own(tmp_path, lang, std):
+    """A C or C++ caller includes the header and nothing else."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc" if lang == "c" else "g++")
+    if cc is None:
+        pytest.skip("no host compiler")
+    src = tmp_path / ("use." + ("c" if lang == "c" else "cpp"))
+    src.write_text('#include "qmm.h"\nint main(void) { return qmm_status_string(QMM_OK) == 0; }\n')
+    r = subprocess.run([cc, std, "-Wall", "-Wextra", "-pedantic", "-Werror", "-fsyntax-only",
+                        "-I", os.path.join(ROOT, "include"), str(src)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+
+
 def test_library_exports_every_declared_symbol(lib):
     raw = ctypes.CDLL(build.LIB_PATH)
     for name in header_symbols():

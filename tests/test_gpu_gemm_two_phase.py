@@ -35,9 +35,11 @@ def _weights(fmt, n, k, seed, stream=0):
 
 
 @pytest.mark.parametrize("fmt", ["q4_0", "q8_0"])
-# two phases when m > 512, or m > 256 with k >= 4096
+# two phases from the third 256-token block on when the fused kernel would
+# not split K (its partial products would not fit, or K has one raw stage),
+# and from the fifth block in any case
 @pytest.mark.parametrize("m,n,k", [(520, 4, 256), (600, 260, 512), (513, 768, 1024),
-                                   (700, 1000, 256), (1024, 384, 2048), (300, 136, 4096)])
+                                   (700, 1000, 256), (1024, 384, 2048), (1100, 136, 4096)])
 def test_two_phase_matches_oracle_and_fused(qmm, oracle_mod, fmt, m, n, k):
     w = _weights(fmt, n, k, seed=m + n)
     xb = synth.activations_bf16(m, k, seed=m + n, stream=5)
@@ -92,16 +94,71 @@ def test_two_phase_geglu(qmm, oracle_mod, m, n, k):
                         rel=GEMM_REL, out_rel=2.0 ** -8)
 
 
-@pytest.mark.parametrize("m,k", [(256, 512), (512, 2048), (256, 4096)])
-def test_short_prompt_ignores_the_workspace(qmm, m, k):
-    n = 512
+@pytest.mark.parametrize("m,n,k", [(256, 512, 512), (512, 512, 2048), (256, 512, 4096)])
+def test_short_prompt_with_a_workspace(qmm, oracle_mod, m, n, k):
+    """Short prompts run the fused kernel; where its tiles leave the GPU idle
+    they split K through the workspace (512 x 2048 at m = 512: 2 parts;
+    512 x 4096 at m = 256: 8 parts; 512 x 512: the parts would not fit the
+    workspace, so no split).  Same bound as the unsplit product, identical to
+    the static-scratch entry, deterministic."""
     w, xb = synth.gemm_case(m, n, k, seed=9)
+    wd, xd = to_dev(w, torch), bf16_tensor(xb, torch)
     ws = _ws(qmm, n, k)
     ws.fill_(0xA5)
-    y = qmm.gemm("q4_0", to_dev(w, torch), bf16_tensor(xb, torch), n, k, workspace=ws)
+    y = qmm.gemm("q4_0", wd, xd, n, k, workspace=ws)
+    y2 = qmm.gemm("q4_0", wd, xd, n, k, workspace=ws)
+    y3 = _prefill(qmm, wd, xd, m, n, k)
     torch.cuda.synchronize()
-    assert bool((ws == 0xA5).all())
-    assert torch.isfinite(y).all()
+    assert qmm.qmm_get_device_error() == 0
+    assert torch.equal(y, y2) and torch.equal(y, y3)
+    y_ref, bound = oracle_mod.gemm_q4_0(w, xb, m, n, k)
+    assert_within(y.cpu().numpy(), y_ref, bound, GEMM_REL, f"short {m}x{n}x{k}")
+
+
+@pytest.mark.parametrize("fmt,m,n,k", [("q4_0", 256, 2048, 8192), ("q4_0", 256, 8192, 2048),
+                                       ("q4_0", 77, 1000, 4096), ("q8_0", 200, 1024, 2048),
+                                       ("q4_0", 1, 4096, 2048), ("q4_0", 128, 300, 1280)])
+def test_short_prompt_k_split(qmm, oracle_mod, fmt, m, n, k):
+    """K split for short prompts (8 parts at 256 x 2048 x 8192, 2 at
+    256 x 8192 x 2048, 8 with ragged tokens and rows, 4 for Q8_0, 4 at one
+    token; 1280 has five raw stages, so no split): every output against the
+    oracle, and against the unsplit fused product within the same bound."""
+    w = _weights(fmt, n, k, seed=m + n)
+    xb = synth.activations_bf16(m, k, seed=m + n, stream=6)
+    wd, xd = to_dev(w, torch), bf16_tensor(xb, torch)
+    y = qmm.gemm(fmt, wd, xd, n, k, workspace=_ws(qmm, n, k))
+    y1 = qmm.gemm(fmt, wd, xd, n, k)
+    torch.cuda.synchronize()
+    assert qmm.qmm_get_device_error() == 0
+    f = oracle_mod.gemv_q4_0 if fmt == "q4_0" else oracle_mod.gemv_q8_0
+    y_ref, bound = f(w, _bf16_to_f32(xb), m, n, k)
+    assert_within(y.cpu().numpy(), y_ref, bound, GEMM_REL, f"split {fmt} {m}x{n}x{k}")
+    assert_within(y1.cpu().numpy(), y_ref, bound, GEMM_REL, f"fused {fmt} {m}x{n}x{k}")
+
+
+@pytest.mark.parametrize("m,n,k,form", [(1024, 2048, 8192, "split"), (600, 2048, 8192, "split"),
+                                        (768, 4096, 4096, "two"), (384, 8192, 8192, "two")])
+def test_medium_prompt_form(qmm, oracle_mod, m, n, k, form):
+    """Two to four token blocks: at 2048 x 8192 the fused kernel's 24-32 pair
+    tiles split K in two (one phase, the workspace holds the parts); at
+    4096 x 4096 (48 tiles) and 8192 x 8192 (64 tiles) no split pays and the
+    product runs in two phases, with the fused kernel's bits.  Sampled
+    outputs against the oracle; the static-scratch entry gives the same bits
+    as the workspace entry in both forms."""
+    w, xb = synth.gemm_case(m, n, k, seed=m + 3)
+    wd, xd = to_dev(w, torch), bf16_tensor(xb, torch)
+    y = qmm.gemm("q4_0", wd, xd, n, k, workspace=_ws(qmm, n, k))
+    y3 = _prefill(qmm, wd, xd, m, n, k)
+    torch.cuda.synchronize()
+    assert qmm.qmm_get_device_error() == 0
+    assert torch.equal(y, y3)
+    if form == "two":
+        assert torch.equal(y, qmm.gemm("q4_0", wd, xd, n, k))
+    rng = np.random.default_rng(m)
+    mi = np.concatenate([rng.integers(0, m, 1500), [0, m - 1, m - 1]])
+    ni = np.concatenate([rng.integers(0, n, 1500), [n - 1, 0, n - 1]])
+    y_ref, bound = oracle_mod.gemm_q4_0_at(w, xb, m, n, k, mi, ni)
+    assert_within(y.cpu().numpy()[mi, ni], y_ref, bound, GEMM_REL, f"{form} {m}x{n}x{k}")
 
 
 def test_workspace_argument_checks(qmm):
@@ -131,7 +188,7 @@ def _prefill(qmm, w, x, m, n, k):
     return y
 
 
-@pytest.mark.parametrize("m,n,k", [(600, 260, 512), (1024, 384, 2048), (200, 512, 512), (300, 256, 4096)])
+@pytest.mark.parametrize("m,n,k", [(600, 260, 512), (1024, 384, 2048), (200, 512, 512), (1100, 256, 4096)])
 def test_prefill_static_scratch_equals_fused(qmm, oracle_mod, m, n, k):
     w, xb = synth.gemm_case(m, n, k, seed=m + 1)
     wd, xd = to_dev(w, torch), bf16_tensor(xb, torch)
@@ -143,8 +200,9 @@ def test_prefill_static_scratch_equals_fused(qmm, oracle_mod, m, n, k):
 
 def test_prefill_static_scratch_column_chunks(qmm, oracle_mod):
     """K = 16384: the 64 MB scratch holds 2048 weight rows, so N = 5000 runs
-    as three column chunks (2048, 2048, 904) written with the full row stride."""
-    m, n, k = 300, 5000, 16384
+    as three column chunks (2048, 2048, 904) written with the full row stride
+    (600 tokens: 60 pair tiles, too many for a K split, so two phases)."""
+    m, n, k = 600, 5000, 16384
     w, xb = synth.gemm_case(m, n, k, seed=77)
     wd, xd = to_dev(w, torch), bf16_tensor(xb, torch)
     y = _prefill(qmm, wd, xd, m, n, k)

@@ -51,8 +51,9 @@ def _with_workspace(qmm, wd, xd, m, n, k):
 def test_prefill_without_workspace_two_calls_in_a_row(qmm, oracle_mod):
     # (m, n, k): one chunk at K = 2048, then K = 131072 (the largest the
     # scratch takes: 256 weight rows per chunk), N = 600 in chunks of 256,
-    # 256 and 88 rows, over what the first call left in the scratch
-    calls = [(700, 1000, 2048, 11), (300, 600, 131072, 12)]
+    # 256 and 88 rows, over what the first call left in the scratch; both in
+    # two phases (1100 tokens: five token blocks)
+    calls = [(700, 1000, 2048, 11), (1100, 600, 131072, 12)]
     for i, (m, n, k, seed) in enumerate(calls):
         w, xb = synth.gemm_case(m, n, k, seed=seed)
         wd, xd = to_dev(w, torch), bf16_tensor(xb, torch)
@@ -66,8 +67,16 @@ def test_prefill_without_workspace_two_calls_in_a_row(qmm, oracle_mod):
         assert qmm.qmm_get_device_error() == 0
         if i > 0:  # warmed up: the call itself takes no device memory
             assert free_before - free_after < (1 << 20), (free_before, free_after)
-        y_ref, bound = oracle_mod.gemm_q4_0(w, xb, m, n, k)
-        y_np, y_ws_np = y.cpu().numpy(), y_ws.cpu().numpy()
+        # the oracle on every output of the first call, on a sample of the
+        # second (every chunk's first and last rows included)
+        rng = np.random.default_rng(i)
+        if i == 0:
+            mi, ni = np.divmod(np.arange(m * n), n)
+        else:
+            mi = np.concatenate([rng.integers(0, m, 3000), [0, m - 1, 5, 9, m - 1]])
+            ni = np.concatenate([rng.integers(0, n, 3000), [0, 255, 256, 511, 599]])
+        y_ref, bound = oracle_mod.gemm_q4_0_at(w, xb, m, n, k, mi, ni)
+        y_np, y_ws_np = y.cpu().numpy()[mi, ni], y_ws.cpu().numpy()[mi, ni]
         # against the workspace entry point, in the GEMM tolerance ...
         lim = GEMM_REL * bound + ABS
         diff = np.abs(y_np.astype(np.float64) - y_ws_np)
