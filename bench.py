@@ -17,7 +17,9 @@ and throttle reasons are sampled with nvidia-smi during the timed region.
 
 `e2e` repeats the step through the public API with host buffers: each step
 copies its activations from pinned host memory, runs the step's calls and
-copies the outputs back (weights stay resident: they are the model).
+copies the outputs back (weights stay resident: they are the model).  The
+copies are the library's qmm_copy launches; the same with cudaMemcpyAsync
+copies is reported beside it.
 
 `--impl reference` times the CPU oracle (the plain C definition) on the
 box's host cores, on a bounded sample of the same workload.
@@ -490,7 +492,8 @@ class DecodeLayer:
         self.pos = k % self.R
 
 
-def measure_e2e(torch, qmm, layer: DecodeLayer, steps: int, dist, graphs: bool):
+def measure_e2e(torch, qmm, layer: DecodeLayer, steps: int, dist, graphs: bool,
+                copy_engine: bool = False):
     """The step through the public C ABI with host buffers: pinned host x ->
     device, the step's four calls, device y -> pinned host, every step; the
     weights stay resident (they are the model).  The step's activations (and
@@ -500,7 +503,11 @@ def measure_e2e(torch, qmm, layer: DecodeLayer, steps: int, dist, graphs: bool):
     Python.  graphs=True: each step replays a CUDA graph captured from those
     same copies and calls (one graph per weight replica), as a decode loop
     that captures its layer once would run it.  Host wall clock over all
-    steps, synchronised at both ends."""
+    steps, synchronised at both ends.
+
+    The copies are the library's qmm_copy launches (the SMs read and write
+    the pinned host buffers); copy_engine=True makes them cudaMemcpyAsync
+    transfers instead (torch's non-blocking copy_), for comparison."""
     x_host = layer.X_flat.cpu().pin_memory()
     y_host = torch.empty(layer.Y_flat.shape, dtype=torch.float32).pin_memory()
     h2d = x_host.numel() * 4
@@ -509,9 +516,15 @@ def measure_e2e(torch, qmm, layer: DecodeLayer, steps: int, dist, graphs: bool):
 
     def one(r):
         with torch.cuda.stream(s):
-            layer.X_flat.copy_(x_host, non_blocking=True)
+            if copy_engine:
+                layer.X_flat.copy_(x_host, non_blocking=True)
+            else:
+                qmm.qmm_copy(layer.X_flat, x_host, h2d, s)
             layer.step(r)
-            y_host.copy_(layer.Y_flat, non_blocking=True)
+            if copy_engine:
+                y_host.copy_(layer.Y_flat, non_blocking=True)
+            else:
+                qmm.qmm_copy(y_host, layer.Y_flat, d2h, s)
 
     if graphs:
         gs = [capture(torch, s, lambda r=r: one(r)) for r in range(layer.R)]
@@ -934,6 +947,8 @@ def run_ours(args, dist):
     e2e_value = aggregate(layer.step_bytes * e2e_steps, dist.max(e2e_el), dist.world) / 1e9
     e2e_el_d, _, _ = measure_e2e(torch, qmm, layer, e2e_steps, dist, graphs=False)
     e2e_direct = aggregate(layer.step_bytes * e2e_steps, dist.max(e2e_el_d), dist.world) / 1e9
+    e2e_el_ce, _, _ = measure_e2e(torch, qmm, layer, e2e_steps, dist, graphs=True, copy_engine=True)
+    e2e_ce = aggregate(layer.step_bytes * e2e_steps, dist.max(e2e_el_ce), dist.world) / 1e9
     step_bytes, launches_per_step, R = layer.step_bytes, layer.launches_per_step, layer.R
     del layer
     torch.cuda.empty_cache()
@@ -994,12 +1009,15 @@ def run_ours(args, dist):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps,
                 "path": "per step: pinned host x (the step's activations, one buffer) -> device "
-                        "in one copy, the step's 4 C-ABI calls, the 7 outputs -> pinned host in "
-                        "one copy; each step replays a CUDA graph captured from those copies and "
-                        "ctypes calls (one per weight replica); host wall clock",
+                        "in one qmm_copy launch, the step's 4 C-ABI calls, the 7 outputs -> "
+                        "pinned host in one qmm_copy launch; each step replays a CUDA graph "
+                        "captured from those calls (one per weight replica); host wall clock",
                 "direct_calls": {"value": round(e2e_direct, 2), "unit": "GB/s",
                                  "path": "the same copies and calls issued from Python every "
-                                         "step (no graph): host-bound"}},
+                                         "step (no graph): host-bound"},
+                "copy_engine": {"value": round(e2e_ce, 2), "unit": "GB/s",
+                                "path": "as `path`, with the two copies made by cudaMemcpyAsync "
+                                        "(torch non-blocking copy_) instead of qmm_copy"}},
         "gpu_launches": args.steps * launches_per_step,
     }
     if not args.no_secondary and dist.rank == 0:

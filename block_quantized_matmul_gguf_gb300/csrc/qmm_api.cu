@@ -122,6 +122,30 @@ qmm_status gemv(Fmt fmt, const qmm_gemv_out *outs, int count, const float *x, in
                                  reinterpret_cast<cudaStream_t>(stream), ctx));
 }
 
+// Memory a kernel on the current device may read and write at address p:
+// that device's memory, managed memory, or page-locked host memory mapped
+// at its host address.  Pageable host memory is refused (a kernel access
+// to it would fault).
+bool device_accessible(const void *p) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        (void)cudaGetLastError();  // the failed query is not a launch error: clear it
+        return false;
+    }
+    switch (a.type) {
+    case cudaMemoryTypeDevice:
+        return a.device == dev;
+    case cudaMemoryTypeManaged:
+        return true;
+    case cudaMemoryTypeHost:
+        return a.devicePointer == p;
+    default:
+        return false;
+    }
+}
+
 qmm_status check_workspace(const void *ws, size_t ws_bytes, size_t need) {
     if (!aligned(ws, 16)) return QMM_ERR_ALIGN;
     if (ws_bytes < need) return QMM_ERR_SHAPE;
@@ -243,6 +267,16 @@ qmm_status qmm_dequant_q4_0(const void *w, float *out, int64_t n, int64_t k,
 qmm_status qmm_dequant_q8_0(const void *w, float *out, int64_t n, int64_t k,
                             qmm_stream_t stream) {
     return dequant(Fmt::Q8_0, w, out, n, k, stream);
+}
+
+qmm_status qmm_copy(void *dst, const void *src, size_t bytes, qmm_stream_t stream) {
+    if (bytes == 0) return QMM_OK;
+    if (!dst || !src) return QMM_ERR_NULL;
+    if (overlaps(dst, bytes, src, bytes)) return QMM_ERR_UNSUPPORTED;
+    if (!device_accessible(src) || !device_accessible(dst)) return QMM_ERR_UNSUPPORTED;
+    cudaError_t e;
+    if (!device_state(&e)) return QMM_ERR_CUDA;  // the SM count for the grid
+    return from_cuda(launch_copy(dst, src, bytes, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 qmm_status qmm_gemv_q4_0(const void *w, const float *x, float *y, int m, int64_t n, int64_t k,
@@ -407,7 +441,7 @@ const char *qmm_status_string(qmm_status status) {
     return "unknown status";
 }
 
-int qmm_version(void) { return 300; }
+int qmm_version(void) { return 400; }  // 0.4.0: qmm_copy added
 
 qmm_status qmm_get_device_error(qmm_stream_t stream) {
     cudaError_t e;

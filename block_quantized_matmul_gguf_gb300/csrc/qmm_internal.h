@@ -87,6 +87,11 @@ bool encode_tmap_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *bas
 cudaError_t launch_dequant(Fmt fmt, const uint8_t *w, float *out, int64_t n, int64_t k,
                            cudaStream_t stream, const LaunchCtx &ctx);
 
+// Stream-ordered copy of `bytes` bytes by the SMs; both pointers device
+// accessible (device memory, or page-locked host memory mapped at its host
+// address), the ranges disjoint.
+cudaError_t launch_copy(void *dst, const void *src, size_t bytes, cudaStream_t stream);
+
 // One weight matrix of a GEMV call: w (n rows of blocks) applied to the
 // call's shared activations, written to y [m][n].
 struct GemvProblem {

@@ -33,7 +33,7 @@ EXPORTED = (
     "qmm_gemm_q4_0", "qmm_gemm_q8_0", "qmm_gemm_q4_0_geglu",
     "qmm_gemm_q4_0_ws", "qmm_gemm_q8_0_ws", "qmm_gemm_q4_0_geglu_ws", "qmm_gemm_q4_0_prefill",
     "qmm_gemm_workspace_bytes", "qmm_gemm_geglu_workspace_bytes", "qmm_status_string", "qmm_version", "qmm_get_device_error",
-    "qmm_set_wait_timeout_ns", "qmm_selftest_wait_timeout",
+    "qmm_set_wait_timeout_ns", "qmm_selftest_wait_timeout", "qmm_copy",
 )
 
 
@@ -86,6 +86,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         "qmm_gemv_q8_0_multi": [ctypes.POINTER(GemvOut), I32, P, I32, I64, P],
         "qmm_get_device_error": [P],
         "qmm_selftest_wait_timeout": [U64, P],
+        "qmm_copy": [P, P, SZ, P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -146,6 +147,24 @@ def qmm_dequant_q4_0(w, out, n: int, k: int, stream=None) -> None:
 def qmm_dequant_q8_0(w, out, n: int, k: int, stream=None) -> None:
     _check(load().qmm_dequant_q8_0(_ptr(w), _ptr(out), n, k, _stream(stream)),
            "qmm_dequant_q8_0")
+
+
+def _ptr_pinned_ok(t) -> int:
+    """Like _ptr, but a page-locked host tensor is accepted too."""
+    if t is None or isinstance(t, int) or t.is_cuda:
+        return _ptr(t)
+    if not t.is_pinned():
+        raise ValueError("host tensor must be page-locked (pin_memory())")
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return t.data_ptr()
+
+
+def qmm_copy(dst, src, nbytes: int, stream=None) -> None:
+    """Stream-ordered copy by the SMs; dst and src are device memory or
+    page-locked host memory."""
+    _check(load().qmm_copy(_ptr_pinned_ok(dst), _ptr_pinned_ok(src), int(nbytes),
+                           _stream(stream)), "qmm_copy")
 
 
 def qmm_gemv_q4_0(w, x, y, m: int, n: int, k: int, stream=None) -> None:

@@ -277,6 +277,29 @@ qmm_status qmm_gemm_q4_0_geglu_ws(const void *wg, const void *wu, const uint16_t
                                   uint16_t *h_bf16, int64_t m, int64_t n, int64_t k,
                                   void *workspace, size_t workspace_bytes, qmm_stream_t stream);
 
+/* ---- Stream-ordered copies by the SMs ----------------------------------
+ * Copies `bytes` bytes from src to dst in stream order, as one kernel launch
+ * that loads and stores through the device's address space.  The pages have
+ * no counterpart of this entry point: it exists for the end-to-end decode
+ * step, whose activations go in and whose outputs come out every step (a
+ * few tens of kilobytes).  There a copy-engine transfer (cudaMemcpyAsync)
+ * costs several microseconds whatever its size, while this launch overlaps
+ * its start with its neighbours like the GEMV launches do.
+ * src, dst : device memory of the current device, or page-locked host memory
+ *            mapped into the device's address space at its host address
+ *            (cudaHostAlloc / cudaMallocHost memory under unified
+ *            addressing, which is how PyTorch's pin_memory allocates); each
+ *            holds `bytes` bytes; any alignment (16-byte aligned pointers
+ *            move 16 bytes per access).  Checked with cudaPointerGetAttributes
+ *            before anything is launched: other memory (pageable host memory,
+ *            another device's memory) returns QMM_ERR_UNSUPPORTED.
+ * Overlapping ranges return QMM_ERR_UNSUPPORTED; bytes == 0 launches
+ * nothing and returns QMM_OK.  The copy is complete, and host memory
+ * written by it visible to the host, once the stream has been synchronised.
+ * It waits for the previous launch on the stream before reading src or
+ * writing dst, so it may read that launch's output or overwrite its input. */
+qmm_status qmm_copy(void *dst, const void *src, size_t bytes, qmm_stream_t stream);
+
 /* ---- Utilities --------------------------------------------------------- */
 
 /* Static English text for a status code (never NULL). */

@@ -63,6 +63,22 @@ def test_status_strings_and_version(lib):
     assert qmm.qmm_version() >= 100
 
 
+def test_copy_argument_checks(lib):
+    """qmm_copy: nothing to copy is OK; a null pointer, overlapping ranges and
+    pageable host memory (a kernel access to it would fault) are refused
+    before any launch."""
+    import numpy as np
+    a = np.zeros(64, np.uint8)
+    b = np.ones(64, np.uint8)
+    L = lib
+    assert L.qmm_copy(None, None, 0, None) == qmm.QMM_OK
+    assert L.qmm_copy(None, b.ctypes.data, 16, None) == qmm.QMM_ERR_NULL
+    assert L.qmm_copy(a.ctypes.data, None, 16, None) == qmm.QMM_ERR_NULL
+    assert L.qmm_copy(b.ctypes.data + 8, b.ctypes.data, 16, None) == qmm.QMM_ERR_UNSUPPORTED
+    assert L.qmm_copy(a.ctypes.data, b.ctypes.data, 64, None) == qmm.QMM_ERR_UNSUPPORTED
+    assert (a == 0).all()
+
+
 def test_null_and_shape_errors_return_before_any_launch(lib):
     L = lib
     assert L.qmm_gemv_q4_0(0, 16, 16, 1, 32, 64, 0) == qmm.QMM_ERR_NULL
