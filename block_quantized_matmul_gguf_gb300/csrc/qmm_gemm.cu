@@ -88,6 +88,9 @@ constexpr int LOOKAHEAD_KK = QMM_GEMM_LOOKAHEAD_KK;
 constexpr int GROUP = QMM_GEMM_GROUP;
 constexpr int NGROUPS = STAGES / GROUP;
 static_assert(STAGES % GROUP == 0, "whole groups in the ring");
+// the MMA thread waits for the next group's first stage while the current
+// group's slots are still held: one group in the ring would wait forever
+static_assert(NGROUPS >= 2, "at least two groups in the ring");
 static_assert((256 / BK) % GROUP == 0, "k % 256 == 0 makes every tile a whole number of groups");
 constexpr int X_STAGE_BYTES = BT_CTA * BK * 2;           // 16 KB
 
@@ -603,9 +606,15 @@ __global__ void __launch_bounds__(256) splitk_sum_kernel(const float *__restrict
 
 // K parts for a plain GEMM whose tiles leave most pairs idle: the split (1,
 // 2, 4 or 8, dividing the raw stages) that best fills the pairs, if its
-// partial products fit `part_bytes` and it fills them clearly better than no
-// split.  An item of a split tile is its K part (fewer stages, same work per
-// stage), so the fill is the share of pair rounds that are busy.
+// partial products fit `part_bytes`, each part keeps at least four raw stages
+// (1024 of K), all its items run in one round, and it fills the pairs
+// clearly better than no split.  Shorter parts do not pay back the second
+// pass: at 256 x 8192 x 1024 two parts of two stages took 15.9 us against
+// 14.0 unsplit.  An item of a split tile is
+// its K part (fewer stages, same work per stage), so the fill is the share of
+// pair rounds that are busy.  Splits over several rounds would only trim the
+// last round's idle pairs, for twice the partial-product traffic: at
+// 512 x 8192 x 8192 eight parts took 101 us against 61 us unsplit.
 int choose_ksplit(int64_t m, int64_t n, int64_t k, int num_tiles, int pairs, size_t part_bytes) {
     if (num_tiles >= pairs) return 1;
     auto fill = [&](int ks) {
@@ -616,7 +625,9 @@ int choose_ksplit(int64_t m, int64_t n, int64_t k, int num_tiles, int pairs, siz
     int best = 1;
     double best_fill = fill(1);
     for (int ks = 2; ks <= 8; ks *= 2) {
-        if ((k / RAW_K) % ks != 0) break;
+        if ((k / RAW_K) % ks != 0 || (k / RAW_K) / ks < 4 ||
+            static_cast<int64_t>(num_tiles) * ks > pairs)
+            break;
         if (static_cast<size_t>(ks) * static_cast<size_t>(m) * static_cast<size_t>(n) * sizeof(float) > part_bytes)
             break;
         const double f = fill(ks);
@@ -699,9 +710,8 @@ int gemm_fused_ksplit(int64_t m, int64_t n, int64_t k, size_t part_bytes) {
 
 bool use_two_phase_gemm(int64_t m, int64_t n, int64_t k) {
     const int64_t blocks = (m + BT - 1) / BT;
-    if (blocks <= 1) return false;
-    if (blocks <= 4 && gemm_fused_ksplit(m, n, k, fused_part_budget(n, k)) > 1) return false;
-    return blocks >= 3 || k >= 8192;
+    if (blocks <= 2) return false;
+    return !(blocks <= 4 && gemm_fused_ksplit(m, n, k, fused_part_budget(n, k)) > 1);
 }
 
 cudaError_t launch_gemm_q4_0(const uint8_t *w, const uint16_t *x, float *y, int64_t m, int64_t n,

@@ -180,15 +180,15 @@ size_t fused_part_budget(int64_t n, int64_t k);
 // N x K = 2048 x 8192, 8192 x 2048, 16384 x 2048, 4096 x 4096 and
 // 8192 x 8192 for m = 256..2048.  The dequant pass costs about 0.65 us per
 // million weights; the fused kernel decodes the weights again for every
-// 256-token block, and a product whose pair tiles fill under half the pairs
-// runs the fused kernel with a K split instead.  So: never for one token
-// block; not for up to four blocks when the fused kernel splits K (the
-// two-phase GEMM has as few tiles and K times longer ones); otherwise from
-// the third block, or from the second at K >= 8192.
+// 256-token block, and a product whose pair tiles leave pairs idle runs the
+// fused kernel with a K split instead.  So: never for one or two token
+// blocks; not for three or four blocks when the fused kernel splits K (the
+// two-phase GEMM has as few tiles, each running all of K); otherwise always.
 bool use_two_phase_gemm(int64_t m, int64_t n, int64_t k);
 
 // The GeGLU form has no K split: two phases from the third token block, or
-// from the second at K >= 4096.
+// from the second at K >= 4096 (where the unsplit fused kernel's few tiles
+// run all of a long K).
 inline bool use_two_phase_geglu(int64_t m, int64_t k) { return m > 512 || (m > 256 && k >= 4096); }
 
 // Two-phase prefill GEMM (weights dequantised once into a bf16 workspace,

@@ -202,10 +202,10 @@ qmm_status qmm_gemm_q8_0(const void *w, const uint16_t *x_bf16, float *y, int64_
  *     them in part order.  Split results differ from qmm_gemm_q4_0's by
  *     rounding only (same bound) and are the same for every workspace of a
  *     call's shape.
- * Two phases are taken from the third 256-token block on (m > 512), or
- * from the second at k >= 8192, except that up to four blocks (m <= 1024)
- * stay in one phase when the fused call splits K there.  For the GeGLU
- * form (no K split): two phases when m > 512, or m > 256 with k >= 4096.
+ * Two phases are taken from the third 256-token block on (m > 512), except
+ * that three or four blocks (m <= 1024) stay in one phase when the fused
+ * call splits K there.  For the GeGLU form (no K split): two phases when
+ * m > 512, or m > 256 with k >= 4096.
  * workspace : caller-owned device memory, 16-byte aligned, at least
  *             qmm_gemm_workspace_bytes(n, k) bytes (qmm_gemm_geglu_
  *             workspace_bytes for the GeGLU form), not overlapping any

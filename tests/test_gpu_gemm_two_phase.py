@@ -36,8 +36,8 @@ def _weights(fmt, n, k, seed, stream=0):
 
 @pytest.mark.parametrize("fmt", ["q4_0", "q8_0"])
 # two phases from the third 256-token block on when the fused kernel would
-# not split K (its partial products would not fit, or K has one raw stage),
-# and from the fifth block in any case
+# not split K (its partial products would not fit, or K is too short), and
+# from the fifth block in any case
 @pytest.mark.parametrize("m,n,k", [(520, 4, 256), (600, 260, 512), (513, 768, 1024),
                                    (700, 1000, 256), (1024, 384, 2048), (1100, 136, 4096)])
 def test_two_phase_matches_oracle_and_fused(qmm, oracle_mod, fmt, m, n, k):
@@ -98,9 +98,9 @@ def test_two_phase_geglu(qmm, oracle_mod, m, n, k):
 def test_short_prompt_with_a_workspace(qmm, oracle_mod, m, n, k):
     """Short prompts run the fused kernel; where its tiles leave the GPU idle
     they split K through the workspace (512 x 2048 at m = 512: 2 parts;
-    512 x 4096 at m = 256: 8 parts; 512 x 512: the parts would not fit the
-    workspace, so no split).  Same bound as the unsplit product, identical to
-    the static-scratch entry, deterministic."""
+    512 x 4096 at m = 256: 4 parts; 512 x 512: two raw stages, too few to
+    split).  Same bound as the unsplit product, identical to the
+    static-scratch entry, deterministic."""
     w, xb = synth.gemm_case(m, n, k, seed=9)
     wd, xd = to_dev(w, torch), bf16_tensor(xb, torch)
     ws = _ws(qmm, n, k)
@@ -120,7 +120,7 @@ def test_short_prompt_with_a_workspace(qmm, oracle_mod, m, n, k):
                                        ("q4_0", 1, 4096, 2048), ("q4_0", 128, 300, 1280)])
 def test_short_prompt_k_split(qmm, oracle_mod, fmt, m, n, k):
     """K split for short prompts (8 parts at 256 x 2048 x 8192, 2 at
-    256 x 8192 x 2048, 8 with ragged tokens and rows, 4 for Q8_0, 4 at one
+    256 x 8192 x 2048, 4 with ragged tokens and rows, 2 for Q8_0, 2 at one
     token; 1280 has five raw stages, so no split): every output against the
     oracle, and against the unsplit fused product within the same bound."""
     w = _weights(fmt, n, k, seed=m + n)
@@ -137,14 +137,15 @@ def test_short_prompt_k_split(qmm, oracle_mod, fmt, m, n, k):
 
 
 @pytest.mark.parametrize("m,n,k,form", [(1024, 2048, 8192, "split"), (600, 2048, 8192, "split"),
-                                        (768, 4096, 4096, "two"), (384, 8192, 8192, "two")])
+                                        (768, 4096, 4096, "two"), (384, 8192, 8192, "fused")])
 def test_medium_prompt_form(qmm, oracle_mod, m, n, k, form):
     """Two to four token blocks: at 2048 x 8192 the fused kernel's 24-32 pair
     tiles split K in two (one phase, the workspace holds the parts); at
-    4096 x 4096 (48 tiles) and 8192 x 8192 (64 tiles) no split pays and the
-    product runs in two phases, with the fused kernel's bits.  Sampled
-    outputs against the oracle; the static-scratch entry gives the same bits
-    as the workspace entry in both forms."""
+    4096 x 4096 with three blocks (48 tiles) no split fits one round and the
+    product runs in two phases; 8192 x 8192 with two blocks runs the fused
+    kernel unsplit.  The last two give the workspace-free fused call's bits.
+    Sampled outputs against the oracle; the static-scratch entry gives the
+    same bits as the workspace entry in every form."""
     w, xb = synth.gemm_case(m, n, k, seed=m + 3)
     wd, xd = to_dev(w, torch), bf16_tensor(xb, torch)
     y = qmm.gemm("q4_0", wd, xd, n, k, workspace=_ws(qmm, n, k))
@@ -152,7 +153,7 @@ def test_medium_prompt_form(qmm, oracle_mod, m, n, k, form):
     torch.cuda.synchronize()
     assert qmm.qmm_get_device_error() == 0
     assert torch.equal(y, y3)
-    if form == "two":
+    if form != "split":
         assert torch.equal(y, qmm.gemm("q4_0", wd, xd, n, k))
     rng = np.random.default_rng(m)
     mi = np.concatenate([rng.integers(0, m, 1500), [0, m - 1, m - 1]])
