@@ -18,7 +18,7 @@
 //    into rank 0's activation slice with remote stores once every rank is
 //    done reading activations, then added in rank order by all of rank 0's
 //    threads).  No global scratch; the summation order is fixed.
-//  * Q4_0 at M >= 10 (the FMA pipe, not the loads, bounds it): the row-pair
+//  * Q4_0 at M >= 11 (the FMA pipe, not the loads, bounds it): the row-pair
 //    form, four rows per lane, two lanes per row, two rows per packed FMA and
 //    the block scale folded into the weights (q4_0_chunk_rp).
 //  * A warp streams its chunks through its own ring of shared-memory stages.
@@ -81,7 +81,7 @@
 #define QMM_GEMV_R_SMALL 1        // rows per lane for the small (two lanes per row) case
 #endif
 #ifndef QMM_GEMV_RP_MIN_M
-#define QMM_GEMV_RP_MIN_M 10      // Q4_0: smallest M that takes the row-pair form
+#define QMM_GEMV_RP_MIN_M 11      // Q4_0: smallest M that takes the row-pair form
 #endif
 #ifndef QMM_GEMV_RP_L
 #define QMM_GEMV_RP_L 2           // row-pair form: lanes per row (each half of the qs words)

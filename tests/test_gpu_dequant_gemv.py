@@ -165,7 +165,7 @@ def test_gemv_deterministic(qmm, m):
 
 
 @pytest.mark.parametrize("cols", [[0, 17, 255, 256, 1023],
-                                  # 12 rows of x: the row-pair form (M >= 10)
+                                  # 12 rows of x: the row-pair form (M >= 11)
                                   [0, 1, 2, 3, 4, 15, 16, 19, 31, 511, 512, 1023]])
 def test_gemv_one_hot_equals_dequant(qmm, cols):
     """x = e_c gives the dequantized column exactly (both on the GPU)."""
@@ -344,11 +344,11 @@ def test_gemv_wide_m_two_rows_per_lane_and_its_fallback(qmm, oracle_mod, fmt, m,
     assert_within(_run_gemv(qmm, fmt, case), y_ref, bound, GEMV_REL, f"{fmt} {m}x{n}x{k}")
 
 
-@pytest.mark.parametrize("m,n,k", [(10, 200, 2048), (13, 1000, 4096), (16, 70, 8192), (11, 3000, 256),
-                                   (16, 130, 16384), (10, 16384, 16384), (16, 130, 32768),
+@pytest.mark.parametrize("m,n,k", [(11, 200, 2048), (13, 1000, 4096), (16, 70, 8192), (11, 3000, 256),
+                                   (16, 130, 16384), (11, 16384, 16384), (16, 130, 32768),
                                    (11, 256, 18432)])
 def test_gemv_row_pairs_and_their_fallback(qmm, oracle_mod, m, n, k):
-    """Q4_0 at M >= 10 packs two weight rows into each FMA with the block scale
+    """Q4_0 at M >= 11 packs two weight rows into each FMA with the block scale
     folded into the weights: ragged 64-row tiles, cluster splits (up to 8 x 8
     K parts at 130 x 16384), several tiles per launch, and 16384 x 16384, where
     each accumulator sums the most products the form allows (8 chunks, 1024

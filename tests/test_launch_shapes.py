@@ -54,7 +54,7 @@ def test_byte_wise_fallback_only_for_very_large_k(report):
 
 
 def test_row_pair_form_refused_only_for_large_k(report):
-    """Q4_0 at M >= 10 leaves the row-pair form (for the per-block forms) only
+    """Q4_0 at M >= 11 leaves the row-pair form (for the per-block forms) only
     where a lane's K share would pass 1024 products (4 chunks per lane at two
     lanes a row: 8 chunks) or shared memory does not fit: K >= 16384, or a
     chunk count with an odd factor of 9 or more (K parts are powers of two).
@@ -64,5 +64,5 @@ def test_row_pair_form_refused_only_for_large_k(report):
     for fmt, m, l, r, k, n in refused:
         chunks = int(k) // 256
         odd = chunks // (chunks & -chunks)
-        assert fmt == "q4_0" and int(m) >= 10 and (int(k) >= 16384 or odd >= 9), (fmt, m, l, r, k, n)
+        assert fmt == "q4_0" and int(m) >= 11 and (int(k) >= 16384 or odd >= 9), (fmt, m, l, r, k, n)
     assert "ROWPAIR_REFUSED q4_0 M=16" in out  # K = 2^20 cannot fit
