@@ -208,13 +208,6 @@ __device__ __forceinline__ void load_portion(const uint8_t *src, uint32_t (&wd)[
     }
 }
 
-// Independent FMA chains per output row: at small M the rows alone do not
-// give the scheduler enough independent work, so each block's sum is split.
-template <int ROWS>
-struct Chains {
-    static constexpr int value = ROWS <= 2 ? 4 : (ROWS <= 4 ? 2 : 1);
-};
-
 // R rows' shares (8/L consecutive Q4_0 blocks, 144/L bytes each; row j at
 // src + j*rstride) of a row chunk, against activations `xk` in shared memory
 // (position 0 of the share for activation row 0; rows XS apart).  Each
@@ -223,10 +216,15 @@ struct Chains {
 // A qs word v holds weights 4i..4i+3 (low nibbles, bits 0,8,16,24) and
 // 16+4i..19+4i (high nibbles, bits 4,12,20,28); bits 0-19 are used in place
 // and bits 20-31 after u = v >> 16, so the nibble sits at s in {0,4,8,12,16}.
+//
+// Each block's sum runs as one packed FMA chain per row and token: splitting
+// it into 2-4 independent chains (as at first, for latency) measured slower
+// once the kernels were issue-bound (decode step 18.64 -> 18.03 us, Q8_0 LM
+// head 97.3 -> 93.0 us, M = 2 at 8192 x 2048 5.12 -> 4.76 us with one chain):
+// merging the chains cost more instructions than their overlap hid.
 template <int M, int L, int R>
 __device__ __forceinline__ void q4_0_chunk(const uint8_t *src, int rstride, const float *xk,
                                            int XS, uint32_t magic, float (&tot)[R][M]) {
-    constexpr int CH = Chains<M * R>::value;
     constexpr int NB = 8 / L;
     uint32_t wd[R][36 / L];
 #pragma unroll
@@ -255,13 +253,11 @@ __device__ __forceinline__ void q4_0_chunk(const uint8_t *src, int rstride, cons
             }
             d[j] = half_bits_to_float(dbits);
         }
-        float2 acc[R][M][CH];
+        float2 acc[R][M];
 #pragma unroll
         for (int j = 0; j < R; ++j)
 #pragma unroll
-            for (int m = 0; m < M; ++m)
-#pragma unroll
-                for (int c = 0; c < CH; ++c) acc[j][m][c] = f2(0.0f, 0.0f);
+            for (int m = 0; m < M; ++m) acc[j][m] = f2(0.0f, 0.0f);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             float4 xa[M], xb[M];
@@ -270,7 +266,6 @@ __device__ __forceinline__ void q4_0_chunk(const uint8_t *src, int rstride, cons
                 xa[m] = lds128f(xk + m * XS + 32 * b + 4 * i);
                 xb[m] = lds128f(xk + m * XS + 32 * b + 16 + 4 * i);
             }
-            const int c = i % CH;
 #pragma unroll
             for (int j = 0; j < R; ++j) {
                 const uint32_t v = q[j][i], u = v >> 16;
@@ -280,32 +275,27 @@ __device__ __forceinline__ void q4_0_chunk(const uint8_t *src, int rstride, cons
                 const float2 p67 = __ffma2_rn(f2(mag(u, 0x000000F0u, magic), mag(u, 0x0000F000u, magic)), s45, b45);
 #pragma unroll
                 for (int m = 0; m < M; ++m) {
-                    acc[j][m][c] = __ffma2_rn(p01, f2(xa[m].x, xa[m].y), acc[j][m][c]);
-                    acc[j][m][c] = __ffma2_rn(p23, f2(xa[m].z, xa[m].w), acc[j][m][c]);
-                    acc[j][m][c] = __ffma2_rn(p45, f2(xb[m].x, xb[m].y), acc[j][m][c]);
-                    acc[j][m][c] = __ffma2_rn(p67, f2(xb[m].z, xb[m].w), acc[j][m][c]);
+                    acc[j][m] = __ffma2_rn(p01, f2(xa[m].x, xa[m].y), acc[j][m]);
+                    acc[j][m] = __ffma2_rn(p23, f2(xa[m].z, xa[m].w), acc[j][m]);
+                    acc[j][m] = __ffma2_rn(p45, f2(xb[m].x, xb[m].y), acc[j][m]);
+                    acc[j][m] = __ffma2_rn(p67, f2(xb[m].z, xb[m].w), acc[j][m]);
                 }
             }
         }
 #pragma unroll
         for (int j = 0; j < R; ++j)
 #pragma unroll
-            for (int m = 0; m < M; ++m) {
-                float2 a = acc[j][m][0];
-#pragma unroll
-                for (int c = 1; c < CH; ++c) a = __fadd2_rn(a, acc[j][m][c]);
-                tot[j][m] = fmaf(d[j], a.x + a.y, tot[j][m]);
-            }
+            for (int m = 0; m < M; ++m) tot[j][m] = fmaf(d[j], acc[j][m].x + acc[j][m].y, tot[j][m]);
     }
 }
 
 // R rows' shares (8/L consecutive Q8_0 blocks, 272/L bytes each) of a row
 // chunk.  Bytes 0 and 2 of a word are used at bits 0-7 (s = 0), bytes 1 and
-// 3 at bits 8-15 (s = 8).
+// 3 at bits 8-15 (s = 8).  One FMA chain per block, row and token, as in
+// q4_0_chunk.
 template <int M, int L, int R>
 __device__ __forceinline__ void q8_0_chunk(const uint8_t *src, int rstride, const float *xk,
                                            int XS, uint32_t magic, float (&tot)[R][M]) {
-    constexpr int CH = Chains<M * R>::value;
     constexpr int NB = 8 / L;
     uint32_t wd[R][68 / L];
 #pragma unroll
@@ -323,19 +313,16 @@ __device__ __forceinline__ void q8_0_chunk(const uint8_t *src, int rstride, cons
 #pragma unroll
         for (int j = 0; j < R; ++j)
             d[j] = half_bits_to_float((b & 1) == 0 ? (wd[j][base] & 0xFFFFu) : (wd[j][base] >> 16));
-        float2 acc[R][M][CH];
+        float2 acc[R][M];
 #pragma unroll
         for (int j = 0; j < R; ++j)
 #pragma unroll
-            for (int m = 0; m < M; ++m)
-#pragma unroll
-                for (int h = 0; h < CH; ++h) acc[j][m][h] = f2(0.0f, 0.0f);
+            for (int m = 0; m < M; ++m) acc[j][m] = f2(0.0f, 0.0f);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             float4 xa[M];
 #pragma unroll
             for (int m = 0; m < M; ++m) xa[m] = lds128f(xk + m * XS + 32 * b + 4 * i);
-            const int h = i % CH;
 #pragma unroll
             for (int j = 0; j < R; ++j) {
                 const uint32_t v = (b & 1) == 0 ? __byte_perm(wd[j][base + i], wd[j][base + i + 1], 0x5432)
@@ -347,20 +334,15 @@ __device__ __forceinline__ void q8_0_chunk(const uint8_t *src, int rstride, cons
                     f2(mag8(u, 0x000000FFu, mf0), mag8(u, 0x0000FF00u, mf1)), sc, bc);
 #pragma unroll
                 for (int m = 0; m < M; ++m) {
-                    acc[j][m][h] = __ffma2_rn(p01, f2(xa[m].x, xa[m].y), acc[j][m][h]);
-                    acc[j][m][h] = __ffma2_rn(p23, f2(xa[m].z, xa[m].w), acc[j][m][h]);
+                    acc[j][m] = __ffma2_rn(p01, f2(xa[m].x, xa[m].y), acc[j][m]);
+                    acc[j][m] = __ffma2_rn(p23, f2(xa[m].z, xa[m].w), acc[j][m]);
                 }
             }
         }
 #pragma unroll
         for (int j = 0; j < R; ++j)
 #pragma unroll
-            for (int m = 0; m < M; ++m) {
-                float2 a = acc[j][m][0];
-#pragma unroll
-                for (int h = 1; h < CH; ++h) a = __fadd2_rn(a, acc[j][m][h]);
-                tot[j][m] = fmaf(d[j], a.x + a.y, tot[j][m]);
-            }
+            for (int m = 0; m < M; ++m) tot[j][m] = fmaf(d[j], acc[j][m].x + acc[j][m].y, tot[j][m]);
     }
 }
 
