@@ -71,6 +71,7 @@
 #ifndef QMM_GEMV_L2_UNITS
 #define QMM_GEMV_L2_UNITS 1024    // (32-row tile x chunk) units up to which 2 lanes share a row
 #endif
+
 #ifndef QMM_GEMV_R2_MAX_M
 #define QMM_GEMV_R2_MAX_M 4       // largest M at which a lane owns two weight rows
 #endif
@@ -1366,6 +1367,20 @@ cudaError_t launch_persist(const GemvProblem &pr, const float *x, int64_t k, cud
     return launch_kernel(kern, dim3(static_cast<unsigned>(sms)), dim3(nw * 32), smem, stream, 1, map, p);
 }
 
+// Whether two lanes per row (QMM_GEMV_R_SMALL rows each) need a smaller
+// cluster split along K than one lane per row with two rows.
+template <Fmt F, int M>
+bool two_lanes_split_less(const GemvProblem *probs, int count, int64_t k) {
+    int64_t t1 = 0, t2 = 0;
+    for (int i = 0; i < count; ++i) {
+        t1 += (probs[i].n + 63) / 64;
+        t2 += (probs[i].n + 16 * QMM_GEMV_R_SMALL - 1) / (16 * QMM_GEMV_R_SMALL);
+    }
+    const int sms = device_sm_count();
+    return stream_shape<F, M, 2, QMM_GEMV_R_SMALL>(t2, k, sms).ksplit <
+           stream_shape<F, M, 1, 2>(t1, k, sms).ksplit;
+}
+
 template <Fmt F, int M, bool G = false>
 cudaError_t launch_m(const GemvProblem *probs, int count, const float *x, int64_t k,
                      cudaStream_t stream, const LaunchCtx &ctx) {
@@ -1415,6 +1430,14 @@ cudaError_t launch_m(const GemvProblem *probs, int count, const float *x, int64_
                 constexpr bool kPersist = F == Fmt::Q4_0 ? QMM_GEMV_PERSIST : QMM_GEMV_PERSIST_Q8_0;
                 e = count == 1 && kPersist ? launch_persist<F, M, 2>(probs[0], x, k, stream, ctx)
                                            : kShapeTooLarge;
+                // M = 1, few rows and a long K (2048 x 8192): two lanes a row give
+                // four times the tiles, so K spreads over clusters of 2 CTAs instead
+                // of 4 (5.97 -> 5.27 us).  Where both forms need the same cluster, one
+                // lane a row (two rows each) is faster (8192 x 2048: 3.99 against
+                // 4.57 us), and so it is at M = 2..4 on any shape (2048 x 8192 at
+                // M = 3: 6.85 against 10.43 us)
+                if (M == 1 && e == kShapeTooLarge && two_lanes_split_less<F, M>(probs, count, k))
+                    e = launch_stream<F, M, 2, QMM_GEMV_R_SMALL>(probs, count, x, k, stream, ctx);
                 if (e == kShapeTooLarge) e = launch_stream<F, M, 1, 2>(probs, count, x, k, stream, ctx);
             }
         } else {

@@ -386,3 +386,21 @@ def test_gemv_persistent_form_deterministic(qmm):
     b = qmm.gemv("q4_0", w, x, case.n, case.k)
     torch.cuda.synchronize()
     assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+@pytest.mark.parametrize("n,k", [(2048, 8192), (2000, 8192), (1000, 16384), (520, 32768), (3000, 4096)])
+def test_gemv_m1_long_k_two_lanes(qmm, oracle_mod, n, k):
+    """M = 1 with few rows and a long K: two lanes per row where that needs a
+    smaller cluster split than one lane per row (2048 x 8192: clusters of 2
+    instead of 4; ragged rows at 2000 and 520; K = 16384 and 32768), one lane
+    per row where both need the same (3000 x 4096).  Every output against
+    the oracle, and the same bits on a second call."""
+    case = synth.gemv_case("q4_0", 1, n, k, seed=n + k)
+    w, x = to_dev(case.w, torch), to_dev(case.x, torch)
+    a = qmm.gemv("q4_0", w, x, n, k)
+    b = qmm.gemv("q4_0", w, x, n, k)
+    torch.cuda.synchronize()
+    assert qmm.qmm_get_device_error() == 0
+    assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    y_ref, bound = _oracle_gemv(oracle_mod, "q4_0", case)
+    assert_within(a.cpu().numpy(), y_ref, bound, GEMV_REL, f"q4_0 1x{n}x{k}")
