@@ -493,7 +493,7 @@ class DecodeLayer:
 
 
 def measure_e2e(torch, qmm, layer: DecodeLayer, steps: int, dist, graphs: bool,
-                copy_engine: bool = False):
+                copy_engine: bool = False, rotation_graph: bool = False):
     """The step through the public C ABI with host buffers: pinned host x ->
     device, the step's four calls, device y -> pinned host, every step; the
     weights stay resident (they are the model).  The step's activations (and
@@ -507,7 +507,12 @@ def measure_e2e(torch, qmm, layer: DecodeLayer, steps: int, dist, graphs: bool,
 
     The copies are the library's qmm_copy launches (the SMs read and write
     the pinned host buffers); copy_engine=True makes them cudaMemcpyAsync
-    transfers instead (torch's non-blocking copy_), for comparison."""
+    transfers instead (torch's non-blocking copy_), for comparison.
+
+    rotation_graph=True (with graphs): one graph holds a whole rotation of R
+    consecutive steps, each still with its own copies in and out, as a decode
+    loop that captures all of a token's layers together would run them;
+    steps is rounded up to whole rotations."""
     x_host = layer.X_flat.cpu().pin_memory()
     y_host = torch.empty(layer.Y_flat.shape, dtype=torch.float32).pin_memory()
     h2d = x_host.numel() * 4
@@ -526,7 +531,15 @@ def measure_e2e(torch, qmm, layer: DecodeLayer, steps: int, dist, graphs: bool,
             else:
                 qmm.qmm_copy(y_host, layer.Y_flat, d2h, s)
 
-    if graphs:
+    if graphs and rotation_graph:
+        steps = -(-steps // layer.R) * layer.R
+        g_rot = capture(torch, s, lambda: [one(r) for r in range(layer.R)])
+        g_rot.replay()
+
+        def run(i):
+            if i % layer.R == 0:
+                g_rot.replay()
+    elif graphs:
         gs = [capture(torch, s, lambda r=r: one(r)) for r in range(layer.R)]
         for g in gs:
             g.replay()
@@ -547,7 +560,7 @@ def measure_e2e(torch, qmm, layer: DecodeLayer, steps: int, dist, graphs: bool,
     el = time.perf_counter() - t0
     if dist:
         dist.barrier()
-    return el, h2d, d2h
+    return el, h2d, d2h, steps
 
 
 def run_secondary(torch, qmm, l2, stream, timer, peaks, sms, only=None):
@@ -943,12 +956,15 @@ def run_ours(args, dist):
     step_achieved = layer.step_bytes / (el_max / args.steps) / 1e9
 
     e2e_steps = max(200, args.steps // 20)
-    e2e_el, h2d, d2h = measure_e2e(torch, qmm, layer, e2e_steps, dist, graphs=True)
+    e2e_el, h2d, d2h, _ = measure_e2e(torch, qmm, layer, e2e_steps, dist, graphs=True)
     e2e_value = aggregate(layer.step_bytes * e2e_steps, dist.max(e2e_el), dist.world) / 1e9
-    e2e_el_d, _, _ = measure_e2e(torch, qmm, layer, e2e_steps, dist, graphs=False)
+    e2e_el_d, _, _, _ = measure_e2e(torch, qmm, layer, e2e_steps, dist, graphs=False)
     e2e_direct = aggregate(layer.step_bytes * e2e_steps, dist.max(e2e_el_d), dist.world) / 1e9
-    e2e_el_ce, _, _ = measure_e2e(torch, qmm, layer, e2e_steps, dist, graphs=True, copy_engine=True)
+    e2e_el_ce, _, _, _ = measure_e2e(torch, qmm, layer, e2e_steps, dist, graphs=True, copy_engine=True)
     e2e_ce = aggregate(layer.step_bytes * e2e_steps, dist.max(e2e_el_ce), dist.world) / 1e9
+    e2e_el_rot, _, _, rot_steps = measure_e2e(torch, qmm, layer, e2e_steps, dist, graphs=True,
+                                              rotation_graph=True)
+    e2e_rot = aggregate(layer.step_bytes * rot_steps, dist.max(e2e_el_rot), dist.world) / 1e9
     step_bytes, launches_per_step, R = layer.step_bytes, layer.launches_per_step, layer.R
     del layer
     torch.cuda.empty_cache()
@@ -1017,7 +1033,11 @@ def run_ours(args, dist):
                                          "step (no graph): host-bound"},
                 "copy_engine": {"value": round(e2e_ce, 2), "unit": "GB/s",
                                 "path": "as `path`, with the two copies made by cudaMemcpyAsync "
-                                        "(torch non-blocking copy_) instead of qmm_copy"}},
+                                        "(torch non-blocking copy_) instead of qmm_copy"},
+                "rotation_graph": {"value": round(e2e_rot, 2), "unit": "GB/s", "steps": rot_steps,
+                                   "path": f"as `path`, with one CUDA graph holding {R} consecutive "
+                                           "steps (one weight rotation), each step still copying "
+                                           "its activations in and its outputs out"}},
         "gpu_launches": args.steps * launches_per_step,
     }
     if not args.no_secondary and dist.rank == 0:
