@@ -162,6 +162,27 @@ def test_medium_prompt_form(qmm, oracle_mod, m, n, k, form):
     assert_within(y.cpu().numpy()[mi, ni], y_ref, bound, GEMM_REL, f"{form} {m}x{n}x{k}")
 
 
+@pytest.mark.parametrize("m,n,k,form", [(1024, 2048, 8192, "split"), (768, 4096, 4096, "two")])
+def test_medium_prompt_form_q8_0(qmm, oracle_mod, m, n, k, form):
+    """The same choice of form for Q8_0 weights: at 2048 x 8192 the fused kernel
+    splits K through the workspace, at 4096 x 4096 with three token blocks the
+    product runs in two phases with the fused kernel's bits.  Sampled outputs
+    against the oracle."""
+    w = _weights("q8_0", n, k, seed=m + 7)
+    xb = synth.activations_bf16(m, k, seed=m + 7, stream=5)
+    wd, xd = to_dev(w, torch), bf16_tensor(xb, torch)
+    y = qmm.gemm("q8_0", wd, xd, n, k, workspace=_ws(qmm, n, k))
+    torch.cuda.synchronize()
+    assert qmm.qmm_get_device_error() == 0
+    if form == "two":
+        assert torch.equal(y, qmm.gemm("q8_0", wd, xd, n, k))
+    rng = np.random.default_rng(m + 1)
+    mi = np.concatenate([rng.integers(0, m, 1500), [0, m - 1]])
+    ni = np.concatenate([rng.integers(0, n, 1500), [n - 1, 0]])
+    y_ref, bound = oracle_mod.gemv_q8_0_at(w, _bf16_to_f32(xb), m, n, k, mi, ni)
+    assert_within(y.cpu().numpy()[mi, ni], y_ref, bound, GEMM_REL, f"q8_0 {form} {m}x{n}x{k}")
+
+
 def test_workspace_argument_checks(qmm):
     m, n, k = 600, 64, 256
     w = torch.zeros(n * (k // 32) * 18, dtype=torch.uint8, device="cuda")
