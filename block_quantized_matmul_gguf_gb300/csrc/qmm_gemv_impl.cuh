@@ -8,9 +8,10 @@
 // is about HBM and issue slots, not tensor cores.
 //
 // Streaming kernel (K % 256 == 0, 16-byte aligned w and x):
-//  * Lane r of a warp owns row r of a 32-row tile; for small problems two
-//    lanes share a row (half a chunk each), and at M <= 10 a lane owns two
-//    rows, so that each activation load feeds both.  K is cut into chunks
+//  * Lane r of a warp owns row r of a 32-row tile; for small problems (and,
+//    at M = 1, where it needs a smaller cluster split) two lanes share a row
+//    (half a chunk each), and at M <= 10 a lane owns two rows, so that each
+//    activation load feeds both.  K is cut into chunks
 //    of 256 weights (8 blocks: 144 bytes of Q4_0, 272 of Q8_0), which keeps
 //    every row chunk 16-byte aligned.  A tile's K range is split over kw
 //    warps of a CTA (partial sums added through shared memory) and, for
@@ -36,7 +37,7 @@
 //    byte) at bit s into the mantissa of 2^23 gives m = 2^23 + v*2^s exactly;
 //    one FMA m*2^-s - (2^23 + 8*2^s)*2^-s (Q4_0; +128 for Q8_0) leaves the
 //    exact integer nibble-8 (or q).  Both that FMA and the product with x run
-//    as packed f32x2 instructions, four independent chains at small M.
+//    as packed f32x2 instructions, one chain per block, row and token.
 //  * Per block: acc = sum_j (nibble_j - 8) * x_j in fp32, then y += d * acc.
 //
 // Persistent kernel (one large matrix, M <= 10): one CTA per SM over an equal
